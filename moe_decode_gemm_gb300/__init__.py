@@ -1,0 +1,221 @@
+"""GB300-native decode projection GEMM + MoE decode block.
+
+Thin ctypes binding over ``libdecgemm.so`` (the C ABI in include/decgemm.h).
+The functions below only marshal arguments: torch tensors give device
+pointers and sizes, the current torch stream gives the CUDA stream. Every
+step of the computation runs in the library's CUDA kernels; there is no
+fallback path. If the library is missing, importing the binding's functions
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdecgemm.so")
+
+DEC_OK = 0
+DEC_EINVAL = -1
+DEC_EUNSUPPORTED = -2
+DEC_ECUDA = -3
+DEC_ETIMEOUT = -4
+DEC_ENOMEM = -5
+DEC_ENODEV = -6
+
+REGIME_NONE, REGIME_SMALLM, REGIME_MMA, REGIME_TC = 0, 1, 2, 3
+REGIME_NAMES = {0: "none", 1: "smallm", 2: "mma", 3: "tc"}
+
+# Names the header declares; the ABI tests check every one is exported.
+EXPORTS = [
+    "dec_linear", "dec_linear_residual", "dec_linear_splitk", "moe_decode",
+    "moe_decode_residual", "l2_prefetch", "dec_add", "dec_last_choice", "dec_last_grid",
+    "dec_strerror", "dec_sync_check", "dec_set_wait_timeout_ns", "dec_selftest_timeout",
+    "dec_launch_count", "dec_probe_begin", "dec_probe_end", "dec_shutdown", "dec_version",
+]
+
+_lib = None
+
+
+class DecError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__("%s failed: %s (%d)" % (what, strerror(code), code))
+
+
+def lib():
+    """The loaded library. Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libdecgemm.so is not built; run "
+                               "`python -m moe_decode_gemm_gb300.build` (no fallback exists)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, SZ, LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_longlong
+        sig = {
+            "dec_linear": (I, [P, P, P, I, I, I, P]),
+            "dec_linear_residual": (I, [P, P, P, P, I, I, I, P]),
+            "dec_linear_splitk": (I, [P, P, P, I, I, I, I, P]),
+            "moe_decode": (I, [P, P, P, P, P, P, P, I, I, I, I, I, P, P, P]),
+            "moe_decode_residual": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, P]),
+            "l2_prefetch": (I, [P, SZ, P]),
+            "dec_add": (I, [P, P, P, SZ, P]),
+            "dec_last_choice": (I, []),
+            "dec_last_grid": (I, []),
+            "dec_strerror": (ctypes.c_char_p, [I]),
+            "dec_sync_check": (I, [P]),
+            "dec_set_wait_timeout_ns": (LL, [LL]),
+            "dec_selftest_timeout": (I, [LL, P]),
+            "dec_launch_count": (LL, []),
+            "dec_probe_begin": (I, [I, I]),
+            "dec_probe_end": (I, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
+            "dec_shutdown": (None, []),
+            "dec_version": (I, []),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().dec_strerror(int(code)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != DEC_OK:
+        raise DecError(rc, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+# ---------------------------------------------------------------- the hot path
+def dec_linear(x, W, y=None, stream=None, residual=None):
+    """y = x·Wᵀ (bf16), or y = residual + x·Wᵀ when ``residual`` is given.
+
+    x: [M,K] bf16, W: [N,K] bf16, y: [M,N] bf16 (allocated if None).
+    """
+    import torch
+
+    M, K = x.shape
+    N = W.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    if residual is None:
+        rc = lib().dec_linear(_ptr(x), _ptr(W), _ptr(y), M, N, K, _stream(stream))
+    else:
+        rc = lib().dec_linear_residual(_ptr(x), _ptr(W), _ptr(residual), _ptr(y), M, N, K,
+                                       _stream(stream))
+    _check(rc, "dec_linear")
+    return y
+
+
+def dec_linear_splitk(x, W, S, y=None, stream=None):
+    """dec_linear with the split factor forced to S (test/tuning hook)."""
+    import torch
+
+    M, K = x.shape
+    N = W.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check(lib().dec_linear_splitk(_ptr(x), _ptr(W), _ptr(y), M, N, K, int(S), _stream(stream)),
+           "dec_linear_splitk")
+    return y
+
+
+def moe_decode(x, Wr, W13, W2, Ws13, Ws2, topk, out=None, topk_idx=None, topk_w=None,
+               stream=None, residual=None):
+    """MoE decode block. Shapes: x [M,H], Wr [E,H], W13 [E,2I,H], W2 [E,H,I],
+    Ws13 [2I,H] / Ws2 [H,I] or both None. Returns out [M,H] bf16 (plus the
+    residual when given)."""
+    import torch
+
+    M, H = x.shape
+    E = Wr.shape[0]
+    I = W13.shape[1] // 2
+    if out is None:
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    args = [_ptr(x), _ptr(Wr), _ptr(W13), _ptr(W2), _ptr(Ws13), _ptr(Ws2)]
+    tail = [M, H, E, int(topk), I, _ptr(topk_idx), _ptr(topk_w), _stream(stream)]
+    if residual is None:
+        rc = lib().moe_decode(*args, _ptr(out), *tail)
+    else:
+        rc = lib().moe_decode_residual(*args, _ptr(residual), _ptr(out), *tail)
+    _check(rc, "moe_decode")
+    return out
+
+
+def l2_prefetch(t_or_ptr, nbytes=None, stream=None):
+    """Warm L2 with a tensor's bytes (or a raw device pointer and byte count)."""
+    if nbytes is None:
+        ptr, nbytes = t_or_ptr.data_ptr(), t_or_ptr.numel() * t_or_ptr.element_size()
+    else:
+        ptr = int(t_or_ptr)
+    _check(lib().l2_prefetch(ctypes.c_void_p(ptr), int(nbytes), _stream(stream)), "l2_prefetch")
+
+
+def dec_add(a, b, out=None, stream=None):
+    """out = bf16(a + b) elementwise."""
+    import torch
+
+    if out is None:
+        out = torch.empty_like(a)
+    _check(lib().dec_add(_ptr(a), _ptr(b), _ptr(out), a.numel(), _stream(stream)), "dec_add")
+    return out
+
+
+# ---------------------------------------------------------------- introspection
+def last_choice():
+    """(regime name, split factor) of this thread's last projection call."""
+    v = lib().dec_last_choice()
+    return REGIME_NAMES.get(v & 0xFF, "?"), v >> 8
+
+
+def last_grid() -> int:
+    return lib().dec_last_grid()
+
+
+def sync_check(stream=None) -> int:
+    return lib().dec_sync_check(_stream(stream))
+
+
+def set_wait_timeout_ns(ns: int) -> int:
+    return lib().dec_set_wait_timeout_ns(int(ns))
+
+
+def selftest_timeout(ns: int, stream=None):
+    _check(lib().dec_selftest_timeout(int(ns), _stream(stream)), "dec_selftest_timeout")
+
+
+def launch_count() -> int:
+    return lib().dec_launch_count()
+
+
+def probe_begin(kind: int, capacity: int):
+    _check(lib().dec_probe_begin(int(kind), int(capacity)), "dec_probe_begin")
+
+
+def probe_end():
+    ms = ctypes.c_double(0.0)
+    n = ctypes.c_int(0)
+    _check(lib().dec_probe_end(ctypes.byref(ms), ctypes.byref(n)), "dec_probe_end")
+    return ms.value, n.value
+
+
+def shutdown():
+    lib().dec_shutdown()
+
+
+PROBE_EXPERT_W13, PROBE_EXPERT_W2, PROBE_LINEAR, PROBE_ROUTER, PROBE_COMBINE = 0, 1, 2, 3, 4

@@ -1,0 +1,490 @@
+// api.cu -- the C ABI: argument validation, kernel-regime selection, the
+// per-device workspace, the shared-expert side stream, launch accounting and
+// the timing probe. Everything here runs on the host; every step of the
+// decode path runs in the kernels of k_linear.cu, k_tc.cu and k_moe.cu.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/decgemm.h"
+#include "launch.h"
+
+namespace dg {
+
+// ------------------------------------------------------------------ tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
+
+bool make_tmap(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
+               bool l2_promote_256) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode || rows == 0 || cols == 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B,
+                        l2_promote_256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                       : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ device state
+struct Buf {
+  void* p = nullptr;
+  size_t bytes = 0;
+};
+
+struct DevState {
+  bool init = false;
+  int sms = 0;
+  int l2 = 0;
+  int cc_major = 0, cc_minor = 0;
+  cudaStream_t side = nullptr;            // shared expert
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  int* status = nullptr;                  // device status word
+  Buf ws_main, ctr_main, ws_side, ctr_side;
+  Buf moe;                                // routing tables + intermediates
+  int moe_M = 0, moe_E = 0, moe_k = 0, moe_I = 0, moe_H = 0;
+  MoeBufs mb = {};
+};
+
+static std::mutex g_mu;
+static std::vector<DevState> g_dev;
+static std::atomic<long long> g_launches{0};
+static long long g_timeout_ns = 2000000000LL;
+static thread_local int t_last_choice = DEC_REGIME_NONE;
+static thread_local int t_last_grid = 0;
+
+// timing probe
+static std::mutex g_probe_mu;
+static int g_probe_kind = -1;
+static int g_probe_cap = 0;
+static std::vector<cudaEvent_t> g_probe_ev;  // start/end pairs
+static int g_probe_n = 0;
+
+static int to_err(cudaError_t e) { return e == cudaSuccess ? DEC_OK : DEC_ECUDA; }
+
+static int get_dev(DevState** out) {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return DEC_ENODEV;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if ((int)g_dev.size() <= d) g_dev.resize(d + 1);
+  DevState& s = g_dev[d];
+  if (!s.init) {
+    cudaDeviceProp p;
+    if (cudaGetDeviceProperties(&p, d) != cudaSuccess) return DEC_ENODEV;
+    if (p.major != 10 || p.minor != 3) return DEC_ENODEV;  // the library is built for sm_103a
+    s.sms = p.multiProcessorCount;
+    s.l2 = p.l2CacheSize;
+    s.cc_major = p.major;
+    s.cc_minor = p.minor;
+    int lo = 0, hi = 0;
+    cudaDeviceGetStreamPriorityRange(&lo, &hi);
+    if (cudaStreamCreateWithPriority(&s.side, cudaStreamNonBlocking, hi) != cudaSuccess)
+      return DEC_ECUDA;
+    if (cudaEventCreateWithFlags(&s.ev_fork, cudaEventDisableTiming) != cudaSuccess) return DEC_ECUDA;
+    if (cudaEventCreateWithFlags(&s.ev_join, cudaEventDisableTiming) != cudaSuccess) return DEC_ECUDA;
+    if (cudaMalloc(&s.status, 256) != cudaSuccess) return DEC_ENOMEM;
+    if (cudaMemset(s.status, 0, 256) != cudaSuccess) return DEC_ECUDA;
+    s.init = true;
+  }
+  *out = &s;
+  return DEC_OK;
+}
+
+// Grow a zero-initialised device buffer. Growing synchronises the device.
+static int ensure(Buf& b, size_t bytes, cudaStream_t st) {
+  if (b.bytes >= bytes) return DEC_OK;
+  if (b.p) {
+    cudaDeviceSynchronize();
+    cudaFree(b.p);
+    b.p = nullptr;
+    b.bytes = 0;
+  }
+  size_t want = bytes + bytes / 4;
+  if (cudaMalloc(&b.p, want) != cudaSuccess) return DEC_ENOMEM;
+  if (cudaMemsetAsync(b.p, 0, want, st) != cudaSuccess) return DEC_ECUDA;
+  b.bytes = want;
+  return DEC_OK;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static Ctx make_ctx(DevState* s, cudaStream_t st) {
+  Ctx c;
+  c.sms = s->sms;
+  c.timeout_ns = g_timeout_ns;
+  c.status = s->status;
+  c.stream = st;
+  c.pdl = true;
+  return c;
+}
+
+// Probe: time launches of one kind with events on their stream.
+struct ProbeScope {
+  bool on = false;
+  cudaStream_t st;
+  int slot = -1;
+  ProbeScope(int kind, cudaStream_t s) : st(s) {
+    std::lock_guard<std::mutex> lk(g_probe_mu);
+    if (kind == g_probe_kind && g_probe_n < g_probe_cap) {
+      slot = g_probe_n++;
+      on = true;
+      cudaEventRecord(g_probe_ev[2 * slot], st);
+    }
+  }
+  ~ProbeScope() {
+    if (on) cudaEventRecord(g_probe_ev[2 * slot + 1], st);
+  }
+};
+
+static int counted(cudaError_t e) {
+  if (e == cudaSuccess) g_launches.fetch_add(1);
+  return to_err(e);
+}
+
+// ------------------------------------------------------------------ projections
+static int regime_for(int M) {
+  const char* f = std::getenv("DEC_FORCE");
+  if (f) {
+    if (!std::strcmp(f, "smallm") && M <= 2) return DEC_REGIME_SMALLM;
+    if (!std::strcmp(f, "mma")) return DEC_REGIME_MMA;
+    if (!std::strcmp(f, "tc") && M >= 16) return DEC_REGIME_TC;
+  }
+  if (M <= 2) return DEC_REGIME_SMALLM;
+  if (M < 16) return DEC_REGIME_MMA;
+  return DEC_REGIME_TC;
+}
+
+static int linear_impl(const void* x, const void* W, const void* res, void* y, int M, int N, int K,
+                       int S, void* stream) {
+  if (!x || !W || !y) return DEC_EINVAL;
+  if (M < 1 || N < 1 || K < 8 || (K % 8) != 0) return DEC_EINVAL;
+  if (!aligned16(x) || !aligned16(W) || !aligned16(y) || (res && !aligned16(res))) return DEC_EINVAL;
+  if (M > 64) return DEC_EUNSUPPORTED;
+  const int KB = (K + 63) / 64;
+  if (S != 0 && (S < 1 || S > KB)) return DEC_EINVAL;
+  DevState* s = nullptr;
+  int rc = get_dev(&s);
+  if (rc) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int regime = regime_for(M);
+  if (regime == DEC_REGIME_TC) regime = DEC_REGIME_MMA;  // tcgen05 path not built yet
+  const int xr = regime == DEC_REGIME_SMALLM ? 8 : (M <= 16 ? 16 : 64);
+  const long long tiles = (N + 127) / 128;
+  const long long T = tiles * KB;
+  long long grid = S ? tiles * S : (T < s->sms ? T : s->sms);
+  if (grid > T) grid = T;
+  if ((rc = ensure(s->ws_main, (size_t)grid * 2 * 128 * xr * sizeof(float), st))) return rc;
+  if ((rc = ensure(s->ctr_main, (size_t)tiles * sizeof(int), st))) return rc;
+  Ctx cx = make_ctx(s, st);
+  long long seff = (KB * grid + T - 1) / T;
+  if (seff < 1) seff = 1;
+  t_last_choice = regime | ((int)seff << 8);
+  t_last_grid = (int)grid;
+  ProbeScope probe(2, st);
+  return counted(launch_dense(cx, xr, regime != DEC_REGIME_SMALLM, res != nullptr, x, W, res, y,
+                              M, N, K, (int)grid,
+                              (float*)s->ws_main.p, (int*)s->ctr_main.p));
+}
+
+// ------------------------------------------------------------------ MoE
+static int moe_bufs(DevState* s, int M, int H, int E, int k, int I, cudaStream_t st) {
+  if (M <= s->moe_M && H <= s->moe_H && E <= s->moe_E && k <= s->moe_k && I <= s->moe_I) return DEC_OK;
+  const int Mx = 64;  // sized for the whole decode envelope at once
+  const int Ex = E > s->moe_E ? E : s->moe_E;
+  const int kx = k > s->moe_k ? k : s->moe_k;
+  const int Ix = I > s->moe_I ? I : s->moe_I;
+  const int Hx = H > s->moe_H ? H : s->moe_H;
+  auto al = [](size_t v) { return (v + 255) & ~size_t(255); };
+  size_t off = 0;
+  size_t o_logits = off; off += al((size_t)Mx * Ex * 4);
+  size_t o_nact = off; off += al(4);
+  size_t o_gexp = off; off += al((size_t)Ex * 4);
+  size_t o_goff = off; off += al((size_t)(Ex + 1) * 4);
+  size_t o_ptok = off; off += al((size_t)Mx * kx * 4);
+  size_t o_pof = off; off += al((size_t)Mx * kx * 4);
+  size_t o_gate = off; off += al((size_t)Mx * kx * 4);
+  size_t o_done = off; off += al(4);
+  size_t o_h = off; off += al((size_t)Mx * kx * Ix * 2);
+  size_t o_o = off; off += al((size_t)Mx * kx * Hx * 4);
+  size_t o_hs = off; off += al((size_t)Mx * Ix * 2);
+  size_t o_s = off; off += al((size_t)Mx * Hx * 4);
+  int rc = ensure(s->moe, off, st);
+  if (rc) return rc;
+  uint8_t* b = (uint8_t*)s->moe.p;
+  s->mb.logits = (float*)(b + o_logits);
+  s->mb.nact = (int*)(b + o_nact);
+  s->mb.grp_exp = (int*)(b + o_gexp);
+  s->mb.grp_off = (int*)(b + o_goff);
+  s->mb.pair_tok = (int*)(b + o_ptok);
+  s->mb.pair_of = (int*)(b + o_pof);
+  s->mb.gate = (float*)(b + o_gate);
+  s->mb.done = (int*)(b + o_done);
+  s->mb.h = (uint16_t*)(b + o_h);
+  s->mb.o = (float*)(b + o_o);
+  s->mb.hs = (uint16_t*)(b + o_hs);
+  s->mb.s = (float*)(b + o_s);
+  s->moe_M = Mx;
+  s->moe_E = Ex;
+  s->moe_k = kx;
+  s->moe_I = Ix;
+  s->moe_H = Hx;
+  return DEC_OK;
+}
+
+static int moe_impl(const void* x, const void* Wr, const void* W13, const void* W2, const void* Ws13,
+                    const void* Ws2, const void* res, void* out, int M, int H, int E, int topk,
+                    int I, int32_t* topk_idx, float* topk_w, void* stream) {
+  if (!x || !Wr || !W13 || !W2 || !out) return DEC_EINVAL;
+  if ((Ws13 == nullptr) != (Ws2 == nullptr)) return DEC_EINVAL;
+  if (M < 1 || H < 8 || E < 1 || topk < 1 || I < 8 || (H % 8) || (I % 8)) return DEC_EINVAL;
+  const void* ptrs[] = {x, Wr, W13, W2, Ws13, Ws2, res, out, topk_idx, topk_w};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return DEC_EINVAL;
+  if (res && res == x) return DEC_EINVAL;
+  if (M > 64 || E > 1024 || topk > 32 || topk > E) return DEC_EUNSUPPORTED;
+  DevState* s = nullptr;
+  int rc = get_dev(&s);
+  if (rc) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = moe_bufs(s, M, H, E, topk, I, st))) return rc;
+  const size_t ws_bytes = (size_t)s->sms * 2 * 128 * 64 * sizeof(float);
+  const int tiles13 = (I + 63) / 64, tiles2 = (H + 127) / 128, tilesr = (E + 127) / 128;
+  int maxt = tiles13 > tiles2 ? tiles13 : tiles2;
+  const size_t ctr_bytes = (size_t)(E * (size_t)maxt + tilesr + 64) * sizeof(int);
+  if ((rc = ensure(s->ws_main, ws_bytes, st))) return rc;
+  if ((rc = ensure(s->ctr_main, ctr_bytes, st))) return rc;
+  const bool shared = Ws13 != nullptr;
+  if (shared) {
+    if ((rc = ensure(s->ws_side, ws_bytes, st))) return rc;
+    if ((rc = ensure(s->ctr_side, (size_t)(maxt + 64) * sizeof(int), st))) return rc;
+  }
+  Ctx cx = make_ctx(s, st);
+  float* ws = (float*)s->ws_main.p;
+  int* ctr = (int*)s->ctr_main.p;
+  // shared expert: fork to the side stream, overlapped with routing and experts
+  if (shared) {
+    if (cudaEventRecord(s->ev_fork, st) != cudaSuccess) return DEC_ECUDA;
+    if (cudaStreamWaitEvent(s->side, s->ev_fork, 0) != cudaSuccess) return DEC_ECUDA;
+    Ctx sx = make_ctx(s, s->side);
+    sx.pdl = false;
+    const int sgrid = s->sms;
+    if ((rc = counted(launch_shared_w13(sx, x, Ws13, M, H, I, s->mb, sgrid, (float*)s->ws_side.p,
+                                        (int*)s->ctr_side.p))))
+      return rc;
+    sx.pdl = true;
+    if ((rc = counted(launch_shared_w2(sx, Ws2, M, H, I, s->mb, sgrid, (float*)s->ws_side.p,
+                                       (int*)s->ctr_side.p))))
+      return rc;
+    if (cudaEventRecord(s->ev_join, s->side) != cudaSuccess) return DEC_ECUDA;
+  }
+  {
+    ProbeScope p(3, st);
+    if ((rc = counted(launch_router(cx, x, Wr, M, H, E, topk, topk_idx, topk_w, s->mb, ws,
+                                    ctr + E * maxt))))
+      return rc;
+  }
+  {
+    ProbeScope p(0, st);
+    if ((rc = counted(launch_experts_w13(cx, x, W13, M, H, E, topk, I, s->mb, ws, ctr)))) return rc;
+  }
+  {
+    ProbeScope p(1, st);
+    if ((rc = counted(launch_experts_w2(cx, W2, M, H, E, topk, I, s->mb, ws, ctr)))) return rc;
+  }
+  if (shared) {
+    if (cudaStreamWaitEvent(st, s->ev_join, 0) != cudaSuccess) return DEC_ECUDA;
+  }
+  // After the join the combine depends on two streams: launch it without PDL
+  // so that both dependencies are complete ones.
+  cx.pdl = !shared;
+  ProbeScope p(4, st);
+  return counted(launch_combine(cx, s->mb, shared, res, out, M, H, topk));
+}
+
+}  // namespace dg
+
+using namespace dg;
+
+extern "C" {
+
+int dec_version(void) { return 100; }
+
+int dec_linear(const void* x, const void* W, void* y, int M, int N, int K, void* stream) {
+  return linear_impl(x, W, nullptr, y, M, N, K, 0, stream);
+}
+
+int dec_linear_residual(const void* x, const void* W, const void* res, void* y, int M, int N, int K,
+                        void* stream) {
+  if (!res) return DEC_EINVAL;
+  return linear_impl(x, W, res, y, M, N, K, 0, stream);
+}
+
+int dec_linear_splitk(const void* x, const void* W, void* y, int M, int N, int K, int S,
+                      void* stream) {
+  if (S < 1) return DEC_EINVAL;
+  return linear_impl(x, W, nullptr, y, M, N, K, S, stream);
+}
+
+int moe_decode(const void* x, const void* Wr, const void* W13, const void* W2, const void* Ws13,
+               const void* Ws2, void* out, int M, int H, int E, int topk, int I, int32_t* topk_idx,
+               float* topk_w, void* stream) {
+  return moe_impl(x, Wr, W13, W2, Ws13, Ws2, nullptr, out, M, H, E, topk, I, topk_idx, topk_w,
+                  stream);
+}
+
+int moe_decode_residual(const void* x, const void* Wr, const void* W13, const void* W2,
+                        const void* Ws13, const void* Ws2, const void* res, void* out, int M, int H,
+                        int E, int topk, int I, int32_t* topk_idx, float* topk_w, void* stream) {
+  if (!res) return DEC_EINVAL;
+  return moe_impl(x, Wr, W13, W2, Ws13, Ws2, res, out, M, H, E, topk, I, topk_idx, topk_w, stream);
+}
+
+int l2_prefetch(const void* ptr, size_t bytes, void* stream) {
+  if (!ptr || !aligned16(ptr)) return DEC_EINVAL;
+  bytes &= ~size_t(15);
+  if (bytes == 0) return DEC_OK;
+  DevState* s = nullptr;
+  int rc = get_dev(&s);
+  if (rc) return rc;
+  const size_t cap = (size_t)s->l2 / 2;
+  if (bytes > cap) bytes = cap;
+  Ctx cx = make_ctx(s, reinterpret_cast<cudaStream_t>(stream));
+  return counted(launch_prefetch(cx, ptr, bytes));
+}
+
+int dec_add(const void* a, const void* b, void* out, size_t n, void* stream) {
+  if (!a || !b || !out) return DEC_EINVAL;
+  if (n == 0) return DEC_OK;
+  DevState* s = nullptr;
+  int rc = get_dev(&s);
+  if (rc) return rc;
+  Ctx cx = make_ctx(s, reinterpret_cast<cudaStream_t>(stream));
+  return counted(launch_add(cx, a, b, out, n));
+}
+
+int dec_last_choice(void) { return t_last_choice; }
+int dec_last_grid(void) { return t_last_grid; }
+
+const char* dec_strerror(int code) {
+  switch (code) {
+    case DEC_OK: return "ok";
+    case DEC_EINVAL: return "invalid argument (null pointer, size, alignment or K % 8)";
+    case DEC_EUNSUPPORTED: return "outside the decode envelope (M > 64, topk > 32 or > E, E > 1024)";
+    case DEC_ECUDA: return "CUDA runtime or launch error";
+    case DEC_ETIMEOUT: return "a bounded device-side wait gave up";
+    case DEC_ENOMEM: return "workspace allocation failed";
+    case DEC_ENODEV: return "no sm_103 (GB300) device is current";
+    default: return "unknown error code";
+  }
+}
+
+int dec_sync_check(void* stream) {
+  DevState* s = nullptr;
+  int rc = get_dev(&s);
+  if (rc) return rc;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return DEC_ECUDA;
+  if (cudaStreamSynchronize(s->side) != cudaSuccess) return DEC_ECUDA;
+  int st = 0;
+  if (cudaMemcpy(&st, s->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DEC_ECUDA;
+  if (st != 0) {
+    // Reset the status word and every arrival counter a timed-out kernel may
+    // have left behind.
+    cudaMemset(s->status, 0, sizeof(int));
+    if (s->ctr_main.p) cudaMemset(s->ctr_main.p, 0, s->ctr_main.bytes);
+    if (s->ctr_side.p) cudaMemset(s->ctr_side.p, 0, s->ctr_side.bytes);
+    if (s->mb.done) cudaMemset(s->mb.done, 0, sizeof(int));
+    cudaDeviceSynchronize();
+    return DEC_ETIMEOUT;
+  }
+  return DEC_OK;
+}
+
+long long dec_set_wait_timeout_ns(long long ns) {
+  long long old = g_timeout_ns;
+  if (ns >= 0) g_timeout_ns = ns;
+  return old;
+}
+
+int dec_selftest_timeout(long long ns, void* stream) {
+  DevState* s = nullptr;
+  int rc = get_dev(&s);
+  if (rc) return rc;
+  Ctx cx = make_ctx(s, reinterpret_cast<cudaStream_t>(stream));
+  return counted(launch_selftest_timeout(cx, ns));
+}
+
+long long dec_launch_count(void) { return g_launches.load(); }
+
+int dec_probe_begin(int kind, int capacity) {
+  std::lock_guard<std::mutex> lk(g_probe_mu);
+  for (cudaEvent_t e : g_probe_ev) cudaEventDestroy(e);
+  g_probe_ev.clear();
+  g_probe_n = 0;
+  g_probe_cap = 0;
+  g_probe_kind = -1;
+  if (capacity <= 0) return DEC_OK;
+  g_probe_ev.resize(2 * (size_t)capacity);
+  for (auto& e : g_probe_ev)
+    if (cudaEventCreate(&e) != cudaSuccess) return DEC_ECUDA;
+  g_probe_cap = capacity;
+  g_probe_kind = kind;
+  return DEC_OK;
+}
+
+int dec_probe_end(double* total_ms, int* launches) {
+  std::lock_guard<std::mutex> lk(g_probe_mu);
+  double tot = 0.0;
+  for (int i = 0; i < g_probe_n; ++i) {
+    if (cudaEventSynchronize(g_probe_ev[2 * i + 1]) != cudaSuccess) return DEC_ECUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, g_probe_ev[2 * i], g_probe_ev[2 * i + 1]) != cudaSuccess)
+      return DEC_ECUDA;
+    tot += ms;
+  }
+  if (total_ms) *total_ms = tot;
+  if (launches) *launches = g_probe_n;
+  g_probe_kind = -1;
+  return DEC_OK;
+}
+
+void dec_shutdown(void) {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if ((int)g_dev.size() <= d || !g_dev[d].init) return;
+  DevState& s = g_dev[d];
+  cudaDeviceSynchronize();
+  Buf* bufs[] = {&s.ws_main, &s.ctr_main, &s.ws_side, &s.ctr_side, &s.moe};
+  for (Buf* b : bufs) {
+    if (b->p) cudaFree(b->p);
+    b->p = nullptr;
+    b->bytes = 0;
+  }
+  if (s.status) cudaFree(s.status);
+  if (s.side) cudaStreamDestroy(s.side);
+  if (s.ev_fork) cudaEventDestroy(s.ev_fork);
+  if (s.ev_join) cudaEventDestroy(s.ev_join);
+  s = DevState();
+}
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// k_linear.cu -- dense decode projections y = x·Wᵀ on the weight-streaming
+// kernel: the CUDA-core small-matrix path (M <= 2) and the mma.sync split-K
+// path (M >= 3). "vLLM 如何用智能体辅助优化 Kimi K3 解码性能", Part 1 §1.
+#include <utility>
+
+#include "launch.h"
+#include "launch_util.cuh"
+#include "wstream.cuh"
+
+namespace dg {
+
+template <int XR>
+constexpr int dense_stages() {
+  return XR == 8 ? 12 : XR == 16 ? 11 : 8;
+}
+
+template <int XR>
+constexpr int dense_smem() {
+  return 1024 + dense_stages<XR>() * (kWBytes + XR * 128) + 2 * 8 * dense_stages<XR>() + 64;
+}
+
+template <int XR, int EPI>
+static cudaError_t run_dense(const Ctx& cx, bool mma, const void* x, const void* W, const void* res,
+                             void* y, int M, int N, int K, int grid, float* ws, int* ctr) {
+  constexpr int S = dense_stages<XR>();
+  constexpr int SMEM = dense_smem<XR>();
+  static_assert(SMEM <= kMaxDynSmem, "shared memory");
+  auto kern = wstream_kernel<XR, S, EPI, false, false, false>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = allow_smem(kern, SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  CUtensorMap wmap, xmap;
+  if (!make_tmap(&wmap, W, (uint64_t)N, (uint64_t)K, kTileRows, true)) return cudaErrorInvalidValue;
+  if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)K, XR, false)) return cudaErrorInvalidValue;
+  StreamArgs a = {};
+  a.K = K;
+  a.KB = (K + kKBlk - 1) / kKBlk;
+  a.TILES = (N + kTileRows - 1) / kTileRows;
+  a.nout = N;
+  a.M = M;
+  a.mma_min_tokens = mma ? 1 : 1 << 30;
+  a.out = y;
+  a.ldo = N;
+  a.res = reinterpret_cast<const uint16_t*>(res);
+  a.ws = ws;
+  a.ctr = ctr;
+  a.status = cx.status;
+  a.timeout_ns = cx.timeout_ns;
+  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
+}
+
+cudaError_t launch_dense(const Ctx& cx, int xr, bool mma, bool residual, const void* x,
+                         const void* W, const void* res, void* y, int M, int N, int K, int grid,
+                         float* ws, int* ctr) {
+  if (xr == 8)
+    return residual ? run_dense<8, EPI_BF16_RES>(cx, mma, x, W, res, y, M, N, K, grid, ws, ctr)
+                    : run_dense<8, EPI_BF16>(cx, mma, x, W, res, y, M, N, K, grid, ws, ctr);
+  if (xr == 16)
+    return residual ? run_dense<16, EPI_BF16_RES>(cx, mma, x, W, res, y, M, N, K, grid, ws, ctr)
+                    : run_dense<16, EPI_BF16>(cx, mma, x, W, res, y, M, N, K, grid, ws, ctr);
+  return residual ? run_dense<64, EPI_BF16_RES>(cx, mma, x, W, res, y, M, N, K, grid, ws, ctr)
+                  : run_dense<64, EPI_BF16>(cx, mma, x, W, res, y, M, N, K, grid, ws, ctr);
+}
+
+}  // namespace dg

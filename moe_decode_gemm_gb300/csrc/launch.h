@@ -1,0 +1,69 @@
+// launch.h -- host-side launchers shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dg {
+
+// Tensor map of a row-major bf16 matrix [rows, cols] read in boxes of
+// 64 columns x box_rows rows with 128-byte swizzle. Returns false on failure.
+bool make_tmap(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
+               bool l2_promote_256);
+
+struct Ctx {
+  int sms;
+  long long timeout_ns;
+  int* status;
+  cudaStream_t stream;
+  bool pdl;
+};
+
+// Dense projection: y = x·Wᵀ (+ res), XR in {8, 16, 64} token rows per stage.
+// grid: CTAs to launch (stream-K ranges). ws/ctr: split-K workspace.
+// mma: reduce with mma.sync (otherwise CUDA-core dot products, M <= 2 only).
+cudaError_t launch_dense(const Ctx& cx, int xr, bool mma, bool residual, const void* x,
+                         const void* W, const void* res, void* y, int M, int N, int K, int grid,
+                         float* ws, int* ctr);
+
+// tcgen05 projection for 16 <= M <= 64.
+cudaError_t launch_dense_tc(const Ctx& cx, bool residual, const void* x, const void* W,
+                            const void* res, void* y, int M, int N, int K, int grid, float* ws,
+                            int* ctr);
+
+struct MoeBufs {
+  float* logits;   // [M,E]
+  int* nact;
+  int* grp_exp;    // [E]
+  int* grp_off;    // [E+1]
+  int* pair_tok;   // [M*k]
+  int* pair_of;    // [M*k]
+  float* gate;     // [M*k]
+  int* done;
+  uint16_t* h;     // [M*k, I]
+  float* o;        // [M*k, H]
+  uint16_t* hs;    // [M, I]
+  float* s;        // [M, H]
+};
+
+cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E, int k,
+                          int32_t* idx_user, float* w_user, const MoeBufs& b, float* ws, int* ctr);
+cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, int M, int H, int E,
+                               int k, int I, const MoeBufs& b, float* ws, int* ctr);
+cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E, int k, int I,
+                              const MoeBufs& b, float* ws, int* ctr);
+cudaError_t launch_shared_w13(const Ctx& cx, const void* x, const void* Ws13, int M, int H, int I,
+                              const MoeBufs& b, int grid, float* ws, int* ctr);
+cudaError_t launch_shared_w2(const Ctx& cx, const void* Ws2, int M, int H, int I,
+                             const MoeBufs& b, int grid, float* ws, int* ctr);
+cudaError_t launch_combine(const Ctx& cx, const MoeBufs& b, bool with_shared, const void* res,
+                           void* out, int M, int H, int k);
+cudaError_t launch_add(const Ctx& cx, const void* a, const void* b, void* out, size_t n);
+cudaError_t launch_prefetch(const Ctx& cx, const void* ptr, size_t bytes);
+cudaError_t launch_selftest_timeout(const Ctx& cx, long long ns);
+
+// Shared memory each dense/MoE kernel needs (bytes), for cudaFuncSetAttribute.
+constexpr int kMaxDynSmem = 232448;
+
+}  // namespace dg

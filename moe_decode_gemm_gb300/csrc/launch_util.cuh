@@ -1,0 +1,34 @@
+// launch_util.cuh -- kernel launch with programmatic dependent launch (PDL).
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace dg {
+
+// Launch `kern` on `stream`. With pdl, the launch carries the programmatic
+// stream serialisation attribute: the kernel may start while the previous
+// kernel in the stream is finishing, and must call griddepcontrol.wait before
+// it touches anything that kernel writes or reads.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t stream, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// Raise a kernel's dynamic shared memory limit once.
+template <typename K>
+cudaError_t allow_smem(K kern, int bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+}  // namespace dg

@@ -1,0 +1,643 @@
+// wstream.cuh -- persistent weight-streaming GEMM for decode shapes (swap-AB:
+// weight rows are the long side, the 1..64 tokens the short side).
+//
+// One producer warp streams 128-row x 64-column bf16 weight tiles (16 KB, 128B
+// swizzle) and the matching token tile into a ring of shared-memory stages
+// with TMA; eight consumer warps reduce them. The work is the list of
+// (group, output tile, 64-wide k block) units, cut into one contiguous range
+// per CTA ("stream-K"), so every CTA streams the same number of weight bytes
+// whatever the shape. An output tile whose k range spans several CTAs is
+// finished by the last CTA to arrive on the tile's counter, which sums the
+// partials in CTA order: the result does not depend on arrival order.
+//
+// Consumers: a CUDA-core path for 1-2 tokens (a GEMV has no dense
+// contraction to give the tensor cores) and an mma.sync m16n8k16 path for
+// more tokens. Groups are the routed experts of an MoE block (the token list
+// of each comes from the router's scheduler) or one dense matrix.
+//
+// Sources: "vLLM 如何用智能体辅助优化 Kimi K3 解码性能", Part 1 §1 (small-matrix
+// kernel at batch 1-2, split-K beyond) and Part 1 §3 (routed experts).
+#pragma once
+
+#include "dg_common.cuh"
+
+namespace dg {
+
+constexpr int kNCW = 8;                    // consumer warps
+constexpr int kThreads = (kNCW + 1) * 32;  // + one producer warp
+constexpr int kTileRows = 128;             // weight rows per stage
+constexpr int kKBlk = 64;                  // k elements per stage (128 bytes)
+constexpr int kWBytes = kTileRows * 128;   // 16 KB
+
+enum Epi : int { EPI_BF16 = 0, EPI_BF16_RES = 1, EPI_F32 = 2, EPI_SWIGLU = 3 };
+
+// Routing tail run by the CTA that completes the router's last logit tile.
+struct RouteArgs {
+  int M, E, k;
+  const float* logits;     // [M,E]
+  int32_t* idx_user;       // optional [M,k]
+  float* w_user;           // optional [M,k]
+  int* nact;               // number of active experts
+  int* grp_exp;            // [E] expert id of active group u
+  int* grp_off;            // [E+1] first pair of group u
+  int* pair_tok;           // [M*k] token of pair p (pairs grouped by expert)
+  int* pair_of;            // [M*k] pair index of (m, j)
+  float* gate;             // [M*k] gate of (m, j)
+  int* done;               // completed-tile counter (reset by the tail)
+  int total_tiles;
+};
+
+struct StreamArgs {
+  int K, KB, TILES;
+  int nout;                  // valid output features per group
+  int M;                     // dense token count
+  int mma_min_tokens;        // groups with at least this many tokens use mma.sync
+  // grouped (MoE) mode; all null in dense mode
+  const int* nact;
+  const int* grp_exp;
+  const int* grp_off;
+  const int* pair_row;       // token-tile row of pair p; null: row p
+  int w_group_rows;          // weight rows per expert
+  int w_up_offset;           // paired (SwiGLU) tiles: row offset of the up block
+  // output
+  void* out;
+  long long ldo;             // elements between output rows
+  const uint16_t* res;       // residual for EPI_BF16_RES ([M, ldo] bf16)
+  // split-K workspace
+  float* ws;                 // [grid][2][128][XR] fp32 partial tiles
+  int* ctr;                  // per output tile arrival counters (zero at rest)
+  int* done;                 // router only: completed tiles
+  int total_tiles_dense;     // router only
+  RouteArgs route;
+  int* status;
+  long long timeout_ns;
+};
+
+struct GroupInfo {
+  int e;       // expert id (0 in dense mode)
+  int p0;      // first output row (pair) of the group
+  int c;       // tokens in the group
+};
+
+template <bool GROUPED>
+__device__ __forceinline__ GroupInfo load_group(const StreamArgs& a, int g) {
+  GroupInfo gi;
+  if (GROUPED) {
+    gi.e = a.grp_exp[g];
+    gi.p0 = a.grp_off[g];
+    gi.c = a.grp_off[g + 1] - gi.p0;
+  } else {
+    gi.e = 0;
+    gi.p0 = 0;
+    gi.c = a.M;
+  }
+  return gi;
+}
+
+// Stage row of local row lr (0..15) of consumer warp w. Paired (SwiGLU)
+// tiles hold 64 gate rows then 64 up rows; a warp owns 8 gate rows and the 8
+// up rows of the same intermediate features, so SwiGLU needs no exchange.
+template <bool PAIRED>
+__device__ __forceinline__ int stage_row(int w, int lr) {
+  if (PAIRED) return lr < 8 ? 8 * w + lr : 64 + 8 * w + (lr - 8);
+  return 16 * w + lr;
+}
+
+__device__ __forceinline__ long long cta_start(long long c, long long T, long long G) {
+  return (c * T) / G;
+}
+
+// CTA whose unit range contains unit v: largest c with start(c) <= v.
+__device__ __forceinline__ long long cta_of(long long v, long long T, long long G) {
+  return ((v + 1) * G + T - 1) / T - 1;
+}
+
+// ------------------------------------------------------------------ epilogue
+template <int EPI, bool GROUPED>
+__device__ __forceinline__ void store_out(const StreamArgs& a, const GroupInfo& gi, int t, int n,
+                                          float v) {
+  const long long row = (long long)gi.p0 + t;
+  if (EPI == EPI_F32) {
+    reinterpret_cast<float*>(a.out)[row * a.ldo + n] = v;
+  } else if (EPI == EPI_BF16_RES) {
+    const float r = bf_bits2f(a.res[row * a.ldo + n]);
+    reinterpret_cast<uint16_t*>(a.out)[row * a.ldo + n] = f2bf_bits(r + v);
+  } else {
+    reinterpret_cast<uint16_t*>(a.out)[row * a.ldo + n] = f2bf_bits(v);
+  }
+}
+
+__device__ __forceinline__ void store_swiglu(const StreamArgs& a, const GroupInfo& gi, int t, int i,
+                                             float gate, float up) {
+  const long long row = (long long)gi.p0 + t;
+  const float h = silu_f(gate) * up;
+  reinterpret_cast<uint16_t*>(a.out)[row * a.ldo + i] = f2bf_bits(h);
+}
+
+// ------------------------------------------------------------------ routing tail
+template <int NT>
+__device__ void route_tail(const RouteArgs& r, int ct, uint8_t* scratch) {
+  // scratch: masks [E] u64 | idx [M*k] int | g [M*k] float | cnt/off [E+1] int | flags
+  const int M = r.M, E = r.E, K = r.k;
+  unsigned long long* mask = reinterpret_cast<unsigned long long*>(scratch);
+  int* s_idx = reinterpret_cast<int*>(mask + E);
+  float* s_g = reinterpret_cast<float*>(s_idx + M * K);
+  int* s_off = reinterpret_cast<int*>(s_g + M * K);      // [E+1]
+  int* s_act = s_off + (E + 1);                          // [E+1] active rank prefix
+  int* s_warp = s_act + (E + 1);                         // [2*32] warp totals
+  const int warp = ct >> 5, lane = ct & 31;
+  const int nwarps = NT / 32;
+
+  // 1) top-k per token: one warp per token, each lane holds E/32 logits.
+  for (int m = warp; m < M; m += nwarps) {
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int e = lane + 32 * j;
+      v[j] = (e < E) ? __ldcg(r.logits + (long long)m * E + e) : -INFINITY;
+    }
+    uint32_t taken = 0;
+    float selv0 = 0.f, myv = 0.f;
+    int mye = 0;
+    for (int j = 0; j < K; ++j) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        const int e = lane + 32 * jj;
+        if (e < E && !((taken >> jj) & 1u) && (v[jj] > bv || (v[jj] == bv && e < be))) {
+          bv = v[jj];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+        if (ov > bv || (ov == bv && oe < be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (j == 0) selv0 = bv;
+      if (lane == j) {
+        myv = bv;
+        mye = be;
+      }
+    }
+    // gates: exp(l_j - l_max) / sum_j' exp(l_j' - l_max), summed j = 0..k-1
+    const float w = (lane < K) ? expf(myv - selv0) : 0.f;
+    float denom = 0.f;
+    for (int j = 0; j < K; ++j) denom += __shfl_sync(0xffffffffu, w, j);
+    if (lane < K) {
+      const float g = w / denom;
+      s_idx[m * K + lane] = mye;
+      s_g[m * K + lane] = g;
+      if (r.idx_user) r.idx_user[m * K + lane] = mye;
+      if (r.w_user) r.w_user[m * K + lane] = g;
+      r.gate[m * K + lane] = g;
+    }
+  }
+  for (int e = ct; e < E; e += NT) mask[e] = 0ull;
+  named_bar_sync(1, NT);
+  // 2) token sets per expert
+  for (int p = ct; p < M * K; p += NT) atomicOr(&mask[s_idx[p]], 1ull << (p / K));
+  named_bar_sync(1, NT);
+  // 3) exclusive scans of token counts and of "expert is active" over E
+  constexpr int PER = 4;  // E <= NT * PER
+  int cnt[PER], act[PER], csum = 0, asum = 0;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int e = ct * PER + q;
+    cnt[q] = (e < E) ? __popcll(mask[e]) : 0;
+    act[q] = cnt[q] > 0 ? 1 : 0;
+    csum += cnt[q];
+    asum += act[q];
+  }
+  int cinc = csum, ainc = asum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int c2 = __shfl_up_sync(0xffffffffu, cinc, off);
+    const int a2 = __shfl_up_sync(0xffffffffu, ainc, off);
+    if (lane >= off) {
+      cinc += c2;
+      ainc += a2;
+    }
+  }
+  if (lane == 31) {
+    s_warp[warp] = cinc;
+    s_warp[32 + warp] = ainc;
+  }
+  named_bar_sync(1, NT);
+  int cbase = 0, abase = 0;
+  for (int w2 = 0; w2 < warp; ++w2) {
+    cbase += s_warp[w2];
+    abase += s_warp[32 + w2];
+  }
+  int cpre = cbase + cinc - csum, apre = abase + ainc - asum;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int e = ct * PER + q;
+    if (e < E) {
+      s_off[e] = cpre;
+      if (act[q]) {
+        r.grp_exp[apre] = e;
+        r.grp_off[apre] = cpre;
+      }
+    }
+    cpre += cnt[q];
+    apre += act[q];
+  }
+  if (ct == NT - 1) {
+    int total_a = 0;
+    for (int w2 = 0; w2 < nwarps; ++w2) total_a += s_warp[32 + w2];
+    r.grp_off[total_a] = M * K;
+    *r.nact = total_a;
+  }
+  named_bar_sync(1, NT);
+  // 4) scatter pairs: pairs of expert e ordered by token
+  for (int p = ct; p < M * K; p += NT) {
+    const int m = p / K;
+    const int e = s_idx[p];
+    const unsigned long long below = (m == 0) ? 0ull : (mask[e] & ((1ull << m) - 1ull));
+    const int pos = s_off[e] + __popcll(below);
+    r.pair_tok[pos] = m;
+    r.pair_of[p] = pos;
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+// XR: token rows per stage (8, 16 or 64). STAGES: ring depth.
+// PAIRED: SwiGLU tiles (64 gate + 64 up rows). GROUPED: MoE groups.
+// ROUTER: dense fp32 logits followed by the routing tail.
+template <int XR, int STAGES, int EPI, bool PAIRED, bool GROUPED, bool ROUTER>
+__global__ void __launch_bounds__(kThreads, 1)
+    wstream_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
+                   const StreamArgs a) {
+  constexpr int kXBytes = XR * 128;
+  constexpr int kStageBytes = kWBytes + kXBytes;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * kStageBytes);
+  uint64_t* empty = full + STAGES;
+  volatile int* s_flags = reinterpret_cast<volatile int*>(empty + STAGES);  // [0]=abort [1]=last
+  uint8_t* scratch = reinterpret_cast<uint8_t*>(const_cast<int*>(s_flags) + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kNCW);
+    }
+    s_flags[0] = 0;
+    s_flags[1] = 0;
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&wmap);
+    prefetch_tmap(&xmap);
+  }
+  __syncthreads();
+  griddep_launch_dependents();
+
+  const long long c = blockIdx.x;
+  const int KB = a.KB, TILES = a.TILES;
+
+  long long T;
+  if (GROUPED) {
+    griddep_wait();
+    T = (long long)(*a.nact) * TILES * KB;
+  } else {
+    T = (long long)TILES * KB;
+  }
+  // Only the first min(grid, T) CTAs take units, so every working CTA has at
+  // least one and the contributors of a tile are exactly the CTAs between
+  // the owners of its first and last unit.
+  const long long G = (long long)gridDim.x < T ? (long long)gridDim.x : T;
+  const long long u0 = c < G ? cta_start(c, T, G) : 0;
+  const long long u1 = c < G ? cta_start(c + 1, T, G) : 0;
+  const int nunits = (int)(u1 - u0);
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      int gcur = -1;
+      GroupInfo gi{0, 0, 0};
+      auto issue_w = [&](int s, long long u) {
+        const long long gt = u / KB;
+        const int kb = (int)(u - gt * KB);
+        const int g = (int)(gt / TILES), tile = (int)(gt - (long long)g * TILES);
+        uint8_t* wdst = smem + s * kStageBytes;
+        const int e = GROUPED ? a.grp_exp[g] : 0;
+        const int rbase = e * a.w_group_rows;
+        if (PAIRED) {
+          tma_load_2d(wdst, &wmap, kb * kKBlk, rbase + tile * 64, &full[s], pol_w);
+          tma_load_2d(wdst + 64 * 128, &wmap, kb * kKBlk, rbase + a.w_up_offset + tile * 64,
+                      &full[s], pol_w);
+        } else {
+          tma_load_2d(wdst, &wmap, kb * kKBlk, rbase + tile * kTileRows, &full[s], pol_w);
+        }
+      };
+      auto issue_x = [&](int s, long long u, const GroupInfo& g_) {
+        const int kb = (int)(u % KB);
+        uint8_t* xdst = smem + s * kStageBytes + kWBytes;
+        if (GROUPED) {
+          for (int t = 0; t < g_.c; ++t) {
+            const int p = g_.p0 + t;
+            const int row = a.pair_row ? a.pair_row[p] : p;
+            tma_load_2d(xdst + t * 128, &xmap, kb * kKBlk, row, &full[s], pol_x);
+          }
+        } else {
+          tma_load_2d(xdst, &xmap, kb * kKBlk, 0, &full[s], pol_x);
+        }
+      };
+      auto group_of = [&](long long u) -> int { return (int)((u / KB) / TILES); };
+      auto xbytes = [&](const GroupInfo& g_) -> uint32_t {
+        return GROUPED ? (uint32_t)(g_.c * 128) : (uint32_t)kXBytes;
+      };
+      const uint32_t wbytes = kWBytes;
+      int i = 0;
+      if (!GROUPED) {
+        // Weights do not depend on the previous kernel: start streaming them
+        // before waiting for it, then fetch the token tiles.
+        const int npre = nunits < STAGES ? nunits : STAGES;
+        gi = load_group<GROUPED>(a, 0);
+        for (; i < npre; ++i) {
+          mbar_arrive_expect_tx(&full[i], wbytes + xbytes(gi));
+          issue_w(i, u0 + i);
+        }
+        griddep_wait();
+        for (int j = 0; j < npre; ++j) issue_x(j, u0 + j, gi);
+      }
+      for (; i < nunits; ++i) {
+        const int s = i % STAGES;
+        if (i >= STAGES) {
+          if (!mbar_wait(&empty[s], ((i / STAGES) + 1) & 1, a.timeout_ns, a.status)) {
+            s_flags[0] = 1;
+            break;
+          }
+        }
+        if (s_flags[0]) break;
+        const long long u = u0 + i;
+        if (GROUPED) {
+          const int g = group_of(u);
+          if (g != gcur) {
+            gcur = g;
+            gi = load_group<GROUPED>(a, g);
+          }
+        }
+        mbar_arrive_expect_tx(&full[s], wbytes + xbytes(gi));
+        issue_w(s, u);
+        issue_x(s, u, gi);
+      }
+      // Drain: wait until every issued copy has landed before the CTA may exit.
+      const int issued = i;
+      for (int s = 0; s < STAGES && s < issued; ++s) {
+        const int uses = (issued - s + STAGES - 1) / STAGES;
+        mbar_wait(&full[s], (uses - 1) & 1, a.timeout_ns, nullptr);
+      }
+    }
+    if (!GROUPED && lane != 0) griddep_wait();
+  } else {
+    // ---------------------------------------------------------------- consumers
+    if (!GROUPED) griddep_wait();
+    const int w = warp - 1;
+    const int ct = threadIdx.x - 32;
+    const int q = lane & 7, rho = lane >> 3;  // CUDA-core path: chunk and row group
+    const int gq = lane >> 2, tq = lane & 3;  // mma path: fragment row and column pair
+
+    float dacc[4][2];
+    float macc[XR / 8][4];
+    long long cur = -1;
+    GroupInfo gi{0, 0, 0};
+    bool use_mma = false;
+
+    auto zero_acc = [&]() {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) dacc[r][0] = dacc[r][1] = 0.f;
+#pragma unroll
+      for (int tg = 0; tg < XR / 8; ++tg)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) macc[tg][j] = 0.f;
+    };
+
+    // Visit every (stage row, token, value) this thread holds for the tile.
+    // The CUDA-core path's values are complete only in lanes with q == 0
+    // after the shuffle reduction.
+    auto reduce_dots = [&]() {
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          float v = dacc[r][t];
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          v += __shfl_xor_sync(0xffffffffu, v, 4);
+          dacc[r][t] = v;
+        }
+    };
+
+    auto finish_tile = [&](long long gt) {
+      const int g = (int)(gt / TILES);
+      const int tile = (int)(gt - (long long)g * TILES);
+      const bool aborted = s_flags[0] != 0;
+      if (!use_mma) reduce_dots();
+      const bool whole = (u0 <= gt * KB) && ((gt + 1) * KB <= u1);
+      float* wsb = a.ws;
+      bool last = whole;
+      long long cf = c, cl = c;
+      if (!whole) {
+        const int slot = (gt == u0 / KB) ? 0 : 1;
+        float* mine = wsb + ((c * 2 + slot) * kTileRows) * XR;
+        // write this CTA's partial tile
+        if (!use_mma) {
+          if (q == 0) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              const int sr = stage_row<PAIRED>(w, rho + 4 * r);
+#pragma unroll
+              for (int t = 0; t < 2; ++t)
+                if (t < gi.c) __stcg(mine + sr * XR + t, dacc[r][t]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int tg = 0; tg < XR / 8; ++tg) {
+            const int t0 = tg * 8 + 2 * tq;
+            const int sr0 = stage_row<PAIRED>(w, gq), sr1 = stage_row<PAIRED>(w, gq + 8);
+            if (t0 < gi.c) {
+              __stcg(mine + sr0 * XR + t0, macc[tg][0]);
+              __stcg(mine + sr1 * XR + t0, macc[tg][2]);
+            }
+            if (t0 + 1 < gi.c) {
+              __stcg(mine + sr0 * XR + t0 + 1, macc[tg][1]);
+              __stcg(mine + sr1 * XR + t0 + 1, macc[tg][3]);
+            }
+          }
+        }
+        named_bar_sync(1, kNCW * 32);
+        cf = cta_of(gt * KB, T, G);
+        cl = cta_of((gt + 1) * KB - 1, T, G);
+        if (ct == 0) {
+          __threadfence();
+          const int old = atomic_add_acq_rel_gpu(&a.ctr[gt], 1);
+          const int is_last = (old == (int)(cl - cf)) ? 1 : 0;
+          if (is_last) a.ctr[gt] = 0;  // every contributor has arrived: reset for the next call
+          s_flags[1] = is_last;
+        }
+        named_bar_sync(1, kNCW * 32);
+        last = s_flags[1] != 0;
+        if (last) __threadfence();
+      }
+      if (last) {
+        auto total = [&](int sr, int t, float own) -> float {
+          if (whole) return own;
+          float v = 0.f;
+          for (long long cc = cf; cc <= cl; ++cc) {
+            const int sl = (gt == cta_start(cc, T, G) / KB) ? 0 : 1;
+            v += __ldcg(wsb + ((cc * 2 + sl) * kTileRows + sr) * XR + t);
+          }
+          return v;
+        };
+        if (!aborted) {
+          if (!use_mma) {
+            if (q == 0) {
+              if (PAIRED) {
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                  const int lr = rho + 4 * r;
+                  const int srg = stage_row<PAIRED>(w, lr), sru = stage_row<PAIRED>(w, lr + 8);
+                  const int i = tile * 64 + 8 * w + lr;
+#pragma unroll
+                  for (int t = 0; t < 2; ++t)
+                    if (t < gi.c && i < a.nout)
+                      store_swiglu(a, gi, t, i, total(srg, t, dacc[r][t]),
+                                   total(sru, t, dacc[r + 2][t]));
+                }
+              } else {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                  const int sr = stage_row<PAIRED>(w, rho + 4 * r);
+                  const int n = tile * kTileRows + sr;
+#pragma unroll
+                  for (int t = 0; t < 2; ++t)
+                    if (t < gi.c && n < a.nout) store_out<EPI, GROUPED>(a, gi, t, n, total(sr, t, dacc[r][t]));
+                }
+              }
+            }
+          } else {
+#pragma unroll
+            for (int tg = 0; tg < XR / 8; ++tg) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int t = tg * 8 + 2 * tq + h;
+                if (t >= gi.c) continue;
+                const int sr0 = stage_row<PAIRED>(w, gq), sr1 = stage_row<PAIRED>(w, gq + 8);
+                const float v0 = total(sr0, t, macc[tg][h]);
+                const float v1 = total(sr1, t, macc[tg][2 + h]);
+                if (PAIRED) {
+                  const int i = tile * 64 + 8 * w + gq;
+                  if (i < a.nout) store_swiglu(a, gi, t, i, v0, v1);
+                } else {
+                  const int n0 = tile * kTileRows + sr0, n1 = tile * kTileRows + sr1;
+                  if (n0 < a.nout) store_out<EPI, GROUPED>(a, gi, t, n0, v0);
+                  if (n1 < a.nout) store_out<EPI, GROUPED>(a, gi, t, n1, v1);
+                }
+              }
+            }
+          }
+        }
+        if (ROUTER) {
+          // count finished tiles; the CTA finishing the last one routes
+          named_bar_sync(1, kNCW * 32);
+          if (ct == 0) {
+            __threadfence();
+            const int old = atomic_add_acq_rel_gpu(a.done, 1);
+            const int fin = (old == a.total_tiles_dense - 1) ? 1 : 0;
+            if (fin) *a.done = 0;
+            s_flags[2] = fin;
+          }
+          named_bar_sync(1, kNCW * 32);
+          if (s_flags[2]) {
+            __threadfence();
+            route_tail<kNCW * 32>(a.route, ct, scratch);
+          }
+        }
+      }
+      named_bar_sync(1, kNCW * 32);  // partial slots and flags may be reused next tile
+    };
+
+    const uint8_t* xs_base = nullptr;
+    for (int i = 0; i < nunits; ++i) {
+      const long long u = u0 + i;
+      const long long gt = u / KB;
+      if (gt != cur) {
+        if (cur >= 0) finish_tile(cur);
+        cur = gt;
+        zero_acc();
+        gi = load_group<GROUPED>(a, (int)(gt / TILES));
+        use_mma = gi.c >= a.mma_min_tokens;
+      }
+      const int s = i % STAGES;
+      if (!s_flags[0]) {
+        if (!mbar_wait(&full[s], (i / STAGES) & 1, a.timeout_ns, a.status)) s_flags[0] = 1;
+      }
+      const uint8_t* wbase = smem + s * kStageBytes;
+      xs_base = wbase + kWBytes;
+      if (!use_mma) {
+        // CUDA-core path: lane reads 16-byte chunk q of rows rho + 4r
+        float xv[2][8];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (t < gi.c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(xs_base + t * 128 + ((q ^ (t & 7)) << 4));
+            unpack8(v, xv[t]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) xv[t][j] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int sr = stage_row<PAIRED>(w, rho + 4 * r);
+          const uint4 wv = *reinterpret_cast<const uint4*>(wbase + sr * 128 + ((q ^ (sr & 7)) << 4));
+          dacc[r][0] = dot8(wv, xv[0], dacc[r][0]);
+          if (gi.c > 1) dacc[r][1] = dot8(wv, xv[1], dacc[r][1]);
+        }
+      } else {
+        const int ntg = (gi.c + 7) >> 3;
+        const uint32_t wb = smem_u32(wbase), xb = smem_u32(xs_base);
+        const int mi = lane >> 3, r8 = lane & 7;
+        const int a_sr = stage_row<PAIRED>(w, (mi & 1) * 8 + r8);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          uint32_t af[4];
+          const int ach = kk * 2 + (mi >> 1);
+          ldmatrix_x4(af[0], af[1], af[2], af[3], wb + a_sr * 128 + ((ach ^ r8) << 4));
+#pragma unroll
+          for (int tg = 0; tg < XR / 8; ++tg) {
+            if (tg < ntg) {
+              const int t = tg * 8 + r8;
+              const int bch = kk * 2 + (mi & 1);
+              uint32_t b0, b1;
+              ldmatrix_x2(b0, b1, xb + t * 128 + ((bch ^ r8) << 4));
+              mma_bf16_16816(macc[tg], af, b0, b1);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (cur >= 0) finish_tile(cur);
+  }
+  __syncthreads();
+}
+
+}  // namespace dg

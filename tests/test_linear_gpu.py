@@ -1,0 +1,168 @@
+"""GPU parity of the decode projection y = x·Wᵀ against the fp64 oracle.
+
+Every call goes through the C ABI (the ctypes binding). Each test asserts the
+kernel regime the dispatcher chose, so a silent change of path shows.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from _util import assert_within_tol, to_f64
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from moe_decode_gemm_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a GPU"
+
+
+import moe_decode_gemm_gb300 as dg  # noqa: E402
+
+
+def _expect_regime(M):
+    return "smallm" if M <= 2 else ("mma" if M < 16 else "tc")
+
+
+def _gpu_linear(x_bits, W_bits, S=None, res_bits=None):
+    x = wl.bits_to_torch(x_bits)
+    W = wl.bits_to_torch(W_bits)
+    res = None if res_bits is None else wl.bits_to_torch(res_bits)
+    if S is None:
+        y = dg.dec_linear(x, W, residual=res)
+    else:
+        y = dg.dec_linear_splitk(x, W, S)
+    choice = dg.last_choice()
+    assert dg.sync_check() == dg.DEC_OK
+    return y, choice
+
+
+def _check_random(M, N, K, key, cols=None, S=None):
+    x = wl.normal_bf16((M, K), 1.0, *key, "x")
+    W = wl.normal_bf16((N, K), 0.02, *key, "W")
+    y, choice = _gpu_linear(x, W, S=S)
+    if cols is None:
+        ref, A = oracle.linear(x, W)
+        got = to_f64(y)
+    else:
+        ref, A = oracle.linear(x, W[cols])
+        got = to_f64(y)[:, cols]
+    assert_within_tol(got, ref, A, "M=%d N=%d K=%d S=%s" % (M, N, K, S))
+    return y, choice
+
+
+def test_single_projection_m1_4096():
+    # M=1, K=N=4096, x ~N(0,1), W ~N(0,0.02), seed 0
+    _, (regime, _) = _check_random(1, 4096, 4096, ("cfg1", 0))
+    assert regime == "smallm"
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8, 15, 16, 17, 32, 33, 64])
+def test_ragged_shapes_every_regime(M):
+    # N not a multiple of the 128-row tile, K not a multiple of the 64-wide block
+    _, (regime, _) = _check_random(M, 300, 520, ("ragged", M))
+    assert regime == _expect_regime(M) or (regime == "mma" and M >= 16)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 8), (2, 1, 8), (3, 5, 16), (64, 1, 8), (1, 129, 72),
+                                   (16, 127, 4096), (64, 7, 24)])
+def test_degenerate_shapes(M, N, K):
+    _check_random(M, N, K, ("degenerate", M, N, K))
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 8, 16, 64])
+@pytest.mark.parametrize("S", [None, 1, 2, 3, 4, 7, 16])
+def test_integer_inputs_bit_exact(M, S):
+    # integer-valued bf16 inputs: fp32 accumulation is exact, so the only
+    # rounding is the final bf16 one, taken on the exact value on both sides
+    K, N = 1024, 384
+    x = wl.integer_bf16((M, K), -2, 2, "int", M, "x")
+    W = wl.integer_bf16((N, K), -2, 2, "int", M, "W")
+    y, _ = _gpu_linear(x, W, S=S)
+    ref, _ = oracle.linear(x, W)
+    assert np.array_equal(wl.torch_to_bits(y), oracle.f64_to_bf16_bits(ref))
+
+
+@pytest.mark.parametrize("M", [1, 2, 5, 16, 64])
+def test_one_hot_rows_reproduce_x(M):
+    K, N = 2048, 520
+    x = wl.normal_bf16((M, K), 1.0, "onehot", M, "x")
+    W, perm = wl.one_hot_rows(N, K, "onehot", M, "W")
+    y, _ = _gpu_linear(x, W)
+    assert np.array_equal(wl.torch_to_bits(y), x[:, perm])
+
+
+@pytest.mark.parametrize("M", [8, 32, 64])
+def test_wide_k_split_factors(M):
+    # M in {8,32,64}, K=16384, N=2048, forced split factors 2..16 and the
+    # dispatcher's own choice; each run twice must be bit-identical
+    K, N = 16384, 2048
+    cols = np.random.default_rng(M).choice(N, 256, replace=False)
+    x = wl.normal_bf16((M, K), 1.0, "cfg3", M, "x")
+    W = wl.normal_bf16((N, K), 0.02, "cfg3", M, "W")
+    ref, A = oracle.linear(x, W[cols])
+    for S in [None, 2, 4, 8, 12, 16]:
+        y1, (_, s_used) = _gpu_linear(x, W, S=S)
+        y2, _ = _gpu_linear(x, W, S=S)
+        assert torch.equal(y1, y2), "split %s not deterministic" % S
+        if S is not None:
+            assert s_used == S
+        assert_within_tol(to_f64(y1)[:, cols], ref, A, "M=%d S=%s" % (M, S))
+
+
+@pytest.mark.parametrize("N", [2048, 7168, 16384])
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32, 64])
+def test_batch_sweep_k7168(M, N):
+    # K=7168 decode projections at every batch size; the oracle checks a
+    # sample of 384 output columns
+    cols = np.random.default_rng(N + M).choice(N, 384, replace=False)
+    _, (regime, _) = _check_random(M, N, 7168, ("cfg2", M, N), cols=cols)
+    assert regime == _expect_regime(M) or (regime == "mma" and M >= 16)
+
+
+@pytest.mark.parametrize("M", [1, 4, 16, 64])
+def test_residual_epilogue(M):
+    K, N = 1536, 640
+    x = wl.normal_bf16((M, K), 1.0, "res", M, "x")
+    W = wl.normal_bf16((N, K), 0.02, "res", M, "W")
+    r = wl.normal_bf16((M, N), 1.0, "res", M, "r")
+    y, _ = _gpu_linear(x, W, res_bits=r)
+    f, A = oracle.linear(x, W)
+    ref, Aref = oracle.residual(r, f, A)
+    assert_within_tol(to_f64(y), ref, Aref, "residual M=%d" % M)
+
+
+def test_forced_regimes_agree():
+    M, N, K = 2, 512, 1024
+    x = wl.integer_bf16((M, K), -2, 2, "force", "x")
+    W = wl.integer_bf16((N, K), -2, 2, "force", "W")
+    outs = {}
+    for f in ["smallm", "mma"]:
+        os.environ["DEC_FORCE"] = f
+        try:
+            y, (regime, _) = _gpu_linear(x, W)
+        finally:
+            del os.environ["DEC_FORCE"]
+        assert regime == f
+        outs[f] = wl.torch_to_bits(y)
+    assert np.array_equal(outs["smallm"], outs["mma"])
+
+
+def test_output_guard_bands_untouched():
+    # the kernel writes exactly [M,N]: sentinel bytes around y stay intact
+    M, N, K = 3, 200, 256
+    x = wl.bits_to_torch(wl.normal_bf16((M, K), 1.0, "guard", "x"))
+    W = wl.bits_to_torch(wl.normal_bf16((N, K), 0.02, "guard", "W"))
+    pad = 4096
+    buf = torch.full((pad + M * N + pad,), 12345, dtype=torch.int16, device="cuda")
+    y = buf[pad:pad + M * N].view(torch.bfloat16).view(M, N)
+    dg.dec_linear(x, W, y)
+    assert dg.sync_check() == dg.DEC_OK
+    assert torch.all(buf[:pad] == 12345) and torch.all(buf[pad + M * N:] == 12345)

@@ -1,0 +1,160 @@
+"""GPU parity of the MoE decode block against the fp64 oracle.
+
+Router inputs are drawn so that the fp64 router scores of every token have
+adjacent gaps of at least 1e-3 among the k+1 largest: the expert choice is
+then unique and the GPU's top-k indices must equal the oracle's exactly.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from _util import assert_within_tol, gap_rows, to_f64
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from moe_decode_gemm_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a GPU"
+
+
+import moe_decode_gemm_gb300 as dg  # noqa: E402
+
+
+def _small_block(M, H, E, I, k, key, std=0.02, shared=True):
+    Wr = wl.normal_bf16((E, H), 1.0 / math.sqrt(H), *key, "Wr")
+    x, _ = gap_rows(Wr, M, H, k, *key, "x")
+    W13 = np.stack([wl.normal_bf16((2 * I, H), std, *key, "W13", e) for e in range(E)])
+    W2 = np.stack([wl.normal_bf16((H, I), std, *key, "W2", e) for e in range(E)])
+    Ws = (wl.normal_bf16((2 * I, H), std, *key, "Ws13"),
+          wl.normal_bf16((H, I), std, *key, "Ws2")) if shared else None
+    return x, Wr, W13, W2, Ws
+
+
+def _gpu_moe(x, Wr, W13, W2, Ws, k, res=None):
+    t = wl.bits_to_torch
+    M = x.shape[0]
+    idx = torch.full((M, k), -1, dtype=torch.int32, device="cuda")
+    gw = torch.zeros((M, k), dtype=torch.float32, device="cuda")
+    out = dg.moe_decode(t(x), t(Wr), t(W13), t(W2), None if Ws is None else t(Ws[0]),
+                        None if Ws is None else t(Ws[1]), k, topk_idx=idx, topk_w=gw,
+                        residual=None if res is None else t(res))
+    assert dg.sync_check() == dg.DEC_OK
+    return out, idx.cpu().numpy(), gw.cpu().numpy()
+
+
+def _check(x, Wr, W13, W2, Ws, k, what, res=None):
+    I = W13.shape[1] // 2
+    out, idx, gw = _gpu_moe(x, Wr, W13, W2, Ws, k, res=res)
+    r = oracle.moe(x, Wr, lambda e: (W13[e], W2[e]), k, I, shared=Ws)
+    assert np.array_equal(idx, r["idx"]), what + ": top-k indices differ"
+    np.testing.assert_allclose(gw, r["gates"], rtol=2e-5, atol=1e-7, err_msg=what + ": gates")
+    ref, A = r["out"], r["absref"]
+    if res is not None:
+        ref, A = oracle.residual(res, ref, A)
+    assert_within_tol(to_f64(out), ref, A, what)
+    return out
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8, 16, 33, 64])
+@pytest.mark.parametrize("shared", [True, False])
+def test_small_block_against_oracle(M, shared):
+    blk = _small_block(M, 256, 64, 128, 8, ("moe-small", M, shared), shared=shared)
+    _check(*blk, 8, "M=%d shared=%s" % (M, shared))
+
+
+def test_ragged_intermediate_and_hidden():
+    # I not a multiple of 64 and H not a multiple of 128: tiles overhang
+    blk = _small_block(9, 200, 24, 72, 3, ("moe-ragged",))
+    _check(*blk, 3, "ragged")
+
+
+def test_every_token_same_expert_pool():
+    # 64 tokens over 8 experts with k = 8: every expert serves all 64 tokens
+    blk = _small_block(64, 128, 8, 64, 8, ("moe-dense",))
+    _check(*blk, 8, "all experts, all tokens")
+
+
+def test_topk_equals_E_with_zero_router_is_dense_mean():
+    E, H, I, M = 16, 128, 64, 5
+    x, Wr, W13, W2, _ = _small_block(M, H, E, I, 8, ("moe-uniform",), shared=False)
+    Wr0 = np.zeros_like(Wr)
+    out, idx, gw = _gpu_moe(x, Wr0, W13, W2, None, E)
+    assert np.all(idx == np.arange(E))                  # ties: smaller index first
+    np.testing.assert_allclose(gw, 1.0 / E, rtol=1e-6)
+    r = oracle.moe(x, Wr0, lambda e: (W13[e], W2[e]), E, I, shared=None)
+    assert_within_tol(to_f64(out), r["out"], r["absref"], "uniform")
+
+
+def test_single_expert_block():
+    blk = _small_block(7, 192, 1, 64, 1, ("moe-one",))
+    _check(*blk, 1, "E=1")
+
+
+def test_zero_routed_down_projection_leaves_shared_expert():
+    x, Wr, W13, W2, Ws = _small_block(6, 256, 32, 128, 4, ("moe-zero",))
+    _check(x, Wr, W13, np.zeros_like(W2), Ws, 4, "zero W2")
+
+
+def test_residual_combine():
+    x, Wr, W13, W2, Ws = _small_block(12, 256, 48, 128, 6, ("moe-res",))
+    res = wl.normal_bf16((12, 256), 1.0, "moe-res", "r")
+    _check(x, Wr, W13, W2, Ws, 6, "residual", res=res)
+
+
+def test_repeat_calls_bit_identical():
+    x, Wr, W13, W2, Ws = _small_block(33, 256, 64, 128, 8, ("moe-det",))
+    a, _, _ = _gpu_moe(x, Wr, W13, W2, Ws, 8)
+    b, _, _ = _gpu_moe(x, Wr, W13, W2, Ws, 8)
+    assert torch.equal(a, b)
+
+
+# ---------------------------------------------------------------- full size
+H, E, K8, I = wl.HIDDEN, wl.EXPERTS, wl.TOPK, wl.INTER
+
+
+@pytest.fixture(scope="module")
+def full_bank():
+    """Routed experts (33.8 GB) and shared expert on the device, ~N(0, 0.02)."""
+    W13 = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device="cuda")
+    W2 = torch.empty((E, H, I), dtype=torch.bfloat16, device="cuda")
+    for e in range(E):
+        wl.normal_bf16_cuda((2 * I, H), wl.WEIGHT_STD, "bank", 0, "W13", e, out=W13[e])
+        wl.normal_bf16_cuda((H, I), wl.WEIGHT_STD, "bank", 0, "W2", e, out=W2[e])
+    Ws13 = wl.normal_bf16_cuda((2 * I, H), wl.WEIGHT_STD, "bank", 0, "Ws13")
+    Ws2 = wl.normal_bf16_cuda((H, I), wl.WEIGHT_STD, "bank", 0, "Ws2")
+    Wr = wl.normal_bf16((E, H), wl.ROUTER_STD, "bank", 0, "Wr")
+    yield W13, W2, Ws13, Ws2, Wr
+    del W13, W2
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("M", [1, 4, 16, 64])
+def test_full_size_block(full_bank, M):
+    # hidden 7168, 384 experts, top-8, intermediate 2048, shared expert;
+    # indices of every token exact, outputs of sampled tokens within tolerance
+    W13, W2, Ws13, Ws2, Wr_bits = full_bank
+    x_bits, _ = gap_rows(Wr_bits, M, H, K8, "full", M)
+    t = wl.bits_to_torch
+    x, Wr = t(x_bits), t(Wr_bits)
+    idx = torch.empty((M, K8), dtype=torch.int32, device="cuda")
+    gw = torch.empty((M, K8), dtype=torch.float32, device="cuda")
+    out = dg.moe_decode(x, Wr, W13, W2, Ws13, Ws2, K8, topk_idx=idx, topk_w=gw)
+    assert dg.sync_check() == dg.DEC_OK
+    logits, _ = oracle.linear(x_bits, Wr_bits)
+    ridx, rg = oracle.topk(logits, K8)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    np.testing.assert_allclose(gw.cpu().numpy(), rg, rtol=2e-5, atol=1e-7)
+    tokens = sorted(set([0, M - 1, M // 2]))
+    fetch = lambda e: (wl.torch_to_bits(W13[e]), wl.torch_to_bits(W2[e]))
+    r = oracle.moe(x_bits, Wr_bits, fetch, K8, I,
+                   shared=(wl.torch_to_bits(Ws13), wl.torch_to_bits(Ws2)), tokens=tokens)
+    got = to_f64(out)
+    assert_within_tol(got[tokens], r["out"][tokens], r["absref"][tokens], "full M=%d" % M)
