@@ -1,0 +1,460 @@
+"""Benchmark: weight-stream TB/s and µs per call of the decode step on GB300.
+
+Default workload -- the synthetic decode layer stack: 4 layers, each
+  q  = x·Wqᵀ (7168 -> 7168),  kv = x·Wkvᵀ (7168 -> 1024),
+  r  = x + q·Woᵀ (7168 -> 7168, residual fused),
+  x' = r + MoE(r)  (hidden 7168, 384 experts, top-8, SwiGLU intermediate 2048,
+                    one shared expert on a second stream),
+plus an L2 prefetch of the next layer's q weights on a third stream. One step
+runs the stack once at each batch size M in {1, 4, 16, 64}; weights stay
+resident in HBM (about 136 GB: no weight is reused within a step, every
+layer's weights are its own and far exceed L2).
+
+Prints one JSON line (rank 0). Usage:
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload stack|moe|linear]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+H, E, K8, I, KV = wl.HIDDEN, wl.EXPERTS, wl.TOPK, wl.INTER, wl.KV_WIDTH
+BATCHES = (1, 4, 16, 64)
+METRIC = "weight-stream TB/s (% of HBM peak) and µs/call, decode GEMM + MoE, batch 1–64"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ weights
+class Layer:
+    def __init__(self, l, device, torch):
+        g = lambda shape, *key: wl.normal_bf16_cuda(shape, wl.WEIGHT_STD, "stack", l, *key,
+                                                    device=device)
+        self.Wq = g((H, H), "Wq")
+        self.Wkv = g((KV, H), "Wkv")
+        self.Wo = g((H, H), "Wo")
+        self.Wr = wl.normal_bf16_cuda((E, H), wl.ROUTER_STD, "stack", l, "Wr", device=device)
+        self.W13 = g((E, 2 * I, H), "W13")
+        self.W2 = g((E, H, I), "W2")
+        self.Ws13 = g((2 * I, H), "Ws13")
+        self.Ws2 = g((H, I), "Ws2")
+
+
+def linear_bytes(M, N, K):
+    return 2 * N * K + 2 * M * K + 2 * M * N
+
+
+def moe_bytes(M, U):
+    return 2 * E * H + U * (2 * 2 * I * H + 2 * H * I) + 3 * 2 * I * H + 2 * 2 * M * H
+
+
+def layer_bytes(M, U):
+    return (linear_bytes(M, H, H) + linear_bytes(M, KV, H) + linear_bytes(M, H, H) + 2 * M * H
+            + moe_bytes(M, U))
+
+
+def w13_launch_bytes(M, U):
+    # routed gate/up kernel: the chosen experts' W13, the tokens, and h
+    return U * 2 * 2 * I * H + 2 * M * H + 2 * M * K8 * I
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import moe_decode_gemm_gb300 as dg
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    nl = args.layers
+    t0 = time.time()
+    layers = [Layer(l, dev, torch) for l in range(nl)]
+    torch.cuda.synchronize()
+    gen_s = time.time() - t0
+
+    main = torch.cuda.Stream(device=dev)
+    pref = torch.cuda.Stream(device=dev)
+    acts = {}
+    for M in BATCHES:
+        x0 = wl.bits_to_torch(wl.token_rows(M, H, "stack-x", M), device=dev)
+        acts[M] = dict(
+            x0=x0,
+            xs=[torch.empty((M, H), dtype=torch.bfloat16, device=dev) for _ in range(nl + 1)],
+            q=torch.empty((M, H), dtype=torch.bfloat16, device=dev),
+            kv=torch.empty((M, KV), dtype=torch.bfloat16, device=dev),
+            r=torch.empty((M, H), dtype=torch.bfloat16, device=dev),
+            idx=[torch.empty((M, K8), dtype=torch.int32, device=dev) for _ in range(nl)],
+        )
+        acts[M]["xs"][0].copy_(x0)
+        acts[M]["x_host"] = x0.cpu().pin_memory()
+        acts[M]["out_host"] = torch.empty((M, H), dtype=torch.bfloat16).pin_memory()
+    ev_fork = [torch.cuda.Event() for _ in range(nl)]
+
+    def stack(M):
+        a = acts[M]
+        for l, L in enumerate(layers):
+            x = a["xs"][l]
+            dg.dec_linear(x, L.Wq, a["q"], stream=main)
+            dg.dec_linear(x, L.Wkv, a["kv"], stream=main)
+            dg.dec_linear(a["q"], L.Wo, a["r"], stream=main, residual=x)
+            if not args.no_prefetch:
+                nxt = layers[(l + 1) % nl]
+                ev_fork[l].record(main)
+                pref.wait_event(ev_fork[l])
+                dg.l2_prefetch(nxt.Wq, stream=pref)
+            dg.moe_decode(a["r"], L.Wr, L.W13, L.W2, L.Ws13, L.Ws2, K8, out=a["xs"][l + 1],
+                          topk_idx=a["idx"][l], stream=main, residual=a["r"])
+
+    def step():
+        for M in BATCHES:
+            stack(M)
+        if not args.no_prefetch:
+            main.wait_stream(pref)
+
+    def step_e2e():
+        for M in BATCHES:
+            a = acts[M]
+            with torch.cuda.stream(main):
+                a["xs"][0].copy_(a["x_host"], non_blocking=True)
+            stack(M)
+            with torch.cuda.stream(main):
+                a["out_host"].copy_(a["xs"][nl], non_blocking=True)
+        if not args.no_prefetch:
+            main.wait_stream(pref)
+
+    # warm-up (allocates the library's workspace outside the timed region)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert dg.sync_check() == dg.DEC_OK
+
+    # active experts per (M, layer), from the returned indices
+    U = {M: [len(set(acts[M]["idx"][l].cpu().numpy().ravel().tolist())) for l in range(nl)]
+         for M in BATCHES}
+    step_bytes = sum(layer_bytes(M, U[M][l]) for M in BATCHES for l in range(nl))
+    w13_bytes = sum(w13_launch_bytes(M, U[M][l]) for M in BATCHES for l in range(nl))
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    clocks = ClockSampler(local_rank)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    launches0 = dg.launch_count()
+    dg.probe_begin(dg.PROBE_EXPERT_W13, args.steps * len(BATCHES) * nl + 8)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    e0.record(main)
+    for _ in range(args.steps):
+        step()
+    e1.record(main)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    launches = dg.launch_count() - launches0
+    w13_ms, w13_n = dg.probe_end()
+    assert dg.sync_check() == dg.DEC_OK
+    ms = e0.elapsed_time(e1)
+
+    # per-batch breakdown (untimed pass structure, same events)
+    per_m = {}
+    for M in BATCHES:
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(main)
+        for _ in range(3):
+            stack(M)
+        f1.record(main)
+        torch.cuda.synchronize()
+        us_layer = f0.elapsed_time(f1) * 1000.0 / (3 * nl)
+        by = sum(layer_bytes(M, U[M][l]) for l in range(nl)) / nl
+        per_m[M] = {"us_per_layer": round(us_layer, 2), "TBps": round(by / us_layer / 1e6, 3),
+                    "active_experts": U[M], "kernels_per_layer": None}
+    if not args.no_prefetch:
+        main.wait_stream(pref)
+    torch.cuda.synchronize()
+
+    # kernel count per layer: launches of one layer at M=1
+    n0 = dg.launch_count()
+    stack(1)
+    torch.cuda.synchronize()
+    kpl = (dg.launch_count() - n0) / nl
+    for M in BATCHES:
+        per_m[M]["kernels_per_layer"] = kpl
+
+    # end to end: host input copied in, output copied out, every step
+    barrier()
+    torch.cuda.synchronize()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(main)
+    for _ in range(args.steps):
+        step_e2e()
+    g1.record(main)
+    torch.cuda.synchronize()
+    barrier()
+    ms_e2e = g0.elapsed_time(g1)
+
+    # max over ranks
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms, ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ms_e2e = t.tolist()
+
+    peak_gbs, peak_kind = peaks()
+    tbps = world * step_bytes * args.steps / (ms / 1e3) / 1e12
+    tbps_e2e = world * step_bytes * args.steps / (ms_e2e / 1e3) / 1e12
+    expect_n = args.steps * len(BATCHES) * nl
+    w13_ach = (w13_bytes * args.steps) / (w13_ms / 1e3) / 1e9 if w13_n == expect_n else None
+    h2d = sum(2 * M * H for M in BATCHES)
+    line = {
+        "metric": METRIC,
+        "value": round(tbps, 4),
+        "unit": "TB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded random-init bf16 weights of the stated shapes, N(0,1) tokens)",
+        "config": {
+            "workload": "decode layer stack: %d layers x (q/kv/o projections 7168->7168/1024/7168 "
+                        "+ MoE H=7168 E=384 top-8 I=2048 + shared expert), batches %s" %
+                        (nl, list(BATCHES)),
+            "layers": nl, "batches": list(BATCHES), "hidden": H, "experts": E, "topk": K8,
+            "inter": I, "l2": "inputs larger than L2 (each step streams ~%.0f GB of distinct "
+                              "weights)" % (step_bytes / 1e9),
+            "prefetch": not args.no_prefetch, "parallelism": "replicas" if world > 1 else "1 GPU",
+        },
+        "pct_of_peak": round(100.0 * tbps * 1e3 / (peak_gbs * world), 2),
+        "us_per_layer": {str(M): per_m[M]["us_per_layer"] for M in BATCHES},
+        "breakdown": {str(M): per_m[M] for M in BATCHES},
+        "e2e": {"value": round(tbps_e2e, 4), "unit": "TB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": h2d},
+        "gpu_launches": launches,
+        "roofline": {
+            "kernel": "routed-expert gate/up (SwiGLU) weight-streaming kernel",
+            "bound": "hbm",
+            "achieved": round(w13_ach, 1) if w13_ach else None,
+            "peak": peak_gbs,
+            "unit": "GB/s",
+            "frac": round(w13_ach / peak_gbs, 4) if w13_ach else None,
+            "peak_kind": peak_kind,
+            "launches_timed": w13_n,
+            "traffic": None,
+        },
+        "clocks": clk,
+        "generation_s": round(gen_s, 1),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(layers[0], acts, budget_s=args.cpu_seconds)
+    return line
+
+
+# ------------------------------------------------------------------ oracle arms
+def oracle_layer_sample(L, x_bits, fetch=None):
+    """fp64 oracle on one layer at the given tokens; returns algorithmic bytes."""
+    import oracle
+    import torch
+
+    to_bits = wl.torch_to_bits
+    Wq, Wkv, Wo, Wr = (to_bits(t) for t in (L.Wq, L.Wkv, L.Wo, L.Wr))
+    shared = (to_bits(L.Ws13), to_bits(L.Ws2))
+    cache = {}
+
+    def fetch_expert(e):
+        if e not in cache:
+            cache[e] = (to_bits(L.W13[e]), to_bits(L.W2[e]))
+        return cache[e]
+
+    # copy everything the oracle reads before timing it
+    logits, _ = oracle.linear(x_bits, Wr)
+    for e in set(oracle.topk(logits, K8)[0].ravel().tolist()):
+        fetch_expert(e)
+    t0 = time.time()
+    r = oracle.decoder_layer(x_bits, Wq, Wkv, Wo, Wr, fetch_expert, K8, I, shared)
+    dt = time.time() - t0
+    M = x_bits.shape[0]
+    return layer_bytes(M, len(set(r["idx"].ravel().tolist()))), dt, r
+
+
+def cpu_baseline(L, acts, budget_s=12.0):
+    import oracle
+
+    x_bits = wl.torch_to_bits(acts[1]["x0"])
+    total_b, total_t, reps = 0, 0.0, 0
+    while total_t < budget_s or reps == 0:
+        b, dt, _ = oracle_layer_sample(L, x_bits)
+        total_b += b
+        total_t += dt
+        reps += 1
+        if reps >= 50:
+            break
+    return {"value": round(total_b / total_t / 1e12, 6), "unit": "TB/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "fp64 oracle on layer 0 of the stack at batch 1 (q/kv/o projections + "
+                      "MoE block with shared expert), %d repetition(s), %.1f s" % (reps, total_t)}
+
+
+def run_reference(args, rank, world, local_rank):
+    """The fp64 CPU oracle as the reference arm, on a bounded sample per step."""
+    import torch
+
+    import oracle
+
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local_rank)
+        dev = torch.device("cuda", local_rank)
+    else:
+        dev = torch.device("cpu")
+    L = Layer(0, dev, torch) if dev.type == "cuda" else None
+    if L is None:
+        return {"impl": "reference", "unavailable": "the reference arm draws its weights on a GPU"}
+    x_bits = wl.token_rows(1, H, "stack-x", 1)
+    for _ in range(args.warmup):
+        oracle_layer_sample(L, x_bits)
+    tb, tt = 0, 0.0
+    for _ in range(args.steps):
+        b, dt, _ = oracle_layer_sample(L, x_bits)
+        tb += b
+        tt += dt
+    v = tb / tt / 1e12
+    cores = oracle.num_threads()
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tt * 1e3 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "decode layer stack (sample: one layer at batch 1 per step)",
+                   "layers": 1, "batches": [1]},
+        "cpu_baseline": {"value": round(v, 6), "unit": "TB/s", "cores": cores, "kind": "oracle",
+                         "sample": "one decode layer at batch 1 per step, fp64"},
+        "e2e": {"value": round(v, 6), "unit": "TB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=4)
+    ap.add_argument("--no-prefetch", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    if args.impl == "reference":
+        if rank == 0:
+            line = run_reference(args, rank, world, local_rank)
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -122,7 +122,7 @@ int dec_linear_splitk(const void* x, const void* W, void* y, int M, int N, int K
  * tokens chose it. The shared expert runs on a library-owned side stream that
  * waits on `stream` at entry and is joined back before the final combine.
  * The number of active experts never returns to the host.
- * Limits: H % 64 == 0, I % 64 == 0, 1 <= topk <= min(E, 32), E <= 1024.
+ * Limits: H % 8 == 0, I % 8 == 0, 1 <= topk <= min(E, 32), E <= 1024.
  * Errors: DEC_EINVAL, DEC_EUNSUPPORTED, DEC_ECUDA, DEC_ENOMEM.
  */
 int moe_decode(const void* x, const void* Wr, const void* W13, const void* W2,
@@ -132,8 +132,9 @@ int moe_decode(const void* x, const void* Wr, const void* W13, const void* W2,
 
 /*
  * moe_decode_residual -- moe_decode whose combine adds a residual:
- * out = bf16(res + sum_j g_j·o_j + shared). res is [M,H] bf16 and may alias out
- * but not x.
+ * out = bf16(res + sum_j g_j·o_j + shared). res is [M,H] bf16 and may alias x
+ * or out (the residual stream of a decode layer is usually the block's own
+ * input). out may alias x: x is last read before the combine starts.
  */
 int moe_decode_residual(const void* x, const void* Wr, const void* W13, const void* W2,
                         const void* Ws13, const void* Ws2, const void* res, void* out,

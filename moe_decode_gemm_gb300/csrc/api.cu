@@ -260,7 +260,6 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   const void* ptrs[] = {x, Wr, W13, W2, Ws13, Ws2, res, out, topk_idx, topk_w};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return DEC_EINVAL;
-  if (res && res == x) return DEC_EINVAL;
   if (M > 64 || E > 1024 || topk > 32 || topk > E) return DEC_EUNSUPPORTED;
   DevState* s = nullptr;
   int rc = get_dev(&s);

@@ -16,7 +16,7 @@ constexpr int dense_stages() {
 
 template <int XR>
 constexpr int dense_smem() {
-  return 1024 + dense_stages<XR>() * (kWBytes + XR * 128) + 2 * 8 * dense_stages<XR>() + 64;
+  return wstream_smem(XR, dense_stages<XR>(), 0);
 }
 
 template <int XR, int EPI>

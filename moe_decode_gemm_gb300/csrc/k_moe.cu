@@ -18,9 +18,7 @@ constexpr int kMoeStages = 8;
 constexpr int kRouterStages = 6;
 constexpr int kRouteScratch = 36 * 1024;
 
-constexpr int moe_smem(int stages, int extra) {
-  return 1024 + stages * (kWBytes + kMoeXR * 128) + 2 * 8 * stages + 64 + extra;
-}
+constexpr int moe_smem(int stages, int extra) { return wstream_smem(kMoeXR, stages, extra); }
 
 template <typename K>
 static cudaError_t smem_once(K kern, int bytes, bool& done) {

@@ -31,6 +31,14 @@ constexpr int kWBytes = kTileRows * 128;   // 16 KB
 
 enum Epi : int { EPI_BF16 = 0, EPI_BF16_RES = 1, EPI_F32 = 2, EPI_SWIGLU = 3 };
 
+constexpr int kMaxSlots = 512;             // contributor slot table entries in shared memory
+
+// Dynamic shared memory of one wstream_kernel instantiation: 1 KB alignment
+// slack, the stage ring, full/empty barriers, flags, slot table, and `extra`.
+constexpr int wstream_smem(int xr, int stages, int extra) {
+  return 1024 + stages * (kWBytes + xr * 128) + 2 * 8 * stages + 32 + 4 * kMaxSlots + extra;
+}
+
 // Routing tail run by the CTA that completes the router's last logit tile.
 struct RouteArgs {
   int M, E, k;
@@ -282,8 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * kStageBytes);
   uint64_t* empty = full + STAGES;
-  volatile int* s_flags = reinterpret_cast<volatile int*>(empty + STAGES);  // [0]=abort [1]=last
-  uint8_t* scratch = reinterpret_cast<uint8_t*>(const_cast<int*>(s_flags) + 8);
+  volatile int* s_flags = reinterpret_cast<volatile int*>(empty + STAGES);  // [0] abort [1] last [2] routed
+  int* s_slot = const_cast<int*>(s_flags) + 8;                                 // [kMaxSlots]
+  uint8_t* scratch = reinterpret_cast<uint8_t*>(s_slot + kMaxSlots);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -443,47 +452,92 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     };
 
+    // Final values held in registers (the CTA covered the tile's whole k range).
+    auto reg_epilogue = [&](int tile) {
+      if (!use_mma) {
+        if (q != 0) return;
+        if (PAIRED) {
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int i = tile * 64 + 8 * w + rho + 4 * r;
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+              if (t < gi.c && i < a.nout) store_swiglu(a, gi, t, i, dacc[r][t], dacc[r + 2][t]);
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int n = tile * kTileRows + stage_row<PAIRED>(w, rho + 4 * r);
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+              if (t < gi.c && n < a.nout) store_out<EPI, GROUPED>(a, gi, t, n, dacc[r][t]);
+          }
+        }
+        return;
+      }
+      const int sr0 = stage_row<PAIRED>(w, gq), sr1 = stage_row<PAIRED>(w, gq + 8);
+#pragma unroll
+      for (int tg = 0; tg < XR / 8; ++tg) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int t = tg * 8 + 2 * tq + h;
+          if (t >= gi.c) continue;
+          if (PAIRED) {
+            const int i = tile * 64 + 8 * w + gq;
+            if (i < a.nout) store_swiglu(a, gi, t, i, macc[tg][h], macc[tg][2 + h]);
+          } else {
+            const int n0 = tile * kTileRows + sr0, n1 = tile * kTileRows + sr1;
+            if (n0 < a.nout) store_out<EPI, GROUPED>(a, gi, t, n0, macc[tg][h]);
+            if (n1 < a.nout) store_out<EPI, GROUPED>(a, gi, t, n1, macc[tg][2 + h]);
+          }
+        }
+      }
+    };
+
+    // This CTA's share of a tile that other CTAs also contribute to, written
+    // to its workspace slot as [token][128 stage rows] fp32.
+    auto write_partial = [&](float* mine) {
+      if (!use_mma) {
+        if (q != 0) return;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int sr = stage_row<PAIRED>(w, rho + 4 * r);
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            if (t < gi.c) __stcg(mine + t * kTileRows + sr, dacc[r][t]);
+        }
+        return;
+      }
+      const int sr0 = stage_row<PAIRED>(w, gq), sr1 = stage_row<PAIRED>(w, gq + 8);
+#pragma unroll
+      for (int tg = 0; tg < XR / 8; ++tg) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int t = tg * 8 + 2 * tq + h;
+          if (t < gi.c) {
+            __stcg(mine + t * kTileRows + sr0, macc[tg][h]);
+            __stcg(mine + t * kTileRows + sr1, macc[tg][2 + h]);
+          }
+        }
+      }
+    };
+
     auto finish_tile = [&](long long gt) {
       const int g = (int)(gt / TILES);
       const int tile = (int)(gt - (long long)g * TILES);
       const bool aborted = s_flags[0] != 0;
       if (!use_mma) reduce_dots();
       const bool whole = (u0 <= gt * KB) && ((gt + 1) * KB <= u1);
-      float* wsb = a.ws;
       bool last = whole;
-      long long cf = c, cl = c;
-      if (!whole) {
+      if (whole) {
+        if (!aborted) reg_epilogue(tile);
+      } else {
+        constexpr long long kSlotFloats = (long long)kTileRows * XR;
         const int slot = (gt == u0 / KB) ? 0 : 1;
-        float* mine = wsb + ((c * 2 + slot) * kTileRows) * XR;
-        // write this CTA's partial tile
-        if (!use_mma) {
-          if (q == 0) {
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              const int sr = stage_row<PAIRED>(w, rho + 4 * r);
-#pragma unroll
-              for (int t = 0; t < 2; ++t)
-                if (t < gi.c) __stcg(mine + sr * XR + t, dacc[r][t]);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int tg = 0; tg < XR / 8; ++tg) {
-            const int t0 = tg * 8 + 2 * tq;
-            const int sr0 = stage_row<PAIRED>(w, gq), sr1 = stage_row<PAIRED>(w, gq + 8);
-            if (t0 < gi.c) {
-              __stcg(mine + sr0 * XR + t0, macc[tg][0]);
-              __stcg(mine + sr1 * XR + t0, macc[tg][2]);
-            }
-            if (t0 + 1 < gi.c) {
-              __stcg(mine + sr0 * XR + t0 + 1, macc[tg][1]);
-              __stcg(mine + sr1 * XR + t0 + 1, macc[tg][3]);
-            }
-          }
-        }
+        write_partial(a.ws + (c * 2 + slot) * kSlotFloats);
         named_bar_sync(1, kNCW * 32);
-        cf = cta_of(gt * KB, T, G);
-        cl = cta_of((gt + 1) * KB - 1, T, G);
+        const long long cf = cta_of(gt * KB, T, G);
+        const long long cl = cta_of((gt + 1) * KB - 1, T, G);
         if (ct == 0) {
           __threadfence();
           const int old = atomic_add_acq_rel_gpu(&a.ctr[gt], 1);
@@ -493,81 +547,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         named_bar_sync(1, kNCW * 32);
         last = s_flags[1] != 0;
-        if (last) __threadfence();
-      }
-      if (last) {
-        auto total = [&](int sr, int t, float own) -> float {
-          if (whole) return own;
-          float v = 0.f;
-          for (long long cc = cf; cc <= cl; ++cc) {
-            const int sl = (gt == cta_start(cc, T, G) / KB) ? 0 : 1;
-            v += __ldcg(wsb + ((cc * 2 + sl) * kTileRows + sr) * XR + t);
-          }
-          return v;
-        };
-        if (!aborted) {
-          if (!use_mma) {
-            if (q == 0) {
-              if (PAIRED) {
+        if (last) {
+          // The last contributor sums every contributor's slot in CTA order
+          // (so the result does not depend on who arrived last), all consumer
+          // threads together, with the loads of up to 8 contributors in flight.
+          __threadfence();
+          const int nc = (int)(cl - cf + 1);
+          auto slot_of = [&](int j) -> long long {
+            const long long cc = cf + j;
+            return cc * 2 + ((gt == cta_start(cc, T, G) / KB) ? 0 : 1);
+          };
+          for (int j = ct; j < nc && j < kMaxSlots; j += kNCW * 32) s_slot[j] = (int)slot_of(j);
+          named_bar_sync(1, kNCW * 32);
+          if (!aborted) {
+            constexpr int R = PAIRED ? 64 : kTileRows;
+            const int nel = R * gi.c;
+            for (int e = ct; e < nel; e += kNCW * 32) {
+              const int t = e / R, r = e - t * R;
+              const int off = t * kTileRows + r;
+              float vg = 0.f, vu = 0.f;
+              for (int j0 = 0; j0 < nc; j0 += 8) {
+                float pg[8], pu[8];
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                  const int lr = rho + 4 * r;
-                  const int srg = stage_row<PAIRED>(w, lr), sru = stage_row<PAIRED>(w, lr + 8);
-                  const int i = tile * 64 + 8 * w + lr;
-#pragma unroll
-                  for (int t = 0; t < 2; ++t)
-                    if (t < gi.c && i < a.nout)
-                      store_swiglu(a, gi, t, i, total(srg, t, dacc[r][t]),
-                                   total(sru, t, dacc[r + 2][t]));
+                for (int j = 0; j < 8; ++j) {
+                  if (j0 + j < nc) {
+                    const long long sl = (j0 + j < kMaxSlots) ? (long long)s_slot[j0 + j] : slot_of(j0 + j);
+                    const float* base = a.ws + sl * kSlotFloats;
+                    pg[j] = __ldcg(base + off);
+                    if (PAIRED) pu[j] = __ldcg(base + off + 64);
+                  }
                 }
-              } else {
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                  const int sr = stage_row<PAIRED>(w, rho + 4 * r);
-                  const int n = tile * kTileRows + sr;
-#pragma unroll
-                  for (int t = 0; t < 2; ++t)
-                    if (t < gi.c && n < a.nout) store_out<EPI, GROUPED>(a, gi, t, n, total(sr, t, dacc[r][t]));
+                for (int j = 0; j < 8; ++j) {
+                  if (j0 + j < nc) {
+                    vg += pg[j];
+                    if (PAIRED) vu += pu[j];
+                  }
                 }
               }
-            }
-          } else {
-#pragma unroll
-            for (int tg = 0; tg < XR / 8; ++tg) {
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const int t = tg * 8 + 2 * tq + h;
-                if (t >= gi.c) continue;
-                const int sr0 = stage_row<PAIRED>(w, gq), sr1 = stage_row<PAIRED>(w, gq + 8);
-                const float v0 = total(sr0, t, macc[tg][h]);
-                const float v1 = total(sr1, t, macc[tg][2 + h]);
-                if (PAIRED) {
-                  const int i = tile * 64 + 8 * w + gq;
-                  if (i < a.nout) store_swiglu(a, gi, t, i, v0, v1);
-                } else {
-                  const int n0 = tile * kTileRows + sr0, n1 = tile * kTileRows + sr1;
-                  if (n0 < a.nout) store_out<EPI, GROUPED>(a, gi, t, n0, v0);
-                  if (n1 < a.nout) store_out<EPI, GROUPED>(a, gi, t, n1, v1);
-                }
+              if (PAIRED) {
+                const int i = tile * 64 + r;
+                if (i < a.nout) store_swiglu(a, gi, t, i, vg, vu);
+              } else {
+                const int n = tile * kTileRows + r;
+                if (n < a.nout) store_out<EPI, GROUPED>(a, gi, t, n, vg);
               }
             }
           }
         }
-        if (ROUTER) {
-          // count finished tiles; the CTA finishing the last one routes
-          named_bar_sync(1, kNCW * 32);
-          if (ct == 0) {
-            __threadfence();
-            const int old = atomic_add_acq_rel_gpu(a.done, 1);
-            const int fin = (old == a.total_tiles_dense - 1) ? 1 : 0;
-            if (fin) *a.done = 0;
-            s_flags[2] = fin;
-          }
-          named_bar_sync(1, kNCW * 32);
-          if (s_flags[2]) {
-            __threadfence();
-            route_tail<kNCW * 32>(a.route, ct, scratch);
-          }
+      }
+      if (last && ROUTER) {
+        // count finished tiles; the CTA finishing the last one routes
+        named_bar_sync(1, kNCW * 32);
+        if (ct == 0) {
+          __threadfence();
+          const int old = atomic_add_acq_rel_gpu(a.done, 1);
+          const int fin = (old == a.total_tiles_dense - 1) ? 1 : 0;
+          if (fin) *a.done = 0;
+          s_flags[2] = fin;
+        }
+        named_bar_sync(1, kNCW * 32);
+        if (s_flags[2]) {
+          __threadfence();
+          route_tail<kNCW * 32>(a.route, ct, scratch);
         }
       }
       named_bar_sync(1, kNCW * 32);  // partial slots and flags may be reused next tile

@@ -89,8 +89,8 @@ def test_moe_rejects(L, kw, code):
     assert _moe(L, **kw) == code
 
 
-def test_moe_residual_may_not_alias_input(L):
-    rc = L.moe_decode_residual(A, A, A, A, None, None, A, A, 4, 64, 16, 4, 64, None, None, None)
+def test_moe_residual_requires_residual(L):
+    rc = L.moe_decode_residual(A, A, A, A, None, None, None, A, 4, 64, 16, 4, 64, None, None, None)
     assert rc == dg.DEC_EINVAL
 
 

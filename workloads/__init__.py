@@ -85,11 +85,11 @@ def token_rows(M, H, *key, attempts=None) -> np.ndarray:
 
 # ----------------------------------------------------------------- CUDA side
 def normal_bf16_cuda(shape, std, *key, device="cuda", out=None):
-    """std * N(0,1) drawn in float32 on the device, rounded to bf16.
+    """N(0, std) drawn on the device straight into a bf16 tensor.
 
-    Writes into ``out`` (a bf16 tensor of ``shape``) when given. Large tensors
-    are drawn in chunks of rows with one generator so peak temporary memory
-    stays small.
+    torch's normal_ on a bf16 tensor draws in float32, scales and rounds once
+    to bf16, writing 2 bytes per element; it writes into ``out`` (a bf16
+    tensor of ``shape``) when given.
     """
     import torch
 
@@ -97,13 +97,7 @@ def normal_bf16_cuda(shape, std, *key, device="cuda", out=None):
     g.manual_seed(seed_for(*key))
     if out is None:
         out = torch.empty(shape, dtype=torch.bfloat16, device=device)
-    flat = out.view(-1)
-    n = flat.numel()
-    chunk = 1 << 27
-    for s in range(0, n, chunk):
-        e = min(n, s + chunk)
-        z = torch.randn(e - s, generator=g, device=device, dtype=torch.float32)
-        flat[s:e].copy_((z * std).to(torch.bfloat16))
+    out.normal_(0.0, float(std), generator=g)
     return out
 
 
