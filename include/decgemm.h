@@ -92,9 +92,10 @@ int dec_linear_residual(const void* x, const void* W, const void* res, void* y,
 
 /*
  * dec_linear_splitk -- dec_linear with the split factor forced to S
- * (1 <= S <= K/64 rounded up): each output tile's K range is cut into S equal
- * chunks of 64-element blocks, one CTA per (tile, chunk). A test and tuning
- * hook for the split-K regime. [tune-shapes]
+ * (1 <= S <= min(256, ceil(K/128))): the grid has S CTAs per 128-row output
+ * tile and each takes an equal share of the tile's 128-wide K chunks (shares
+ * differ by at most one chunk when S does not divide the chunk count). A test
+ * and tuning hook for the split-K regime. [tune-shapes]
  */
 int dec_linear_splitk(const void* x, const void* W, void* y, int M, int N, int K,
                       int S, void* stream);

@@ -96,9 +96,11 @@ static int get_dev(DevState** out) {
     s.l2 = p.l2CacheSize;
     s.cc_major = p.major;
     s.cc_minor = p.minor;
+    // The shared expert's stream has the lowest priority: the routed path
+    // (router -> experts) is the critical one and must not queue behind it.
     int lo = 0, hi = 0;
     cudaDeviceGetStreamPriorityRange(&lo, &hi);
-    if (cudaStreamCreateWithPriority(&s.side, cudaStreamNonBlocking, hi) != cudaSuccess)
+    if (cudaStreamCreateWithPriority(&s.side, cudaStreamNonBlocking, lo) != cudaSuccess)
       return DEC_ECUDA;
     if (cudaEventCreateWithFlags(&s.ev_fork, cudaEventDisableTiming) != cudaSuccess) return DEC_ECUDA;
     if (cudaEventCreateWithFlags(&s.ev_join, cudaEventDisableTiming) != cudaSuccess) return DEC_ECUDA;
@@ -180,15 +182,16 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
   if (M < 1 || N < 1 || K < 8 || (K % 8) != 0) return DEC_EINVAL;
   if (!aligned16(x) || !aligned16(W) || !aligned16(y) || (res && !aligned16(res))) return DEC_EINVAL;
   if (M > 64) return DEC_EUNSUPPORTED;
-  const int KB = (K + 63) / 64;
-  if (S != 0 && (S < 1 || S > KB)) return DEC_EINVAL;
+  const int KB = (K + 127) / 128;  // 128-wide k chunks (one pipeline stage each)
+  if (S != 0 && (S < 1 || S > KB || S > 256)) return DEC_EINVAL;
   DevState* s = nullptr;
   int rc = get_dev(&s);
   if (rc) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  int regime = regime_for(M);
-  if (regime == DEC_REGIME_TC) regime = DEC_REGIME_MMA;  // tcgen05 path not built yet
-  const int xr = regime == DEC_REGIME_SMALLM ? 8 : (M <= 16 ? 16 : 64);
+  const int regime = regime_for(M);
+  // token rows per stage of the CUDA-core / mma.sync kernel; the tcgen05
+  // kernel's partial tiles always hold 64 token columns
+  const int xr = regime == DEC_REGIME_TC ? 64 : regime == DEC_REGIME_SMALLM ? 8 : (M <= 16 ? 16 : 64);
   const long long tiles = (N + 127) / 128;
   const long long T = tiles * KB;
   long long grid = S ? tiles * S : (T < s->sms ? T : s->sms);
@@ -201,6 +204,9 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
   t_last_choice = regime | ((int)seff << 8);
   t_last_grid = (int)grid;
   ProbeScope probe(2, st);
+  if (regime == DEC_REGIME_TC)
+    return counted(launch_dense_tc(cx, res != nullptr, x, W, res, y, M, N, K, (int)grid,
+                                   (float*)s->ws_main.p, (int*)s->ctr_main.p));
   return counted(launch_dense(cx, xr, regime != DEC_REGIME_SMALLM, res != nullptr, x, W, res, y,
                               M, N, K, (int)grid,
                               (float*)s->ws_main.p, (int*)s->ctr_main.p));
@@ -286,7 +292,9 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
     if (cudaStreamWaitEvent(s->side, s->ev_fork, 0) != cudaSuccess) return DEC_ECUDA;
     Ctx sx = make_ctx(s, s->side);
     sx.pdl = false;
-    const int sgrid = s->sms;
+    // A quarter of the SMs: the shared expert is a small share of the block's
+    // bytes and must leave room for the router and the routed experts.
+    const int sgrid = s->sms / 4 > 0 ? s->sms / 4 : 1;
     if ((rc = counted(launch_shared_w13(sx, x, Ws13, M, H, I, s->mb, sgrid, (float*)s->ws_side.p,
                                         (int*)s->ctr_side.p))))
       return rc;

@@ -56,14 +56,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete. Gives up after
-// timeout_ns of %globaltimer: sets the status word and returns false.
+// about timeout_ns (counted in SM clock cycles at 2 GHz, so a slower clock
+// only lengthens the bound): sets the status word and returns false. The
+// clock is read only every 64 polls, so a wait that succeeds costs nothing
+// extra.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long timeout_ns,
                                           int* status) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
+  const long long t0 = clock64();
+  const long long limit = timeout_ns * 2;
+  for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((long long)(globaltimer_ns() - t0) > timeout_ns) {
+    if ((n & 63u) == 0 && clock64() - t0 > limit) {
       if (status) atomicOr(status, kStatusTimeout);
       return false;
     }
@@ -95,6 +99,20 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::"
       "cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// TMA gather: four rows r0..r3 (any order, repeats allowed) of 64 columns
+// starting at column c0, written as four consecutive 128-byte rows at dst.
+// The tensor map's box must be 64 columns x 1 row.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, int c0, int r0,
+                                            int r1, int r2, int r3, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
 

@@ -11,7 +11,7 @@ namespace dg {
 
 template <int XR>
 constexpr int dense_stages() {
-  return XR == 8 ? 12 : XR == 16 ? 11 : 8;
+  return XR == 8 ? 6 : XR == 16 ? 6 : 4;
 }
 
 template <int XR>
@@ -37,7 +37,7 @@ static cudaError_t run_dense(const Ctx& cx, bool mma, const void* x, const void*
   if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)K, XR, false)) return cudaErrorInvalidValue;
   StreamArgs a = {};
   a.K = K;
-  a.KB = (K + kKBlk - 1) / kKBlk;
+  a.KB = (K + kKChunk - 1) / kKChunk;
   a.TILES = (N + kTileRows - 1) / kTileRows;
   a.nout = N;
   a.M = M;

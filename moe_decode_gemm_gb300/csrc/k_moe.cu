@@ -14,8 +14,8 @@
 namespace dg {
 
 constexpr int kMoeXR = 64;
-constexpr int kMoeStages = 8;
-constexpr int kRouterStages = 6;
+constexpr int kMoeStages = 4;
+constexpr int kRouterStages = 3;
 constexpr int kRouteScratch = 36 * 1024;
 
 constexpr int moe_smem(int stages, int extra) { return wstream_smem(kMoeXR, stages, extra); }
@@ -51,7 +51,7 @@ cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, i
   if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)H, kMoeXR, false)) return cudaErrorInvalidValue;
   StreamArgs a = base_args(cx, ws, ctr);
   a.K = H;
-  a.KB = (H + kKBlk - 1) / kKBlk;
+  a.KB = (H + kKChunk - 1) / kKChunk;
   a.TILES = (E + kTileRows - 1) / kTileRows;
   a.nout = E;
   a.M = M;
@@ -73,8 +73,12 @@ cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, i
   a.route.gate = b.gate;
   a.route.done = b.done;
   a.route.total_tiles = a.TILES;
+  // The router streams only E*H bf16 (5.5 MB for 384 x 7168) and is latency
+  // bound: a third of the SMs keeps the number of CTAs per output tile, and so
+  // the split-K fixup, small.
   const long long T = (long long)a.TILES * a.KB;
-  const int grid = (int)(T < cx.sms ? T : cx.sms);
+  const int cap = cx.sms / 3 > 0 ? cx.sms / 3 : 1;
+  const int grid = (int)(T < cap ? T : cap);
   return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
 }
 
@@ -90,7 +94,7 @@ cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, in
   if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)H, 1, false)) return cudaErrorInvalidValue;
   StreamArgs a = base_args(cx, ws, ctr);
   a.K = H;
-  a.KB = (H + kKBlk - 1) / kKBlk;
+  a.KB = (H + kKChunk - 1) / kKChunk;
   a.TILES = (I + 63) / 64;
   a.nout = I;
   a.M = M;
@@ -117,7 +121,7 @@ cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E
   if (!make_tmap(&xmap, b.h, (uint64_t)M * k, (uint64_t)I, 1, false)) return cudaErrorInvalidValue;
   StreamArgs a = base_args(cx, ws, ctr);
   a.K = I;
-  a.KB = (I + kKBlk - 1) / kKBlk;
+  a.KB = (I + kKChunk - 1) / kKChunk;
   a.TILES = (H + kTileRows - 1) / kTileRows;
   a.nout = H;
   a.M = M;
@@ -143,7 +147,7 @@ cudaError_t launch_shared_w13(const Ctx& cx, const void* x, const void* Ws13, in
   if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)H, kMoeXR, false)) return cudaErrorInvalidValue;
   StreamArgs a = base_args(cx, ws, ctr);
   a.K = H;
-  a.KB = (H + kKBlk - 1) / kKBlk;
+  a.KB = (H + kKChunk - 1) / kKChunk;
   a.TILES = (I + 63) / 64;
   a.nout = I;
   a.M = M;
@@ -167,7 +171,7 @@ cudaError_t launch_shared_w2(const Ctx& cx, const void* Ws2, int M, int H, int I
   if (!make_tmap(&xmap, b.hs, (uint64_t)M, (uint64_t)I, kMoeXR, false)) return cudaErrorInvalidValue;
   StreamArgs a = base_args(cx, ws, ctr);
   a.K = I;
-  a.KB = (I + kKBlk - 1) / kKBlk;
+  a.KB = (I + kKChunk - 1) / kKChunk;
   a.TILES = (H + kTileRows - 1) / kTileRows;
   a.nout = H;
   a.M = M;

@@ -1,0 +1,324 @@
+// k_tc.cu -- decode projection y = x·Wᵀ on the tcgen05 tensor cores, for
+// 16 <= M <= 64 tokens, where the projection is a real dense contraction
+// (up to 64 flops per weight byte).
+//
+// Swap-AB: the weight tile is the MMA's A operand (128 rows x 64 k, K-major,
+// 128B swizzle, straight from TMA) and the token tile its B operand (N = M
+// rounded up to 16). The 128 x N fp32 accumulator lives in tensor memory,
+// double-buffered so the epilogue of one output tile overlaps the MMAs of
+// the next. Work is split stream-K exactly as in the CUDA-core/mma.sync
+// kernel: one contiguous range of (tile, 128-wide k chunk) units per CTA,
+// tiles shared by several CTAs finished by the last arriver in CTA order.
+//
+// Warp roles: warp 0 issues TMA, warp 1 allocates tensor memory and issues
+// the MMAs (one thread), warps 2-5 drain the accumulator (each warp owns the
+// 32 tensor-memory lanes of its quarter).
+//
+// "vLLM 如何用智能体辅助优化 Kimi K3 解码性能", Part 1 §1 "针对工作负载调优形状"
+// (split-K projections at larger batch).
+#include <utility>
+
+#include "launch.h"
+#include "launch_util.cuh"
+#include "tc_common.cuh"
+#include "wstream.cuh"
+
+namespace dg {
+
+constexpr int kTcStages = 4;
+constexpr int kTcXRows = 64;
+constexpr int kTcXSub = kTcXRows * 128;                   // 8 KB per box column
+constexpr int kTcStageBytes = kWBytes + kKSub * kTcXSub;  // 48 KB
+constexpr int kTcThreads = 192;
+constexpr int kTcEpi = 128;
+constexpr int kTmemCols = 128;  // two 64-column accumulators
+
+constexpr int tc_smem() {
+  return 1024 + kTcStages * kTcStageBytes + 8 * (2 * kTcStages + 5) + 64 + 4 * kMaxSlots;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_linear_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
+                     const StreamArgs a, const int NP, const uint32_t idesc) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTcStages * kTcStageBytes);
+  uint64_t* empty = full + kTcStages;
+  uint64_t* tfull = empty + kTcStages;   // [2] accumulator ready
+  uint64_t* tempty = tfull + 2;          // [2] accumulator drained
+  uint64_t* mma_done = tempty + 2;       // [1]
+  volatile int* s_flags = reinterpret_cast<volatile int*>(mma_done + 1);  // [0] abort [1] last
+  uint32_t* s_taddr = reinterpret_cast<uint32_t*>(const_cast<int*>(s_flags) + 8);
+  int* s_slot = reinterpret_cast<int*>(s_taddr + 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], kTcEpi / 32);
+    }
+    mbar_init(mma_done, 1);
+    s_flags[0] = 0;
+    s_flags[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(s_taddr, kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&wmap);
+    prefetch_tmap(&xmap);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t taddr = *s_taddr;
+  griddep_launch_dependents();
+
+  const int KB = a.KB, TILES = a.TILES;
+  const long long T = (long long)TILES * KB;
+  const long long c = blockIdx.x;
+  const long long G = (long long)gridDim.x < T ? (long long)gridDim.x : T;
+  const long long u0 = c < G ? cta_start(c, T, G) : 0;
+  const long long u1 = c < G ? cta_start(c + 1, T, G) : 0;
+  const int nunits = (int)(u1 - u0);
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      const uint32_t bytes = kWBytes + kKSub * NP * 128;
+      auto issue_w = [&](int s, long long u) {
+        const long long gt = u / KB;
+        const int kc = (int)(u - gt * KB);
+#pragma unroll
+        for (int sb = 0; sb < kKSub; ++sb)
+          tma_load_2d(smem + s * kTcStageBytes + sb * kWSub, &wmap, (kc * kKSub + sb) * kKBlk,
+                      (int)gt * kTileRows, &full[s], pol_w);
+      };
+      auto issue_x = [&](int s, long long u) {
+        const int kc = (int)(u % KB);
+#pragma unroll
+        for (int sb = 0; sb < kKSub; ++sb)
+          tma_load_2d(smem + s * kTcStageBytes + kWBytes + sb * kTcXSub, &xmap,
+                      (kc * kKSub + sb) * kKBlk, 0, &full[s], pol_x);
+      };
+      // weights first (independent of the previous kernel), then tokens
+      const int npre = nunits < kTcStages ? nunits : kTcStages;
+      int i = 0;
+      for (; i < npre; ++i) {
+        mbar_arrive_expect_tx(&full[i], bytes);
+        issue_w(i, u0 + i);
+      }
+      griddep_wait();
+      for (int j = 0; j < npre; ++j) issue_x(j, u0 + j);
+      for (; i < nunits; ++i) {
+        const int s = i % kTcStages;
+        if (!mbar_wait(&empty[s], ((i / kTcStages) + 1) & 1, a.timeout_ns, a.status)) {
+          s_flags[0] = 1;
+          break;
+        }
+        if (s_flags[0]) break;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        issue_w(s, u0 + i);
+        issue_x(s, u0 + i);
+      }
+      const int issued = i;
+      for (int s = 0; s < kTcStages && s < issued; ++s) {
+        const int uses = (issued - s + kTcStages - 1) / kTcStages;
+        mbar_wait(&full[s], (uses - 1) & 1, a.timeout_ns, nullptr);
+      }
+    } else {
+      griddep_wait();
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA
+    griddep_wait();
+    if (lane == 0) {
+      long long cur = -1;
+      int jt = -1;
+      for (int i = 0; i < nunits; ++i) {
+        const long long u = u0 + i;
+        const long long gt = u / KB;
+        const bool first = gt != cur;
+        if (first) {
+          cur = gt;
+          ++jt;
+          if (jt >= 2 && !s_flags[0]) {
+            if (!mbar_wait(&tempty[jt & 1], ((jt >> 1) - 1) & 1, a.timeout_ns, a.status))
+              s_flags[0] = 1;
+          }
+          tc_fence_after();
+        }
+        const int s = i % kTcStages;
+        if (!s_flags[0]) {
+          if (!mbar_wait(&full[s], (i / kTcStages) & 1, a.timeout_ns, a.status)) s_flags[0] = 1;
+        }
+        tc_fence_after();
+        const uint32_t d = taddr + (uint32_t)((jt & 1) * 64);
+        if (!s_flags[0]) {
+          const uint32_t wb = smem_u32(smem + s * kTcStageBytes);
+          const uint32_t xb = wb + kWBytes;
+#pragma unroll
+          for (int sb = 0; sb < kKSub; ++sb)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = umma_desc_sw128(wb + sb * kWSub + kk * 32);
+              const uint64_t bd = umma_desc_sw128(xb + sb * kTcXSub + kk * 32);
+              umma_bf16(d, ad, bd, idesc, (first && sb == 0 && kk == 0) ? 0u : 1u);
+            }
+        }
+        umma_commit(&empty[s]);
+        if (i == nunits - 1 || ((u + 1) % KB) == 0) umma_commit(&tfull[jt & 1]);
+      }
+      umma_commit(mma_done);
+      mbar_wait(mma_done, 0, a.timeout_ns, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    griddep_wait();
+    const int et = threadIdx.x - 64;         // 0..127
+    const int quarter = warp & 3;            // TMEM lanes this warp may access
+    const int r = quarter * 32 + lane;       // tile row = TMEM lane
+    const GroupInfo gi{0, 0, a.M};
+    if (nunits > 0) {
+      const long long gfirst = u0 / KB, glast = (u1 - 1) / KB;
+      int jt = -1;
+      for (long long gt = gfirst; gt <= glast; ++gt) {
+        ++jt;
+        const int buf = jt & 1;
+        if (!s_flags[0]) {
+          if (!mbar_wait(&tfull[buf], (jt >> 1) & 1, a.timeout_ns, a.status)) s_flags[0] = 1;
+        }
+        tc_fence_after();
+        float v[kTcXRows];
+#pragma unroll
+        for (int cc = 0; cc < kTcXRows / 16; ++cc)
+          if (cc * 16 < NP)
+            tmem_ld16_sync(taddr + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * 64 + cc * 16),
+                           v + cc * 16);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+        const bool aborted = s_flags[0] != 0;
+        const int tile = (int)gt;
+        const int n = tile * kTileRows + r;
+        const bool whole = (u0 <= gt * KB) && ((gt + 1) * KB <= u1);
+        if (whole) {
+          if (!aborted && n < a.nout) {
+#pragma unroll
+            for (int t = 0; t < kTcXRows; ++t)
+              if (t < gi.c) store_out<EPI, false>(a, gi, t, n, v[t]);
+          }
+        } else {
+          constexpr long long kSlotFloats = (long long)kTileRows * kTcXRows;
+          const int slot = (gt == u0 / KB) ? 0 : 1;
+          float* mine = a.ws + (c * 2 + slot) * kSlotFloats;
+#pragma unroll
+          for (int t = 0; t < kTcXRows; ++t)
+            if (t < gi.c) __stcg(mine + t * kTileRows + r, v[t]);
+          named_bar_sync(1, kTcEpi);
+          const long long cf = cta_of(gt * KB, T, G);
+          const long long cl = cta_of((gt + 1) * KB - 1, T, G);
+          if (et == 0) {
+            __threadfence();
+            const int old = atomic_add_acq_rel_gpu(&a.ctr[gt], 1);
+            const int is_last = (old == (int)(cl - cf)) ? 1 : 0;
+            if (is_last) a.ctr[gt] = 0;
+            s_flags[1] = is_last;
+          }
+          named_bar_sync(1, kTcEpi);
+          if (s_flags[1]) {
+            __threadfence();
+            const int nc = (int)(cl - cf + 1);
+            auto slot_of = [&](int j) -> long long {
+              const long long cc = cf + j;
+              return cc * 2 + ((gt == cta_start(cc, T, G) / KB) ? 0 : 1);
+            };
+            for (int j = et; j < nc && j < kMaxSlots; j += kTcEpi) s_slot[j] = (int)slot_of(j);
+            named_bar_sync(1, kTcEpi);
+            if (!aborted && n < a.nout) {
+              for (int t0 = 0; t0 < gi.c; t0 += 8) {
+                float acc[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+                for (int j = 0; j < nc; ++j) {
+                  const long long sl = j < kMaxSlots ? (long long)s_slot[j] : slot_of(j);
+                  const float* base = a.ws + sl * kSlotFloats + r;
+                  float pv[8];
+#pragma unroll
+                  for (int q = 0; q < 8; ++q)
+                    pv[q] = (t0 + q < gi.c) ? __ldcg(base + (t0 + q) * kTileRows) : 0.f;
+#pragma unroll
+                  for (int q = 0; q < 8; ++q) acc[q] += pv[q];
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                  if (t0 + q < gi.c) store_out<EPI, false>(a, gi, t0 + q, n, acc[q]);
+              }
+            }
+          }
+          named_bar_sync(1, kTcEpi);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(taddr, kTmemCols);
+  }
+}
+
+template <int EPI>
+static cudaError_t run_tc(const Ctx& cx, const void* x, const void* W, const void* res, void* y,
+                          int M, int N, int K, int grid, float* ws, int* ctr) {
+  constexpr int SMEM = tc_smem();
+  static_assert(SMEM <= kMaxDynSmem, "shared memory");
+  auto kern = tc_linear_kernel<EPI>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = allow_smem(kern, SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int NP = (M + 15) / 16 * 16;
+  CUtensorMap wmap, xmap;
+  if (!make_tmap(&wmap, W, (uint64_t)N, (uint64_t)K, kTileRows, true)) return cudaErrorInvalidValue;
+  if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)K, (uint32_t)NP, false)) return cudaErrorInvalidValue;
+  StreamArgs a = {};
+  a.K = K;
+  a.KB = (K + kKChunk - 1) / kKChunk;
+  a.TILES = (N + kTileRows - 1) / kTileRows;
+  a.nout = N;
+  a.M = M;
+  a.out = y;
+  a.ldo = N;
+  a.res = reinterpret_cast<const uint16_t*>(res);
+  a.ws = ws;
+  a.ctr = ctr;
+  a.status = cx.status;
+  a.timeout_ns = cx.timeout_ns;
+  return launch_k(kern, dim3(grid), dim3(kTcThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a, NP,
+                  umma_idesc_bf16(128, NP));
+}
+
+cudaError_t launch_dense_tc(const Ctx& cx, bool residual, const void* x, const void* W,
+                            const void* res, void* y, int M, int N, int K, int grid, float* ws,
+                            int* ctr) {
+  if (M < 16 || M > kTcXRows) return cudaErrorInvalidValue;
+  return residual ? run_tc<EPI_BF16_RES>(cx, x, W, res, y, M, N, K, grid, ws, ctr)
+                  : run_tc<EPI_BF16>(cx, x, W, res, y, M, N, K, grid, ws, ctr);
+}
+
+}  // namespace dg

@@ -26,8 +26,11 @@ namespace dg {
 constexpr int kNCW = 8;                    // consumer warps
 constexpr int kThreads = (kNCW + 1) * 32;  // + one producer warp
 constexpr int kTileRows = 128;             // weight rows per stage
-constexpr int kKBlk = 64;                  // k elements per stage (128 bytes)
-constexpr int kWBytes = kTileRows * 128;   // 16 KB
+constexpr int kKBlk = 64;                  // k elements per TMA box (128 bytes, one swizzle span)
+constexpr int kKSub = 2;                   // boxes along k per stage
+constexpr int kKChunk = kKBlk * kKSub;     // k elements per stage (one work unit)
+constexpr int kWSub = kTileRows * 128;     // 16 KB of weights per box column
+constexpr int kWBytes = kWSub * kKSub;     // 32 KB of weights per stage
 
 enum Epi : int { EPI_BF16 = 0, EPI_BF16_RES = 1, EPI_F32 = 2, EPI_SWIGLU = 3 };
 
@@ -36,7 +39,8 @@ constexpr int kMaxSlots = 512;             // contributor slot table entries in 
 // Dynamic shared memory of one wstream_kernel instantiation: 1 KB alignment
 // slack, the stage ring, full/empty barriers, flags, slot table, and `extra`.
 constexpr int wstream_smem(int xr, int stages, int extra) {
-  return 1024 + stages * (kWBytes + xr * 128) + 2 * 8 * stages + 32 + 4 * kMaxSlots + extra;
+  return 1024 + stages * (kWBytes + kKSub * xr * 128) + 2 * 8 * stages + 32 + 4 * kMaxSlots +
+         4 * xr + extra;
 }
 
 // Routing tail run by the CTA that completes the router's last logit tile.
@@ -283,7 +287,8 @@ template <int XR, int STAGES, int EPI, bool PAIRED, bool GROUPED, bool ROUTER>
 __global__ void __launch_bounds__(kThreads, 1)
     wstream_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const StreamArgs a) {
-  constexpr int kXBytes = XR * 128;
+  constexpr int kXSub = XR * 128;              // token rows of one box column
+  constexpr int kXBytes = kXSub * kKSub;
   constexpr int kStageBytes = kWBytes + kXBytes;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -292,7 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + STAGES;
   volatile int* s_flags = reinterpret_cast<volatile int*>(empty + STAGES);  // [0] abort [1] last [2] routed
   int* s_slot = const_cast<int*>(s_flags) + 8;                                 // [kMaxSlots]
-  uint8_t* scratch = reinterpret_cast<uint8_t*>(s_slot + kMaxSlots);
+  int* s_rows = s_slot + kMaxSlots;                                            // [XR] token rows
+  uint8_t* scratch = reinterpret_cast<uint8_t*>(s_rows + XR);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -340,35 +346,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       GroupInfo gi{0, 0, 0};
       auto issue_w = [&](int s, long long u) {
         const long long gt = u / KB;
-        const int kb = (int)(u - gt * KB);
-        const int g = (int)(gt / TILES), tile = (int)(gt - (long long)g * TILES);
+        const int kc = (int)(u - gt * KB);
+        const int tile = (int)(gt % TILES);
         uint8_t* wdst = smem + s * kStageBytes;
-        const int e = GROUPED ? a.grp_exp[g] : 0;
-        const int rbase = e * a.w_group_rows;
-        if (PAIRED) {
-          tma_load_2d(wdst, &wmap, kb * kKBlk, rbase + tile * 64, &full[s], pol_w);
-          tma_load_2d(wdst + 64 * 128, &wmap, kb * kKBlk, rbase + a.w_up_offset + tile * 64,
-                      &full[s], pol_w);
-        } else {
-          tma_load_2d(wdst, &wmap, kb * kKBlk, rbase + tile * kTileRows, &full[s], pol_w);
+        const int rbase = gi.e * a.w_group_rows;
+#pragma unroll
+        for (int sb = 0; sb < kKSub; ++sb) {
+          const int k0 = (kc * kKSub + sb) * kKBlk;
+          uint8_t* d = wdst + sb * kWSub;
+          if (PAIRED) {
+            tma_load_2d(d, &wmap, k0, rbase + tile * 64, &full[s], pol_w);
+            tma_load_2d(d + 64 * 128, &wmap, k0, rbase + a.w_up_offset + tile * 64, &full[s],
+                        pol_w);
+          } else {
+            tma_load_2d(d, &wmap, k0, rbase + tile * kTileRows, &full[s], pol_w);
+          }
         }
       };
       auto issue_x = [&](int s, long long u, const GroupInfo& g_) {
-        const int kb = (int)(u % KB);
+        const int kc = (int)(u % KB);
         uint8_t* xdst = smem + s * kStageBytes + kWBytes;
-        if (GROUPED) {
-          for (int t = 0; t < g_.c; ++t) {
-            const int p = g_.p0 + t;
-            const int row = a.pair_row ? a.pair_row[p] : p;
-            tma_load_2d(xdst + t * 128, &xmap, kb * kKBlk, row, &full[s], pol_x);
+#pragma unroll
+        for (int sb = 0; sb < kKSub; ++sb) {
+          const int k0 = (kc * kKSub + sb) * kKBlk;
+          uint8_t* d = xdst + sb * kXSub;
+          if (GROUPED) {
+            // the group's token rows, four per gather (the last gather repeats
+            // its first row into rows the consumers never read)
+            for (int t = 0; t < g_.c; t += 4) {
+              const int r0 = s_rows[t];
+              const int r1 = t + 1 < g_.c ? s_rows[t + 1] : r0;
+              const int r2 = t + 2 < g_.c ? s_rows[t + 2] : r0;
+              const int r3 = t + 3 < g_.c ? s_rows[t + 3] : r0;
+              tma_gather4(d + t * 128, &xmap, k0, r0, r1, r2, r3, &full[s], pol_x);
+            }
+          } else {
+            tma_load_2d(d, &xmap, k0, 0, &full[s], pol_x);
           }
-        } else {
-          tma_load_2d(xdst, &xmap, kb * kKBlk, 0, &full[s], pol_x);
         }
       };
       auto group_of = [&](long long u) -> int { return (int)((u / KB) / TILES); };
       auto xbytes = [&](const GroupInfo& g_) -> uint32_t {
-        return GROUPED ? (uint32_t)(g_.c * 128) : (uint32_t)kXBytes;
+        return GROUPED ? (uint32_t)(((g_.c + 3) & ~3) * 128 * kKSub) : (uint32_t)kXBytes;
       };
       const uint32_t wbytes = kWBytes;
       int i = 0;
@@ -397,8 +416,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (GROUPED) {
           const int g = group_of(u);
           if (g != gcur) {
+            // new expert: read its id, pair range and token rows once
             gcur = g;
             gi = load_group<GROUPED>(a, g);
+            for (int t = 0; t < gi.c; ++t) {
+              const int p = gi.p0 + t;
+              s_rows[t] = a.pair_row ? a.pair_row[p] : p;
+            }
           }
         }
         mbar_arrive_expect_tx(&full[s], wbytes + xbytes(gi));
@@ -630,46 +654,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!s_flags[0]) {
         if (!mbar_wait(&full[s], (i / STAGES) & 1, a.timeout_ns, a.status)) s_flags[0] = 1;
       }
-      const uint8_t* wbase = smem + s * kStageBytes;
-      xs_base = wbase + kWBytes;
-      if (!use_mma) {
-        // CUDA-core path: lane reads 16-byte chunk q of rows rho + 4r
-        float xv[2][8];
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (t < gi.c) {
-            const uint4 v = *reinterpret_cast<const uint4*>(xs_base + t * 128 + ((q ^ (t & 7)) << 4));
-            unpack8(v, xv[t]);
-          } else {
+      for (int sb = 0; sb < kKSub; ++sb) {
+        const uint8_t* wbase = smem + s * kStageBytes + sb * kWSub;
+        xs_base = smem + s * kStageBytes + kWBytes + sb * kXSub;
+        if (!use_mma) {
+          // CUDA-core path: lane reads 16-byte chunk q of rows rho + 4r
+          float xv[2][8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) xv[t][j] = 0.f;
+          for (int t = 0; t < 2; ++t) {
+            if (t < gi.c) {
+              const uint4 v =
+                  *reinterpret_cast<const uint4*>(xs_base + t * 128 + ((q ^ (t & 7)) << 4));
+              unpack8(v, xv[t]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) xv[t][j] = 0.f;
+            }
           }
-        }
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int sr = stage_row<PAIRED>(w, rho + 4 * r);
-          const uint4 wv = *reinterpret_cast<const uint4*>(wbase + sr * 128 + ((q ^ (sr & 7)) << 4));
-          dacc[r][0] = dot8(wv, xv[0], dacc[r][0]);
-          if (gi.c > 1) dacc[r][1] = dot8(wv, xv[1], dacc[r][1]);
-        }
-      } else {
-        const int ntg = (gi.c + 7) >> 3;
-        const uint32_t wb = smem_u32(wbase), xb = smem_u32(xs_base);
-        const int mi = lane >> 3, r8 = lane & 7;
-        const int a_sr = stage_row<PAIRED>(w, (mi & 1) * 8 + r8);
+          for (int r = 0; r < 4; ++r) {
+            const int sr = stage_row<PAIRED>(w, rho + 4 * r);
+            const uint4 wv =
+                *reinterpret_cast<const uint4*>(wbase + sr * 128 + ((q ^ (sr & 7)) << 4));
+            dacc[r][0] = dot8(wv, xv[0], dacc[r][0]);
+            if (gi.c > 1) dacc[r][1] = dot8(wv, xv[1], dacc[r][1]);
+          }
+        } else {
+          const int ntg = (gi.c + 7) >> 3;
+          const uint32_t wb = smem_u32(wbase), xb = smem_u32(xs_base);
+          const int mi = lane >> 3, r8 = lane & 7;
+          const int a_sr = stage_row<PAIRED>(w, (mi & 1) * 8 + r8);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          uint32_t af[4];
-          const int ach = kk * 2 + (mi >> 1);
-          ldmatrix_x4(af[0], af[1], af[2], af[3], wb + a_sr * 128 + ((ach ^ r8) << 4));
+          for (int kk = 0; kk < 4; ++kk) {
+            uint32_t af[4];
+            const int ach = kk * 2 + (mi >> 1);
+            ldmatrix_x4(af[0], af[1], af[2], af[3], wb + a_sr * 128 + ((ach ^ r8) << 4));
 #pragma unroll
-          for (int tg = 0; tg < XR / 8; ++tg) {
-            if (tg < ntg) {
-              const int t = tg * 8 + r8;
-              const int bch = kk * 2 + (mi & 1);
-              uint32_t b0, b1;
-              ldmatrix_x2(b0, b1, xb + t * 128 + ((bch ^ r8) << 4));
-              mma_bf16_16816(macc[tg], af, b0, b1);
+            for (int tg = 0; tg < XR / 8; ++tg) {
+              if (tg < ntg) {
+                const int t = tg * 8 + r8;
+                const int bch = kk * 2 + (mi & 1);
+                uint32_t b0, b1;
+                ldmatrix_x2(b0, b1, xb + t * 128 + ((bch ^ r8) << 4));
+                mma_bf16_16816(macc[tg], af, b0, b1);
+              }
             }
           }
         }

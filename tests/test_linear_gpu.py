@@ -68,7 +68,7 @@ def test_single_projection_m1_4096():
 def test_ragged_shapes_every_regime(M):
     # N not a multiple of the 128-row tile, K not a multiple of the 64-wide block
     _, (regime, _) = _check_random(M, 300, 520, ("ragged", M))
-    assert regime == _expect_regime(M) or (regime == "mma" and M >= 16)
+    assert regime == _expect_regime(M)
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 1, 8), (2, 1, 8), (3, 5, 16), (64, 1, 8), (1, 129, 72),
@@ -82,7 +82,7 @@ def test_degenerate_shapes(M, N, K):
 def test_integer_inputs_bit_exact(M, S):
     # integer-valued bf16 inputs: fp32 accumulation is exact, so the only
     # rounding is the final bf16 one, taken on the exact value on both sides
-    K, N = 1024, 384
+    K, N = 2048, 384
     x = wl.integer_bf16((M, K), -2, 2, "int", M, "x")
     W = wl.integer_bf16((N, K), -2, 2, "int", M, "W")
     y, _ = _gpu_linear(x, W, S=S)
@@ -124,7 +124,7 @@ def test_batch_sweep_k7168(M, N):
     # sample of 384 output columns
     cols = np.random.default_rng(N + M).choice(N, 384, replace=False)
     _, (regime, _) = _check_random(M, N, 7168, ("cfg2", M, N), cols=cols)
-    assert regime == _expect_regime(M) or (regime == "mma" and M >= 16)
+    assert regime == _expect_regime(M)
 
 
 @pytest.mark.parametrize("M", [1, 4, 16, 64])
@@ -139,12 +139,15 @@ def test_residual_epilogue(M):
     assert_within_tol(to_f64(y), ref, Aref, "residual M=%d" % M)
 
 
-def test_forced_regimes_agree():
-    M, N, K = 2, 512, 1024
-    x = wl.integer_bf16((M, K), -2, 2, "force", "x")
-    W = wl.integer_bf16((N, K), -2, 2, "force", "W")
+@pytest.mark.parametrize("M,forces", [(2, ["smallm", "mma"]), (16, ["mma", "tc"]),
+                                      (40, ["mma", "tc"])])
+def test_forced_regimes_agree(M, forces):
+    # integer inputs: every regime must give the same bits
+    N, K = 512, 1024
+    x = wl.integer_bf16((M, K), -2, 2, "force", M, "x")
+    W = wl.integer_bf16((N, K), -2, 2, "force", M, "W")
     outs = {}
-    for f in ["smallm", "mma"]:
+    for f in forces:
         os.environ["DEC_FORCE"] = f
         try:
             y, (regime, _) = _gpu_linear(x, W)
@@ -152,7 +155,7 @@ def test_forced_regimes_agree():
             del os.environ["DEC_FORCE"]
         assert regime == f
         outs[f] = wl.torch_to_bits(y)
-    assert np.array_equal(outs["smallm"], outs["mma"])
+    assert np.array_equal(outs[forces[0]], outs[forces[1]])
 
 
 def test_output_guard_bands_untouched():
