@@ -209,6 +209,43 @@ long long dec_launch_count(void);
 int dec_probe_begin(int kind, int capacity);
 int dec_probe_end(double* total_ms, int* launches);
 
+/*
+ * dec_linear_noalloc -- dec_linear for callers that must not allocate device
+ * memory. The pages describe no counterpart: this entry point exists for
+ * integration, not for the method.
+ *
+ * Who needs it: code whose device memory is owned by someone else (a
+ * framework's caching allocator that has reserved the GPU, an engine with a
+ * memory budget fixed before the first request) and latency-critical loops
+ * in which cudaMalloc/cudaFree, which may synchronise the device, must never
+ * run. dec_linear allocates its split-K workspace on first use and grows it
+ * for larger shapes; this variant allocates nothing and calls no allocating
+ * routine.
+ *
+ * Same arguments, layouts and result as dec_linear (fp32 accumulation, one
+ * bf16 rounding), computed by the same weight-streaming kernel: CUDA-core for
+ * M <= 2, mma.sync for 3 <= M <= 16. Its split-K partial sums and arrival
+ * counters live in one 4 MiB array compiled into the library; every GPU that
+ * loads the library holds that array until the process exits.
+ *
+ * Limits (DEC_EUNSUPPORTED beyond them): M <= 16; ceil(N/128) <= 16384 output
+ * tiles; the partial tiles of the launch, min(SMs, ceil(N/128)*ceil(K/128))
+ * CTAs x 2 x 128 x (8 if M <= 2 else 16) floats, within 4 MiB - 64 KiB - 256 B
+ * (a 152-SM GB300 needs at most 2.4 MiB, so every N and K fit there).
+ * Argument errors as for dec_linear (DEC_EINVAL); DEC_ENODEV without an sm_103
+ * device; DEC_ECUDA if a runtime call fails.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture. Every call shares the one array, which keeps the
+ * last call's contents (each call clears the counters it uses): calls that can
+ * overlap on the GPU -- on unordered streams or from several host threads --
+ * race and corrupt each other's results. A bounded device-side wait that
+ * gives up ends the kernel as in dec_linear, but is not reported through
+ * dec_sync_check. Does not update dec_last_choice or dec_launch_count.
+ */
+int dec_linear_noalloc(const void* x, const void* W, void* y, int M, int N, int K, void* stream);
+
 /* dec_shutdown -- free the workspace, side stream and events of the current device. */
 void dec_shutdown(void);
 

@@ -32,6 +32,7 @@ EXPORTS = [
     "moe_decode_residual", "l2_prefetch", "dec_add", "dec_last_choice", "dec_last_grid",
     "dec_strerror", "dec_sync_check", "dec_set_wait_timeout_ns", "dec_selftest_timeout",
     "dec_launch_count", "dec_probe_begin", "dec_probe_end", "dec_shutdown", "dec_version",
+    "dec_linear_noalloc",
 ]
 
 _lib = None
@@ -71,6 +72,7 @@ def lib():
             "dec_probe_end": (I, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
             "dec_shutdown": (None, []),
             "dec_version": (I, []),
+            "dec_linear_noalloc": (I, [P, P, P, I, I, I, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -119,6 +121,17 @@ def dec_linear(x, W, y=None, stream=None, residual=None):
         rc = lib().dec_linear_residual(_ptr(x), _ptr(W), _ptr(residual), _ptr(y), M, N, K,
                                        _stream(stream))
     _check(rc, "dec_linear")
+    return y
+
+
+def dec_linear_noalloc(x, W, y, stream=None):
+    """dec_linear that allocates nothing: its split-K scratch is a fixed array
+    inside the library (for callers that cannot allocate device memory).
+    ``y`` must be given. Calls that may overlap on the GPU race."""
+    M, K = x.shape
+    N = W.shape[0]
+    _check(lib().dec_linear_noalloc(_ptr(x), _ptr(W), _ptr(y), M, N, K, _stream(stream)),
+           "dec_linear_noalloc")
     return y
 
 
