@@ -224,8 +224,9 @@ static int moe_bufs(DevState* s, int M, int H, int E, int k, int I, cudaStream_t
   size_t off = 0;
   size_t o_logits = off; off += al((size_t)Mx * Ex * 4);
   size_t o_nact = off; off += al(4);
-  size_t o_gexp = off; off += al((size_t)Ex * 4);
-  size_t o_goff = off; off += al((size_t)(Ex + 1) * 4);
+  const size_t Gx = (size_t)Ex + ((size_t)Mx * kx + 15) / 16;  // expert groups (16 tokens each at most)
+  size_t o_gexp = off; off += al(Gx * 4);
+  size_t o_goff = off; off += al((Gx + 1) * 4);
   size_t o_ptok = off; off += al((size_t)Mx * kx * 4);
   size_t o_pof = off; off += al((size_t)Mx * kx * 4);
   size_t o_gate = off; off += al((size_t)Mx * kx * 4);
@@ -275,7 +276,10 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   const size_t ws_bytes = (size_t)s->sms * 2 * 128 * 64 * sizeof(float);
   const int tiles13 = (I + 63) / 64, tiles2 = (H + 127) / 128, tilesr = (E + 127) / 128;
   int maxt = tiles13 > tiles2 ? tiles13 : tiles2;
-  const size_t ctr_bytes = (size_t)(E * (size_t)maxt + tilesr + 64) * sizeof(int);
+  // an expert chosen by more than 16 tokens forms several groups: at most
+  // E + M*topk/16 groups, each with its own tile counters
+  const int max_groups = E + (M * topk + 15) / 16;
+  const size_t ctr_bytes = (size_t)(max_groups * (size_t)maxt + tilesr + 64) * sizeof(int);
   if ((rc = ensure(s->ws_main, ws_bytes, st))) return rc;
   if ((rc = ensure(s->ctr_main, ctr_bytes, st))) return rc;
   const bool shared = Ws13 != nullptr;
@@ -307,7 +311,7 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   {
     ProbeScope p(3, st);
     if ((rc = counted(launch_router(cx, x, Wr, M, H, E, topk, topk_idx, topk_w, s->mb, ws,
-                                    ctr + E * maxt))))
+                                    ctr + (size_t)max_groups * maxt))))
       return rc;
   }
   {

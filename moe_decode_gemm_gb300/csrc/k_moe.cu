@@ -13,12 +13,15 @@
 
 namespace dg {
 
-constexpr int kMoeXR = 64;
+constexpr int kMoeXR = 64;                  // router and shared expert: every token (M <= 64)
 constexpr int kMoeStages = 4;
 constexpr int kRouterStages = 3;
+constexpr int kExpertXR = kGroupTokens;     // routed experts: one group's tokens
+constexpr int kExpertStages = 6;
 constexpr int kRouteScratch = 36 * 1024;
 
 constexpr int moe_smem(int stages, int extra) { return wstream_smem(kMoeXR, stages, extra); }
+constexpr int expert_smem() { return wstream_smem(kExpertXR, kExpertStages, 0); }
 
 template <typename K>
 static cudaError_t smem_once(K kern, int bytes, bool& done) {
@@ -84,8 +87,9 @@ cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, i
 
 cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, int M, int H, int E,
                                int k, int I, const MoeBufs& b, float* ws, int* ctr) {
-  constexpr int SMEM = moe_smem(kMoeStages, 0);
-  auto kern = wstream_kernel<kMoeXR, kMoeStages, EPI_SWIGLU, true, true, false>;
+  constexpr int SMEM = expert_smem();
+  static_assert(SMEM <= kMaxDynSmem, "shared memory");
+  auto kern = wstream_kernel<kExpertXR, kExpertStages, EPI_SWIGLU, true, true, false>;
   static bool done = false;
   cudaError_t e = smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;
@@ -111,8 +115,8 @@ cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, in
 
 cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E, int k, int I,
                               const MoeBufs& b, float* ws, int* ctr) {
-  constexpr int SMEM = moe_smem(kMoeStages, 0);
-  auto kern = wstream_kernel<kMoeXR, kMoeStages, EPI_F32, false, true, false>;
+  constexpr int SMEM = expert_smem();
+  auto kern = wstream_kernel<kExpertXR, kExpertStages, EPI_F32, false, true, false>;
   static bool done = false;
   cudaError_t e = smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;

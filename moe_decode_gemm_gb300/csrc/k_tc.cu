@@ -246,25 +246,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             };
             for (int j = et; j < nc && j < kMaxSlots; j += kTcEpi) s_slot[j] = (int)slot_of(j);
             named_bar_sync(1, kTcEpi);
-            if (!aborted && n < a.nout) {
-              for (int t0 = 0; t0 < gi.c; t0 += 8) {
-                float acc[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-                for (int j = 0; j < nc; ++j) {
-                  const long long sl = j < kMaxSlots ? (long long)s_slot[j] : slot_of(j);
-                  const float* base = a.ws + sl * kSlotFloats + r;
-                  float pv[8];
-#pragma unroll
-                  for (int q = 0; q < 8; ++q)
-                    pv[q] = (t0 + q < gi.c) ? __ldcg(base + (t0 + q) * kTileRows) : 0.f;
-#pragma unroll
-                  for (int q = 0; q < 8; ++q) acc[q] += pv[q];
-                }
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                  if (t0 + q < gi.c) store_out<EPI, false>(a, gi, t0 + q, n, acc[q]);
-              }
+            if (!aborted) {
+              auto slot_at = [&](int j) -> long long {
+                return j < kMaxSlots ? (long long)s_slot[j] : slot_of(j);
+              };
+              auto store = [&](int t, int rr, float v0, float) {
+                const int nn = tile * kTileRows + rr;
+                if (nn < a.nout) store_out<EPI, false>(a, gi, t, nn, v0);
+              };
+              reduce_partials<kTcEpi, false>(a.ws, kSlotFloats, nc, gi.c, et, slot_at, store);
             }
           }
           named_bar_sync(1, kTcEpi);

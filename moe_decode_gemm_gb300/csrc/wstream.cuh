@@ -34,6 +34,11 @@ constexpr int kWBytes = kWSub * kKSub;     // 32 KB of weights per stage
 
 enum Epi : int { EPI_BF16 = 0, EPI_BF16_RES = 1, EPI_F32 = 2, EPI_SWIGLU = 3 };
 
+// An expert chosen by more tokens than this is split into several groups of
+// at most this many (its weights are then streamed once per group). It sizes
+// the token rows of an expert kernel's pipeline stage.
+constexpr int kGroupTokens = 16;
+
 constexpr int kMaxSlots = 512;             // contributor slot table entries in shared memory
 
 // Dynamic shared memory of one wstream_kernel instantiation: 1 KB alignment
@@ -223,7 +228,7 @@ __device__ void route_tail(const RouteArgs& r, int ct, uint8_t* scratch) {
   for (int q = 0; q < PER; ++q) {
     const int e = ct * PER + q;
     cnt[q] = (e < E) ? __popcll(mask[e]) : 0;
-    act[q] = cnt[q] > 0 ? 1 : 0;
+    act[q] = (cnt[q] + kGroupTokens - 1) / kGroupTokens;  // groups of expert e
     csum += cnt[q];
     asum += act[q];
   }
@@ -253,9 +258,9 @@ __device__ void route_tail(const RouteArgs& r, int ct, uint8_t* scratch) {
     const int e = ct * PER + q;
     if (e < E) {
       s_off[e] = cpre;
-      if (act[q]) {
-        r.grp_exp[apre] = e;
-        r.grp_off[apre] = cpre;
+      for (int j = 0; j < act[q]; ++j) {
+        r.grp_exp[apre + j] = e;
+        r.grp_off[apre + j] = cpre + j * kGroupTokens;
       }
     }
     cpre += cnt[q];
@@ -276,6 +281,78 @@ __device__ void route_tail(const RouteArgs& r, int ct, uint8_t* scratch) {
     const int pos = s_off[e] + __popcll(below);
     r.pair_tok[pos] = m;
     r.pair_of[p] = pos;
+  }
+}
+
+// ------------------------------------------------------------------ split-K fixup
+// Sum the partial tiles of all nc contributors of one output tile, in
+// contributor order, and hand each total to `store(t, r, v_row_r, v_row_r+64)`.
+// Partial slots are [token][128 rows] fp32 at ws + slot * slot_floats. Rows
+// 0..R-1 are stored (R = 64 for SwiGLU tiles, whose rows r and r+64 are the
+// gate and up halves of one feature; 128 otherwise). Each thread takes two
+// groups of 4 rows and keeps 4 contributors' loads in flight for each, so the
+// reduction costs a few L2 round trips rather than one per contributor.
+template <int NT, bool PAIRED, typename Slot, typename Store>
+__device__ __forceinline__ void reduce_partials(const float* ws, long long slot_floats, int nc,
+                                                int c, int tid, Slot slot_of, Store store) {
+  constexpr int R = PAIRED ? 64 : kTileRows;
+  constexpr int R4 = R / 4;
+  constexpr int EB = 2;
+  const int nel4 = R4 * c;
+  for (int e0 = tid * EB; e0 < nel4; e0 += NT * EB) {
+    float4 g[EB], u[EB];
+    int off[EB];
+#pragma unroll
+    for (int q = 0; q < EB; ++q) {
+      g[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      u[q] = g[q];
+      const int e = e0 + q < nel4 ? e0 + q : e0;
+      const int t = e / R4;
+      off[q] = t * kTileRows + (e - t * R4) * 4;
+    }
+    int j = 0;
+    for (; j + 4 <= nc; j += 4) {
+      float4 pg[4][EB], pu[4][EB];
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const float* b = ws + slot_of(j + jj) * slot_floats;
+#pragma unroll
+        for (int q = 0; q < EB; ++q) {
+          pg[jj][q] = __ldcg(reinterpret_cast<const float4*>(b + off[q]));
+          if (PAIRED) pu[jj][q] = __ldcg(reinterpret_cast<const float4*>(b + off[q] + 64));
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+        for (int q = 0; q < EB; ++q) {
+          g[q].x += pg[jj][q].x; g[q].y += pg[jj][q].y; g[q].z += pg[jj][q].z; g[q].w += pg[jj][q].w;
+          if (PAIRED) {
+            u[q].x += pu[jj][q].x; u[q].y += pu[jj][q].y; u[q].z += pu[jj][q].z; u[q].w += pu[jj][q].w;
+          }
+        }
+    }
+    for (; j < nc; ++j) {
+      const float* b = ws + slot_of(j) * slot_floats;
+#pragma unroll
+      for (int q = 0; q < EB; ++q) {
+        const float4 a = __ldcg(reinterpret_cast<const float4*>(b + off[q]));
+        g[q].x += a.x; g[q].y += a.y; g[q].z += a.z; g[q].w += a.w;
+        if (PAIRED) {
+          const float4 d = __ldcg(reinterpret_cast<const float4*>(b + off[q] + 64));
+          u[q].x += d.x; u[q].y += d.y; u[q].z += d.z; u[q].w += d.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < EB; ++q) {
+      if (e0 + q >= nel4) continue;
+      const int t = off[q] / kTileRows, r = off[q] - t * kTileRows;
+      store(t, r + 0, g[q].x, u[q].x);
+      store(t, r + 1, g[q].y, u[q].y);
+      store(t, r + 2, g[q].z, u[q].z);
+      store(t, r + 3, g[q].w, u[q].w);
+    }
   }
 }
 
@@ -584,31 +661,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = ct; j < nc && j < kMaxSlots; j += kNCW * 32) s_slot[j] = (int)slot_of(j);
           named_bar_sync(1, kNCW * 32);
           if (!aborted) {
-            constexpr int R = PAIRED ? 64 : kTileRows;
-            const int nel = R * gi.c;
-            for (int e = ct; e < nel; e += kNCW * 32) {
-              const int t = e / R, r = e - t * R;
-              const int off = t * kTileRows + r;
-              float vg = 0.f, vu = 0.f;
-              for (int j0 = 0; j0 < nc; j0 += 8) {
-                float pg[8], pu[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  if (j0 + j < nc) {
-                    const long long sl = (j0 + j < kMaxSlots) ? (long long)s_slot[j0 + j] : slot_of(j0 + j);
-                    const float* base = a.ws + sl * kSlotFloats;
-                    pg[j] = __ldcg(base + off);
-                    if (PAIRED) pu[j] = __ldcg(base + off + 64);
-                  }
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  if (j0 + j < nc) {
-                    vg += pg[j];
-                    if (PAIRED) vu += pu[j];
-                  }
-                }
-              }
+            auto slot_at = [&](int j) -> long long {
+              return j < kMaxSlots ? (long long)s_slot[j] : slot_of(j);
+            };
+            auto store = [&](int t, int r, float vg, float vu) {
               if (PAIRED) {
                 const int i = tile * 64 + r;
                 if (i < a.nout) store_swiglu(a, gi, t, i, vg, vu);
@@ -616,7 +672,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n = tile * kTileRows + r;
                 if (n < a.nout) store_out<EPI, GROUPED>(a, gi, t, n, vg);
               }
-            }
+            };
+            reduce_partials<kNCW * 32, PAIRED>(a.ws, kSlotFloats, nc, gi.c, ct, slot_at, store);
           }
         }
       }
