@@ -231,6 +231,7 @@ static int moe_bufs(DevState* s, int M, int H, int E, int k, int I, cudaStream_t
   size_t o_pof = off; off += al((size_t)Mx * kx * 4);
   size_t o_gate = off; off += al((size_t)Mx * kx * 4);
   size_t o_done = off; off += al(4);
+  size_t o_xs = off; off += al((size_t)Mx * kx * Hx * 2);
   size_t o_h = off; off += al((size_t)Mx * kx * Ix * 2);
   size_t o_o = off; off += al((size_t)Mx * kx * Hx * 4);
   size_t o_hs = off; off += al((size_t)Mx * Ix * 2);
@@ -246,6 +247,7 @@ static int moe_bufs(DevState* s, int M, int H, int E, int k, int I, cudaStream_t
   s->mb.pair_of = (int*)(b + o_pof);
   s->mb.gate = (float*)(b + o_gate);
   s->mb.done = (int*)(b + o_done);
+  s->mb.xs = (uint16_t*)(b + o_xs);
   s->mb.h = (uint16_t*)(b + o_h);
   s->mb.o = (float*)(b + o_o);
   s->mb.hs = (uint16_t*)(b + o_hs);
@@ -314,6 +316,7 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
                                     ctr + (size_t)max_groups * maxt))))
       return rc;
   }
+  if ((rc = counted(launch_gather(cx, x, M, H, topk, s->mb)))) return rc;
   {
     ProbeScope p(0, st);
     if ((rc = counted(launch_experts_w13(cx, x, W13, M, H, E, topk, I, s->mb, ws, ctr)))) return rc;

@@ -102,20 +102,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// TMA gather: four rows r0..r3 (any order, repeats allowed) of 64 columns
-// starting at column c0, written as four consecutive 128-byte rows at dst.
-// The tensor map's box must be 64 columns x 1 row.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, int c0, int r0,
-                                            int r1, int r2, int r3, uint64_t* bar,
-                                            uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-      "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
 // Untiled bulk prefetch of [src, src+bytes) into L2 (bytes % 16 == 0).
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");

@@ -95,7 +95,8 @@ cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, in
   if (e != cudaSuccess) return e;
   CUtensorMap wmap, xmap;
   if (!make_tmap(&wmap, W13, (uint64_t)E * 2 * I, (uint64_t)H, 64, true)) return cudaErrorInvalidValue;
-  if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)H, 1, false)) return cudaErrorInvalidValue;
+  if (!make_tmap(&xmap, b.xs, (uint64_t)M * k, (uint64_t)H, kExpertXR, false))
+    return cudaErrorInvalidValue;
   StreamArgs a = base_args(cx, ws, ctr);
   a.K = H;
   a.KB = (H + kKChunk - 1) / kKChunk;
@@ -105,7 +106,6 @@ cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, in
   a.nact = b.nact;
   a.grp_exp = b.grp_exp;
   a.grp_off = b.grp_off;
-  a.pair_row = b.pair_tok;
   a.w_group_rows = 2 * I;
   a.w_up_offset = I;
   a.out = b.h;
@@ -122,7 +122,8 @@ cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E
   if (e != cudaSuccess) return e;
   CUtensorMap wmap, xmap;
   if (!make_tmap(&wmap, W2, (uint64_t)E * H, (uint64_t)I, kTileRows, true)) return cudaErrorInvalidValue;
-  if (!make_tmap(&xmap, b.h, (uint64_t)M * k, (uint64_t)I, 1, false)) return cudaErrorInvalidValue;
+  if (!make_tmap(&xmap, b.h, (uint64_t)M * k, (uint64_t)I, kExpertXR, false))
+    return cudaErrorInvalidValue;
   StreamArgs a = base_args(cx, ws, ctr);
   a.K = I;
   a.KB = (I + kKChunk - 1) / kKChunk;
@@ -132,7 +133,6 @@ cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E
   a.nact = b.nact;
   a.grp_exp = b.grp_exp;
   a.grp_off = b.grp_off;
-  a.pair_row = nullptr;
   a.w_group_rows = H;
   a.out = b.o;
   a.ldo = H;
@@ -184,6 +184,36 @@ cudaError_t launch_shared_w2(const Ctx& cx, const void* Ws2, int M, int H, int I
   const long long T = (long long)a.TILES * a.KB;
   if (grid > T) grid = (int)T;
   return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
+}
+
+// ------------------------------------------------------------------ token gather
+// xs[p] = x[pair_tok[p]] for every (token, slot) pair p: the routed experts'
+// token rows in expert order, so that each expert group's rows are contiguous
+// and reach shared memory as one TMA box. 16-byte vectors, grid-stride.
+__global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x,
+                                                     const int* __restrict__ pair_tok,
+                                                     uint4* __restrict__ xs, int npairs,
+                                                     int row_vecs) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const long long total = (long long)npairs * row_vecs;
+  for (long long v = blockIdx.x * (long long)blockDim.x + threadIdx.x; v < total;
+       v += (long long)gridDim.x * blockDim.x) {
+    const int p = (int)(v / row_vecs);
+    const int c = (int)(v - (long long)p * row_vecs);
+    xs[v] = x[(long long)pair_tok[p] * row_vecs + c];
+  }
+}
+
+cudaError_t launch_gather(const Ctx& cx, const void* x, int M, int H, int k, const MoeBufs& b) {
+  const int row_vecs = H / 8;
+  const long long total = (long long)M * k * row_vecs;
+  long long grid = (total + 255) / 256;
+  if (grid > 2 * cx.sms) grid = 2 * cx.sms;
+  if (grid < 1) grid = 1;
+  return launch_k(gather_kernel, dim3((unsigned)grid), dim3(256), 0, cx.stream, cx.pdl,
+                  reinterpret_cast<const uint4*>(x), (const int*)b.pair_tok,
+                  reinterpret_cast<uint4*>(b.xs), M * k, row_vecs);
 }
 
 // ------------------------------------------------------------------ combine

@@ -41,6 +41,7 @@ struct MoeBufs {
   int* pair_of;    // [M*k]
   float* gate;     // [M*k]
   int* done;
+  uint16_t* xs;    // [M*k, H] token rows in expert-sorted pair order
   uint16_t* h;     // [M*k, I]
   float* o;        // [M*k, H]
   uint16_t* hs;    // [M, I]
@@ -49,6 +50,7 @@ struct MoeBufs {
 
 cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E, int k,
                           int32_t* idx_user, float* w_user, const MoeBufs& b, float* ws, int* ctr);
+cudaError_t launch_gather(const Ctx& cx, const void* x, int M, int H, int k, const MoeBufs& b);
 cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, int M, int H, int E,
                                int k, int I, const MoeBufs& b, float* ws, int* ctr);
 cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E, int k, int I,

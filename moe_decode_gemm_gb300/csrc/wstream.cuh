@@ -44,8 +44,7 @@ constexpr int kMaxSlots = 512;             // contributor slot table entries in 
 // Dynamic shared memory of one wstream_kernel instantiation: 1 KB alignment
 // slack, the stage ring, full/empty barriers, flags, slot table, and `extra`.
 constexpr int wstream_smem(int xr, int stages, int extra) {
-  return 1024 + stages * (kWBytes + kKSub * xr * 128) + 2 * 8 * stages + 32 + 4 * kMaxSlots +
-         4 * xr + extra;
+  return 1024 + stages * (kWBytes + kKSub * xr * 128) + 2 * 8 * stages + 32 + 4 * kMaxSlots + extra;
 }
 
 // Routing tail run by the CTA that completes the router's last logit tile.
@@ -73,7 +72,6 @@ struct StreamArgs {
   const int* nact;
   const int* grp_exp;
   const int* grp_off;
-  const int* pair_row;       // token-tile row of pair p; null: row p
   int w_group_rows;          // weight rows per expert
   int w_up_offset;           // paired (SwiGLU) tiles: row offset of the up block
   // output
@@ -374,8 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + STAGES;
   volatile int* s_flags = reinterpret_cast<volatile int*>(empty + STAGES);  // [0] abort [1] last [2] routed
   int* s_slot = const_cast<int*>(s_flags) + 8;                                 // [kMaxSlots]
-  int* s_rows = s_slot + kMaxSlots;                                            // [XR] token rows
-  uint8_t* scratch = reinterpret_cast<uint8_t*>(s_rows + XR);
+  uint8_t* scratch = reinterpret_cast<uint8_t*>(s_slot + kMaxSlots);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -447,24 +444,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int sb = 0; sb < kKSub; ++sb) {
           const int k0 = (kc * kKSub + sb) * kKBlk;
           uint8_t* d = xdst + sb * kXSub;
-          if (GROUPED) {
-            // the group's token rows, four per gather (the last gather repeats
-            // its first row into rows the consumers never read)
-            for (int t = 0; t < g_.c; t += 4) {
-              const int r0 = s_rows[t];
-              const int r1 = t + 1 < g_.c ? s_rows[t + 1] : r0;
-              const int r2 = t + 2 < g_.c ? s_rows[t + 2] : r0;
-              const int r3 = t + 3 < g_.c ? s_rows[t + 3] : r0;
-              tma_gather4(d + t * 128, &xmap, k0, r0, r1, r2, r3, &full[s], pol_x);
-            }
-          } else {
-            tma_load_2d(d, &xmap, k0, 0, &full[s], pol_x);
-          }
+          // Grouped: the token rows of a group are contiguous in the token
+          // tensor (pairs are stored in expert order), so one box of XR rows
+          // at the group's first pair covers them; rows past the group are
+          // never read.
+          tma_load_2d(d, &xmap, k0, GROUPED ? g_.p0 : 0, &full[s], pol_x);
         }
       };
       auto group_of = [&](long long u) -> int { return (int)((u / KB) / TILES); };
       auto xbytes = [&](const GroupInfo& g_) -> uint32_t {
-        return GROUPED ? (uint32_t)(((g_.c + 3) & ~3) * 128 * kKSub) : (uint32_t)kXBytes;
+        (void)g_;
+        return (uint32_t)kXBytes;
       };
       const uint32_t wbytes = kWBytes;
       int i = 0;
@@ -493,13 +483,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (GROUPED) {
           const int g = group_of(u);
           if (g != gcur) {
-            // new expert: read its id, pair range and token rows once
+            // new expert group: read its id and pair range once
             gcur = g;
             gi = load_group<GROUPED>(a, g);
-            for (int t = 0; t < gi.c; ++t) {
-              const int p = gi.p0 + t;
-              s_rows[t] = a.pair_row ? a.pair_row[p] : p;
-            }
           }
         }
         mbar_arrive_expect_tx(&full[s], wbytes + xbytes(gi));
