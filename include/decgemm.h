@@ -121,7 +121,8 @@ int dec_linear_splitk(const void* x, const void* W, void* y, int M, int N, int K
  *   out    = bf16( sum_{j=0..topk-1} g_j · h_j·W2ᵀ  +  shared(x) ).
  * Only the chosen experts' weights are read, each once per call however many
  * tokens chose it. The shared expert runs on a library-owned side stream that
- * waits on `stream` at entry and is joined back before the final combine.
+ * waits on `stream` at entry, streams its weights on the SMs the router leaves
+ * free while the router runs, and is joined back before the routed experts.
  * The number of active experts never returns to the host.
  * Limits: H % 8 == 0, I % 8 == 0, 1 <= topk <= min(E, 32), E <= 1024.
  * Errors: DEC_EINVAL, DEC_EUNSUPPORTED, DEC_ECUDA, DEC_ENOMEM.

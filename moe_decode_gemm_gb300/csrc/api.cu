@@ -275,8 +275,9 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   if (rc) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if ((rc = moe_bufs(s, M, H, E, topk, I, st))) return rc;
-  const size_t ws_bytes = (size_t)s->sms * 2 * 128 * 64 * sizeof(float);
-  const int tiles13 = (I + 63) / 64, tiles2 = (H + 127) / 128, tilesr = (E + 127) / 128;
+  // partial slots: 2 per CTA, up to 256 rows (gate + up halves) x 64 tokens
+  const size_t ws_bytes = (size_t)s->sms * 2 * 256 * 64 * sizeof(float);
+  const int tiles13 = (I + 127) / 128, tiles2 = (H + 127) / 128, tilesr = (E + 127) / 128;
   int maxt = tiles13 > tiles2 ? tiles13 : tiles2;
   // an expert chosen by more than 16 tokens forms several groups: at most
   // E + M*topk/16 groups, each with its own tile counters
@@ -292,15 +293,18 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   Ctx cx = make_ctx(s, st);
   float* ws = (float*)s->ws_main.p;
   int* ctr = (int*)s->ctr_main.p;
-  // shared expert: fork to the side stream, overlapped with routing and experts
+  // Shared expert: forked to the side stream so that it streams its weights
+  // while the router, a short latency-bound kernel on a third of the SMs,
+  // runs on the main stream. It gets the other SMs, and the routed experts
+  // start only after both have finished: their work is split statically
+  // across all SMs, so nothing else should hold an SM while they run.
+  const int router_grid = s->sms / 3 > 0 ? s->sms / 3 : 1;
   if (shared) {
     if (cudaEventRecord(s->ev_fork, st) != cudaSuccess) return DEC_ECUDA;
     if (cudaStreamWaitEvent(s->side, s->ev_fork, 0) != cudaSuccess) return DEC_ECUDA;
     Ctx sx = make_ctx(s, s->side);
     sx.pdl = false;
-    // A quarter of the SMs: the shared expert is a small share of the block's
-    // bytes and must leave room for the router and the routed experts.
-    const int sgrid = s->sms / 4 > 0 ? s->sms / 4 : 1;
+    const int sgrid = s->sms - router_grid > 0 ? s->sms - router_grid : 1;
     if ((rc = counted(launch_shared_w13(sx, x, Ws13, M, H, I, s->mb, sgrid, (float*)s->ws_side.p,
                                         (int*)s->ctr_side.p))))
       return rc;
@@ -317,20 +321,21 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
       return rc;
   }
   if ((rc = counted(launch_gather(cx, x, M, H, topk, s->mb)))) return rc;
+  if (shared) {
+    // join: the gate/up kernel then depends on two streams, so it is
+    // launched without the programmatic (early-start) dependency
+    if (cudaStreamWaitEvent(st, s->ev_join, 0) != cudaSuccess) return DEC_ECUDA;
+  }
   {
+    Ctx cw = cx;
+    cw.pdl = !shared;
     ProbeScope p(0, st);
-    if ((rc = counted(launch_experts_w13(cx, x, W13, M, H, E, topk, I, s->mb, ws, ctr)))) return rc;
+    if ((rc = counted(launch_experts_w13(cw, x, W13, M, H, E, topk, I, s->mb, ws, ctr)))) return rc;
   }
   {
     ProbeScope p(1, st);
     if ((rc = counted(launch_experts_w2(cx, W2, M, H, E, topk, I, s->mb, ws, ctr)))) return rc;
   }
-  if (shared) {
-    if (cudaStreamWaitEvent(st, s->ev_join, 0) != cudaSuccess) return DEC_ECUDA;
-  }
-  // After the join the combine depends on two streams: launch it without PDL
-  // so that both dependencies are complete ones.
-  cx.pdl = !shared;
   ProbeScope p(4, st);
   return counted(launch_combine(cx, s->mb, shared, res, out, M, H, topk));
 }

@@ -17,11 +17,14 @@ constexpr int kMoeXR = 64;                  // router and shared expert: every t
 constexpr int kMoeStages = 4;
 constexpr int kRouterStages = 3;
 constexpr int kExpertXR = kGroupTokens;     // routed experts: one group's tokens
-constexpr int kExpertStages = 6;
+constexpr int kExpertStages = 6;            // down projection: 32 KB weight stages
+constexpr int kExpertPairStages = 3;        // gate/up: 64 KB stages (gate and up halves)
+constexpr int kSharedPairStages = 2;        // shared gate/up: 64 KB + 16 KB of tokens
 constexpr int kRouteScratch = 36 * 1024;
 
 constexpr int moe_smem(int stages, int extra) { return wstream_smem(kMoeXR, stages, extra); }
 constexpr int expert_smem() { return wstream_smem(kExpertXR, kExpertStages, 0); }
+constexpr int expert_pair_smem() { return wstream_smem(kExpertXR, kExpertPairStages, 0, true); }
 
 template <typename K>
 static cudaError_t smem_once(K kern, int bytes, bool& done) {
@@ -80,27 +83,28 @@ cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, i
   // bound: a third of the SMs keeps the number of CTAs per output tile, and so
   // the split-K fixup, small.
   const long long T = (long long)a.TILES * a.KB;
-  const int cap = cx.sms / 3 > 0 ? cx.sms / 3 : 1;
+  const int cap = cx.sms / 3 > 0 ? cx.sms / 3 : 1;  // the shared expert uses the other SMs
   const int grid = (int)(T < cap ? T : cap);
   return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
 }
 
 cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, int M, int H, int E,
                                int k, int I, const MoeBufs& b, float* ws, int* ctr) {
-  constexpr int SMEM = expert_smem();
+  constexpr int SMEM = expert_pair_smem();
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
-  auto kern = wstream_kernel<kExpertXR, kExpertStages, EPI_SWIGLU, true, true, false>;
+  auto kern = wstream_kernel<kExpertXR, kExpertPairStages, EPI_SWIGLU, true, true, false>;
   static bool done = false;
   cudaError_t e = smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;
   CUtensorMap wmap, xmap;
-  if (!make_tmap(&wmap, W13, (uint64_t)E * 2 * I, (uint64_t)H, 64, true)) return cudaErrorInvalidValue;
+  if (!make_tmap(&wmap, W13, (uint64_t)E * 2 * I, (uint64_t)H, kTileRows, true))
+    return cudaErrorInvalidValue;
   if (!make_tmap(&xmap, b.xs, (uint64_t)M * k, (uint64_t)H, kExpertXR, false))
     return cudaErrorInvalidValue;
   StreamArgs a = base_args(cx, ws, ctr);
   a.K = H;
   a.KB = (H + kKChunk - 1) / kKChunk;
-  a.TILES = (I + 63) / 64;
+  a.TILES = (I + kTileRows - 1) / kTileRows;
   a.nout = I;
   a.M = M;
   a.nact = b.nact;
@@ -141,18 +145,20 @@ cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E
 
 cudaError_t launch_shared_w13(const Ctx& cx, const void* x, const void* Ws13, int M, int H, int I,
                               const MoeBufs& b, int grid, float* ws, int* ctr) {
-  constexpr int SMEM = moe_smem(kMoeStages, 0);
-  auto kern = wstream_kernel<kMoeXR, kMoeStages, EPI_SWIGLU, true, false, false>;
+  constexpr int SMEM = wstream_smem(kMoeXR, kSharedPairStages, 0, true);
+  static_assert(SMEM <= kMaxDynSmem, "shared memory");
+  auto kern = wstream_kernel<kMoeXR, kSharedPairStages, EPI_SWIGLU, true, false, false>;
   static bool done = false;
   cudaError_t e = smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;
   CUtensorMap wmap, xmap;
-  if (!make_tmap(&wmap, Ws13, (uint64_t)2 * I, (uint64_t)H, 64, true)) return cudaErrorInvalidValue;
+  if (!make_tmap(&wmap, Ws13, (uint64_t)2 * I, (uint64_t)H, kTileRows, true))
+    return cudaErrorInvalidValue;
   if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)H, kMoeXR, false)) return cudaErrorInvalidValue;
   StreamArgs a = base_args(cx, ws, ctr);
   a.K = H;
   a.KB = (H + kKChunk - 1) / kKChunk;
-  a.TILES = (I + 63) / 64;
+  a.TILES = (I + kTileRows - 1) / kTileRows;
   a.nout = I;
   a.M = M;
   a.w_up_offset = I;

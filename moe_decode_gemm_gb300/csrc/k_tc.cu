@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int nn = tile * kTileRows + rr;
                 if (nn < a.nout) store_out<EPI, false>(a, gi, t, nn, v0);
               };
-              reduce_partials<kTcEpi, false>(a.ws, kSlotFloats, nc, gi.c, et, slot_at, store);
+              reduce_partials<kTcEpi, false, kTileRows>(a.ws, kSlotFloats, nc, gi.c, et, slot_at, store);
             }
           }
           named_bar_sync(1, kTcEpi);

@@ -43,8 +43,9 @@ constexpr int kMaxSlots = 512;             // contributor slot table entries in 
 
 // Dynamic shared memory of one wstream_kernel instantiation: 1 KB alignment
 // slack, the stage ring, full/empty barriers, flags, slot table, and `extra`.
-constexpr int wstream_smem(int xr, int stages, int extra) {
-  return 1024 + stages * (kWBytes + kKSub * xr * 128) + 2 * 8 * stages + 32 + 4 * kMaxSlots + extra;
+constexpr int wstream_smem(int xr, int stages, int extra, bool paired = false) {
+  return 1024 + stages * ((paired ? 2 : 1) * kWBytes + kKSub * xr * 128) + 2 * 8 * stages + 32 +
+         4 * kMaxSlots + extra;
 }
 
 // Routing tail run by the CTA that completes the router's last logit tile.
@@ -107,15 +108,6 @@ __device__ __forceinline__ GroupInfo load_group(const StreamArgs& a, int g) {
     gi.c = a.M;
   }
   return gi;
-}
-
-// Stage row of local row lr (0..15) of consumer warp w. Paired (SwiGLU)
-// tiles hold 64 gate rows then 64 up rows; a warp owns 8 gate rows and the 8
-// up rows of the same intermediate features, so SwiGLU needs no exchange.
-template <bool PAIRED>
-__device__ __forceinline__ int stage_row(int w, int lr) {
-  if (PAIRED) return lr < 8 ? 8 * w + lr : 64 + 8 * w + (lr - 8);
-  return 16 * w + lr;
 }
 
 __device__ __forceinline__ long long cta_start(long long c, long long T, long long G) {
@@ -284,29 +276,29 @@ __device__ void route_tail(const RouteArgs& r, int ct, uint8_t* scratch) {
 
 // ------------------------------------------------------------------ split-K fixup
 // Sum the partial tiles of all nc contributors of one output tile, in
-// contributor order, and hand each total to `store(t, r, v_row_r, v_row_r+64)`.
-// Partial slots are [token][128 rows] fp32 at ws + slot * slot_floats. Rows
-// 0..R-1 are stored (R = 64 for SwiGLU tiles, whose rows r and r+64 are the
-// gate and up halves of one feature; 128 otherwise). Each thread takes two
-// groups of 4 rows and keeps 4 contributors' loads in flight for each, so the
-// reduction costs a few L2 round trips rather than one per contributor.
-template <int NT, bool PAIRED, typename Slot, typename Store>
+// contributor order, and hand each total to `store(t, r, v, v_up)`. A partial
+// slot is [token][STRIDE] fp32 at ws + slot * slot_floats: 128 rows of output
+// features, followed for SwiGLU tiles (PAIRED) by the 128 matching up rows.
+// Each thread takes two groups of 4 rows and keeps 4 contributors' loads in
+// flight for each, so the reduction costs a few L2 round trips rather than one
+// per contributor.
+template <int NT, bool PAIRED, int STRIDE, typename Slot, typename Store>
 __device__ __forceinline__ void reduce_partials(const float* ws, long long slot_floats, int nc,
                                                 int c, int tid, Slot slot_of, Store store) {
-  constexpr int R = PAIRED ? 64 : kTileRows;
-  constexpr int R4 = R / 4;
+  constexpr int R4 = kTileRows / 4;
   constexpr int EB = 2;
   const int nel4 = R4 * c;
   for (int e0 = tid * EB; e0 < nel4; e0 += NT * EB) {
     float4 g[EB], u[EB];
-    int off[EB];
+    int off[EB], tt[EB], rr[EB];
 #pragma unroll
     for (int q = 0; q < EB; ++q) {
       g[q] = make_float4(0.f, 0.f, 0.f, 0.f);
       u[q] = g[q];
       const int e = e0 + q < nel4 ? e0 + q : e0;
-      const int t = e / R4;
-      off[q] = t * kTileRows + (e - t * R4) * 4;
+      tt[q] = e / R4;
+      rr[q] = (e - tt[q] * R4) * 4;
+      off[q] = tt[q] * STRIDE + rr[q];
     }
     int j = 0;
     for (; j + 4 <= nc; j += 4) {
@@ -317,7 +309,7 @@ __device__ __forceinline__ void reduce_partials(const float* ws, long long slot_
 #pragma unroll
         for (int q = 0; q < EB; ++q) {
           pg[jj][q] = __ldcg(reinterpret_cast<const float4*>(b + off[q]));
-          if (PAIRED) pu[jj][q] = __ldcg(reinterpret_cast<const float4*>(b + off[q] + 64));
+          if (PAIRED) pu[jj][q] = __ldcg(reinterpret_cast<const float4*>(b + off[q] + kTileRows));
         }
       }
 #pragma unroll
@@ -334,10 +326,10 @@ __device__ __forceinline__ void reduce_partials(const float* ws, long long slot_
       const float* b = ws + slot_of(j) * slot_floats;
 #pragma unroll
       for (int q = 0; q < EB; ++q) {
-        const float4 a = __ldcg(reinterpret_cast<const float4*>(b + off[q]));
-        g[q].x += a.x; g[q].y += a.y; g[q].z += a.z; g[q].w += a.w;
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(b + off[q]));
+        g[q].x += v.x; g[q].y += v.y; g[q].z += v.z; g[q].w += v.w;
         if (PAIRED) {
-          const float4 d = __ldcg(reinterpret_cast<const float4*>(b + off[q] + 64));
+          const float4 d = __ldcg(reinterpret_cast<const float4*>(b + off[q] + kTileRows));
           u[q].x += d.x; u[q].y += d.y; u[q].z += d.z; u[q].w += d.w;
         }
       }
@@ -345,26 +337,28 @@ __device__ __forceinline__ void reduce_partials(const float* ws, long long slot_
 #pragma unroll
     for (int q = 0; q < EB; ++q) {
       if (e0 + q >= nel4) continue;
-      const int t = off[q] / kTileRows, r = off[q] - t * kTileRows;
-      store(t, r + 0, g[q].x, u[q].x);
-      store(t, r + 1, g[q].y, u[q].y);
-      store(t, r + 2, g[q].z, u[q].z);
-      store(t, r + 3, g[q].w, u[q].w);
+      store(tt[q], rr[q] + 0, g[q].x, u[q].x);
+      store(tt[q], rr[q] + 1, g[q].y, u[q].y);
+      store(tt[q], rr[q] + 2, g[q].z, u[q].z);
+      store(tt[q], rr[q] + 3, g[q].w, u[q].w);
     }
   }
 }
 
 // ------------------------------------------------------------------ the kernel
 // XR: token rows per stage (8, 16 or 64). STAGES: ring depth.
-// PAIRED: SwiGLU tiles (64 gate + 64 up rows). GROUPED: MoE groups.
+// PAIRED: SwiGLU tiles (128 gate rows and the 128 matching up rows per stage
+// column). GROUPED: MoE groups.
 // ROUTER: dense fp32 logits followed by the routing tail.
 template <int XR, int STAGES, int EPI, bool PAIRED, bool GROUPED, bool ROUTER>
 __global__ void __launch_bounds__(kThreads, 1)
     wstream_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const StreamArgs a) {
+  constexpr int H2 = PAIRED ? 2 : 1;            // 128-row weight halves per box column
   constexpr int kXSub = XR * 128;              // token rows of one box column
   constexpr int kXBytes = kXSub * kKSub;
-  constexpr int kStageBytes = kWBytes + kXBytes;
+  constexpr int kWStage = H2 * kWBytes;
+  constexpr int kStageBytes = kWStage + kXBytes;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -427,19 +421,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int sb = 0; sb < kKSub; ++sb) {
           const int k0 = (kc * kKSub + sb) * kKBlk;
-          uint8_t* d = wdst + sb * kWSub;
-          if (PAIRED) {
-            tma_load_2d(d, &wmap, k0, rbase + tile * 64, &full[s], pol_w);
-            tma_load_2d(d + 64 * 128, &wmap, k0, rbase + a.w_up_offset + tile * 64, &full[s],
+          uint8_t* d = wdst + sb * H2 * kWSub;
+          tma_load_2d(d, &wmap, k0, rbase + tile * kTileRows, &full[s], pol_w);
+          if (PAIRED)
+            tma_load_2d(d + kWSub, &wmap, k0, rbase + a.w_up_offset + tile * kTileRows, &full[s],
                         pol_w);
-          } else {
-            tma_load_2d(d, &wmap, k0, rbase + tile * kTileRows, &full[s], pol_w);
-          }
         }
       };
       auto issue_x = [&](int s, long long u, const GroupInfo& g_) {
         const int kc = (int)(u % KB);
-        uint8_t* xdst = smem + s * kStageBytes + kWBytes;
+        uint8_t* xdst = smem + s * kStageBytes + kWStage;
 #pragma unroll
         for (int sb = 0; sb < kKSub; ++sb) {
           const int k0 = (kc * kKSub + sb) * kKBlk;
@@ -456,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         (void)g_;
         return (uint32_t)kXBytes;
       };
-      const uint32_t wbytes = kWBytes;
+      const uint32_t wbytes = kWStage;
       int i = 0;
       if (!GROUPED) {
         // Weights do not depend on the previous kernel: start streaming them
@@ -508,105 +499,104 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = lane & 7, rho = lane >> 3;  // CUDA-core path: chunk and row group
     const int gq = lane >> 2, tq = lane & 3;  // mma path: fragment row and column pair
 
-    float dacc[4][2];
-    float macc[XR / 8][4];
+    // Thread-held rows (within each 128-row half of a stage):
+    //   CUDA-core path: rows 16w + rho + 4r, r = 0..3, 16-byte chunk q of each;
+    //   mma path: rows 16w + gq and 16w + gq + 8 of the m16 fragment.
+    // Half 0 is the plain weight tile (or the gate rows), half 1 the up rows.
+    constexpr int kSlotStride = H2 * kTileRows;  // floats per token in a partial slot
+    float dacc[H2][4][2];
+    float macc[H2][XR / 8][4];
     long long cur = -1;
     GroupInfo gi{0, 0, 0};
     bool use_mma = false;
 
     auto zero_acc = [&]() {
 #pragma unroll
-      for (int r = 0; r < 4; ++r) dacc[r][0] = dacc[r][1] = 0.f;
+      for (int h = 0; h < H2; ++h) {
 #pragma unroll
-      for (int tg = 0; tg < XR / 8; ++tg)
+        for (int r = 0; r < 4; ++r) dacc[h][r][0] = dacc[h][r][1] = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) macc[tg][j] = 0.f;
+        for (int tg = 0; tg < XR / 8; ++tg)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) macc[h][tg][j] = 0.f;
+      }
     };
 
-    // Visit every (stage row, token, value) this thread holds for the tile.
-    // The CUDA-core path's values are complete only in lanes with q == 0
-    // after the shuffle reduction.
+    // The CUDA-core path's sums are complete only in lanes with q == 0 after
+    // this shuffle reduction over the 8 chunks of a row.
     auto reduce_dots = [&]() {
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
+      for (int h = 0; h < H2; ++h)
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          float v = dacc[r][t];
-          v += __shfl_xor_sync(0xffffffffu, v, 1);
-          v += __shfl_xor_sync(0xffffffffu, v, 2);
-          v += __shfl_xor_sync(0xffffffffu, v, 4);
-          dacc[r][t] = v;
-        }
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            float v = dacc[h][r][t];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            dacc[h][r][t] = v;
+          }
+    };
+
+    // One output: SwiGLU of the gate and up sums, or the plain sum.
+    auto emit = [&](int tile, int row, int t, float v0, float v1) {
+      const int n = tile * kTileRows + row;
+      if (n >= a.nout) return;
+      if (PAIRED) store_swiglu(a, gi, t, n, v0, v1);
+      else store_out<EPI, GROUPED>(a, gi, t, n, v0);
     };
 
     // Final values held in registers (the CTA covered the tile's whole k range).
     auto reg_epilogue = [&](int tile) {
       if (!use_mma) {
         if (q != 0) return;
-        if (PAIRED) {
 #pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const int i = tile * 64 + 8 * w + rho + 4 * r;
+        for (int r = 0; r < 4; ++r)
 #pragma unroll
-            for (int t = 0; t < 2; ++t)
-              if (t < gi.c && i < a.nout) store_swiglu(a, gi, t, i, dacc[r][t], dacc[r + 2][t]);
-          }
-        } else {
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int n = tile * kTileRows + stage_row<PAIRED>(w, rho + 4 * r);
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-              if (t < gi.c && n < a.nout) store_out<EPI, GROUPED>(a, gi, t, n, dacc[r][t]);
-          }
-        }
+          for (int t = 0; t < 2; ++t)
+            if (t < gi.c) emit(tile, 16 * w + rho + 4 * r, t, dacc[0][r][t], dacc[H2 - 1][r][t]);
         return;
       }
-      const int sr0 = stage_row<PAIRED>(w, gq), sr1 = stage_row<PAIRED>(w, gq + 8);
 #pragma unroll
-      for (int tg = 0; tg < XR / 8; ++tg) {
+      for (int tg = 0; tg < XR / 8; ++tg)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int t = tg * 8 + 2 * tq + h;
+        for (int hh = 0; hh < 2; ++hh) {
+          const int t = tg * 8 + 2 * tq + hh;
           if (t >= gi.c) continue;
-          if (PAIRED) {
-            const int i = tile * 64 + 8 * w + gq;
-            if (i < a.nout) store_swiglu(a, gi, t, i, macc[tg][h], macc[tg][2 + h]);
-          } else {
-            const int n0 = tile * kTileRows + sr0, n1 = tile * kTileRows + sr1;
-            if (n0 < a.nout) store_out<EPI, GROUPED>(a, gi, t, n0, macc[tg][h]);
-            if (n1 < a.nout) store_out<EPI, GROUPED>(a, gi, t, n1, macc[tg][2 + h]);
-          }
+          emit(tile, 16 * w + gq, t, macc[0][tg][hh], macc[H2 - 1][tg][hh]);
+          emit(tile, 16 * w + gq + 8, t, macc[0][tg][2 + hh], macc[H2 - 1][tg][2 + hh]);
         }
-      }
     };
 
     // This CTA's share of a tile that other CTAs also contribute to, written
-    // to its workspace slot as [token][128 stage rows] fp32.
+    // to its workspace slot as [token][kSlotStride] fp32.
     auto write_partial = [&](float* mine) {
       if (!use_mma) {
         if (q != 0) return;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int sr = stage_row<PAIRED>(w, rho + 4 * r);
+        for (int h = 0; h < H2; ++h)
 #pragma unroll
-          for (int t = 0; t < 2; ++t)
-            if (t < gi.c) __stcg(mine + t * kTileRows + sr, dacc[r][t]);
-        }
+          for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+              if (t < gi.c)
+                __stcg(mine + t * kSlotStride + h * kTileRows + 16 * w + rho + 4 * r, dacc[h][r][t]);
         return;
       }
-      const int sr0 = stage_row<PAIRED>(w, gq), sr1 = stage_row<PAIRED>(w, gq + 8);
 #pragma unroll
-      for (int tg = 0; tg < XR / 8; ++tg) {
+      for (int h = 0; h < H2; ++h)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int t = tg * 8 + 2 * tq + h;
-          if (t < gi.c) {
-            __stcg(mine + t * kTileRows + sr0, macc[tg][h]);
-            __stcg(mine + t * kTileRows + sr1, macc[tg][2 + h]);
+        for (int tg = 0; tg < XR / 8; ++tg)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int t = tg * 8 + 2 * tq + hh;
+            if (t < gi.c) {
+              float* p = mine + t * kSlotStride + h * kTileRows + 16 * w + gq;
+              __stcg(p, macc[h][tg][hh]);
+              __stcg(p + 8, macc[h][tg][2 + hh]);
+            }
           }
-        }
-      }
     };
 
     auto finish_tile = [&](long long gt) {
@@ -619,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (whole) {
         if (!aborted) reg_epilogue(tile);
       } else {
-        constexpr long long kSlotFloats = (long long)kTileRows * XR;
+        constexpr long long kSlotFloats = (long long)kSlotStride * XR;
         const int slot = (gt == u0 / KB) ? 0 : 1;
         write_partial(a.ws + (c * 2 + slot) * kSlotFloats);
         named_bar_sync(1, kNCW * 32);
@@ -636,8 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         last = s_flags[1] != 0;
         if (last) {
           // The last contributor sums every contributor's slot in CTA order
-          // (so the result does not depend on who arrived last), all consumer
-          // threads together, with the loads of up to 8 contributors in flight.
+          // (so the result does not depend on who arrived last).
           __threadfence();
           const int nc = (int)(cl - cf + 1);
           auto slot_of = [&](int j) -> long long {
@@ -650,16 +639,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto slot_at = [&](int j) -> long long {
               return j < kMaxSlots ? (long long)s_slot[j] : slot_of(j);
             };
-            auto store = [&](int t, int r, float vg, float vu) {
-              if (PAIRED) {
-                const int i = tile * 64 + r;
-                if (i < a.nout) store_swiglu(a, gi, t, i, vg, vu);
-              } else {
-                const int n = tile * kTileRows + r;
-                if (n < a.nout) store_out<EPI, GROUPED>(a, gi, t, n, vg);
-              }
-            };
-            reduce_partials<kNCW * 32, PAIRED>(a.ws, kSlotFloats, nc, gi.c, ct, slot_at, store);
+            auto store = [&](int t, int r, float vg, float vu) { emit(tile, r, t, vg, vu); };
+            reduce_partials<kNCW * 32, PAIRED, kSlotStride>(a.ws, kSlotFloats, nc, gi.c, ct,
+                                                            slot_at, store);
           }
         }
       }
@@ -682,7 +664,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(1, kNCW * 32);  // partial slots and flags may be reused next tile
     };
 
-    const uint8_t* xs_base = nullptr;
     for (int i = 0; i < nunits; ++i) {
       const long long u = u0 + i;
       const long long gt = u / KB;
@@ -699,10 +680,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int sb = 0; sb < kKSub; ++sb) {
-        const uint8_t* wbase = smem + s * kStageBytes + sb * kWSub;
-        xs_base = smem + s * kStageBytes + kWBytes + sb * kXSub;
+        const uint8_t* wbase = smem + s * kStageBytes + sb * H2 * kWSub;
+        const uint8_t* xs_base = smem + s * kStageBytes + kWStage + sb * kXSub;
         if (!use_mma) {
-          // CUDA-core path: lane reads 16-byte chunk q of rows rho + 4r
+          // CUDA-core path: lane reads 16-byte chunk q of rows 16w + rho + 4r
           float xv[2][8];
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
@@ -717,22 +698,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
-            const int sr = stage_row<PAIRED>(w, rho + 4 * r);
-            const uint4 wv =
-                *reinterpret_cast<const uint4*>(wbase + sr * 128 + ((q ^ (sr & 7)) << 4));
-            dacc[r][0] = dot8(wv, xv[0], dacc[r][0]);
-            if (gi.c > 1) dacc[r][1] = dot8(wv, xv[1], dacc[r][1]);
+            const int row = 16 * w + rho + 4 * r;
+#pragma unroll
+            for (int h = 0; h < H2; ++h) {
+              const uint4 wv = *reinterpret_cast<const uint4*>(wbase + h * kWSub + row * 128 +
+                                                               ((q ^ (row & 7)) << 4));
+              dacc[h][r][0] = dot8(wv, xv[0], dacc[h][r][0]);
+              if (gi.c > 1) dacc[h][r][1] = dot8(wv, xv[1], dacc[h][r][1]);
+            }
           }
         } else {
           const int ntg = (gi.c + 7) >> 3;
           const uint32_t wb = smem_u32(wbase), xb = smem_u32(xs_base);
           const int mi = lane >> 3, r8 = lane & 7;
-          const int a_sr = stage_row<PAIRED>(w, (mi & 1) * 8 + r8);
+          const int a_row = 16 * w + (mi & 1) * 8 + r8;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            uint32_t af[4];
+            uint32_t af[H2][4];
             const int ach = kk * 2 + (mi >> 1);
-            ldmatrix_x4(af[0], af[1], af[2], af[3], wb + a_sr * 128 + ((ach ^ r8) << 4));
+#pragma unroll
+            for (int h = 0; h < H2; ++h)
+              ldmatrix_x4(af[h][0], af[h][1], af[h][2], af[h][3],
+                          wb + h * kWSub + a_row * 128 + ((ach ^ r8) << 4));
 #pragma unroll
             for (int tg = 0; tg < XR / 8; ++tg) {
               if (tg < ntg) {
@@ -740,7 +727,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int bch = kk * 2 + (mi & 1);
                 uint32_t b0, b1;
                 ldmatrix_x2(b0, b1, xb + t * 128 + ((bch ^ r8) << 4));
-                mma_bf16_16816(macc[tg], af, b0, b1);
+#pragma unroll
+                for (int h = 0; h < H2; ++h) mma_bf16_16816(macc[h][tg], af[h], b0, b1);
               }
             }
           }
