@@ -17,13 +17,11 @@ constexpr int kMoeXR = 64;                  // router and shared expert: every t
 constexpr int kMoeStages = 4;
 constexpr int kRouterStages = 3;
 constexpr int kExpertXR = kGroupTokens;     // routed experts: one group's tokens
-constexpr int kExpertStages = 6;            // down projection: 32 KB weight stages
 constexpr int kExpertPairStages = 3;        // gate/up: 64 KB stages (gate and up halves)
 constexpr int kSharedPairStages = 2;        // shared gate/up: 64 KB + 16 KB of tokens
 constexpr int kRouteScratch = 36 * 1024;
 
 constexpr int moe_smem(int stages, int extra) { return wstream_smem(kMoeXR, stages, extra); }
-constexpr int expert_smem() { return wstream_smem(kExpertXR, kExpertStages, 0); }
 constexpr int expert_pair_smem() { return wstream_smem(kExpertXR, kExpertPairStages, 0, true); }
 
 template <typename K>
@@ -119,8 +117,9 @@ cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, in
 
 cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E, int k, int I,
                               const MoeBufs& b, float* ws, int* ctr) {
-  constexpr int SMEM = expert_smem();
-  auto kern = wstream_kernel<kExpertXR, kExpertStages, EPI_F32, false, true, false>;
+  // 256-row output tiles: two 128-row halves, 64 KB weight stages
+  constexpr int SMEM = expert_pair_smem();
+  auto kern = wstream_kernel<kExpertXR, kExpertPairStages, EPI_F32, false, true, false, true>;
   static bool done = false;
   cudaError_t e = smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;
@@ -131,7 +130,7 @@ cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E
   StreamArgs a = base_args(cx, ws, ctr);
   a.K = I;
   a.KB = (I + kKChunk - 1) / kKChunk;
-  a.TILES = (H + kTileRows - 1) / kTileRows;
+  a.TILES = (H + 2 * kTileRows - 1) / (2 * kTileRows);
   a.nout = H;
   a.M = M;
   a.nact = b.nact;

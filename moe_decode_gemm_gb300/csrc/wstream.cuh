@@ -285,7 +285,7 @@ __device__ void route_tail(const RouteArgs& r, int ct, uint8_t* scratch) {
 template <int NT, bool PAIRED, int STRIDE, typename Slot, typename Store>
 __device__ __forceinline__ void reduce_partials(const float* ws, long long slot_floats, int nc,
                                                 int c, int tid, Slot slot_of, Store store) {
-  constexpr int R4 = kTileRows / 4;
+  constexpr int R4 = (PAIRED ? kTileRows : STRIDE) / 4;  // output rows per token, in fours
   constexpr int EB = 2;
   const int nel4 = R4 * c;
   for (int e0 = tid * EB; e0 < nel4; e0 += NT * EB) {
@@ -348,13 +348,15 @@ __device__ __forceinline__ void reduce_partials(const float* ws, long long slot_
 // ------------------------------------------------------------------ the kernel
 // XR: token rows per stage (8, 16 or 64). STAGES: ring depth.
 // PAIRED: SwiGLU tiles (128 gate rows and the 128 matching up rows per stage
-// column). GROUPED: MoE groups.
+// column). WIDE: 256-row output tiles (two 128-row halves per stage column).
+// GROUPED: MoE groups.
 // ROUTER: dense fp32 logits followed by the routing tail.
-template <int XR, int STAGES, int EPI, bool PAIRED, bool GROUPED, bool ROUTER>
+template <int XR, int STAGES, int EPI, bool PAIRED, bool GROUPED, bool ROUTER, bool WIDE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     wstream_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const StreamArgs a) {
-  constexpr int H2 = PAIRED ? 2 : 1;            // 128-row weight halves per box column
+  constexpr int H2 = (PAIRED || WIDE) ? 2 : 1;  // 128-row weight halves per box column
+  constexpr int kTileOut = PAIRED ? kTileRows : H2 * kTileRows;  // output features per tile
   constexpr int kXSub = XR * 128;              // token rows of one box column
   constexpr int kXBytes = kXSub * kKSub;
   constexpr int kWStage = H2 * kWBytes;
@@ -422,10 +424,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int sb = 0; sb < kKSub; ++sb) {
           const int k0 = (kc * kKSub + sb) * kKBlk;
           uint8_t* d = wdst + sb * H2 * kWSub;
-          tma_load_2d(d, &wmap, k0, rbase + tile * kTileRows, &full[s], pol_w);
-          if (PAIRED)
-            tma_load_2d(d + kWSub, &wmap, k0, rbase + a.w_up_offset + tile * kTileRows, &full[s],
-                        pol_w);
+          tma_load_2d(d, &wmap, k0, rbase + tile * kTileOut, &full[s], pol_w);
+          if (H2 == 2)
+            tma_load_2d(d + kWSub, &wmap, k0,
+                        rbase + (PAIRED ? a.w_up_offset + tile * kTileRows
+                                        : tile * kTileOut + kTileRows),
+                        &full[s], pol_w);
         }
       };
       auto issue_x = [&](int s, long long u, const GroupInfo& g_) {
@@ -539,9 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
     };
 
-    // One output: SwiGLU of the gate and up sums, or the plain sum.
-    auto emit = [&](int tile, int row, int t, float v0, float v1) {
-      const int n = tile * kTileRows + row;
+    // One output of tile row r (0 .. kTileOut-1): SwiGLU of the gate sum v0
+    // and the up sum v1, or the plain sum v0.
+    auto emit = [&](int tile, int r, int t, float v0, float v1) {
+      const int n = tile * kTileOut + r;
       if (n >= a.nout) return;
       if (PAIRED) store_swiglu(a, gi, t, n, v0, v1);
       else store_out<EPI, GROUPED>(a, gi, t, n, v0);
@@ -554,8 +559,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int r = 0; r < 4; ++r)
 #pragma unroll
-          for (int t = 0; t < 2; ++t)
-            if (t < gi.c) emit(tile, 16 * w + rho + 4 * r, t, dacc[0][r][t], dacc[H2 - 1][r][t]);
+          for (int t = 0; t < 2; ++t) {
+            if (t >= gi.c) continue;
+            const int row = 16 * w + rho + 4 * r;
+            if (PAIRED) {
+              emit(tile, row, t, dacc[0][r][t], dacc[1][r][t]);
+            } else {
+#pragma unroll
+              for (int h = 0; h < H2; ++h) emit(tile, h * kTileRows + row, t, dacc[h][r][t], 0.f);
+            }
+          }
         return;
       }
 #pragma unroll
@@ -564,8 +577,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int hh = 0; hh < 2; ++hh) {
           const int t = tg * 8 + 2 * tq + hh;
           if (t >= gi.c) continue;
-          emit(tile, 16 * w + gq, t, macc[0][tg][hh], macc[H2 - 1][tg][hh]);
-          emit(tile, 16 * w + gq + 8, t, macc[0][tg][2 + hh], macc[H2 - 1][tg][2 + hh]);
+          if (PAIRED) {
+            emit(tile, 16 * w + gq, t, macc[0][tg][hh], macc[1][tg][hh]);
+            emit(tile, 16 * w + gq + 8, t, macc[0][tg][2 + hh], macc[1][tg][2 + hh]);
+          } else {
+#pragma unroll
+            for (int h = 0; h < H2; ++h) {
+              emit(tile, h * kTileRows + 16 * w + gq, t, macc[h][tg][hh], 0.f);
+              emit(tile, h * kTileRows + 16 * w + gq + 8, t, macc[h][tg][2 + hh], 0.f);
+            }
+          }
         }
     };
 
