@@ -192,11 +192,16 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
   // token rows per stage of the CUDA-core / mma.sync kernel; the tcgen05
   // kernel's partial tiles always hold 64 token columns
   const int xr = regime == DEC_REGIME_TC ? 64 : regime == DEC_REGIME_SMALLM ? 8 : (M <= 16 ? 16 : 64);
-  const long long tiles = (N + 127) / 128;
+  // 256-row tiles with 64 KB stages stream faster; they are used when every
+  // CTA still gets ten or more stages of work (so the split stays balanced).
+  const long long wide_units = ((N + 255) / 256) * (long long)KB;
+  const bool wide = S == 0 && regime != DEC_REGIME_TC && xr <= 16 && wide_units >= 10LL * s->sms;
+  const long long tiles = wide ? (N + 255) / 256 : (N + 127) / 128;
   const long long T = tiles * KB;
   long long grid = S ? tiles * S : (T < s->sms ? T : s->sms);
   if (grid > T) grid = T;
-  if ((rc = ensure(s->ws_main, (size_t)grid * 2 * 128 * xr * sizeof(float), st))) return rc;
+  const size_t slot_rows = wide ? 256 : 128;
+  if ((rc = ensure(s->ws_main, (size_t)grid * 2 * slot_rows * xr * sizeof(float), st))) return rc;
   if ((rc = ensure(s->ctr_main, (size_t)tiles * sizeof(int), st))) return rc;
   Ctx cx = make_ctx(s, st);
   long long seff = (KB * grid + T - 1) / T;
@@ -207,6 +212,10 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
   if (regime == DEC_REGIME_TC)
     return counted(launch_dense_tc(cx, res != nullptr, x, W, res, y, M, N, K, (int)grid,
                                    (float*)s->ws_main.p, (int*)s->ctr_main.p));
+  if (wide)
+    return counted(launch_dense_wide(cx, xr, regime != DEC_REGIME_SMALLM, res != nullptr, x, W,
+                                     res, y, M, N, K, (int)grid, (float*)s->ws_main.p,
+                                     (int*)s->ctr_main.p));
   return counted(launch_dense(cx, xr, regime != DEC_REGIME_SMALLM, res != nullptr, x, W, res, y,
                               M, N, K, (int)grid,
                               (float*)s->ws_main.p, (int*)s->ctr_main.p));
@@ -294,17 +303,17 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   float* ws = (float*)s->ws_main.p;
   int* ctr = (int*)s->ctr_main.p;
   // Shared expert: forked to the side stream so that it streams its weights
-  // while the router, a short latency-bound kernel on a third of the SMs,
+  // while the router, a short latency-bound kernel on a sixth of the SMs,
   // runs on the main stream. It gets the other SMs, and the routed experts
   // start only after both have finished: their work is split statically
   // across all SMs, so nothing else should hold an SM while they run.
-  const int router_grid = s->sms / 3 > 0 ? s->sms / 3 : 1;
+  const int rgrid = router_grid(s->sms);
   if (shared) {
     if (cudaEventRecord(s->ev_fork, st) != cudaSuccess) return DEC_ECUDA;
     if (cudaStreamWaitEvent(s->side, s->ev_fork, 0) != cudaSuccess) return DEC_ECUDA;
     Ctx sx = make_ctx(s, s->side);
     sx.pdl = false;
-    const int sgrid = s->sms - router_grid > 0 ? s->sms - router_grid : 1;
+    const int sgrid = s->sms - rgrid > 0 ? s->sms - rgrid : 1;
     if ((rc = counted(launch_shared_w13(sx, x, Ws13, M, H, I, s->mb, sgrid, (float*)s->ws_side.p,
                                         (int*)s->ctr_side.p))))
       return rc;

@@ -9,36 +9,38 @@
 
 namespace dg {
 
-template <int XR>
+template <int XR, bool WIDE>
 constexpr int dense_stages() {
-  return XR == 8 ? 6 : XR == 16 ? 6 : 4;
+  return WIDE ? 3 : (XR == 8 ? 6 : XR == 16 ? 6 : 4);
 }
 
-template <int XR>
+template <int XR, bool WIDE>
 constexpr int dense_smem() {
-  return wstream_smem(XR, dense_stages<XR>(), 0);
+  return wstream_smem(XR, dense_stages<XR, WIDE>(), 0, WIDE);
 }
 
-template <int XR, int EPI>
+// WIDE: 256-row output tiles, 64 KB weight stages (two 128-row halves).
+template <int XR, int EPI, bool WIDE = false>
 static cudaError_t run_dense(const Ctx& cx, bool mma, const void* x, const void* W, const void* res,
                              void* y, int M, int N, int K, int grid, float* ws, int* ctr) {
-  constexpr int S = dense_stages<XR>();
-  constexpr int SMEM = dense_smem<XR>();
+  constexpr int S = dense_stages<XR, WIDE>();
+  constexpr int SMEM = dense_smem<XR, WIDE>();
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
-  auto kern = wstream_kernel<XR, S, EPI, false, false, false>;
+  auto kern = wstream_kernel<XR, S, EPI, false, false, false, WIDE>;
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = allow_smem(kern, SMEM);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
+  constexpr int kTile = WIDE ? 2 * kTileRows : kTileRows;
   CUtensorMap wmap, xmap;
   if (!make_tmap(&wmap, W, (uint64_t)N, (uint64_t)K, kTileRows, true)) return cudaErrorInvalidValue;
   if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)K, XR, false)) return cudaErrorInvalidValue;
   StreamArgs a = {};
   a.K = K;
   a.KB = (K + kKChunk - 1) / kKChunk;
-  a.TILES = (N + kTileRows - 1) / kTileRows;
+  a.TILES = (N + kTile - 1) / kTile;
   a.nout = N;
   a.M = M;
   a.mma_min_tokens = mma ? 1 : 1 << 30;
@@ -50,6 +52,20 @@ static cudaError_t run_dense(const Ctx& cx, bool mma, const void* x, const void*
   a.status = cx.status;
   a.timeout_ns = cx.timeout_ns;
   return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
+}
+
+cudaError_t launch_dense_wide(const Ctx& cx, int xr, bool mma, bool residual, const void* x,
+                              const void* W, const void* res, void* y, int M, int N, int K,
+                              int grid, float* ws, int* ctr) {
+  if (xr == 8)
+    return residual
+               ? run_dense<8, EPI_BF16_RES, true>(cx, mma, x, W, res, y, M, N, K, grid, ws, ctr)
+               : run_dense<8, EPI_BF16, true>(cx, mma, x, W, res, y, M, N, K, grid, ws, ctr);
+  if (xr == 16)
+    return residual
+               ? run_dense<16, EPI_BF16_RES, true>(cx, mma, x, W, res, y, M, N, K, grid, ws, ctr)
+               : run_dense<16, EPI_BF16, true>(cx, mma, x, W, res, y, M, N, K, grid, ws, ctr);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_dense(const Ctx& cx, int xr, bool mma, bool residual, const void* x,

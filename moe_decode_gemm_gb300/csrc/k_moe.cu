@@ -78,10 +78,10 @@ cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, i
   a.route.done = b.done;
   a.route.total_tiles = a.TILES;
   // The router streams only E*H bf16 (5.5 MB for 384 x 7168) and is latency
-  // bound: a third of the SMs keeps the number of CTAs per output tile, and so
+  // bound: a sixth of the SMs keeps the number of CTAs per output tile, and so
   // the split-K fixup, small.
   const long long T = (long long)a.TILES * a.KB;
-  const int cap = cx.sms / 3 > 0 ? cx.sms / 3 : 1;  // the shared expert uses the other SMs
+  const int cap = router_grid(cx.sms);  // the shared expert uses the other SMs
   const int grid = (int)(T < cap ? T : cap);
   return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
 }

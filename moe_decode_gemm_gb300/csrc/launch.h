@@ -27,6 +27,12 @@ cudaError_t launch_dense(const Ctx& cx, int xr, bool mma, bool residual, const v
                          const void* W, const void* res, void* y, int M, int N, int K, int grid,
                          float* ws, int* ctr);
 
+// Same with 256-row output tiles and 64 KB weight stages (xr 8 or 16): for
+// matrices large enough that every CTA gets ten or more stages of work.
+cudaError_t launch_dense_wide(const Ctx& cx, int xr, bool mma, bool residual, const void* x,
+                              const void* W, const void* res, void* y, int M, int N, int K,
+                              int grid, float* ws, int* ctr);
+
 // tcgen05 projection for 16 <= M <= 64.
 cudaError_t launch_dense_tc(const Ctx& cx, bool residual, const void* x, const void* W,
                             const void* res, void* y, int M, int N, int K, int grid, float* ws,
@@ -47,6 +53,9 @@ struct MoeBufs {
   uint16_t* hs;    // [M, I]
   float* s;        // [M, H]
 };
+
+// CTAs of the router kernel (the rest of the SMs stream the shared expert).
+inline int router_grid(int sms) { return sms / 6 > 0 ? sms / 6 : 1; }
 
 cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E, int k,
                           int32_t* idx_user, float* w_user, const MoeBufs& b, float* ws, int* ctr);

@@ -142,8 +142,16 @@ __device__ __forceinline__ void store_swiglu(const StreamArgs& a, const GroupInf
 }
 
 // ------------------------------------------------------------------ routing tail
+// Order-preserving map of a float to uint32 (larger float, larger key).
+__device__ __forceinline__ uint32_t float_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// `stage`: shared memory that can hold the M x E router scores (the pipeline
+// ring, idle by now), or null to read them from global memory.
 template <int NT>
-__device__ void route_tail(const RouteArgs& r, int ct, uint8_t* scratch) {
+__device__ void route_tail(const RouteArgs& r, int ct, uint8_t* scratch, float* stage) {
   // scratch: masks [E] u64 | idx [M*k] int | g [M*k] float | cnt/off [E+1] int | flags
   const int M = r.M, E = r.E, K = r.k;
   unsigned long long* mask = reinterpret_cast<unsigned long long*>(scratch);
@@ -155,42 +163,52 @@ __device__ void route_tail(const RouteArgs& r, int ct, uint8_t* scratch) {
   const int warp = ct >> 5, lane = ct & 31;
   const int nwarps = NT / 32;
 
-  // 1) top-k per token: one warp per token, each lane holds E/32 logits.
+  // 0) all scores into shared memory in one pass (coalesced)
+  const float* scores = r.logits;
+  if (stage) {
+    const int n = M * E;
+    for (int i = ct; i < n; i += NT) stage[i] = __ldcg(r.logits + i);
+    named_bar_sync(1, NT);
+    scores = stage;
+  }
+  const int per = (E + 31) / 32;  // scores per lane (E <= 1024)
+
+  // 1) top-k per token, one warp per token. Each round takes every lane's
+  // best remaining score, then the warp maximum of an order-preserving key
+  // and, among lanes holding that maximum, the smallest expert index
+  // (ties: smaller index first).
   for (int m = warp; m < M; m += nwarps) {
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const int e = lane + 32 * j;
-      v[j] = (e < E) ? __ldcg(r.logits + (long long)m * E + e) : -INFINITY;
+      v[j] = (j < per && e < E) ? scores[(long long)m * E + e] : -INFINITY;
     }
-    uint32_t taken = 0;
     float selv0 = 0.f, myv = 0.f;
     int mye = 0;
     for (int j = 0; j < K; ++j) {
       float bv = -INFINITY;
-      int be = 0x7fffffff;
+      int bj = 0;
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const int e = lane + 32 * jj;
-        if (e < E && !((taken >> jj) & 1u) && (v[jj] > bv || (v[jj] == bv && e < be))) {
+      for (int jj = 0; jj < 32; ++jj)
+        if (jj < per && v[jj] > bv) {  // strict: the smallest jj (smallest index) on ties
           bv = v[jj];
-          be = e;
+          bj = jj;
         }
-      }
+      const uint32_t key = float_key(bv);
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+      const uint32_t cand = (key == kmax) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
+      const uint32_t emin = __reduce_min_sync(0xffffffffu, cand);
+      const float wv = __shfl_sync(0xffffffffu, bv, emin & 31);
+      if ((int)(emin & 31) == lane) {
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
-        }
+        for (int jj = 0; jj < 32; ++jj)
+          if (jj == bj) v[jj] = -INFINITY;
       }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (j == 0) selv0 = bv;
+      if (j == 0) selv0 = wv;
       if (lane == j) {
-        myv = bv;
-        mye = be;
+        myv = wv;
+        mye = (int)emin;
       }
     }
     // gates: exp(l_j - l_max) / sum_j' exp(l_j' - l_max), summed j = 0..k-1
@@ -679,7 +697,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(1, kNCW * 32);
         if (s_flags[2]) {
           __threadfence();
-          route_tail<kNCW * 32>(a.route, ct, scratch);
+          // the ring is idle now (every unit of every CTA has been consumed)
+          const bool fits = (long long)a.route.M * a.route.E * 4 <= (long long)STAGES * kStageBytes;
+          route_tail<kNCW * 32>(a.route, ct, scratch,
+                                fits ? reinterpret_cast<float*>(smem) : nullptr);
         }
       }
       named_bar_sync(1, kNCW * 32);  // partial slots and flags may be reused next tile
