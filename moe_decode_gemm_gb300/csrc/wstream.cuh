@@ -151,7 +151,7 @@ __device__ __forceinline__ uint32_t float_key(float f) {
 // `stage`: shared memory that can hold the M x E router scores (the pipeline
 // ring, idle by now), or null to read them from global memory.
 template <int NT>
-__device__ void route_tail(const RouteArgs& r, int ct, uint8_t* scratch, float* stage) {
+__device__ __noinline__ void route_tail(const RouteArgs& r, int ct, uint8_t* scratch, float* stage) {
   // scratch: masks [E] u64 | idx [M*k] int | g [M*k] float | cnt/off [E+1] int | flags
   const int M = r.M, E = r.E, K = r.k;
   unsigned long long* mask = reinterpret_cast<unsigned long long*>(scratch);
@@ -163,48 +163,70 @@ __device__ void route_tail(const RouteArgs& r, int ct, uint8_t* scratch, float* 
   const int warp = ct >> 5, lane = ct & 31;
   const int nwarps = NT / 32;
 
-  // 0) all scores into shared memory in one pass (coalesced)
+  // 0) all scores into shared memory, 16-byte loads, 8 in flight per thread
   const float* scores = r.logits;
   if (stage) {
     const int n = M * E;
-    for (int i = ct; i < n; i += NT) stage[i] = __ldcg(r.logits + i);
+    const int n4 = n / 4;
+    const float4* src4 = reinterpret_cast<const float4*>(r.logits);
+    float4* dst4 = reinterpret_cast<float4*>(stage);
+    for (int i0 = ct; i0 < n4; i0 += NT * 8) {
+      float4 t[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (i0 + q * NT < n4) t[q] = __ldcg(src4 + i0 + q * NT);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (i0 + q * NT < n4) dst4[i0 + q * NT] = t[q];
+    }
+    for (int i = n4 * 4 + ct; i < n; i += NT) stage[i] = __ldcg(r.logits + i);
     named_bar_sync(1, NT);
     scores = stage;
   }
   const int per = (E + 31) / 32;  // scores per lane (E <= 1024)
 
-  // 1) top-k per token, one warp per token. Each round takes every lane's
-  // best remaining score, then the warp maximum of an order-preserving key
-  // and, among lanes holding that maximum, the smallest expert index
-  // (ties: smaller index first).
+  // 1) top-k per token, one warp per token. A lane holds its scores
+  // e = lane + 32 j as order-preserving keys (0 = none or already taken).
+  // Each round: the lane's best key by a compare tree (smaller j on ties),
+  // then the warp's maximum key and, among lanes holding it, the smallest
+  // expert index (ties: smaller index first).
   for (int m = warp; m < M; m += nwarps) {
-    float v[32];
+    uint32_t kv[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const int e = lane + 32 * j;
-      v[j] = (j < per && e < E) ? scores[(long long)m * E + e] : -INFINITY;
+      kv[j] = (j < per && e < E) ? float_key(scores[(long long)m * E + e]) : 0u;
     }
     float selv0 = 0.f, myv = 0.f;
     int mye = 0;
     for (int j = 0; j < K; ++j) {
-      float bv = -INFINITY;
-      int bj = 0;
+      uint32_t bk[16];
+      int bj[16];
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj)
-        if (jj < per && v[jj] > bv) {  // strict: the smallest jj (smallest index) on ties
-          bv = v[jj];
-          bj = jj;
+      for (int i = 0; i < 16; ++i) {
+        const bool left = kv[2 * i] >= kv[2 * i + 1];
+        bk[i] = left ? kv[2 * i] : kv[2 * i + 1];
+        bj[i] = left ? 2 * i : 2 * i + 1;
+      }
+#pragma unroll
+      for (int w2 = 8; w2 >= 1; w2 >>= 1)
+#pragma unroll
+        for (int i = 0; i < w2; ++i) {
+          const bool left = bk[2 * i] >= bk[2 * i + 1];
+          bk[i] = left ? bk[2 * i] : bk[2 * i + 1];
+          bj[i] = left ? bj[2 * i] : bj[2 * i + 1];
         }
-      const uint32_t key = float_key(bv);
-      const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
-      const uint32_t cand = (key == kmax) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk[0]);
+      const uint32_t cand = (bk[0] == kmax && kmax != 0u) ? (uint32_t)(lane + 32 * bj[0]) : 0xffffffffu;
       const uint32_t emin = __reduce_min_sync(0xffffffffu, cand);
-      const float wv = __shfl_sync(0xffffffffu, bv, emin & 31);
       if ((int)(emin & 31) == lane) {
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj)
-          if (jj == bj) v[jj] = -INFINITY;
+          if (jj == bj[0]) kv[jj] = 0u;
       }
+      // the chosen score, recovered from its key
+      const uint32_t u = (kmax & 0x80000000u) ? (kmax ^ 0x80000000u) : ~kmax;
+      const float wv = __uint_as_float(u);
       if (j == 0) selv0 = wv;
       if (lane == j) {
         myv = wv;
