@@ -239,7 +239,7 @@ static int moe_bufs(DevState* s, int M, int H, int E, int k, int I, cudaStream_t
   size_t o_ptok = off; off += al((size_t)Mx * kx * 4);
   size_t o_pof = off; off += al((size_t)Mx * kx * 4);
   size_t o_gate = off; off += al((size_t)Mx * kx * 4);
-  size_t o_done = off; off += al(4);
+  size_t o_topk = off; off += al((size_t)Mx * kx * 4);
   size_t o_xs = off; off += al((size_t)Mx * kx * Hx * 2);
   size_t o_h = off; off += al((size_t)Mx * kx * Ix * 2);
   size_t o_o = off; off += al((size_t)Mx * kx * Hx * 4);
@@ -255,7 +255,7 @@ static int moe_bufs(DevState* s, int M, int H, int E, int k, int I, cudaStream_t
   s->mb.pair_tok = (int*)(b + o_ptok);
   s->mb.pair_of = (int*)(b + o_pof);
   s->mb.gate = (float*)(b + o_gate);
-  s->mb.done = (int*)(b + o_done);
+  s->mb.topk = (int*)(b + o_topk);
   s->mb.xs = (uint16_t*)(b + o_xs);
   s->mb.h = (uint16_t*)(b + o_h);
   s->mb.o = (float*)(b + o_o);
@@ -325,11 +325,12 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   }
   {
     ProbeScope p(3, st);
-    if ((rc = counted(launch_router(cx, x, Wr, M, H, E, topk, topk_idx, topk_w, s->mb, ws,
+    if ((rc = counted(launch_router(cx, x, Wr, M, H, E, s->mb, ws,
                                     ctr + (size_t)max_groups * maxt))))
       return rc;
   }
-  if ((rc = counted(launch_gather(cx, x, M, H, topk, s->mb)))) return rc;
+  if ((rc = counted(launch_topk(cx, M, E, topk, topk_idx, topk_w, s->mb)))) return rc;
+  if ((rc = counted(launch_gather(cx, x, M, H, E, topk, s->mb)))) return rc;
   if (shared) {
     // join: the gate/up kernel then depends on two streams, so it is
     // launched without the programmatic (early-start) dependency
@@ -440,7 +441,6 @@ int dec_sync_check(void* stream) {
     cudaMemset(s->status, 0, sizeof(int));
     if (s->ctr_main.p) cudaMemset(s->ctr_main.p, 0, s->ctr_main.bytes);
     if (s->ctr_side.p) cudaMemset(s->ctr_side.p, 0, s->ctr_side.bytes);
-    if (s->mb.done) cudaMemset(s->mb.done, 0, sizeof(int));
     cudaDeviceSynchronize();
     return DEC_ETIMEOUT;
   }

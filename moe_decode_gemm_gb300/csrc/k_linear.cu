@@ -26,7 +26,7 @@ static cudaError_t run_dense(const Ctx& cx, bool mma, const void* x, const void*
   constexpr int S = dense_stages<XR, WIDE>();
   constexpr int SMEM = dense_smem<XR, WIDE>();
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
-  auto kern = wstream_kernel<XR, S, EPI, false, false, false, WIDE>;
+  auto kern = wstream_kernel<XR, S, EPI, false, false, WIDE>;
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = allow_smem(kern, SMEM);

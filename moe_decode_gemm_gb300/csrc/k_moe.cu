@@ -1,8 +1,8 @@
-// k_moe.cu -- the MoE decode block's kernels: router scoring with the
-// top-k / gate / expert-gather tail, the routed experts' gate-up (SwiGLU) and
-// down projections over the selected experts only, the shared expert, and the
-// gate-weighted combine. Plus the residual add, the L2 prefetch kernel and the
-// failure-detection self test.
+// k_moe.cu -- the MoE decode block's kernels: router scoring, top-k with
+// renormalised gates, the expert-gather schedule and token gather, the routed
+// experts' gate-up (SwiGLU) and down projections over the selected experts
+// only, the shared expert, and the gate-weighted combine. Plus the residual
+// add, the L2 prefetch kernel and the failure-detection self test.
 // "vLLM 如何用智能体辅助优化 Kimi K3 解码性能", Part 1 §3 "改进 MoE 调度与重叠" and
 // Part 1 §4 "将即将使用的权重预取到缓存".
 #include <utility>
@@ -13,13 +13,11 @@
 
 namespace dg {
 
-constexpr int kMoeXR = 64;                  // router and shared expert: every token (M <= 64)
+constexpr int kMoeXR = 64;                  // shared expert: every token (M <= 64)
 constexpr int kMoeStages = 4;
-constexpr int kRouterStages = 3;
 constexpr int kExpertXR = kGroupTokens;     // routed experts: one group's tokens
 constexpr int kExpertPairStages = 3;        // gate/up: 64 KB stages (gate and up halves)
 constexpr int kSharedPairStages = 2;        // shared gate/up: 64 KB + 16 KB of tokens
-constexpr int kRouteScratch = 36 * 1024;
 
 constexpr int moe_smem(int stages, int extra) { return wstream_smem(kMoeXR, stages, extra); }
 constexpr int expert_pair_smem() { return wstream_smem(kExpertXR, kExpertPairStages, 0, true); }
@@ -42,17 +40,22 @@ static StreamArgs base_args(const Ctx& cx, float* ws, int* ctr) {
   return a;
 }
 
-cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E, int k,
-                          int32_t* idx_user, float* w_user, const MoeBufs& b, float* ws, int* ctr) {
-  constexpr int SMEM = moe_smem(kRouterStages, kRouteScratch);
+// ------------------------------------------------------------------ router
+// logits[m, e] = x[m]·Wr[e] in fp32 (not rounded): the weight-streaming kernel
+// with fp32 output, token rows per stage sized to M.
+template <int XR>
+static cudaError_t run_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E,
+                              const MoeBufs& b, float* ws, int* ctr) {
+  constexpr int STAGES = XR == 64 ? 4 : 6;
+  constexpr int SMEM = wstream_smem(XR, STAGES, 0);
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
-  auto kern = wstream_kernel<kMoeXR, kRouterStages, EPI_F32, false, false, true>;
+  auto kern = wstream_kernel<XR, STAGES, EPI_F32, false, false>;
   static bool done = false;
   cudaError_t e = smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;
   CUtensorMap wmap, xmap;
   if (!make_tmap(&wmap, Wr, (uint64_t)E, (uint64_t)H, kTileRows, true)) return cudaErrorInvalidValue;
-  if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)H, kMoeXR, false)) return cudaErrorInvalidValue;
+  if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)H, XR, false)) return cudaErrorInvalidValue;
   StreamArgs a = base_args(cx, ws, ctr);
   a.K = H;
   a.KB = (H + kKChunk - 1) / kKChunk;
@@ -61,36 +64,231 @@ cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, i
   a.M = M;
   a.out = b.logits;
   a.ldo = E;
-  a.done = b.done;
-  a.total_tiles_dense = a.TILES;
-  a.route.M = M;
-  a.route.E = E;
-  a.route.k = k;
-  a.route.logits = b.logits;
-  a.route.idx_user = idx_user;
-  a.route.w_user = w_user;
-  a.route.nact = b.nact;
-  a.route.grp_exp = b.grp_exp;
-  a.route.grp_off = b.grp_off;
-  a.route.pair_tok = b.pair_tok;
-  a.route.pair_of = b.pair_of;
-  a.route.gate = b.gate;
-  a.route.done = b.done;
-  a.route.total_tiles = a.TILES;
   // The router streams only E*H bf16 (5.5 MB for 384 x 7168) and is latency
   // bound: a sixth of the SMs keeps the number of CTAs per output tile, and so
-  // the split-K fixup, small.
+  // the split-K fixup, small; the shared expert streams on the other SMs.
   const long long T = (long long)a.TILES * a.KB;
-  const int cap = router_grid(cx.sms);  // the shared expert uses the other SMs
+  const int cap = router_grid(cx.sms);
   const int grid = (int)(T < cap ? T : cap);
   return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
+}
+
+cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E,
+                          const MoeBufs& b, float* ws, int* ctr) {
+  if (M <= 8) return run_router<8>(cx, x, Wr, M, H, E, b, ws, ctr);
+  if (M <= 16) return run_router<16>(cx, x, Wr, M, H, E, b, ws, ctr);
+  return run_router<64>(cx, x, Wr, M, H, E, b, ws, ctr);
+}
+
+// ------------------------------------------------------------------ top-k
+// Order-preserving map of a float to uint32 (larger float, larger key); 0 is
+// below every float's key.
+__device__ __forceinline__ uint32_t float_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
+}
+
+// One warp per token: the topk largest scores, ordered by (value desc,
+// index asc), and gates g_j = exp(l_j - l_max) / sum_j' exp(l_j' - l_max)
+// summed j = 0..topk-1. A lane holds scores e = lane + 32 j, j < PER, as keys
+// in registers; each round takes the lane's best, the warp's maximum key and,
+// among lanes holding it, the smallest index.
+template <int PER>
+__global__ void __launch_bounds__(32) topk_kernel(const float* __restrict__ logits, int E, int K,
+                                                  int* __restrict__ idx, float* __restrict__ gate,
+                                                  int32_t* idx_user, float* w_user) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int m = blockIdx.x, lane = threadIdx.x;
+  const float* row = logits + (long long)m * E;
+  uint32_t kv[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = lane + 32 * j;
+    kv[j] = e < E ? float_key(__ldcg(row + e)) : 0u;
+  }
+  float selv0 = 0.f, myv = 0.f;
+  int mye = 0;
+  for (int j = 0; j < K; ++j) {
+    uint32_t bk = kv[0];
+    int bj = 0;
+#pragma unroll
+    for (int jj = 1; jj < PER; ++jj)
+      if (kv[jj] > bk) {  // strict: the smallest jj (smallest index) on ties
+        bk = kv[jj];
+        bj = jj;
+      }
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t cand = (bk == kmax && kmax != 0u) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
+    const uint32_t emin = __reduce_min_sync(0xffffffffu, cand);
+    if ((int)(emin & 31) == lane) {
+#pragma unroll
+      for (int jj = 0; jj < PER; ++jj)
+        if (jj == bj) kv[jj] = 0u;
+    }
+    const float wv = key_float(kmax);
+    if (j == 0) selv0 = wv;
+    if (lane == j) {
+      myv = wv;
+      mye = (int)emin;
+    }
+  }
+  const float w = (lane < K) ? expf(myv - selv0) : 0.f;
+  float denom = 0.f;
+  for (int j = 0; j < K; ++j) denom += __shfl_sync(0xffffffffu, w, j);
+  if (lane < K) {
+    const float g = w / denom;
+    idx[m * K + lane] = mye;
+    gate[m * K + lane] = g;
+    if (idx_user) idx_user[m * K + lane] = mye;
+    if (w_user) w_user[m * K + lane] = g;
+  }
+}
+
+cudaError_t launch_topk(const Ctx& cx, int M, int E, int k, int32_t* idx_user, float* w_user,
+                        const MoeBufs& b) {
+  const int per = (E + 31) / 32;
+  auto go = [&](auto kern) {
+    return launch_k(kern, dim3(M), dim3(32), 0, cx.stream, cx.pdl, (const float*)b.logits, E, k,
+                    b.topk, b.gate, idx_user, w_user);
+  };
+  if (per <= 4) return go(topk_kernel<4>);
+  if (per <= 8) return go(topk_kernel<8>);
+  if (per <= 12) return go(topk_kernel<12>);
+  if (per <= 16) return go(topk_kernel<16>);
+  return go(topk_kernel<32>);
+}
+
+// ------------------------------------------------------------------ schedule + gather
+// Every CTA builds the expert-gather schedule from the M x k chosen indices
+// (cheap: at most 2048 pairs over at most 1024 experts); CTA 0 publishes it:
+//   groups  : experts with at least one token, in expert order, split into
+//             groups of at most kGroupTokens tokens (grp_exp, grp_off, nact);
+//   pairs   : (token, slot) pairs in expert order, by token within an expert
+//             (pair_tok = token of pair p, pair_of[m*k + j] = pair of (m, j)).
+// Then all CTAs copy xs[p] = x[pair_tok[p]] (16-byte vectors), so each expert
+// group's token rows are contiguous for the expert kernels' TMA boxes.
+constexpr int kSchedThreads = 256;
+constexpr int kMaxE = 1024;
+constexpr int kMaxPairs = 64 * 32;
+
+__global__ void __launch_bounds__(kSchedThreads) schedule_gather_kernel(
+    const uint4* __restrict__ x, const int* __restrict__ topk, int M, int E, int K, int row_vecs,
+    uint4* __restrict__ xs, int* nact, int* grp_exp, int* grp_off, int* pair_tok, int* pair_of) {
+  __shared__ unsigned long long s_mask[kMaxE];
+  __shared__ int s_idx[kMaxPairs];
+  __shared__ int s_off[kMaxE];
+  __shared__ int s_tok[kMaxPairs];
+  __shared__ int s_warp[64];
+  griddep_launch_dependents();
+  griddep_wait();
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int P = M * K;
+  const bool publish = blockIdx.x == 0;
+  for (int p = t; p < P; p += kSchedThreads) s_idx[p] = topk[p];
+  for (int e = t; e < E; e += kSchedThreads) s_mask[e] = 0ull;
+  __syncthreads();
+  for (int p = t; p < P; p += kSchedThreads) atomicOr(&s_mask[s_idx[p]], 1ull << (p / K));
+  __syncthreads();
+  // exclusive scans over experts of token counts and of group counts
+  constexpr int PER = kMaxE / kSchedThreads;  // 4 experts per thread
+  int cnt[PER], grp[PER], csum = 0, gsum = 0;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int e = t * PER + q;
+    cnt[q] = (e < E) ? __popcll(s_mask[e]) : 0;
+    grp[q] = (cnt[q] + kGroupTokens - 1) / kGroupTokens;
+    csum += cnt[q];
+    gsum += grp[q];
+  }
+  int cinc = csum, ginc = gsum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int c2 = __shfl_up_sync(0xffffffffu, cinc, off);
+    const int g2 = __shfl_up_sync(0xffffffffu, ginc, off);
+    if (lane >= off) {
+      cinc += c2;
+      ginc += g2;
+    }
+  }
+  if (lane == 31) {
+    s_warp[warp] = cinc;
+    s_warp[32 + warp] = ginc;
+  }
+  __syncthreads();
+  int cpre = 0, gpre = 0;
+  for (int w2 = 0; w2 < warp; ++w2) {
+    cpre += s_warp[w2];
+    gpre += s_warp[32 + w2];
+  }
+  cpre += cinc - csum;
+  gpre += ginc - gsum;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int e = t * PER + q;
+    if (e < E) {
+      s_off[e] = cpre;
+      if (publish)
+        for (int j = 0; j < grp[q]; ++j) {
+          grp_exp[gpre + j] = e;
+          grp_off[gpre + j] = cpre + j * kGroupTokens;
+        }
+    }
+    cpre += cnt[q];
+    gpre += grp[q];
+  }
+  if (publish && t == kSchedThreads - 1) {
+    int total = 0;
+    for (int w2 = 0; w2 < kSchedThreads / 32; ++w2) total += s_warp[32 + w2];
+    grp_off[total] = P;
+    *nact = total;
+  }
+  __syncthreads();
+  // pairs: position of (m, j) among expert e's pairs = tokens below m that chose e
+  for (int p = t; p < P; p += kSchedThreads) {
+    const int m = p / K;
+    const int e = s_idx[p];
+    const unsigned long long below = (m == 0) ? 0ull : (s_mask[e] & ((1ull << m) - 1ull));
+    const int pos = s_off[e] + __popcll(below);
+    s_tok[pos] = m;
+    if (publish) {
+      pair_tok[pos] = m;
+      pair_of[p] = pos;
+    }
+  }
+  __syncthreads();
+  // gather this CTA's share of the token rows
+  const long long total = (long long)P * row_vecs;
+  for (long long v = blockIdx.x * (long long)kSchedThreads + t; v < total;
+       v += (long long)gridDim.x * kSchedThreads) {
+    const int p = (int)(v / row_vecs);
+    const int c = (int)(v - (long long)p * row_vecs);
+    xs[v] = x[(long long)s_tok[p] * row_vecs + c];
+  }
+}
+
+cudaError_t launch_gather(const Ctx& cx, const void* x, int M, int H, int E, int k,
+                          const MoeBufs& b) {
+  const int row_vecs = H / 8;
+  const long long total = (long long)M * k * row_vecs;
+  long long grid = (total + kSchedThreads - 1) / kSchedThreads;
+  if (grid > cx.sms) grid = cx.sms;
+  if (grid < 1) grid = 1;
+  return launch_k(schedule_gather_kernel, dim3((unsigned)grid), dim3(kSchedThreads), 0, cx.stream,
+                  cx.pdl, reinterpret_cast<const uint4*>(x), (const int*)b.topk, M, E, k,
+                  row_vecs, reinterpret_cast<uint4*>(b.xs), b.nact, b.grp_exp, b.grp_off,
+                  b.pair_tok, b.pair_of);
 }
 
 cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, int M, int H, int E,
                                int k, int I, const MoeBufs& b, float* ws, int* ctr) {
   constexpr int SMEM = expert_pair_smem();
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
-  auto kern = wstream_kernel<kExpertXR, kExpertPairStages, EPI_SWIGLU, true, true, false>;
+  auto kern = wstream_kernel<kExpertXR, kExpertPairStages, EPI_SWIGLU, true, true>;
   static bool done = false;
   cudaError_t e = smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;
@@ -119,7 +317,7 @@ cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E
                               const MoeBufs& b, float* ws, int* ctr) {
   // 256-row output tiles: two 128-row halves, 64 KB weight stages
   constexpr int SMEM = expert_pair_smem();
-  auto kern = wstream_kernel<kExpertXR, kExpertPairStages, EPI_F32, false, true, false, true>;
+  auto kern = wstream_kernel<kExpertXR, kExpertPairStages, EPI_F32, false, true, true>;
   static bool done = false;
   cudaError_t e = smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;
@@ -146,7 +344,7 @@ cudaError_t launch_shared_w13(const Ctx& cx, const void* x, const void* Ws13, in
                               const MoeBufs& b, int grid, float* ws, int* ctr) {
   constexpr int SMEM = wstream_smem(kMoeXR, kSharedPairStages, 0, true);
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
-  auto kern = wstream_kernel<kMoeXR, kSharedPairStages, EPI_SWIGLU, true, false, false>;
+  auto kern = wstream_kernel<kMoeXR, kSharedPairStages, EPI_SWIGLU, true, false>;
   static bool done = false;
   cudaError_t e = smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;
@@ -171,7 +369,7 @@ cudaError_t launch_shared_w13(const Ctx& cx, const void* x, const void* Ws13, in
 cudaError_t launch_shared_w2(const Ctx& cx, const void* Ws2, int M, int H, int I, const MoeBufs& b,
                              int grid, float* ws, int* ctr) {
   constexpr int SMEM = moe_smem(kMoeStages, 0);
-  auto kern = wstream_kernel<kMoeXR, kMoeStages, EPI_F32, false, false, false>;
+  auto kern = wstream_kernel<kMoeXR, kMoeStages, EPI_F32, false, false>;
   static bool done = false;
   cudaError_t e = smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;
@@ -189,36 +387,6 @@ cudaError_t launch_shared_w2(const Ctx& cx, const void* Ws2, int M, int H, int I
   const long long T = (long long)a.TILES * a.KB;
   if (grid > T) grid = (int)T;
   return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
-}
-
-// ------------------------------------------------------------------ token gather
-// xs[p] = x[pair_tok[p]] for every (token, slot) pair p: the routed experts'
-// token rows in expert order, so that each expert group's rows are contiguous
-// and reach shared memory as one TMA box. 16-byte vectors, grid-stride.
-__global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x,
-                                                     const int* __restrict__ pair_tok,
-                                                     uint4* __restrict__ xs, int npairs,
-                                                     int row_vecs) {
-  griddep_launch_dependents();
-  griddep_wait();
-  const long long total = (long long)npairs * row_vecs;
-  for (long long v = blockIdx.x * (long long)blockDim.x + threadIdx.x; v < total;
-       v += (long long)gridDim.x * blockDim.x) {
-    const int p = (int)(v / row_vecs);
-    const int c = (int)(v - (long long)p * row_vecs);
-    xs[v] = x[(long long)pair_tok[p] * row_vecs + c];
-  }
-}
-
-cudaError_t launch_gather(const Ctx& cx, const void* x, int M, int H, int k, const MoeBufs& b) {
-  const int row_vecs = H / 8;
-  const long long total = (long long)M * k * row_vecs;
-  long long grid = (total + 255) / 256;
-  if (grid > 2 * cx.sms) grid = 2 * cx.sms;
-  if (grid < 1) grid = 1;
-  return launch_k(gather_kernel, dim3((unsigned)grid), dim3(256), 0, cx.stream, cx.pdl,
-                  reinterpret_cast<const uint4*>(x), (const int*)b.pair_tok,
-                  reinterpret_cast<uint4*>(b.xs), M * k, row_vecs);
 }
 
 // ------------------------------------------------------------------ combine

@@ -46,7 +46,7 @@ struct MoeBufs {
   int* pair_tok;   // [M*k]
   int* pair_of;    // [M*k]
   float* gate;     // [M*k]
-  int* done;
+  int* topk;       // [M*k] chosen experts
   uint16_t* xs;    // [M*k, H] token rows in expert-sorted pair order
   uint16_t* h;     // [M*k, I]
   float* o;        // [M*k, H]
@@ -57,9 +57,12 @@ struct MoeBufs {
 // CTAs of the router kernel (the rest of the SMs stream the shared expert).
 inline int router_grid(int sms) { return sms / 6 > 0 ? sms / 6 : 1; }
 
-cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E, int k,
-                          int32_t* idx_user, float* w_user, const MoeBufs& b, float* ws, int* ctr);
-cudaError_t launch_gather(const Ctx& cx, const void* x, int M, int H, int k, const MoeBufs& b);
+cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E,
+                          const MoeBufs& b, float* ws, int* ctr);
+cudaError_t launch_topk(const Ctx& cx, int M, int E, int k, int32_t* idx_user, float* w_user,
+                        const MoeBufs& b);
+cudaError_t launch_gather(const Ctx& cx, const void* x, int M, int H, int E, int k,
+                          const MoeBufs& b);
 cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, int M, int H, int E,
                                int k, int I, const MoeBufs& b, float* ws, int* ctr);
 cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E, int k, int I,

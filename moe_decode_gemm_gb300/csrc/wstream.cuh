@@ -48,22 +48,6 @@ constexpr int wstream_smem(int xr, int stages, int extra, bool paired = false) {
          4 * kMaxSlots + extra;
 }
 
-// Routing tail run by the CTA that completes the router's last logit tile.
-struct RouteArgs {
-  int M, E, k;
-  const float* logits;     // [M,E]
-  int32_t* idx_user;       // optional [M,k]
-  float* w_user;           // optional [M,k]
-  int* nact;               // number of active experts
-  int* grp_exp;            // [E] expert id of active group u
-  int* grp_off;            // [E+1] first pair of group u
-  int* pair_tok;           // [M*k] token of pair p (pairs grouped by expert)
-  int* pair_of;            // [M*k] pair index of (m, j)
-  float* gate;             // [M*k] gate of (m, j)
-  int* done;               // completed-tile counter (reset by the tail)
-  int total_tiles;
-};
-
 struct StreamArgs {
   int K, KB, TILES;
   int nout;                  // valid output features per group
@@ -82,9 +66,6 @@ struct StreamArgs {
   // split-K workspace
   float* ws;                 // [grid][2][128][XR] fp32 partial tiles
   int* ctr;                  // per output tile arrival counters (zero at rest)
-  int* done;                 // router only: completed tiles
-  int total_tiles_dense;     // router only
-  RouteArgs route;
   int* status;
   long long timeout_ns;
 };
@@ -142,178 +123,6 @@ __device__ __forceinline__ void store_swiglu(const StreamArgs& a, const GroupInf
 }
 
 // ------------------------------------------------------------------ routing tail
-// Order-preserving map of a float to uint32 (larger float, larger key).
-__device__ __forceinline__ uint32_t float_key(float f) {
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// `stage`: shared memory that can hold the M x E router scores (the pipeline
-// ring, idle by now), or null to read them from global memory.
-template <int NT>
-__device__ __noinline__ void route_tail(const RouteArgs& r, int ct, uint8_t* scratch, float* stage) {
-  // scratch: masks [E] u64 | idx [M*k] int | g [M*k] float | cnt/off [E+1] int | flags
-  const int M = r.M, E = r.E, K = r.k;
-  unsigned long long* mask = reinterpret_cast<unsigned long long*>(scratch);
-  int* s_idx = reinterpret_cast<int*>(mask + E);
-  float* s_g = reinterpret_cast<float*>(s_idx + M * K);
-  int* s_off = reinterpret_cast<int*>(s_g + M * K);      // [E+1]
-  int* s_act = s_off + (E + 1);                          // [E+1] active rank prefix
-  int* s_warp = s_act + (E + 1);                         // [2*32] warp totals
-  const int warp = ct >> 5, lane = ct & 31;
-  const int nwarps = NT / 32;
-
-  // 0) all scores into shared memory, 16-byte loads, 8 in flight per thread
-  const float* scores = r.logits;
-  if (stage) {
-    const int n = M * E;
-    const int n4 = n / 4;
-    const float4* src4 = reinterpret_cast<const float4*>(r.logits);
-    float4* dst4 = reinterpret_cast<float4*>(stage);
-    for (int i0 = ct; i0 < n4; i0 += NT * 8) {
-      float4 t[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (i0 + q * NT < n4) t[q] = __ldcg(src4 + i0 + q * NT);
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (i0 + q * NT < n4) dst4[i0 + q * NT] = t[q];
-    }
-    for (int i = n4 * 4 + ct; i < n; i += NT) stage[i] = __ldcg(r.logits + i);
-    named_bar_sync(1, NT);
-    scores = stage;
-  }
-  const int per = (E + 31) / 32;  // scores per lane (E <= 1024)
-
-  // 1) top-k per token, one warp per token. A lane holds its scores
-  // e = lane + 32 j as order-preserving keys (0 = none or already taken).
-  // Each round: the lane's best key by a compare tree (smaller j on ties),
-  // then the warp's maximum key and, among lanes holding it, the smallest
-  // expert index (ties: smaller index first).
-  for (int m = warp; m < M; m += nwarps) {
-    uint32_t kv[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int e = lane + 32 * j;
-      kv[j] = (j < per && e < E) ? float_key(scores[(long long)m * E + e]) : 0u;
-    }
-    float selv0 = 0.f, myv = 0.f;
-    int mye = 0;
-    for (int j = 0; j < K; ++j) {
-      uint32_t bk[16];
-      int bj[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const bool left = kv[2 * i] >= kv[2 * i + 1];
-        bk[i] = left ? kv[2 * i] : kv[2 * i + 1];
-        bj[i] = left ? 2 * i : 2 * i + 1;
-      }
-#pragma unroll
-      for (int w2 = 8; w2 >= 1; w2 >>= 1)
-#pragma unroll
-        for (int i = 0; i < w2; ++i) {
-          const bool left = bk[2 * i] >= bk[2 * i + 1];
-          bk[i] = left ? bk[2 * i] : bk[2 * i + 1];
-          bj[i] = left ? bj[2 * i] : bj[2 * i + 1];
-        }
-      const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk[0]);
-      const uint32_t cand = (bk[0] == kmax && kmax != 0u) ? (uint32_t)(lane + 32 * bj[0]) : 0xffffffffu;
-      const uint32_t emin = __reduce_min_sync(0xffffffffu, cand);
-      if ((int)(emin & 31) == lane) {
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj)
-          if (jj == bj[0]) kv[jj] = 0u;
-      }
-      // the chosen score, recovered from its key
-      const uint32_t u = (kmax & 0x80000000u) ? (kmax ^ 0x80000000u) : ~kmax;
-      const float wv = __uint_as_float(u);
-      if (j == 0) selv0 = wv;
-      if (lane == j) {
-        myv = wv;
-        mye = (int)emin;
-      }
-    }
-    // gates: exp(l_j - l_max) / sum_j' exp(l_j' - l_max), summed j = 0..k-1
-    const float w = (lane < K) ? expf(myv - selv0) : 0.f;
-    float denom = 0.f;
-    for (int j = 0; j < K; ++j) denom += __shfl_sync(0xffffffffu, w, j);
-    if (lane < K) {
-      const float g = w / denom;
-      s_idx[m * K + lane] = mye;
-      s_g[m * K + lane] = g;
-      if (r.idx_user) r.idx_user[m * K + lane] = mye;
-      if (r.w_user) r.w_user[m * K + lane] = g;
-      r.gate[m * K + lane] = g;
-    }
-  }
-  for (int e = ct; e < E; e += NT) mask[e] = 0ull;
-  named_bar_sync(1, NT);
-  // 2) token sets per expert
-  for (int p = ct; p < M * K; p += NT) atomicOr(&mask[s_idx[p]], 1ull << (p / K));
-  named_bar_sync(1, NT);
-  // 3) exclusive scans of token counts and of "expert is active" over E
-  constexpr int PER = 4;  // E <= NT * PER
-  int cnt[PER], act[PER], csum = 0, asum = 0;
-#pragma unroll
-  for (int q = 0; q < PER; ++q) {
-    const int e = ct * PER + q;
-    cnt[q] = (e < E) ? __popcll(mask[e]) : 0;
-    act[q] = (cnt[q] + kGroupTokens - 1) / kGroupTokens;  // groups of expert e
-    csum += cnt[q];
-    asum += act[q];
-  }
-  int cinc = csum, ainc = asum;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int c2 = __shfl_up_sync(0xffffffffu, cinc, off);
-    const int a2 = __shfl_up_sync(0xffffffffu, ainc, off);
-    if (lane >= off) {
-      cinc += c2;
-      ainc += a2;
-    }
-  }
-  if (lane == 31) {
-    s_warp[warp] = cinc;
-    s_warp[32 + warp] = ainc;
-  }
-  named_bar_sync(1, NT);
-  int cbase = 0, abase = 0;
-  for (int w2 = 0; w2 < warp; ++w2) {
-    cbase += s_warp[w2];
-    abase += s_warp[32 + w2];
-  }
-  int cpre = cbase + cinc - csum, apre = abase + ainc - asum;
-#pragma unroll
-  for (int q = 0; q < PER; ++q) {
-    const int e = ct * PER + q;
-    if (e < E) {
-      s_off[e] = cpre;
-      for (int j = 0; j < act[q]; ++j) {
-        r.grp_exp[apre + j] = e;
-        r.grp_off[apre + j] = cpre + j * kGroupTokens;
-      }
-    }
-    cpre += cnt[q];
-    apre += act[q];
-  }
-  if (ct == NT - 1) {
-    int total_a = 0;
-    for (int w2 = 0; w2 < nwarps; ++w2) total_a += s_warp[32 + w2];
-    r.grp_off[total_a] = M * K;
-    *r.nact = total_a;
-  }
-  named_bar_sync(1, NT);
-  // 4) scatter pairs: pairs of expert e ordered by token
-  for (int p = ct; p < M * K; p += NT) {
-    const int m = p / K;
-    const int e = s_idx[p];
-    const unsigned long long below = (m == 0) ? 0ull : (mask[e] & ((1ull << m) - 1ull));
-    const int pos = s_off[e] + __popcll(below);
-    r.pair_tok[pos] = m;
-    r.pair_of[p] = pos;
-  }
-}
-
 // ------------------------------------------------------------------ split-K fixup
 // Sum the partial tiles of all nc contributors of one output tile, in
 // contributor order, and hand each total to `store(t, r, v, v_up)`. A partial
@@ -390,8 +199,7 @@ __device__ __forceinline__ void reduce_partials(const float* ws, long long slot_
 // PAIRED: SwiGLU tiles (128 gate rows and the 128 matching up rows per stage
 // column). WIDE: 256-row output tiles (two 128-row halves per stage column).
 // GROUPED: MoE groups.
-// ROUTER: dense fp32 logits followed by the routing tail.
-template <int XR, int STAGES, int EPI, bool PAIRED, bool GROUPED, bool ROUTER, bool WIDE = false>
+template <int XR, int STAGES, int EPI, bool PAIRED, bool GROUPED, bool WIDE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     wstream_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const StreamArgs a) {
@@ -406,9 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * kStageBytes);
   uint64_t* empty = full + STAGES;
-  volatile int* s_flags = reinterpret_cast<volatile int*>(empty + STAGES);  // [0] abort [1] last [2] routed
+  volatile int* s_flags = reinterpret_cast<volatile int*>(empty + STAGES);  // [0] abort [1] last
   int* s_slot = const_cast<int*>(s_flags) + 8;                                 // [kMaxSlots]
-  uint8_t* scratch = reinterpret_cast<uint8_t*>(s_slot + kMaxSlots);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -704,25 +511,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             reduce_partials<kNCW * 32, PAIRED, kSlotStride>(a.ws, kSlotFloats, nc, gi.c, ct,
                                                             slot_at, store);
           }
-        }
-      }
-      if (last && ROUTER) {
-        // count finished tiles; the CTA finishing the last one routes
-        named_bar_sync(1, kNCW * 32);
-        if (ct == 0) {
-          __threadfence();
-          const int old = atomic_add_acq_rel_gpu(a.done, 1);
-          const int fin = (old == a.total_tiles_dense - 1) ? 1 : 0;
-          if (fin) *a.done = 0;
-          s_flags[2] = fin;
-        }
-        named_bar_sync(1, kNCW * 32);
-        if (s_flags[2]) {
-          __threadfence();
-          // the ring is idle now (every unit of every CTA has been consumed)
-          const bool fits = (long long)a.route.M * a.route.E * 4 <= (long long)STAGES * kStageBytes;
-          route_tail<kNCW * 32>(a.route, ct, scratch,
-                                fits ? reinterpret_cast<float*>(smem) : nullptr);
         }
       }
       named_bar_sync(1, kNCW * 32);  // partial slots and flags may be reused next tile
