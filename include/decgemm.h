@@ -120,9 +120,12 @@ int dec_linear_splitk(const void* x, const void* W, void* y, int M, int N, int K
  *   h      = silu(x·W1ᵀ) * (x·W3ᵀ) per chosen expert (rounded to bf16);
  *   out    = bf16( sum_{j=0..topk-1} g_j · h_j·W2ᵀ  +  shared(x) ).
  * Only the chosen experts' weights are read, each once per call however many
- * tokens chose it. The shared expert runs on a library-owned side stream that
- * waits on `stream` at entry, streams its weights on the SMs the router leaves
- * free while the router runs, and is joined back before the routed experts.
+ * tokens chose it. Kernels on `stream`: router projection, top-k (one warp per
+ * token), schedule + token gather, expert gate/up with SwiGLU, expert down,
+ * combine. The shared expert runs on a library-owned side stream of the
+ * lowest priority that waits on `stream` at entry and is spread over every
+ * SM, so it streams its weights while routing runs and yields SMs to the
+ * routed experts; `stream` joins it before the combine.
  * The number of active experts never returns to the host.
  * Limits: H % 8 == 0, I % 8 == 0, 1 <= topk <= min(E, 32), E <= 1024.
  * Errors: DEC_EINVAL, DEC_EUNSUPPORTED, DEC_ECUDA, DEC_ENOMEM.

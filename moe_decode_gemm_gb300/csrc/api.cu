@@ -302,18 +302,19 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   Ctx cx = make_ctx(s, st);
   float* ws = (float*)s->ws_main.p;
   int* ctr = (int*)s->ctr_main.p;
-  // Shared expert: forked to the side stream so that it streams its weights
-  // while the router, a short latency-bound kernel on a sixth of the SMs,
-  // runs on the main stream. It gets the other SMs, and the routed experts
-  // start only after both have finished: their work is split statically
-  // across all SMs, so nothing else should hold an SM while they run.
-  const int rgrid = router_grid(s->sms);
+  // Shared expert: forked to the side stream, which has the lowest priority,
+  // and spread over every SM. Its CTAs stream its weights while the router,
+  // top-k and gather (few CTAs, latency bound) run; as the routed experts'
+  // CTAs arrive the scheduler gives them the SMs first, so the shared
+  // expert's remaining work fills the gaps. The streams join before the
+  // combine.
+  const int sgrid = s->sms;
+  const int egrid = s->sms;
   if (shared) {
     if (cudaEventRecord(s->ev_fork, st) != cudaSuccess) return DEC_ECUDA;
     if (cudaStreamWaitEvent(s->side, s->ev_fork, 0) != cudaSuccess) return DEC_ECUDA;
     Ctx sx = make_ctx(s, s->side);
     sx.pdl = false;
-    const int sgrid = s->sms - rgrid > 0 ? s->sms - rgrid : 1;
     if ((rc = counted(launch_shared_w13(sx, x, Ws13, M, H, I, s->mb, sgrid, (float*)s->ws_side.p,
                                         (int*)s->ctr_side.p))))
       return rc;
@@ -331,21 +332,22 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   }
   if ((rc = counted(launch_topk(cx, M, E, topk, topk_idx, topk_w, s->mb)))) return rc;
   if ((rc = counted(launch_gather(cx, x, M, H, E, topk, s->mb)))) return rc;
-  if (shared) {
-    // join: the gate/up kernel then depends on two streams, so it is
-    // launched without the programmatic (early-start) dependency
-    if (cudaStreamWaitEvent(st, s->ev_join, 0) != cudaSuccess) return DEC_ECUDA;
-  }
   {
-    Ctx cw = cx;
-    cw.pdl = !shared;
     ProbeScope p(0, st);
-    if ((rc = counted(launch_experts_w13(cw, x, W13, M, H, E, topk, I, s->mb, ws, ctr)))) return rc;
+    if ((rc = counted(launch_experts_w13(cx, x, W13, M, H, E, topk, I, s->mb, egrid, ws, ctr))))
+      return rc;
   }
   {
     ProbeScope p(1, st);
-    if ((rc = counted(launch_experts_w2(cx, W2, M, H, E, topk, I, s->mb, ws, ctr)))) return rc;
+    if ((rc = counted(launch_experts_w2(cx, W2, M, H, E, topk, I, s->mb, egrid, ws, ctr))))
+      return rc;
   }
+  if (shared) {
+    if (cudaStreamWaitEvent(st, s->ev_join, 0) != cudaSuccess) return DEC_ECUDA;
+  }
+  // After the join the combine depends on two streams: launch it without the
+  // programmatic (early-start) dependency so both are complete ones.
+  cx.pdl = !shared;
   ProbeScope p(4, st);
   return counted(launch_combine(cx, s->mb, shared, res, out, M, H, topk));
 }

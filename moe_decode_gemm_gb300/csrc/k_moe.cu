@@ -13,13 +13,9 @@
 
 namespace dg {
 
-constexpr int kMoeXR = 64;                  // shared expert: every token (M <= 64)
-constexpr int kMoeStages = 4;
 constexpr int kExpertXR = kGroupTokens;     // routed experts: one group's tokens
 constexpr int kExpertPairStages = 3;        // gate/up: 64 KB stages (gate and up halves)
-constexpr int kSharedPairStages = 2;        // shared gate/up: 64 KB + 16 KB of tokens
 
-constexpr int moe_smem(int stages, int extra) { return wstream_smem(kMoeXR, stages, extra); }
 constexpr int expert_pair_smem() { return wstream_smem(kExpertXR, kExpertPairStages, 0, true); }
 
 template <typename K>
@@ -285,7 +281,7 @@ cudaError_t launch_gather(const Ctx& cx, const void* x, int M, int H, int E, int
 }
 
 cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, int M, int H, int E,
-                               int k, int I, const MoeBufs& b, float* ws, int* ctr) {
+                               int k, int I, const MoeBufs& b, int grid, float* ws, int* ctr) {
   constexpr int SMEM = expert_pair_smem();
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
   auto kern = wstream_kernel<kExpertXR, kExpertPairStages, EPI_SWIGLU, true, true>;
@@ -310,11 +306,11 @@ cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, in
   a.w_up_offset = I;
   a.out = b.h;
   a.ldo = I;
-  return launch_k(kern, dim3(cx.sms), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
+  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
 }
 
 cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E, int k, int I,
-                              const MoeBufs& b, float* ws, int* ctr) {
+                              const MoeBufs& b, int grid, float* ws, int* ctr) {
   // 256-row output tiles: two 128-row halves, 64 KB weight stages
   constexpr int SMEM = expert_pair_smem();
   auto kern = wstream_kernel<kExpertXR, kExpertPairStages, EPI_F32, false, true, true>;
@@ -337,21 +333,26 @@ cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E
   a.w_group_rows = H;
   a.out = b.o;
   a.ldo = H;
-  return launch_k(kern, dim3(cx.sms), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
+  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
 }
 
-cudaError_t launch_shared_w13(const Ctx& cx, const void* x, const void* Ws13, int M, int H, int I,
-                              const MoeBufs& b, int grid, float* ws, int* ctr) {
-  constexpr int SMEM = wstream_smem(kMoeXR, kSharedPairStages, 0, true);
+// Shared expert: a dense (ungrouped) pass over every token, token rows per
+// stage sized to M like the dense projections: 8 rows for 1-2 tokens (CUDA-core
+// dots), 16 for up to 16 tokens, 64 beyond (mma.sync).
+template <int XR>
+static cudaError_t run_shared_w13(const Ctx& cx, const void* x, const void* Ws13, int M, int H,
+                                  int I, const MoeBufs& b, int grid, float* ws, int* ctr) {
+  constexpr int STAGES = XR == 64 ? 2 : 3;  // 64 KB of gate + up weights per stage
+  constexpr int SMEM = wstream_smem(XR, STAGES, 0, true);
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
-  auto kern = wstream_kernel<kMoeXR, kSharedPairStages, EPI_SWIGLU, true, false>;
+  auto kern = wstream_kernel<XR, STAGES, EPI_SWIGLU, true, false>;
   static bool done = false;
   cudaError_t e = smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;
   CUtensorMap wmap, xmap;
   if (!make_tmap(&wmap, Ws13, (uint64_t)2 * I, (uint64_t)H, kTileRows, true))
     return cudaErrorInvalidValue;
-  if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)H, kMoeXR, false)) return cudaErrorInvalidValue;
+  if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)H, XR, false)) return cudaErrorInvalidValue;
   StreamArgs a = base_args(cx, ws, ctr);
   a.K = H;
   a.KB = (H + kKChunk - 1) / kKChunk;
@@ -366,16 +367,19 @@ cudaError_t launch_shared_w13(const Ctx& cx, const void* x, const void* Ws13, in
   return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
 }
 
-cudaError_t launch_shared_w2(const Ctx& cx, const void* Ws2, int M, int H, int I, const MoeBufs& b,
-                             int grid, float* ws, int* ctr) {
-  constexpr int SMEM = moe_smem(kMoeStages, 0);
-  auto kern = wstream_kernel<kMoeXR, kMoeStages, EPI_F32, false, false>;
+template <int XR>
+static cudaError_t run_shared_w2(const Ctx& cx, const void* Ws2, int M, int H, int I,
+                                 const MoeBufs& b, int grid, float* ws, int* ctr) {
+  constexpr int STAGES = XR == 64 ? 4 : 6;
+  constexpr int SMEM = wstream_smem(XR, STAGES, 0);
+  static_assert(SMEM <= kMaxDynSmem, "shared memory");
+  auto kern = wstream_kernel<XR, STAGES, EPI_F32, false, false>;
   static bool done = false;
   cudaError_t e = smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;
   CUtensorMap wmap, xmap;
   if (!make_tmap(&wmap, Ws2, (uint64_t)H, (uint64_t)I, kTileRows, true)) return cudaErrorInvalidValue;
-  if (!make_tmap(&xmap, b.hs, (uint64_t)M, (uint64_t)I, kMoeXR, false)) return cudaErrorInvalidValue;
+  if (!make_tmap(&xmap, b.hs, (uint64_t)M, (uint64_t)I, XR, false)) return cudaErrorInvalidValue;
   StreamArgs a = base_args(cx, ws, ctr);
   a.K = I;
   a.KB = (I + kKChunk - 1) / kKChunk;
@@ -387,6 +391,20 @@ cudaError_t launch_shared_w2(const Ctx& cx, const void* Ws2, int M, int H, int I
   const long long T = (long long)a.TILES * a.KB;
   if (grid > T) grid = (int)T;
   return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
+}
+
+cudaError_t launch_shared_w13(const Ctx& cx, const void* x, const void* Ws13, int M, int H, int I,
+                              const MoeBufs& b, int grid, float* ws, int* ctr) {
+  if (M <= 2) return run_shared_w13<8>(cx, x, Ws13, M, H, I, b, grid, ws, ctr);
+  if (M <= 16) return run_shared_w13<16>(cx, x, Ws13, M, H, I, b, grid, ws, ctr);
+  return run_shared_w13<64>(cx, x, Ws13, M, H, I, b, grid, ws, ctr);
+}
+
+cudaError_t launch_shared_w2(const Ctx& cx, const void* Ws2, int M, int H, int I, const MoeBufs& b,
+                             int grid, float* ws, int* ctr) {
+  if (M <= 2) return run_shared_w2<8>(cx, Ws2, M, H, I, b, grid, ws, ctr);
+  if (M <= 16) return run_shared_w2<16>(cx, Ws2, M, H, I, b, grid, ws, ctr);
+  return run_shared_w2<64>(cx, Ws2, M, H, I, b, grid, ws, ctr);
 }
 
 // ------------------------------------------------------------------ combine

@@ -54,7 +54,7 @@ struct MoeBufs {
   float* s;        // [M, H]
 };
 
-// CTAs of the router kernel (the rest of the SMs stream the shared expert).
+// CTAs of the router kernel: a sixth of the SMs (it is latency bound).
 inline int router_grid(int sms) { return sms / 6 > 0 ? sms / 6 : 1; }
 
 cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E,
@@ -63,10 +63,11 @@ cudaError_t launch_topk(const Ctx& cx, int M, int E, int k, int32_t* idx_user, f
                         const MoeBufs& b);
 cudaError_t launch_gather(const Ctx& cx, const void* x, int M, int H, int E, int k,
                           const MoeBufs& b);
+// grid: CTAs (the expert kernels split their work statically over them).
 cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, int M, int H, int E,
-                               int k, int I, const MoeBufs& b, float* ws, int* ctr);
+                               int k, int I, const MoeBufs& b, int grid, float* ws, int* ctr);
 cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E, int k, int I,
-                              const MoeBufs& b, float* ws, int* ctr);
+                              const MoeBufs& b, int grid, float* ws, int* ctr);
 cudaError_t launch_shared_w13(const Ctx& cx, const void* x, const void* Ws13, int M, int H, int I,
                               const MoeBufs& b, int grid, float* ws, int* ctr);
 cudaError_t launch_shared_w2(const Ctx& cx, const void* Ws2, int M, int H, int I,
