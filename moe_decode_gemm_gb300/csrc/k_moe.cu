@@ -45,7 +45,7 @@ static cudaError_t run_router(const Ctx& cx, const void* x, const void* Wr, int 
   constexpr int STAGES = XR == 64 ? 4 : 6;
   constexpr int SMEM = wstream_smem(XR, STAGES, 0);
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
-  auto kern = wstream_kernel<XR, STAGES, EPI_F32, false, false>;
+  auto kern = wstream_kernel<XR, STAGES, EPI_F32, false, false, false, ROLE_ROUTER>;
   static bool done = false;
   cudaError_t e = smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;
@@ -284,7 +284,8 @@ cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, in
                                int k, int I, const MoeBufs& b, int grid, float* ws, int* ctr) {
   constexpr int SMEM = expert_pair_smem();
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
-  auto kern = wstream_kernel<kExpertXR, kExpertPairStages, EPI_SWIGLU, true, true>;
+  auto kern =
+      wstream_kernel<kExpertXR, kExpertPairStages, EPI_SWIGLU, true, true, false, ROLE_EXPERT>;
   static bool done = false;
   cudaError_t e = smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;
@@ -313,7 +314,8 @@ cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E
                               const MoeBufs& b, int grid, float* ws, int* ctr) {
   // 256-row output tiles: two 128-row halves, 64 KB weight stages
   constexpr int SMEM = expert_pair_smem();
-  auto kern = wstream_kernel<kExpertXR, kExpertPairStages, EPI_F32, false, true, true>;
+  auto kern =
+      wstream_kernel<kExpertXR, kExpertPairStages, EPI_F32, false, true, true, ROLE_EXPERT>;
   static bool done = false;
   cudaError_t e = smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;
@@ -345,7 +347,7 @@ static cudaError_t run_shared_w13(const Ctx& cx, const void* x, const void* Ws13
   constexpr int STAGES = XR == 64 ? 2 : 3;  // 64 KB of gate + up weights per stage
   constexpr int SMEM = wstream_smem(XR, STAGES, 0, true);
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
-  auto kern = wstream_kernel<XR, STAGES, EPI_SWIGLU, true, false>;
+  auto kern = wstream_kernel<XR, STAGES, EPI_SWIGLU, true, false, false, ROLE_SHARED>;
   static bool done = false;
   cudaError_t e = smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;
@@ -373,7 +375,7 @@ static cudaError_t run_shared_w2(const Ctx& cx, const void* Ws2, int M, int H, i
   constexpr int STAGES = XR == 64 ? 4 : 6;
   constexpr int SMEM = wstream_smem(XR, STAGES, 0);
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
-  auto kern = wstream_kernel<XR, STAGES, EPI_F32, false, false>;
+  auto kern = wstream_kernel<XR, STAGES, EPI_F32, false, false, false, ROLE_SHARED>;
   static bool done = false;
   cudaError_t e = smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;

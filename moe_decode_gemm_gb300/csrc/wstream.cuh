@@ -198,8 +198,12 @@ __device__ __forceinline__ void reduce_partials(const float* ws, long long slot_
 // XR: token rows per stage (8, 16 or 64). STAGES: ring depth.
 // PAIRED: SwiGLU tiles (128 gate rows and the 128 matching up rows per stage
 // column). WIDE: 256-row output tiles (two 128-row halves per stage column).
-// GROUPED: MoE groups.
-template <int XR, int STAGES, int EPI, bool PAIRED, bool GROUPED, bool WIDE = false>
+// GROUPED: MoE groups. ROLE: which step of the decode layer launches the
+// instantiation; it changes no code, only the kernel's name, so that launch
+// lists and profiles tell the router and shared expert from the projections.
+enum Role : int { ROLE_PROJECTION = 0, ROLE_ROUTER = 1, ROLE_EXPERT = 2, ROLE_SHARED = 3 };
+template <int XR, int STAGES, int EPI, bool PAIRED, bool GROUPED, bool WIDE = false,
+          int ROLE = ROLE_PROJECTION>
 __global__ void __launch_bounds__(kThreads, 1)
     wstream_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const StreamArgs a) {
