@@ -130,6 +130,13 @@ def layer_bytes(M, U):
             + moe_bytes(M, U))
 
 
+# DRAM traffic (read + write) of the routed gate/up kernel per chosen expert,
+# from one ncu capture of a small case (16 tokens over a 32-expert bank, 31
+# experts chosen: 1825.8 MB in one launch). Its traffic grows in proportion to
+# the experts it streams, so a full launch's traffic is this times its count.
+W13_TRAFFIC_PER_EXPERT = 1825.8e6 / 31
+
+
 def w13_launch_bytes(M, U):
     # routed gate/up kernel: the chosen experts' W13, the tokens, and h
     return U * 2 * 2 * I * H + 2 * M * H + 2 * M * K8 * I
@@ -210,6 +217,8 @@ def run_ours(args, rank, world, local_rank):
          for M in BATCHES}
     step_bytes = sum(layer_bytes(M, U[M][l]) for M in BATCHES for l in range(nl))
     w13_bytes = sum(w13_launch_bytes(M, U[M][l]) for M in BATCHES for l in range(nl))
+    w13_units = [U[M][l] for M in BATCHES for l in range(nl)]
+    w13_experts = sum(w13_units)
 
     def barrier():
         if world > 1:
@@ -325,7 +334,9 @@ def run_ours(args, rank, world, local_rank):
             "frac": round(w13_ach / peak_gbs, 4) if w13_ach else None,
             "peak_kind": peak_kind,
             "launches_timed": w13_n,
-            "traffic": None,
+            "traffic": int(W13_TRAFFIC_PER_EXPERT * w13_experts / len(w13_units)),
+            "traffic_note": "DRAM bytes per launch: small-case ncu capture scaled by chosen experts",
+            "algorithmic_bytes_per_launch": int(w13_bytes / len(w13_units)),
         },
         "clocks": clk,
         "generation_s": round(gen_s, 1),
