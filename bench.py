@@ -5,14 +5,15 @@ Default workload -- the synthetic decode layer stack: 4 layers, each
   r  = x + q·Woᵀ (7168 -> 7168, residual fused),
   x' = r + MoE(r)  (hidden 7168, 384 experts, top-8, SwiGLU intermediate 2048,
                     one shared expert on a second stream),
-plus an L2 prefetch of the next layer's q weights on a third stream. One step
+plus an L2 prefetch of the next layer's q weights (at most half of L2) on a
+third stream; the decode stream itself runs at high priority. One step
 runs the stack once at each batch size M in {1, 4, 16, 64}; weights stay
 resident in HBM (about 136 GB: no weight is reused within a step, every
 layer's weights are its own and far exceed L2).
 
 Prints one JSON line (rank 0). Usage:
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload stack|moe|linear]
+                  [--layers L] [--no-prefetch] [--no-cpu-baseline] [--cpu-seconds S]
 """
 from __future__ import annotations
 
@@ -156,8 +157,15 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     gen_s = time.time() - t0
 
-    main = torch.cuda.Stream(device=dev)
+    # The decode stream runs at high priority: the library's shared-expert
+    # stream and the prefetch stream (default priority) then only take SMs
+    # the decode path leaves free.
+    main = torch.cuda.Stream(device=dev, priority=-1)
     pref = torch.cuda.Stream(device=dev)
+    # Prefetch at most half of L2, so the lines it brings in are not evicted
+    # by the weights still streaming through L2 before the next layer reads them.
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    pf_bytes = min(H * H * 2, l2_bytes // 2)
     acts = {}
     for M in BATCHES:
         x0 = wl.bits_to_torch(wl.token_rows(M, H, "stack-x", M), device=dev)
@@ -185,7 +193,7 @@ def run_ours(args, rank, world, local_rank):
                 nxt = layers[(l + 1) % nl]
                 ev_fork[l].record(main)
                 pref.wait_event(ev_fork[l])
-                dg.l2_prefetch(nxt.Wq, stream=pref)
+                dg.l2_prefetch(nxt.Wq.data_ptr(), pf_bytes, stream=pref)
             dg.moe_decode(a["r"], L.Wr, L.W13, L.W2, L.Ws13, L.Ws2, K8, out=a["xs"][l + 1],
                           topk_idx=a["idx"][l], stream=main, residual=a["r"])
 
@@ -317,7 +325,10 @@ def run_ours(args, rank, world, local_rank):
             "layers": nl, "batches": list(BATCHES), "hidden": H, "experts": E, "topk": K8,
             "inter": I, "l2": "inputs larger than L2 (each step streams ~%.0f GB of distinct "
                               "weights)" % (step_bytes / 1e9),
-            "prefetch": not args.no_prefetch, "parallelism": "replicas" if world > 1 else "1 GPU",
+            "prefetch": (False if args.no_prefetch else
+                         "next layer's Wq, first %d bytes (half of L2), side stream" % pf_bytes),
+            "streams": "decode stream priority -1 (high); shared expert and prefetch on "
+                       "lower-priority side streams", "parallelism": "replicas" if world > 1 else "1 GPU",
         },
         "pct_of_peak": round(100.0 * tbps * 1e3 / (peak_gbs * world), 2),
         "us_per_layer": {str(M): per_m[M]["us_per_layer"] for M in BATCHES},

@@ -9,9 +9,18 @@
 
 namespace dg {
 
+// Narrow tiles at 8 or 16 token rows: 3 stages (about 105 KB of shared memory)
+// so that two CTAs fit on an SM -- the next call's CTA starts and streams its
+// weights while the previous call's CTA on that SM finishes its split-K
+// reduction. Wide tiles and 64 token rows: one CTA per SM, deeper rings.
+template <int XR, bool WIDE>
+constexpr int dense_minb() {
+  return (!WIDE && XR <= 16) ? 2 : 1;
+}
+
 template <int XR, bool WIDE>
 constexpr int dense_stages() {
-  return WIDE ? 3 : (XR == 8 ? 6 : XR == 16 ? 6 : 4);
+  return WIDE ? 3 : dense_minb<XR, WIDE>() == 2 ? 3 : 4;
 }
 
 template <int XR, bool WIDE>
@@ -24,13 +33,20 @@ template <int XR, int EPI, bool WIDE = false>
 static cudaError_t run_dense(const Ctx& cx, bool mma, const void* x, const void* W, const void* res,
                              void* y, int M, int N, int K, int grid, float* ws, int* ctr) {
   constexpr int S = dense_stages<XR, WIDE>();
+  constexpr int MINB = dense_minb<XR, WIDE>();
   constexpr int SMEM = dense_smem<XR, WIDE>();
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
-  auto kern = wstream_kernel<XR, S, EPI, false, false, WIDE>;
+  static_assert(MINB == 1 || 2 * (SMEM + 1024) <= kSmemPerSm, "two CTAs per SM");
+  auto kern = wstream_kernel<XR, S, EPI, false, false, WIDE, ROLE_PROJECTION, MINB>;
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = allow_smem(kern, SMEM);
     if (e != cudaSuccess) return e;
+    if (MINB > 1) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
+      if (e != cudaSuccess) return e;
+    }
     attr_done = true;
   }
   constexpr int kTile = WIDE ? 2 * kTileRows : kTileRows;

@@ -229,8 +229,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           named_bar_sync(1, kTcEpi);
           const long long cf = cta_of(gt * KB, T, G);
           const long long cl = cta_of((gt + 1) * KB - 1, T, G);
+          // barrier + release (and acquire + barrier on the last arriver)
+          // order the partial slots; no separate fence needed
           if (et == 0) {
-            __threadfence();
             const int old = atomic_add_acq_rel_gpu(&a.ctr[gt], 1);
             const int is_last = (old == (int)(cl - cf)) ? 1 : 0;
             if (is_last) a.ctr[gt] = 0;
@@ -238,7 +239,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           named_bar_sync(1, kTcEpi);
           if (s_flags[1]) {
-            __threadfence();
             const int nc = (int)(cl - cf + 1);
             auto slot_of = [&](int j) -> long long {
               const long long cc = cf + j;
@@ -254,7 +254,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int nn = tile * kTileRows + rr;
                 if (nn < a.nout) store_out<EPI, false>(a, gi, t, nn, v0);
               };
-              reduce_partials<kTcEpi, false, kTileRows>(a.ws, kSlotFloats, nc, gi.c, et, slot_at, store);
+              // 4 items x 4 contributors: 16 loads in flight per thread
+              reduce_partials<kTcEpi, false, kTileRows, 4, 4>(a.ws, kSlotFloats, nc, gi.c, et,
+                                                              slot_at, store);
             }
           }
           named_bar_sync(1, kTcEpi);

@@ -80,5 +80,6 @@ cudaError_t launch_selftest_timeout(const Ctx& cx, long long ns);
 
 // Shared memory each dense/MoE kernel needs (bytes), for cudaFuncSetAttribute.
 constexpr int kMaxDynSmem = 232448;
+constexpr int kSmemPerSm = 233472;  // per SM; each resident CTA also reserves 1 KB
 
 }  // namespace dg

@@ -39,7 +39,11 @@ enum Epi : int { EPI_BF16 = 0, EPI_BF16_RES = 1, EPI_F32 = 2, EPI_SWIGLU = 3 };
 // the token rows of an expert kernel's pipeline stage.
 constexpr int kGroupTokens = 16;
 
-constexpr int kMaxSlots = 512;             // contributor slot table entries in shared memory
+constexpr int kMaxSlots = 512;
+// Weight bytes per CTA a plain projection prefetches into L2 before waiting
+// for its predecessor, beyond the ones its ring loads (152 CTAs: 39 MB, under
+// a third of L2).
+constexpr int kPrefetchBytes = 256 * 1024;             // contributor slot table entries in shared memory
 
 // Dynamic shared memory of one wstream_kernel instantiation: 1 KB alignment
 // slack, the stage ring, full/empty barriers, flags, slot table, and `extra`.
@@ -128,46 +132,53 @@ __device__ __forceinline__ void store_swiglu(const StreamArgs& a, const GroupInf
 // contributor order, and hand each total to `store(t, r, v, v_up)`. A partial
 // slot is [token][STRIDE] fp32 at ws + slot * slot_floats: 128 rows of output
 // features, followed for SwiGLU tiles (PAIRED) by the 128 matching up rows.
-// Each thread takes two groups of 4 rows and keeps 4 contributors' loads in
-// flight for each, so the reduction costs a few L2 round trips rather than one
-// per contributor.
-template <int NT, bool PAIRED, int STRIDE, typename Slot, typename Store>
+// Work item e is one float4 (4 rows of one token); thread tid takes items
+// tid, tid + NT, ... so that every warp-wide load reads 512 contiguous bytes.
+// A round loads EB items from JB contributors at once, so each thread keeps
+// EB x JB loads in flight (twice that for SwiGLU tiles); each item's
+// contributions are still added in contributor order.
+template <int NT, bool PAIRED, int STRIDE, int EB, int JB, typename Slot, typename Store>
 __device__ __forceinline__ void reduce_partials(const float* ws, long long slot_floats, int nc,
                                                 int c, int tid, Slot slot_of, Store store) {
   constexpr int R4 = (PAIRED ? kTileRows : STRIDE) / 4;  // output rows per token, in fours
-  constexpr int EB = 2;
   const int nel4 = R4 * c;
-  for (int e0 = tid * EB; e0 < nel4; e0 += NT * EB) {
+  for (int base = 0; base < nel4; base += NT * EB) {
     float4 g[EB], u[EB];
-    int off[EB], tt[EB], rr[EB];
+    int off[EB];
+    bool ok[EB];
 #pragma unroll
     for (int q = 0; q < EB; ++q) {
       g[q] = make_float4(0.f, 0.f, 0.f, 0.f);
       u[q] = g[q];
-      const int e = e0 + q < nel4 ? e0 + q : e0;
-      tt[q] = e / R4;
-      rr[q] = (e - tt[q] * R4) * 4;
-      off[q] = tt[q] * STRIDE + rr[q];
+      const int e = base + q * NT + tid;
+      ok[q] = e < nel4;
+      const int t = e / R4;
+      off[q] = t * STRIDE + (e - t * R4) * 4;
     }
+    auto add = [](float4& acc, const float4& v) {
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    };
     int j = 0;
-    for (; j + 4 <= nc; j += 4) {
-      float4 pg[4][EB], pu[4][EB];
+    for (; j + JB <= nc; j += JB) {
+      float4 pg[JB][EB], pu[JB][EB];
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
+      for (int jj = 0; jj < JB; ++jj) {
         const float* b = ws + slot_of(j + jj) * slot_floats;
 #pragma unroll
         for (int q = 0; q < EB; ++q) {
-          pg[jj][q] = __ldcg(reinterpret_cast<const float4*>(b + off[q]));
-          if (PAIRED) pu[jj][q] = __ldcg(reinterpret_cast<const float4*>(b + off[q] + kTileRows));
+          if (ok[q]) {
+            pg[jj][q] = __ldcg(reinterpret_cast<const float4*>(b + off[q]));
+            if (PAIRED) pu[jj][q] = __ldcg(reinterpret_cast<const float4*>(b + off[q] + kTileRows));
+          }
         }
       }
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj)
+      for (int jj = 0; jj < JB; ++jj)
 #pragma unroll
         for (int q = 0; q < EB; ++q) {
-          g[q].x += pg[jj][q].x; g[q].y += pg[jj][q].y; g[q].z += pg[jj][q].z; g[q].w += pg[jj][q].w;
-          if (PAIRED) {
-            u[q].x += pu[jj][q].x; u[q].y += pu[jj][q].y; u[q].z += pu[jj][q].z; u[q].w += pu[jj][q].w;
+          if (ok[q]) {
+            add(g[q], pg[jj][q]);
+            if (PAIRED) add(u[q], pu[jj][q]);
           }
         }
     }
@@ -175,23 +186,37 @@ __device__ __forceinline__ void reduce_partials(const float* ws, long long slot_
       const float* b = ws + slot_of(j) * slot_floats;
 #pragma unroll
       for (int q = 0; q < EB; ++q) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(b + off[q]));
-        g[q].x += v.x; g[q].y += v.y; g[q].z += v.z; g[q].w += v.w;
-        if (PAIRED) {
-          const float4 d = __ldcg(reinterpret_cast<const float4*>(b + off[q] + kTileRows));
-          u[q].x += d.x; u[q].y += d.y; u[q].z += d.z; u[q].w += d.w;
+        if (ok[q]) {
+          add(g[q], __ldcg(reinterpret_cast<const float4*>(b + off[q])));
+          if (PAIRED) add(u[q], __ldcg(reinterpret_cast<const float4*>(b + off[q] + kTileRows)));
         }
       }
     }
 #pragma unroll
     for (int q = 0; q < EB; ++q) {
-      if (e0 + q >= nel4) continue;
-      store(tt[q], rr[q] + 0, g[q].x, u[q].x);
-      store(tt[q], rr[q] + 1, g[q].y, u[q].y);
-      store(tt[q], rr[q] + 2, g[q].z, u[q].z);
-      store(tt[q], rr[q] + 3, g[q].w, u[q].w);
+      if (!ok[q]) continue;
+      const int e = base + q * NT + tid;
+      const int t = e / R4, r = (e - t * R4) * 4;
+      store(t, r + 0, g[q].x, u[q].x);
+      store(t, r + 1, g[q].y, u[q].y);
+      store(t, r + 2, g[q].z, u[q].z);
+      store(t, r + 3, g[q].w, u[q].w);
     }
   }
+}
+
+// Items per thread and round for reduce_partials, for at most `loads` float4
+// loads in flight per thread (SwiGLU tiles load two halves per item): as many
+// items as one round needs at XR token rows, the rest of the budget spent on
+// contributors.
+constexpr int reduce_eb(int nt, bool paired, int stride, int xr, int loads) {
+  const int per = ((paired ? kTileRows : stride) / 4) * xr / nt;
+  const int cap = paired ? loads / 2 : loads;
+  return per < 1 ? 1 : per > cap ? cap : per;
+}
+constexpr int reduce_jb(bool paired, int eb, int loads) {
+  const int jb = loads / (eb * (paired ? 2 : 1));
+  return jb < 1 ? 1 : jb;
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -201,10 +226,13 @@ __device__ __forceinline__ void reduce_partials(const float* ws, long long slot_
 // GROUPED: MoE groups. ROLE: which step of the decode layer launches the
 // instantiation; it changes no code, only the kernel's name, so that launch
 // lists and profiles tell the router and shared expert from the projections.
+// MINB: CTAs per SM the build must fit (registers and shared memory). With 2,
+// a call's CTA can start on an SM while the previous call's CTA there is
+// still finishing, and stream its weights before waiting for that call.
 enum Role : int { ROLE_PROJECTION = 0, ROLE_ROUTER = 1, ROLE_EXPERT = 2, ROLE_SHARED = 3 };
 template <int XR, int STAGES, int EPI, bool PAIRED, bool GROUPED, bool WIDE = false,
-          int ROLE = ROLE_PROJECTION>
-__global__ void __launch_bounds__(kThreads, 1)
+          int ROLE = ROLE_PROJECTION, int MINB = 1>
+__global__ void __launch_bounds__(kThreads, MINB)
     wstream_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const StreamArgs a) {
   constexpr int H2 = (PAIRED || WIDE) ? 2 : 1;  // 128-row weight halves per box column
@@ -297,6 +325,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(d, &xmap, k0, GROUPED ? g_.p0 : 0, &full[s], pol_x);
         }
       };
+      // The same weight boxes as issue_w, into L2 only.
+      auto prefetch_w = [&](long long u) {
+        const long long gt = u / KB;
+        const int kc = (int)(u - gt * KB);
+        const int tile = (int)(gt % TILES);
+        const int rbase = gi.e * a.w_group_rows;
+#pragma unroll
+        for (int sb = 0; sb < kKSub; ++sb) {
+          const int k0 = (kc * kKSub + sb) * kKBlk;
+          tma_prefetch_2d(&wmap, k0, rbase + tile * kTileOut);
+          if (H2 == 2)
+            tma_prefetch_2d(&wmap, k0,
+                            rbase + (PAIRED ? a.w_up_offset + tile * kTileRows
+                                            : tile * kTileOut + kTileRows));
+        }
+      };
       auto group_of = [&](long long u) -> int { return (int)((u / KB) / TILES); };
       auto xbytes = [&](const GroupInfo& g_) -> uint32_t {
         (void)g_;
@@ -313,6 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&full[i], wbytes + xbytes(gi));
           issue_w(i, u0 + i);
         }
+        // The units beyond the ring: pull up to kPrefetchBytes of them into
+        // L2 while the previous kernel finishes, so that after the wait they
+        // arrive at L2 rather than HBM latency and bandwidth.
+        constexpr int kPfUnits = kPrefetchBytes / kWStage;
+        const int npf = nunits - npre < kPfUnits ? nunits - npre : kPfUnits;
+        for (int j = 0; j < npf; ++j) prefetch_w(u0 + npre + j);
         griddep_wait();
         for (int j = 0; j < npre; ++j) issue_x(j, u0 + j, gi);
       }
@@ -487,8 +537,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(1, kNCW * 32);
         const long long cf = cta_of(gt * KB, T, G);
         const long long cl = cta_of((gt + 1) * KB - 1, T, G);
+        // The barrier orders every consumer thread's partial stores before
+        // thread 0's release; the acquire side of the same atomic, followed by
+        // the next barrier, orders the last arriver's reads of the other
+        // slots after every contributor's release. No separate fence needed.
         if (ct == 0) {
-          __threadfence();
           const int old = atomic_add_acq_rel_gpu(&a.ctr[gt], 1);
           const int is_last = (old == (int)(cl - cf)) ? 1 : 0;
           if (is_last) a.ctr[gt] = 0;  // every contributor has arrived: reset for the next call
@@ -499,7 +552,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (last) {
           // The last contributor sums every contributor's slot in CTA order
           // (so the result does not depend on who arrived last).
-          __threadfence();
           const int nc = (int)(cl - cf + 1);
           auto slot_of = [&](int j) -> long long {
             const long long cc = cf + j;
@@ -512,8 +564,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               return j < kMaxSlots ? (long long)s_slot[j] : slot_of(j);
             };
             auto store = [&](int t, int r, float vg, float vu) { emit(tile, r, t, vg, vu); };
-            reduce_partials<kNCW * 32, PAIRED, kSlotStride>(a.ws, kSlotFloats, nc, gi.c, ct,
-                                                            slot_at, store);
+            // fewer registers for two CTAs per SM, and for SwiGLU tiles at 64
+            // token rows, whose accumulators take most of them
+            constexpr int kLoads = (MINB == 2 || (PAIRED && XR == 64)) ? 4 : 8;
+            constexpr int kEB = reduce_eb(kNCW * 32, PAIRED, kSlotStride, XR, kLoads);
+            constexpr int kJB = reduce_jb(PAIRED, kEB, kLoads);
+            reduce_partials<kNCW * 32, PAIRED, kSlotStride, kEB, kJB>(a.ws, kSlotFloats, nc, gi.c,
+                                                                      ct, slot_at, store);
           }
         }
       }
