@@ -123,9 +123,9 @@ int dec_linear_splitk(const void* x, const void* W, void* y, int M, int N, int K
  * tokens chose it. Kernels on `stream`: router projection, top-k (one warp per
  * token), schedule + token gather, expert gate/up with SwiGLU, expert down,
  * combine. The shared expert runs on a library-owned side stream of the
- * lowest priority that waits on `stream` at entry and is spread over every
- * SM, so it streams its weights while routing runs and yields SMs to the
- * routed experts; `stream` joins it before the combine.
+ * lowest priority that waits on `stream` at entry: its kernels take the SMs
+ * the router leaves free and stream their weights while routing runs;
+ * `stream` joins it before the combine.
  * The number of active experts never returns to the host.
  * Limits: H % 8 == 0, I % 8 == 0, 1 <= topk <= min(E, 32), E <= 1024.
  * Errors: DEC_EINVAL, DEC_EUNSUPPORTED, DEC_ECUDA, DEC_ENOMEM.

@@ -96,8 +96,10 @@ static int get_dev(DevState** out) {
     s.l2 = p.l2CacheSize;
     s.cc_major = p.major;
     s.cc_minor = p.minor;
-    // The shared expert's stream has the lowest priority: the routed path
-    // (router -> experts) is the critical one and must not queue behind it.
+    // The shared expert's stream has the lowest priority: a CTA of the
+    // routed path (router -> top-k -> gather -> experts) never waits behind
+    // one of its CTAs for an SM. (A pending CTA of a higher-priority stream
+    // also holds back the dispatch of every lower-priority launch.)
     int lo = 0, hi = 0;
     cudaDeviceGetStreamPriorityRange(&lo, &hi);
     if (cudaStreamCreateWithPriority(&s.side, cudaStreamNonBlocking, lo) != cudaSuccess)
@@ -302,15 +304,16 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   Ctx cx = make_ctx(s, st);
   float* ws = (float*)s->ws_main.p;
   int* ctr = (int*)s->ctr_main.p;
-  // Shared expert: forked to the side stream, which has the lowest priority,
-  // and spread over every SM. Its CTAs stream its weights while the router,
-  // top-k and gather (few CTAs, latency bound) run; as the routed experts'
-  // CTAs arrive the scheduler gives them the SMs first, so the shared
-  // expert's remaining work fills the gaps. The streams join before the
-  // combine.
-  const int sgrid = s->sms;
+  // Shared expert, forked first to the side stream (lowest priority), one CTA
+  // on each SM the router leaves free, so its weights stream while the
+  // latency-bound router, top-k and gather run on the other SMs. Its down
+  // projection is launched without the early-start dependency, so its CTAs do
+  // not take SMs early and sit waiting for the gate/up kernel. The routed
+  // experts take the SMs as the shared expert's CTAs leave them; the streams
+  // join before the combine.
   const int egrid = s->sms;
   if (shared) {
+    const int sgrid = s->sms - router_grid(s->sms);
     if (cudaEventRecord(s->ev_fork, st) != cudaSuccess) return DEC_ECUDA;
     if (cudaStreamWaitEvent(s->side, s->ev_fork, 0) != cudaSuccess) return DEC_ECUDA;
     Ctx sx = make_ctx(s, s->side);
@@ -318,7 +321,6 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
     if ((rc = counted(launch_shared_w13(sx, x, Ws13, M, H, I, s->mb, sgrid, (float*)s->ws_side.p,
                                         (int*)s->ctr_side.p))))
       return rc;
-    sx.pdl = true;
     if ((rc = counted(launch_shared_w2(sx, Ws2, M, H, I, s->mb, sgrid, (float*)s->ws_side.p,
                                        (int*)s->ctr_side.p))))
       return rc;

@@ -175,10 +175,14 @@ constexpr int kMaxPairs = 64 * 32;
 __global__ void __launch_bounds__(kSchedThreads) schedule_gather_kernel(
     const uint4* __restrict__ x, const int* __restrict__ topk, int M, int E, int K, int row_vecs,
     uint4* __restrict__ xs, int* nact, int* grp_exp, int* grp_off, int* pair_tok, int* pair_of) {
-  __shared__ unsigned long long s_mask[kMaxE];
-  __shared__ int s_idx[kMaxPairs];
-  __shared__ int s_off[kMaxE];
-  __shared__ int s_tok[kMaxPairs];
+  // Dynamic shared memory sized to E and M*k (about 9 KB at E = 384, M = 64,
+  // k = 8), so a CTA fits on an SM beside a weight-streaming CTA:
+  // [E] token masks, [E] pair offsets, [M*k] chosen experts, [M*k] pair tokens.
+  extern __shared__ __align__(16) uint8_t s_dyn[];
+  unsigned long long* s_mask = reinterpret_cast<unsigned long long*>(s_dyn);
+  int* s_off = reinterpret_cast<int*>(s_mask + E);
+  int* s_idx = s_off + E;
+  int* s_tok = s_idx + M * K;
   __shared__ int s_warp[64];
   griddep_launch_dependents();
   griddep_wait();
@@ -274,7 +278,8 @@ cudaError_t launch_gather(const Ctx& cx, const void* x, int M, int H, int E, int
   long long grid = (total + kSchedThreads - 1) / kSchedThreads;
   if (grid > cx.sms) grid = cx.sms;
   if (grid < 1) grid = 1;
-  return launch_k(schedule_gather_kernel, dim3((unsigned)grid), dim3(kSchedThreads), 0, cx.stream,
+  const int smem = E * 8 + E * 4 + 2 * M * k * 4;
+  return launch_k(schedule_gather_kernel, dim3((unsigned)grid), dim3(kSchedThreads), smem, cx.stream,
                   cx.pdl, reinterpret_cast<const uint4*>(x), (const int*)b.topk, M, E, k,
                   row_vecs, reinterpret_cast<uint4*>(b.xs), b.nact, b.grp_exp, b.grp_off,
                   b.pair_tok, b.pair_of);
