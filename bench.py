@@ -133,9 +133,9 @@ def layer_bytes(M, U):
 
 # DRAM traffic (read + write) of the routed gate/up kernel per chosen expert,
 # from one ncu capture of a small case (16 tokens over a 32-expert bank, 31
-# experts chosen: 1825.8 MB in one launch). Its traffic grows in proportion to
+# experts chosen: 1826.1 MB in one launch). Its traffic grows in proportion to
 # the experts it streams, so a full launch's traffic is this times its count.
-W13_TRAFFIC_PER_EXPERT = 1825.8e6 / 31
+W13_TRAFFIC_PER_EXPERT = 1826.1e6 / 31
 
 
 def w13_launch_bytes(M, U):
@@ -345,6 +345,9 @@ def run_ours(args, rank, world, local_rank):
             "frac": round(w13_ach / peak_gbs, 4) if w13_ach else None,
             "peak_kind": peak_kind,
             "launches_timed": w13_n,
+            # the kernel's share of the timed device time (compare with the
+            # share in the ncu launch list)
+            "share_of_step": round(w13_ms / ms, 4) if w13_n == expect_n else None,
             "traffic": int(W13_TRAFFIC_PER_EXPERT * w13_experts / len(w13_units)),
             "traffic_note": "DRAM bytes per launch: small-case ncu capture scaled by chosen experts",
             "algorithmic_bytes_per_launch": int(w13_bytes / len(w13_units)),

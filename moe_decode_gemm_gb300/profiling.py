@@ -36,15 +36,18 @@ _TRUE = ("true", "1")
 
 def kernel_label(name):
     """Readable label for one (demangled) kernel name."""
-    m = re.search(r"wstream_kernel<(\d+), (\d+), (\d+), (\w+), (\w+), (\w+)(?:, (\d+))?>", name)
+    m = re.search(r"wstream_kernel<(\d+), (\d+), (\d+), (\w+), (\w+), (\w+)(?:, (\d+))?"
+                  r"(?:, (\d+))?>", name)
     if m:
-        xr, st, epi, paired, grouped, wide, role = m.groups()
+        xr, st, epi, paired, grouped, wide, role, minb = m.groups()
         role = _ROLE.get(role or "0", role)
         part = ""
         if role in ("routed expert", "shared expert"):
             part = " gate/up" if paired in _TRUE else " down"
         tile = "256-row" if wide in _TRUE else "128-row"
-        return "%s%s [wstream XR=%s S=%s %s %s]" % (role, part, xr, st, _EPI.get(epi, epi), tile)
+        occ = " 2/SM" if minb == "2" else ""
+        return "%s%s [wstream XR=%s S=%s %s %s%s]" % (role, part, xr, st, _EPI.get(epi, epi), tile,
+                                                     occ)
     m = re.search(r"tc_linear_kernel<(\d+)>", name)
     if m:
         return "projection [tcgen05 %s]" % _EPI.get(m.group(1), m.group(1))
@@ -141,7 +144,7 @@ def case(kind, *args):
         for i in range(calls):
             dg.dec_linear(x, Ws[i % 2], y)
         torch.cuda.synchronize()
-        print("linear M=%d N=%d K=%d regime=%d calls=%d" % (M, N, K, dg.last_choice(), calls))
+        print("linear M=%d N=%d K=%d regime=%s calls=%d" % (M, N, K, dg.last_choice(), calls))
     else:
         sys.exit(__doc__)
     if dg.sync_check() != 0:
