@@ -521,58 +521,80 @@ __global__ void __launch_bounds__(kThreads, MINB)
           }
     };
 
-    auto finish_tile = [&](long long gt) {
-      const int g = (int)(gt / TILES);
-      const int tile = (int)(gt - (long long)g * TILES);
+    constexpr long long kSlotFloats = (long long)kSlotStride * XR;
+    // Contributors of split tile gt: CTAs cf..cl.
+    auto first_cta = [&](long long gt) { return cta_of(gt * KB, T, G); };
+    auto last_cta = [&](long long gt) { return cta_of((gt + 1) * KB - 1, T, G); };
+
+    // The last contributor of tile gt sums every contributor's slot in CTA
+    // order (so the result does not depend on who arrived last). Called by all
+    // consumer threads after the arrival atomic's result is in s_flags[1].
+    auto reduce_tile = [&](long long gt, bool aborted) {
+      const int tile = (int)(gt % TILES);
+      const long long cf = first_cta(gt);
+      const int nc = (int)(last_cta(gt) - cf + 1);
+      auto slot_of = [&](int j) -> long long {
+        const long long cc = cf + j;
+        return cc * 2 + ((gt == cta_start(cc, T, G) / KB) ? 0 : 1);
+      };
+      for (int j = ct; j < nc && j < kMaxSlots; j += kNCW * 32) s_slot[j] = (int)slot_of(j);
+      named_bar_sync(1, kNCW * 32);
+      if (!aborted) {
+        auto slot_at = [&](int j) -> long long {
+          return j < kMaxSlots ? (long long)s_slot[j] : slot_of(j);
+        };
+        auto store = [&](int t, int r, float vg, float vu) { emit(tile, r, t, vg, vu); };
+        // fewer registers for two CTAs per SM, and for SwiGLU tiles at 64
+        // token rows, whose accumulators take most of them
+        constexpr int kLoads = (MINB == 2 || (PAIRED && XR == 64)) ? 4 : 8;
+        constexpr int kEB = reduce_eb(kNCW * 32, PAIRED, kSlotStride, XR, kLoads);
+        constexpr int kJB = reduce_jb(PAIRED, kEB, kLoads);
+        reduce_partials<kNCW * 32, PAIRED, kSlotStride, kEB, kJB>(a.ws, kSlotFloats, nc, gi.c, ct,
+                                                                  slot_at, store);
+      }
+    };
+
+    // Thread 0's share of the arrival on tile gt's counter, given the counter's
+    // value before its own increment: flags the last contributor and resets
+    // the counter for the next call.
+    auto settle = [&](long long gt, int old) {
+      const int is_last = (old == (int)(last_cta(gt) - first_cta(gt))) ? 1 : 0;
+      if (is_last) a.ctr[gt] = 0;
+      s_flags[1] = is_last;
+    };
+
+    // A split tile met in the middle of the range (the CTA's first tile, whose
+    // other contributors precede it) has its arrival deferred: the atomic is
+    // issued and the consumers move on to the next tile at once; its result is
+    // read, and the tile reduced if this CTA arrived last, after the range.
+    long long dgt = -1;  // deferred tile
+    int dold = 0;        // its counter's value before this CTA's increment (thread 0)
+    GroupInfo dgi{0, 0, 0};
+
+    auto finish_tile = [&](long long gt, bool defer) {
+      const int tile = (int)(gt % TILES);
       const bool aborted = s_flags[0] != 0;
       if (!use_mma) reduce_dots();
       const bool whole = (u0 <= gt * KB) && ((gt + 1) * KB <= u1);
-      bool last = whole;
       if (whole) {
         if (!aborted) reg_epilogue(tile);
       } else {
-        constexpr long long kSlotFloats = (long long)kSlotStride * XR;
         const int slot = (gt == u0 / KB) ? 0 : 1;
         write_partial(a.ws + (c * 2 + slot) * kSlotFloats);
-        named_bar_sync(1, kNCW * 32);
-        const long long cf = cta_of(gt * KB, T, G);
-        const long long cl = cta_of((gt + 1) * KB - 1, T, G);
         // The barrier orders every consumer thread's partial stores before
         // thread 0's release; the acquire side of the same atomic, followed by
-        // the next barrier, orders the last arriver's reads of the other
-        // slots after every contributor's release. No separate fence needed.
-        if (ct == 0) {
-          const int old = atomic_add_acq_rel_gpu(&a.ctr[gt], 1);
-          const int is_last = (old == (int)(cl - cf)) ? 1 : 0;
-          if (is_last) a.ctr[gt] = 0;  // every contributor has arrived: reset for the next call
-          s_flags[1] = is_last;
-        }
+        // a barrier, orders the last arriver's reads of the other slots after
+        // every contributor's release. No separate fence needed.
         named_bar_sync(1, kNCW * 32);
-        last = s_flags[1] != 0;
-        if (last) {
-          // The last contributor sums every contributor's slot in CTA order
-          // (so the result does not depend on who arrived last).
-          const int nc = (int)(cl - cf + 1);
-          auto slot_of = [&](int j) -> long long {
-            const long long cc = cf + j;
-            return cc * 2 + ((gt == cta_start(cc, T, G) / KB) ? 0 : 1);
-          };
-          for (int j = ct; j < nc && j < kMaxSlots; j += kNCW * 32) s_slot[j] = (int)slot_of(j);
-          named_bar_sync(1, kNCW * 32);
-          if (!aborted) {
-            auto slot_at = [&](int j) -> long long {
-              return j < kMaxSlots ? (long long)s_slot[j] : slot_of(j);
-            };
-            auto store = [&](int t, int r, float vg, float vu) { emit(tile, r, t, vg, vu); };
-            // fewer registers for two CTAs per SM, and for SwiGLU tiles at 64
-            // token rows, whose accumulators take most of them
-            constexpr int kLoads = (MINB == 2 || (PAIRED && XR == 64)) ? 4 : 8;
-            constexpr int kEB = reduce_eb(kNCW * 32, PAIRED, kSlotStride, XR, kLoads);
-            constexpr int kJB = reduce_jb(PAIRED, kEB, kLoads);
-            reduce_partials<kNCW * 32, PAIRED, kSlotStride, kEB, kJB>(a.ws, kSlotFloats, nc, gi.c,
-                                                                      ct, slot_at, store);
-          }
+        if (defer) {
+          if (ct == 0) dold = atomic_add_acq_rel_gpu(&a.ctr[gt], 1);
+          dgt = gt;
+          dgi = gi;
+          return;
         }
+        if (ct == 0) settle(gt, atomic_add_acq_rel_gpu(&a.ctr[gt], 1));
+        named_bar_sync(1, kNCW * 32);
+        if (s_flags[1]) reduce_tile(gt, aborted);
       }
       named_bar_sync(1, kNCW * 32);  // partial slots and flags may be reused next tile
     };
@@ -581,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
       const long long u = u0 + i;
       const long long gt = u / KB;
       if (gt != cur) {
-        if (cur >= 0) finish_tile(cur);
+        if (cur >= 0) finish_tile(cur, cur == u0 / KB);
         cur = gt;
         zero_acc();
         gi = load_group<GROUPED>(a, (int)(gt / TILES));
@@ -650,7 +672,15 @@ __global__ void __launch_bounds__(kThreads, MINB)
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
-    if (cur >= 0) finish_tile(cur);
+    if (cur >= 0) finish_tile(cur, false);
+    if (dgt >= 0) {
+      if (ct == 0) settle(dgt, dold);
+      named_bar_sync(1, kNCW * 32);
+      if (s_flags[1]) {
+        gi = dgi;
+        reduce_tile(dgt, s_flags[0] != 0);
+      }
+    }
   }
   __syncthreads();
 }
