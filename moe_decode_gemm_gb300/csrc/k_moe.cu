@@ -184,7 +184,9 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_gather_kernel(
   int* s_idx = s_off + E;
   int* s_tok = s_idx + M * K;
   __shared__ int s_warp[64];
-  griddep_launch_dependents();
+  // The expert kernel that follows can do nothing before this schedule is
+  // complete: it is let launch only at the end (see below), so that its CTAs
+  // do not take SMs early and sit idle while routing runs.
   griddep_wait();
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int P = M * K;
@@ -269,10 +271,12 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_gather_kernel(
     const int c = (int)(v - (long long)p * row_vecs);
     xs[v] = x[(long long)s_tok[p] * row_vecs + c];
   }
+  griddep_launch_dependents();
 }
 
 cudaError_t launch_gather(const Ctx& cx, const void* x, int M, int H, int E, int k,
                           const MoeBufs& b) {
+  if (E > kMaxE || M * k > kMaxPairs) return cudaErrorInvalidValue;
   const int row_vecs = H / 8;
   const long long total = (long long)M * k * row_vecs;
   long long grid = (total + kSchedThreads - 1) / kSchedThreads;
@@ -338,6 +342,7 @@ cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E
   a.grp_exp = b.grp_exp;
   a.grp_off = b.grp_off;
   a.w_group_rows = H;
+  a.tables_ready = 1;  // the gate/up kernel lets this one launch only after its own wait
   a.out = b.o;
   a.ldo = H;
   return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);

@@ -63,6 +63,10 @@ struct StreamArgs {
   const int* grp_off;
   int w_group_rows;          // weight rows per expert
   int w_up_offset;           // paired (SwiGLU) tiles: row offset of the up block
+  // grouped mode: the group tables were complete before the previous kernel
+  // let this one launch (it does so only after its own wait), so they may be
+  // read, and the weights streamed, before waiting for it
+  int tables_ready;
   // output
   void* out;
   long long ldo;             // elements between output rows
@@ -266,14 +270,23 @@ __global__ void __launch_bounds__(kThreads, MINB)
     prefetch_tmap(&xmap);
   }
   __syncthreads();
-  griddep_launch_dependents();
+  // Kernels that can stream weights before their predecessor finishes let
+  // their own dependents launch at once. A grouped kernel that must wait for
+  // the group tables does so only after that wait: its dependents' CTAs would
+  // otherwise take SMs early and sit idle there, and they may then read the
+  // tables before waiting.
+  const bool early = !GROUPED || a.tables_ready;
+  if (early) griddep_launch_dependents();
 
   const long long c = blockIdx.x;
   const int KB = a.KB, TILES = a.TILES;
 
   long long T;
   if (GROUPED) {
-    griddep_wait();
+    if (!early) {
+      griddep_wait();
+      griddep_launch_dependents();
+    }
     T = (long long)(*a.nact) * TILES * KB;
   } else {
     T = (long long)TILES * KB;
@@ -325,12 +338,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
           tma_load_2d(d, &xmap, k0, GROUPED ? g_.p0 : 0, &full[s], pol_x);
         }
       };
-      // The same weight boxes as issue_w, into L2 only.
-      auto prefetch_w = [&](long long u) {
+      // The same weight boxes as issue_w for expert e, into L2 only.
+      auto prefetch_w = [&](long long u, int e) {
         const long long gt = u / KB;
         const int kc = (int)(u - gt * KB);
         const int tile = (int)(gt % TILES);
-        const int rbase = gi.e * a.w_group_rows;
+        const int rbase = e * a.w_group_rows;
 #pragma unroll
         for (int sb = 0; sb < kKSub; ++sb) {
           const int k0 = (kc * kKSub + sb) * kKBlk;
@@ -348,23 +361,39 @@ __global__ void __launch_bounds__(kThreads, MINB)
       };
       const uint32_t wbytes = kWStage;
       int i = 0;
-      if (!GROUPED) {
+      if (early) {
         // Weights do not depend on the previous kernel: start streaming them
         // before waiting for it, then fetch the token tiles.
         const int npre = nunits < STAGES ? nunits : STAGES;
-        gi = load_group<GROUPED>(a, 0);
+        GroupInfo pg[STAGES];
         for (; i < npre; ++i) {
+          const long long u = u0 + i;
+          const int g = GROUPED ? group_of(u) : 0;
+          if (g != gcur) {
+            gcur = g;
+            gi = load_group<GROUPED>(a, g);
+          }
+          pg[i] = gi;
           mbar_arrive_expect_tx(&full[i], wbytes + xbytes(gi));
-          issue_w(i, u0 + i);
+          issue_w(i, u);
         }
         // The units beyond the ring: pull up to kPrefetchBytes of them into
         // L2 while the previous kernel finishes, so that after the wait they
         // arrive at L2 rather than HBM latency and bandwidth.
         constexpr int kPfUnits = kPrefetchBytes / kWStage;
         const int npf = nunits - npre < kPfUnits ? nunits - npre : kPfUnits;
-        for (int j = 0; j < npf; ++j) prefetch_w(u0 + npre + j);
+        int pgrp = -1, pexp = 0;
+        for (int j = 0; j < npf; ++j) {
+          const long long u = u0 + npre + j;
+          const int g = GROUPED ? group_of(u) : 0;
+          if (g != pgrp) {
+            pgrp = g;
+            pexp = load_group<GROUPED>(a, g).e;
+          }
+          prefetch_w(u, pexp);
+        }
         griddep_wait();
-        for (int j = 0; j < npre; ++j) issue_x(j, u0 + j, gi);
+        for (int j = 0; j < npre; ++j) issue_x(j, u0 + j, pg[j]);
       }
       for (; i < nunits; ++i) {
         const int s = i % STAGES;
@@ -395,10 +424,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
         mbar_wait(&full[s], (uses - 1) & 1, a.timeout_ns, nullptr);
       }
     }
-    if (!GROUPED && lane != 0) griddep_wait();
+    if (early && lane != 0) griddep_wait();
   } else {
     // ---------------------------------------------------------------- consumers
-    if (!GROUPED) griddep_wait();
+    if (early) griddep_wait();
     const int w = warp - 1;
     const int ct = threadIdx.x - 32;
     const int q = lane & 7, rho = lane >> 3;  // CUDA-core path: chunk and row group
