@@ -105,13 +105,17 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ weights
 class Layer:
-    def __init__(self, l, device, torch):
+    def __init__(self, l, device, torch, skew=0.0):
         g = lambda shape, *key: wl.normal_bf16_cuda(shape, wl.WEIGHT_STD, "stack", l, *key,
                                                     device=device)
         self.Wq = g((H, H), "Wq")
         self.Wkv = g((KV, H), "Wkv")
         self.Wo = g((H, H), "Wo")
         self.Wr = wl.normal_bf16_cuda((E, H), wl.ROUTER_STD, "stack", l, "Wr", device=device)
+        if skew > 0:
+            # skewed-routing workload: row e scaled by c_e (power-law popularity)
+            c = torch.tensor(wl.router_scales(E, skew), dtype=torch.float32, device=device)
+            self.Wr.copy_((self.Wr.float() * c[:, None]).to(torch.bfloat16))
         self.W13 = g((E, 2 * I, H), "W13")
         self.W2 = g((E, H, I), "W2")
         self.Ws13 = g((2 * I, H), "Ws13")
@@ -153,7 +157,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     nl = args.layers
     t0 = time.time()
-    layers = [Layer(l, dev, torch) for l in range(nl)]
+    layers = [Layer(l, dev, torch, args.router_skew) for l in range(nl)]
     torch.cuda.synchronize()
     gen_s = time.time() - t0
 
@@ -323,7 +327,10 @@ def run_ours(args, rank, world, local_rank):
                         "+ MoE H=7168 E=384 top-8 I=2048 + shared expert), batches %s" %
                         (nl, list(BATCHES)),
             "layers": nl, "batches": list(BATCHES), "hidden": H, "experts": E, "topk": K8,
-            "inter": I, "l2": "inputs larger than L2 (each step streams ~%.0f GB of distinct "
+            "inter": I,
+            "routing": ("uniform (iid router scores)" if args.router_skew <= 0 else
+                        "skewed: router row e scaled by (e+1)^-%g, normalised" % args.router_skew),
+            "l2": "inputs larger than L2 (each step streams ~%.0f GB of distinct "
                               "weights)" % (step_bytes / 1e9),
             "prefetch": (False if args.no_prefetch else
                          "next layer's Wq, first %d bytes (half of L2), side stream" % pf_bytes),
@@ -416,7 +423,7 @@ def run_reference(args, rank, world, local_rank):
         dev = torch.device("cuda", local_rank)
     else:
         dev = torch.device("cpu")
-    L = Layer(0, dev, torch) if dev.type == "cuda" else None
+    L = Layer(0, dev, torch, args.router_skew) if dev.type == "cuda" else None
     if L is None:
         return {"impl": "reference", "unavailable": "the reference arm draws its weights on a GPU"}
     x_bits = wl.token_rows(1, H, "stack-x", 1)
@@ -454,6 +461,8 @@ def main():
     ap.add_argument("--no-prefetch", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--router-skew", type=float, default=0.0,
+                    help="power-law expert popularity (0 = the uniform workload)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

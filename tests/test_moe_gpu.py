@@ -109,6 +109,30 @@ def test_residual_combine():
     _check(x, Wr, W13, W2, Ws, 6, "residual", res=res)
 
 
+def test_routing_limits_topk32_of_1024_experts_64_tokens():
+    # the largest routing problem the block accepts: 2048 (token, slot) pairs
+    # over 1024 experts, 32 chosen per token
+    M, H, E, I, k = 64, 128, 1024, 64, 32
+    blk = _small_block(M, H, E, I, k, ("moe-limits",), shared=True)
+    _check(*blk, k, "E=1024 k=32 M=64")
+
+
+def test_skewed_routing_shares_experts_across_groups():
+    # power-law expert popularity: the most popular experts serve more than
+    # 16 tokens (several token groups each) and many experts serve none
+    M, H, E, I, k = 64, 256, 64, 128, 8
+    key = ("moe-skew",)
+    Wr = wl.skewed_router_bf16(E, H, 1.0, *key, "Wr")
+    x, _ = gap_rows(Wr, M, H, k, *key, "x")
+    W13 = np.stack([wl.normal_bf16((2 * I, H), 0.02, *key, "W13", e) for e in range(E)])
+    W2 = np.stack([wl.normal_bf16((H, I), 0.02, *key, "W2", e) for e in range(E)])
+    Ws = (wl.normal_bf16((2 * I, H), 0.02, *key, "Ws13"), wl.normal_bf16((H, I), 0.02, *key, "Ws2"))
+    idx = oracle.moe(x, Wr, lambda e: (W13[e], W2[e]), k, I, shared=None)["idx"]
+    counts = np.bincount(idx.ravel(), minlength=E)
+    assert counts.max() > 16 and (counts == 0).sum() > 0, counts
+    _check(x, Wr, W13, W2, Ws, k, "skewed routing")
+
+
 def test_repeat_calls_bit_identical():
     x, Wr, W13, W2, Ws = _small_block(33, 256, 64, 128, 8, ("moe-det",))
     a, _, _ = _gpu_moe(x, Wr, W13, W2, Ws, 8)

@@ -344,3 +344,12 @@ def test_generators_are_deterministic_and_scaled():
     xr = wl.token_rows(3, 128, "gen", "x", attempts=[0, 1, 0])
     assert np.array_equal(xr[0], wl.token_rows(1, 128, "gen", "x")[0])
     assert not np.array_equal(xr[1], wl.token_rows(2, 128, "gen", "x")[1])
+
+
+def test_skewed_router_scales():
+    c = wl.router_scales(384, 1.0)
+    assert abs(c.mean() - 1.0) < 1e-12 and np.all(np.diff(c) < 0)
+    assert np.allclose(wl.router_scales(16, 0.0), 1.0)
+    W = _dec(wl.skewed_router_bf16(8, 4096, 1.0, "gen", "Wr"))
+    sd = W.std(axis=1) / wl.ROUTER_STD
+    assert np.allclose(sd, wl.router_scales(8, 1.0), rtol=0.05)

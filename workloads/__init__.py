@@ -71,6 +71,25 @@ def one_hot_rows(N, K, *key):
     return f32_to_bf16_bits(W), perm
 
 
+def router_scales(E, s) -> np.ndarray:
+    """Per-expert scale of the router rows for a skewed-routing workload.
+
+    Row e of the router is drawn with standard deviation ROUTER_STD * c_e,
+    c_e = (e + 1)^-s normalised to mean 1: a token's score for expert e is
+    then ~N(0, c_e^2), so low-index experts win the top-k far more often
+    (popularity falls off roughly like a power law), tokens share experts and
+    fewer distinct experts are read. s = 0 is the uniform workload.
+    """
+    c = (np.arange(E, dtype=np.float64) + 1.0) ** (-float(s))
+    return c / c.mean()
+
+
+def skewed_router_bf16(E, H, s, *key) -> np.ndarray:
+    """[E, H] router weights of the skewed-routing workload, as bf16 bits."""
+    c = router_scales(E, s)
+    return np.stack([normal_bf16((H,), ROUTER_STD * c[e], *key, "row", e) for e in range(E)])
+
+
 def token_rows(M, H, *key, attempts=None) -> np.ndarray:
     """x rows ~N(0,1) as bf16 bits; row m is drawn from key (+m, attempt).
 
