@@ -163,9 +163,12 @@ int dec_add(const void* a, const void* b, void* out, size_t n, void* stream);
 
 /*
  * dec_last_choice -- regime and split of this thread's last dec_linear* call.
- * [trace-path] Returns regime | (S << 8) where regime is a DEC_REGIME_* value
- * and S the number of CTAs that share each output tile's K range (1 = none),
- * rounded up. DEC_REGIME_NONE before any call.
+ * [trace-path] Returns regime | (S << 8) | (C << 16) where regime is a
+ * DEC_REGIME_* value, S the number of CTAs that share each output tile's K
+ * range (1 = none), rounded up, and C is 1 when those S CTAs form one
+ * thread-block cluster and sum their partial tiles through distributed shared
+ * memory (small projections: few 128-row tiles, M <= 16), 0 when the split is
+ * the stream-K one with a last-arriver fixup. DEC_REGIME_NONE before any call.
  */
 int dec_last_choice(void);
 

@@ -193,7 +193,12 @@ def dec_add(a, b, out=None, stream=None):
 def last_choice():
     """(regime name, split factor) of this thread's last projection call."""
     v = lib().dec_last_choice()
-    return REGIME_NAMES.get(v & 0xFF, "?"), v >> 8
+    return REGIME_NAMES.get(v & 0xFF, "?"), (v >> 8) & 0xFF
+
+
+def last_cluster() -> bool:
+    """Whether this thread's last projection call used the cluster split."""
+    return bool((lib().dec_last_choice() >> 16) & 1)
 
 
 def last_grid() -> int:

@@ -200,6 +200,29 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
   const bool wide = S == 0 && regime != DEC_REGIME_TC && xr <= 16 && wide_units >= 10LL * s->sms;
   const long long tiles = wide ? (N + 255) / 256 : (N + 127) / 128;
   const long long T = tiles * KB;
+  // Cluster split for small narrow projections: cl CTAs per 128-row tile (a
+  // thread-block cluster), the largest portable size (<= 8) with
+  // tiles * cl <= SMs and cl <= KB. Used when it keeps at least three quarters
+  // of the SMs busy and each CTA streams at most 320 KB of weights: there the
+  // split-K fixup's latency dominates; beyond, all SMs' bandwidth does. No
+  // split-K workspace, counters or atomics.
+  int cl = 0;
+  if (S == 0 && regime != DEC_REGIME_TC && !wide && xr <= 16) {
+    for (int c = 8; c >= 2; c >>= 1)
+      if (tiles * c <= s->sms && c <= KB) {
+        cl = c;
+        break;
+      }
+    if (cl && (tiles * cl * 4 < 3LL * s->sms || 256LL * K / cl > 320LL * 1024)) cl = 0;
+  }
+  if (cl) {
+    Ctx cx = make_ctx(s, st);
+    t_last_choice = regime | (cl << 8) | (1 << 16);
+    t_last_grid = (int)(tiles * cl);
+    ProbeScope probe(2, st);
+    return counted(launch_dense_cluster(cx, xr, regime != DEC_REGIME_SMALLM, res != nullptr, x, W,
+                                        res, y, M, N, K, cl));
+  }
   long long grid = S ? tiles * S : (T < s->sms ? T : s->sms);
   if (grid > T) grid = T;
   const size_t slot_rows = wide ? 256 : 128;

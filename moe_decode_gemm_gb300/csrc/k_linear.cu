@@ -29,15 +29,19 @@ constexpr int dense_smem() {
 }
 
 // WIDE: 256-row output tiles, 64 KB weight stages (two 128-row halves).
-template <int XR, int EPI, bool WIDE = false>
+// CL > 0: cluster split, CL CTAs per output tile (grid = tiles * CL).
+template <int XR, int EPI, bool WIDE = false, bool CLUSTER = false>
 static cudaError_t run_dense(const Ctx& cx, bool mma, const void* x, const void* W, const void* res,
-                             void* y, int M, int N, int K, int grid, float* ws, int* ctr) {
+                             void* y, int M, int N, int K, int grid, float* ws, int* ctr,
+                             int cl = 0) {
   constexpr int S = dense_stages<XR, WIDE>();
   constexpr int MINB = dense_minb<XR, WIDE>();
   constexpr int SMEM = dense_smem<XR, WIDE>();
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
   static_assert(MINB == 1 || 2 * (SMEM + 1024) <= kSmemPerSm, "two CTAs per SM");
-  auto kern = wstream_kernel<XR, S, EPI, false, false, WIDE, ROLE_PROJECTION, MINB>;
+  static_assert(!CLUSTER || kTileRows * XR * 4 <= S * (kWBytes + kKSub * XR * 128),
+                "the partial tile fits in the stage ring");
+  auto kern = wstream_kernel<XR, S, EPI, false, false, WIDE, ROLE_PROJECTION, MINB, CLUSTER>;
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = allow_smem(kern, SMEM);
@@ -67,7 +71,26 @@ static cudaError_t run_dense(const Ctx& cx, bool mma, const void* x, const void*
   a.ctr = ctr;
   a.status = cx.status;
   a.timeout_ns = cx.timeout_ns;
+  if (CLUSTER)
+    return launch_kc(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, cl, wmap, xmap, a);
   return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
+}
+
+cudaError_t launch_dense_cluster(const Ctx& cx, int xr, bool mma, bool residual, const void* x,
+                                 const void* W, const void* res, void* y, int M, int N, int K,
+                                 int cl) {
+  const int grid = (N + kTileRows - 1) / kTileRows * cl;
+  if (xr == 8)
+    return residual ? run_dense<8, EPI_BF16_RES, false, true>(cx, mma, x, W, res, y, M, N, K, grid,
+                                                              nullptr, nullptr, cl)
+                    : run_dense<8, EPI_BF16, false, true>(cx, mma, x, W, res, y, M, N, K, grid,
+                                                          nullptr, nullptr, cl);
+  if (xr == 16)
+    return residual ? run_dense<16, EPI_BF16_RES, false, true>(cx, mma, x, W, res, y, M, N, K,
+                                                               grid, nullptr, nullptr, cl)
+                    : run_dense<16, EPI_BF16, false, true>(cx, mma, x, W, res, y, M, N, K, grid,
+                                                           nullptr, nullptr, cl);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_dense_wide(const Ctx& cx, int xr, bool mma, bool residual, const void* x,

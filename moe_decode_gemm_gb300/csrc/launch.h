@@ -29,6 +29,11 @@ cudaError_t launch_dense(const Ctx& cx, int xr, bool mma, bool residual, const v
 
 // Same with 256-row output tiles and 64 KB weight stages (xr 8 or 16): for
 // matrices large enough that every CTA gets ten or more stages of work.
+// Cluster split for narrow projections (xr 8 or 16): cl CTAs per 128-row tile,
+// 2 <= cl <= 8 and cl <= ceil(K/128); needs no workspace.
+cudaError_t launch_dense_cluster(const Ctx& cx, int xr, bool mma, bool residual, const void* x,
+                                 const void* W, const void* res, void* y, int M, int N, int K,
+                                 int cl);
 cudaError_t launch_dense_wide(const Ctx& cx, int xr, bool mma, bool residual, const void* x,
                               const void* W, const void* res, void* y, int M, int N, int K,
                               int grid, float* ws, int* ctr);

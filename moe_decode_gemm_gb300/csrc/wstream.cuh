@@ -233,9 +233,14 @@ constexpr int reduce_jb(bool paired, int eb, int loads) {
 // MINB: CTAs per SM the build must fit (registers and shared memory). With 2,
 // a call's CTA can start on an SM while the previous call's CTA there is
 // still finishing, and stream its weights before waiting for that call.
+// CLUSTER (dense 128-row tiles only): the kernel is launched in clusters of S
+// CTAs, cluster i owning output tile i and CTA r of it the r-th of S equal
+// shares of its k chunks; the S partial tiles are summed through distributed
+// shared memory, in rank order, behind two cluster barriers -- no global
+// partials, counters or atomics.
 enum Role : int { ROLE_PROJECTION = 0, ROLE_ROUTER = 1, ROLE_EXPERT = 2, ROLE_SHARED = 3 };
 template <int XR, int STAGES, int EPI, bool PAIRED, bool GROUPED, bool WIDE = false,
-          int ROLE = ROLE_PROJECTION, int MINB = 1>
+          int ROLE = ROLE_PROJECTION, int MINB = 1, bool CLUSTER = false>
 __global__ void __launch_bounds__(kThreads, MINB)
     wstream_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const StreamArgs a) {
@@ -295,8 +300,18 @@ __global__ void __launch_bounds__(kThreads, MINB)
   // least one and the contributors of a tile are exactly the CTAs between
   // the owners of its first and last unit.
   const long long G = (long long)gridDim.x < T ? (long long)gridDim.x : T;
-  const long long u0 = c < G ? cta_start(c, T, G) : 0;
-  const long long u1 = c < G ? cta_start(c + 1, T, G) : 0;
+  long long u0, u1;
+  if (CLUSTER) {
+    static_assert(!CLUSTER || (!GROUPED && !PAIRED && !WIDE), "cluster split: dense 128-row tiles");
+    const long long cs = cluster_size(), cr = cluster_rank();
+    const long long tile = c / cs;
+    u0 = tile * KB + cr * KB / cs;
+    u1 = tile * KB + (cr + 1) * KB / cs;
+    if (tile >= TILES) u0 = u1 = 0;
+  } else {
+    u0 = c < G ? cta_start(c, T, G) : 0;
+    u1 = c < G ? cta_start(c + 1, T, G) : 0;
+  }
   const int nunits = (int)(u1 - u0);
 
   if (warp == 0) {
@@ -425,6 +440,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
       }
     }
     if (early && lane != 0) griddep_wait();
+    if (CLUSTER) {
+      // the producer warp takes part in the consumers' two cluster barriers
+      __syncwarp();
+      cluster_sync_all();
+      cluster_sync_all();
+    }
   } else {
     // ---------------------------------------------------------------- consumers
     if (early) griddep_wait();
@@ -522,6 +543,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
 
     // This CTA's share of a tile that other CTAs also contribute to, written
     // to its workspace slot as [token][kSlotStride] fp32.
+    // Partial tiles go to global memory (L2) for the split-K fixup, or to
+    // this CTA's shared memory in cluster mode.
+    auto put = [](float* p, float v) {
+      if (CLUSTER) *p = v;
+      else __stcg(p, v);
+    };
     auto write_partial = [&](float* mine) {
       if (!use_mma) {
         if (q != 0) return;
@@ -532,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
 #pragma unroll
             for (int t = 0; t < 2; ++t)
               if (t < gi.c)
-                __stcg(mine + t * kSlotStride + h * kTileRows + 16 * w + rho + 4 * r, dacc[h][r][t]);
+                put(mine + t * kSlotStride + h * kTileRows + 16 * w + rho + 4 * r, dacc[h][r][t]);
         return;
       }
 #pragma unroll
@@ -544,8 +571,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
             const int t = tg * 8 + 2 * tq + hh;
             if (t < gi.c) {
               float* p = mine + t * kSlotStride + h * kTileRows + 16 * w + gq;
-              __stcg(p, macc[h][tg][hh]);
-              __stcg(p + 8, macc[h][tg][2 + hh]);
+              put(p, macc[h][tg][hh]);
+              put(p + 8, macc[h][tg][2 + hh]);
             }
           }
     };
@@ -701,7 +728,38 @@ __global__ void __launch_bounds__(kThreads, MINB)
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
-    if (cur >= 0) finish_tile(cur, false);
+    if (CLUSTER) {
+      // Partial tile [token][128] at the start of this CTA's shared memory
+      // (every stage has been consumed and no copy is in flight once all
+      // consumer warps are past their last stage).
+      float* part = reinterpret_cast<float*>(smem);
+      const bool aborted = s_flags[0] != 0;
+      if (cur >= 0 && !use_mma) reduce_dots();
+      named_bar_sync(1, kNCW * 32);
+      if (cur >= 0) {
+        write_partial(part);
+      } else {
+        // no k chunks (more ranks than chunks): this rank's share is zero
+        for (int e = ct; e < a.M * kTileRows; e += kNCW * 32) part[e] = 0.f;
+      }
+      cluster_sync_all();
+      // Rank r sums rows [r*128/S, (r+1)*128/S) of every token over the S
+      // partials, in rank order, and writes them.
+      const int cs = (int)cluster_size(), cr = (int)cluster_rank();
+      const int R = kTileRows / cs;
+      const int tile = (int)(blockIdx.x / cs);
+      if (!aborted && tile < TILES && nunits > 0) {
+        for (int e = ct; e < R * gi.c; e += kNCW * 32) {
+          const int t = e / R, r = cr * R + (e - t * R);
+          float v = 0.f;
+          for (int qr = 0; qr < cs; ++qr) v += ld_dsmem_f32(part + t * kTileRows + r, (uint32_t)qr);
+          emit(tile, r, t, v, 0.f);
+        }
+      }
+      cluster_sync_all();  // no CTA leaves while another still reads its partial
+    } else if (cur >= 0) {
+      finish_tile(cur, false);
+    }
     if (dgt >= 0) {
       if (ct == 0) settle(dgt, dold);
       named_bar_sync(1, kNCW * 32);

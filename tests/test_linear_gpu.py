@@ -158,6 +158,52 @@ def test_forced_regimes_agree(M, forces):
     assert np.array_equal(outs[forces[0]], outs[forces[1]])
 
 
+# ---------------------------------------------------------------- cluster split
+# Narrow projections with few 128-row tiles (M <= 16) split each tile's k
+# chunks over the CTAs of one thread-block cluster and sum the partial tiles
+# through distributed shared memory.
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4000, 1000), (3, 4000, 1288), (8, 2048, 1160),
+                                   (15, 1900, 904), (2, 4096, 4096)])
+def test_cluster_split_shapes(M, N, K):
+    # ragged last tile and last k chunk; uneven k shares between the ranks
+    y, (regime, cl) = _check_random(M, N, K, ("cluster", M, N, K))
+    assert dg.last_cluster() and cl >= 2 and regime == _expect_regime(M)
+    y2, _ = _gpu_linear(wl.normal_bf16((M, K), 1.0, "cluster", M, N, K, "x"),
+                        wl.normal_bf16((N, K), 0.02, "cluster", M, N, K, "W"))
+    assert torch.equal(y, y2), "cluster split not deterministic"
+
+
+@pytest.mark.parametrize("M", [1, 4, 15])
+def test_cluster_split_integer_inputs_match_stream_k(M):
+    # exact fp32 sums: the cluster split, the stream-K split and the oracle
+    # give the same bits
+    K, N = 2048, 4096
+    x = wl.integer_bf16((M, K), -2, 2, "cl-int", M, "x")
+    W = wl.integer_bf16((N, K), -2, 2, "cl-int", M, "W")
+    y, _ = _gpu_linear(x, W)
+    assert dg.last_cluster()
+    ys, (_, s_used) = _gpu_linear(x, W, S=4)
+    assert not dg.last_cluster() and s_used == 4
+    ref, _ = oracle.linear(x, W)
+    assert np.array_equal(wl.torch_to_bits(y), oracle.f64_to_bf16_bits(ref))
+    assert torch.equal(y, ys)
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_cluster_split_residual(M):
+    K, N = 1024, 4096
+    x = wl.normal_bf16((M, K), 1.0, "cl-res", M, "x")
+    W = wl.normal_bf16((N, K), 0.02, "cl-res", M, "W")
+    r = wl.normal_bf16((M, N), 1.0, "cl-res", M, "r")
+    y, _ = _gpu_linear(x, W, res_bits=r)
+    assert dg.last_cluster()
+    f, A = oracle.linear(x, W)
+    ref, Aref = oracle.residual(r, f, A)
+    assert_within_tol(to_f64(y), ref, Aref, "cluster residual M=%d" % M)
+
+
 def test_output_guard_bands_untouched():
     # the kernel writes exactly [M,N]: sentinel bytes around y stay intact
     M, N, K = 3, 200, 256
