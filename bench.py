@@ -147,6 +147,33 @@ def w13_launch_bytes(M, U):
     return U * 2 * 2 * I * H + 2 * M * H + 2 * M * K8 * I
 
 
+# ------------------------------------------------------------------ replicas
+# On N GPUs every rank runs its own replica of the workload on its own inputs
+# (the path has no cross-GPU step); the job's time is the slowest rank's and
+# its throughput the bytes all ranks streamed over that time.
+def replica_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def replica_max(values, world):
+    """Max over ranks of each value (every rank gets the result)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tbps(world, step_bytes, steps, ms):
+    """Whole-job TB/s: every rank's bytes over the slowest rank's time."""
+    return world * step_bytes * steps / (ms / 1e3) / 1e12
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -233,9 +260,7 @@ def run_ours(args, rank, world, local_rank):
     w13_experts = sum(w13_units)
 
     def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
+        replica_barrier(world)
 
     clocks = ClockSampler(local_rank)
     e0 = torch.cuda.Event(enable_timing=True)
@@ -297,15 +322,11 @@ def run_ours(args, rank, world, local_rank):
     ms_e2e = g0.elapsed_time(g1)
 
     # max over ranks
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_e2e = t.tolist()
+    ms, ms_e2e = replica_max([ms, ms_e2e], world)
 
     peak_gbs, peak_kind = peaks()
-    tbps = world * step_bytes * args.steps / (ms / 1e3) / 1e12
-    tbps_e2e = world * step_bytes * args.steps / (ms_e2e / 1e3) / 1e12
+    tbps = job_tbps(world, step_bytes, args.steps, ms)
+    tbps_e2e = job_tbps(world, step_bytes, args.steps, ms_e2e)
     expect_n = args.steps * len(BATCHES) * nl
     w13_ach = (w13_bytes * args.steps) / (w13_ms / 1e3) / 1e9 if w13_n == expect_n else None
     h2d = sum(2 * M * H for M in BATCHES)
