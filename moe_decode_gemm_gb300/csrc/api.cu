@@ -336,7 +336,8 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   // join before the combine.
   const int egrid = s->sms;
   if (shared) {
-    const int sgrid = s->sms - router_grid(s->sms);
+    const int rc_ctas = router_ctas(E, H);
+    const int sgrid = s->sms - rc_ctas > 0 ? s->sms - rc_ctas : 1;
     if (cudaEventRecord(s->ev_fork, st) != cudaSuccess) return DEC_ECUDA;
     if (cudaStreamWaitEvent(s->side, s->ev_fork, 0) != cudaSuccess) return DEC_ECUDA;
     Ctx sx = make_ctx(s, s->side);
@@ -351,9 +352,7 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   }
   {
     ProbeScope p(3, st);
-    if ((rc = counted(launch_router(cx, x, Wr, M, H, E, s->mb, ws,
-                                    ctr + (size_t)max_groups * maxt))))
-      return rc;
+    if ((rc = counted(launch_router(cx, x, Wr, M, H, E, s->mb)))) return rc;
   }
   if ((rc = counted(launch_topk(cx, M, E, topk, topk_idx, topk_w, s->mb)))) return rc;
   if ((rc = counted(launch_gather(cx, x, M, H, E, topk, s->mb)))) return rc;

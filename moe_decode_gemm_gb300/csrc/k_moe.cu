@@ -38,21 +38,26 @@ static StreamArgs base_args(const Ctx& cx, float* ws, int* ctr) {
 
 // ------------------------------------------------------------------ router
 // logits[m, e] = x[m]·Wr[e] in fp32 (not rounded): the weight-streaming kernel
-// with fp32 output, token rows per stage sized to M.
+// with fp32 output, token rows per stage sized to M. The router streams only
+// E*H bf16 (5.5 MB for 384 x 7168) and is latency bound: it runs in the
+// cluster split, router_clusters(H) CTAs per 128-row tile of experts summing
+// their partial tiles through distributed shared memory, so no split-K fixup
+// through L2 sits on the routing path; the shared expert streams on the
+// other SMs meanwhile.
 template <int XR>
 static cudaError_t run_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E,
-                              const MoeBufs& b, float* ws, int* ctr) {
+                              const MoeBufs& b) {
   constexpr int STAGES = XR == 64 ? 4 : 6;
   constexpr int SMEM = wstream_smem(XR, STAGES, 0);
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
-  auto kern = wstream_kernel<XR, STAGES, EPI_F32, false, false, false, ROLE_ROUTER>;
+  auto kern = wstream_kernel<XR, STAGES, EPI_F32, false, false, false, ROLE_ROUTER, 1, true>;
   static bool done = false;
   cudaError_t e = smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;
   CUtensorMap wmap, xmap;
   if (!make_tmap(&wmap, Wr, (uint64_t)E, (uint64_t)H, kTileRows, true)) return cudaErrorInvalidValue;
   if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)H, XR, false)) return cudaErrorInvalidValue;
-  StreamArgs a = base_args(cx, ws, ctr);
+  StreamArgs a = base_args(cx, nullptr, nullptr);
   a.K = H;
   a.KB = (H + kKChunk - 1) / kKChunk;
   a.TILES = (E + kTileRows - 1) / kTileRows;
@@ -60,20 +65,16 @@ static cudaError_t run_router(const Ctx& cx, const void* x, const void* Wr, int 
   a.M = M;
   a.out = b.logits;
   a.ldo = E;
-  // The router streams only E*H bf16 (5.5 MB for 384 x 7168) and is latency
-  // bound: a sixth of the SMs keeps the number of CTAs per output tile, and so
-  // the split-K fixup, small; the shared expert streams on the other SMs.
-  const long long T = (long long)a.TILES * a.KB;
-  const int cap = router_grid(cx.sms);
-  const int grid = (int)(T < cap ? T : cap);
-  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
+  const int cl = router_clusters(H);
+  return launch_kc(kern, dim3(a.TILES * cl), dim3(kThreads), SMEM, cx.stream, cx.pdl, cl, wmap,
+                   xmap, a);
 }
 
 cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E,
-                          const MoeBufs& b, float* ws, int* ctr) {
-  if (M <= 8) return run_router<8>(cx, x, Wr, M, H, E, b, ws, ctr);
-  if (M <= 16) return run_router<16>(cx, x, Wr, M, H, E, b, ws, ctr);
-  return run_router<64>(cx, x, Wr, M, H, E, b, ws, ctr);
+                          const MoeBufs& b) {
+  if (M <= 8) return run_router<8>(cx, x, Wr, M, H, E, b);
+  if (M <= 16) return run_router<16>(cx, x, Wr, M, H, E, b);
+  return run_router<64>(cx, x, Wr, M, H, E, b);
 }
 
 // ------------------------------------------------------------------ top-k

@@ -59,11 +59,16 @@ struct MoeBufs {
   float* s;        // [M, H]
 };
 
-// CTAs of the router kernel: a sixth of the SMs (it is latency bound).
-inline int router_grid(int sms) { return sms / 6 > 0 ? sms / 6 : 1; }
+// Router: CTAs per 128-row tile of experts (one thread-block cluster each),
+// at most 8 and at most the number of 128-wide k chunks; and its CTA count.
+inline int router_clusters(int H) {
+  const int kb = (H + 127) / 128;
+  return kb < 8 ? kb : 8;
+}
+inline int router_ctas(int E, int H) { return (E + 127) / 128 * router_clusters(H); }
 
 cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E,
-                          const MoeBufs& b, float* ws, int* ctr);
+                          const MoeBufs& b);
 cudaError_t launch_topk(const Ctx& cx, int M, int E, int k, int32_t* idx_user, float* w_user,
                         const MoeBufs& b);
 cudaError_t launch_gather(const Ctx& cx, const void* x, int M, int H, int E, int k,

@@ -395,7 +395,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
         // The units beyond the ring: pull up to kPrefetchBytes of them into
         // L2 while the previous kernel finishes, so that after the wait they
         // arrive at L2 rather than HBM latency and bandwidth.
-        constexpr int kPfUnits = kPrefetchBytes / kWStage;
+        // (not in cluster mode: there the shares are small and it did not pay)
+        constexpr int kPfUnits = CLUSTER ? 0 : kPrefetchBytes / kWStage;
         const int npf = nunits - npre < kPfUnits ? nunits - npre : kPfUnits;
         int pgrp = -1, pexp = 0;
         for (int j = 0; j < npf; ++j) {
