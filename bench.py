@@ -1,8 +1,8 @@
 """Benchmark: weight-stream TB/s and µs per call of the decode step on GB300.
 
 Default workload -- the synthetic decode layer stack: 4 layers, each
-  q  = x·Wqᵀ (7168 -> 7168),  kv = x·Wkvᵀ (7168 -> 1024),
-  r  = x + q·Woᵀ (7168 -> 7168, residual fused),
+  [q | kv] = x·[Wq; Wkv]ᵀ  (7168 -> 7168 | 1024, one fused projection),
+  r  = x + q·Woᵀ (7168 -> 7168, residual fused; q read in place),
   x' = r + MoE(r)  (hidden 7168, 384 experts, top-8, SwiGLU intermediate 2048,
                     one shared expert on a second stream),
 plus an L2 prefetch of the next layer's q weights (at most half of L2) on a
@@ -108,8 +108,13 @@ class Layer:
     def __init__(self, l, device, torch, skew=0.0):
         g = lambda shape, *key: wl.normal_bf16_cuda(shape, wl.WEIGHT_STD, "stack", l, *key,
                                                     device=device)
-        self.Wq = g((H, H), "Wq")
-        self.Wkv = g((KV, H), "Wkv")
+        # q and kv weights stored as one [H + KV, H] matrix: one fused projection
+        self.Wqkv = torch.empty((H + KV, H), dtype=torch.bfloat16, device=device)
+        wl.normal_bf16_cuda((H, H), wl.WEIGHT_STD, "stack", l, "Wq", device=device,
+                            out=self.Wqkv[:H])
+        wl.normal_bf16_cuda((KV, H), wl.WEIGHT_STD, "stack", l, "Wkv", device=device,
+                            out=self.Wqkv[H:])
+        self.Wq, self.Wkv = self.Wqkv[:H], self.Wqkv[H:]
         self.Wo = g((H, H), "Wo")
         self.Wr = wl.normal_bf16_cuda((E, H), wl.ROUTER_STD, "stack", l, "Wr", device=device)
         if skew > 0:
@@ -131,8 +136,8 @@ def moe_bytes(M, U):
 
 
 def layer_bytes(M, U):
-    return (linear_bytes(M, H, H) + linear_bytes(M, KV, H) + linear_bytes(M, H, H) + 2 * M * H
-            + moe_bytes(M, U))
+    # fused q|kv projection (x read once), o projection, residual add fused
+    return linear_bytes(M, H + KV, H) + linear_bytes(M, H, H) + 2 * M * H + moe_bytes(M, U)
 
 
 # DRAM traffic (read + write) of the routed gate/up kernel per chosen expert,
@@ -203,8 +208,7 @@ def run_ours(args, rank, world, local_rank):
         acts[M] = dict(
             x0=x0,
             xs=[torch.empty((M, H), dtype=torch.bfloat16, device=dev) for _ in range(nl + 1)],
-            q=torch.empty((M, H), dtype=torch.bfloat16, device=dev),
-            kv=torch.empty((M, KV), dtype=torch.bfloat16, device=dev),
+            qkv=torch.empty((M, H + KV), dtype=torch.bfloat16, device=dev),
             r=torch.empty((M, H), dtype=torch.bfloat16, device=dev),
             idx=[torch.empty((M, K8), dtype=torch.int32, device=dev) for _ in range(nl)],
         )
@@ -217,9 +221,9 @@ def run_ours(args, rank, world, local_rank):
         a = acts[M]
         for l, L in enumerate(layers):
             x = a["xs"][l]
-            dg.dec_linear(x, L.Wq, a["q"], stream=main)
-            dg.dec_linear(x, L.Wkv, a["kv"], stream=main)
-            dg.dec_linear(a["q"], L.Wo, a["r"], stream=main, residual=x)
+            # q and kv in one projection; o reads q in place (row stride H + KV)
+            dg.dec_linear(x, L.Wqkv, a["qkv"], stream=main)
+            dg.dec_linear(a["qkv"][:, :H], L.Wo, a["r"], stream=main, residual=x)
             if not args.no_prefetch:
                 nxt = layers[(l + 1) % nl]
                 ev_fork[l].record(main)
@@ -344,9 +348,9 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "bf16",
         "data": "synthetic (seeded random-init bf16 weights of the stated shapes, N(0,1) tokens)",
         "config": {
-            "workload": "decode layer stack: %d layers x (q/kv/o projections 7168->7168/1024/7168 "
-                        "+ MoE H=7168 E=384 top-8 I=2048 + shared expert), batches %s" %
-                        (nl, list(BATCHES)),
+            "workload": "decode layer stack: %d layers x (q/kv/o projections 7168->7168/1024/7168, "
+                        "q and kv as one fused 7168->8192 projection, + MoE H=7168 E=384 top-8 "
+                        "I=2048 + shared expert), batches %s" % (nl, list(BATCHES)),
             "layers": nl, "batches": list(BATCHES), "hidden": H, "experts": E, "topk": K8,
             "inter": I,
             "routing": ("uniform (iid router scores)" if args.router_skew <= 0 else

@@ -91,6 +91,17 @@ int dec_linear_residual(const void* x, const void* W, const void* res, void* y,
                         int M, int N, int K, void* stream);
 
 /*
+ * dec_linear_ex -- dec_linear with a row stride for x and an optional residual:
+ * y = bf16(x·Wᵀ), or bf16(res + x·Wᵀ) when res is not NULL, where row m of x
+ * starts ldx elements after row m-1 (ldx >= K, ldx % 8 == 0). A column slice
+ * of a wider activation -- the q part of a fused q|kv projection's output,
+ * say -- is then read in place. res ([M,N] bf16) may alias y. x must be
+ * 16-byte aligned. Errors as dec_linear; DEC_EINVAL also for a bad ldx.
+ */
+int dec_linear_ex(const void* x, int ldx, const void* W, const void* res, void* y,
+                  int M, int N, int K, void* stream);
+
+/*
  * dec_linear_splitk -- dec_linear with the split factor forced to S
  * (1 <= S <= min(256, ceil(K/128))): the grid has S CTAs per 128-row output
  * tile and each takes an equal share of the tile's 128-wide K chunks (shares

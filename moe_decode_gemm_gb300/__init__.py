@@ -28,7 +28,7 @@ REGIME_NAMES = {0: "none", 1: "smallm", 2: "mma", 3: "tc"}
 
 # Names the header declares; the ABI tests check every one is exported.
 EXPORTS = [
-    "dec_linear", "dec_linear_residual", "dec_linear_splitk", "moe_decode",
+    "dec_linear", "dec_linear_residual", "dec_linear_ex", "dec_linear_splitk", "moe_decode",
     "moe_decode_residual", "l2_prefetch", "dec_add", "dec_last_choice", "dec_last_grid",
     "dec_strerror", "dec_sync_check", "dec_set_wait_timeout_ns", "dec_selftest_timeout",
     "dec_launch_count", "dec_probe_begin", "dec_probe_end", "dec_shutdown", "dec_version",
@@ -56,6 +56,7 @@ def lib():
         sig = {
             "dec_linear": (I, [P, P, P, I, I, I, P]),
             "dec_linear_residual": (I, [P, P, P, P, I, I, I, P]),
+            "dec_linear_ex": (I, [P, I, P, P, P, I, I, I, P]),
             "dec_linear_splitk": (I, [P, P, P, I, I, I, I, P]),
             "moe_decode": (I, [P, P, P, P, P, P, P, I, I, I, I, I, P, P, P]),
             "moe_decode_residual": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, P]),
@@ -107,7 +108,9 @@ def _stream(stream):
 def dec_linear(x, W, y=None, stream=None, residual=None):
     """y = x·Wᵀ (bf16), or y = residual + x·Wᵀ when ``residual`` is given.
 
-    x: [M,K] bf16, W: [N,K] bf16, y: [M,N] bf16 (allocated if None).
+    x: [M,K] bf16 with unit column stride; its rows may be further apart than
+    K (a column slice of a wider tensor, read in place through dec_linear_ex).
+    W: [N,K] bf16, y: [M,N] bf16 (allocated if None).
     """
     import torch
 
@@ -115,7 +118,13 @@ def dec_linear(x, W, y=None, stream=None, residual=None):
     N = W.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
-    if residual is None:
+    ldx = x.stride(0) if M > 1 else K
+    if x.stride(1) != 1:
+        raise ValueError("dec_linear: x needs unit column stride")
+    if ldx != K:
+        rc = lib().dec_linear_ex(_ptr(x), ldx, _ptr(W), _ptr(residual), _ptr(y), M, N, K,
+                                 _stream(stream))
+    elif residual is None:
         rc = lib().dec_linear(_ptr(x), _ptr(W), _ptr(y), M, N, K, _stream(stream))
     else:
         rc = lib().dec_linear_residual(_ptr(x), _ptr(W), _ptr(residual), _ptr(y), M, N, K,

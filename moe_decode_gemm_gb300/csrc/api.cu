@@ -23,7 +23,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 static std::once_flag g_encode_once;
 
 bool make_tmap(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
-               bool l2_promote_256) {
+               bool l2_promote_256, uint64_t ld) {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -34,7 +34,7 @@ bool make_tmap(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, 
   });
   if (!g_encode || rows == 0 || cols == 0) return false;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
+  cuuint64_t strides[1] = {(ld ? ld : cols) * 2};  // bytes between rows
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
@@ -179,9 +179,10 @@ static int regime_for(int M) {
 }
 
 static int linear_impl(const void* x, const void* W, const void* res, void* y, int M, int N, int K,
-                       int S, void* stream) {
+                       int S, void* stream, long long ldx = 0) {
   if (!x || !W || !y) return DEC_EINVAL;
   if (M < 1 || N < 1 || K < 8 || (K % 8) != 0) return DEC_EINVAL;
+  if (ldx != 0 && (ldx < K || (ldx % 8) != 0)) return DEC_EINVAL;
   if (!aligned16(x) || !aligned16(W) || !aligned16(y) || (res && !aligned16(res))) return DEC_EINVAL;
   if (M > 64) return DEC_EUNSUPPORTED;
   const int KB = (K + 127) / 128;  // 128-wide k chunks (one pipeline stage each)
@@ -217,6 +218,7 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
   }
   if (cl) {
     Ctx cx = make_ctx(s, st);
+    cx.ldx = ldx;
     t_last_choice = regime | (cl << 8) | (1 << 16);
     t_last_grid = (int)(tiles * cl);
     ProbeScope probe(2, st);
@@ -229,6 +231,7 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
   if ((rc = ensure(s->ws_main, (size_t)grid * 2 * slot_rows * xr * sizeof(float), st))) return rc;
   if ((rc = ensure(s->ctr_main, (size_t)tiles * sizeof(int), st))) return rc;
   Ctx cx = make_ctx(s, st);
+  cx.ldx = ldx;
   long long seff = (KB * grid + T - 1) / T;
   if (seff < 1) seff = 1;
   t_last_choice = regime | ((int)seff << 8);
@@ -392,6 +395,12 @@ int dec_linear_residual(const void* x, const void* W, const void* res, void* y, 
                         void* stream) {
   if (!res) return DEC_EINVAL;
   return linear_impl(x, W, res, y, M, N, K, 0, stream);
+}
+
+int dec_linear_ex(const void* x, int ldx, const void* W, const void* res, void* y, int M, int N,
+                  int K, void* stream) {
+  if (ldx < 1) return DEC_EINVAL;
+  return linear_impl(x, W, res, y, M, N, K, 0, stream, ldx);
 }
 
 int dec_linear_splitk(const void* x, const void* W, void* y, int M, int N, int K, int S,

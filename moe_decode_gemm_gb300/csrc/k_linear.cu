@@ -56,7 +56,8 @@ static cudaError_t run_dense(const Ctx& cx, bool mma, const void* x, const void*
   constexpr int kTile = WIDE ? 2 * kTileRows : kTileRows;
   CUtensorMap wmap, xmap;
   if (!make_tmap(&wmap, W, (uint64_t)N, (uint64_t)K, kTileRows, true)) return cudaErrorInvalidValue;
-  if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)K, XR, false)) return cudaErrorInvalidValue;
+  if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)K, XR, false, (uint64_t)cx.ldx))
+    return cudaErrorInvalidValue;
   StreamArgs a = {};
   a.K = K;
   a.KB = (K + kKChunk - 1) / kKChunk;

@@ -287,7 +287,8 @@ static cudaError_t run_tc(const Ctx& cx, const void* x, const void* W, const voi
   const int NP = (M + 15) / 16 * 16;
   CUtensorMap wmap, xmap;
   if (!make_tmap(&wmap, W, (uint64_t)N, (uint64_t)K, kTileRows, true)) return cudaErrorInvalidValue;
-  if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)K, (uint32_t)NP, false)) return cudaErrorInvalidValue;
+  if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)K, (uint32_t)NP, false, (uint64_t)cx.ldx))
+    return cudaErrorInvalidValue;
   StreamArgs a = {};
   a.K = K;
   a.KB = (K + kKChunk - 1) / kKChunk;

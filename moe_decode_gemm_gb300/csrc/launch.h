@@ -10,7 +10,7 @@ namespace dg {
 // Tensor map of a row-major bf16 matrix [rows, cols] read in boxes of
 // 64 columns x box_rows rows with 128-byte swizzle. Returns false on failure.
 bool make_tmap(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
-               bool l2_promote_256);
+               bool l2_promote_256, uint64_t ld = 0);
 
 struct Ctx {
   int sms;
@@ -18,6 +18,7 @@ struct Ctx {
   int* status;
   cudaStream_t stream;
   bool pdl;
+  long long ldx = 0;  // dense projections: elements between rows of x (0: K)
 };
 
 // Dense projection: y = x·Wᵀ (+ res), XR in {8, 16, 64} token rows per stage.

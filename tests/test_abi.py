@@ -54,6 +54,12 @@ def test_linear_rejects(L, args, code):
     assert L.dec_linear(*args, None) == code
 
 
+@pytest.mark.parametrize("ldx", [0, -8, 32, 68, 100])
+def test_linear_ex_rejects_bad_row_stride(L, ldx):
+    # K = 64: the row stride must be >= K and a multiple of 8
+    assert L.dec_linear_ex(A, ldx, A, None, A, 1, 16, 64, None) == dg.DEC_EINVAL
+
+
 def test_splitk_rejects_bad_split(L):
     assert L.dec_linear_splitk(A, A, A, 4, 16, 64, 0, None) == dg.DEC_EINVAL
     assert L.dec_linear_splitk(A, A, A, 4, 16, 64, 2, None) == dg.DEC_EINVAL  # S > K/64

@@ -204,6 +204,30 @@ def test_cluster_split_residual(M):
     assert_within_tol(to_f64(y), ref, Aref, "cluster residual M=%d" % M)
 
 
+@pytest.mark.parametrize("M,N,K,ldx", [(1, 7168, 7168, 8192), (4, 4096, 2048, 2056),
+                                       (16, 1024, 2048, 4096), (64, 640, 1536, 1544),
+                                       (2, 4096, 4096, 8192)])
+def test_row_strided_input_reads_a_column_slice(M, N, K, ldx):
+    # x is the first K columns of a [M, ldx] activation (the q part of a fused
+    # q|kv output, say): read in place, with and without a residual
+    wide = wl.normal_bf16((M, ldx), 1.0, "ldx", M, N, K, "xw")
+    W = wl.normal_bf16((N, K), 0.02, "ldx", M, N, K, "W")
+    r = wl.normal_bf16((M, N), 1.0, "ldx", M, N, K, "r")
+    xt = wl.bits_to_torch(wide)[:, :K]
+    assert xt.stride(0) == ldx
+    f, A = oracle.linear(wide[:, :K], W)
+    y = dg.dec_linear(xt, wl.bits_to_torch(W))
+    assert dg.sync_check() == dg.DEC_OK
+    assert_within_tol(to_f64(y), f, A, "ldx=%d" % ldx)
+    y2 = dg.dec_linear(xt, wl.bits_to_torch(W), residual=wl.bits_to_torch(r))
+    assert dg.sync_check() == dg.DEC_OK
+    ref, Aref = oracle.residual(r, f, A)
+    assert_within_tol(to_f64(y2), ref, Aref, "ldx=%d residual" % ldx)
+    # the same bits as on a contiguous copy
+    y3 = dg.dec_linear(xt.contiguous(), wl.bits_to_torch(W))
+    assert torch.equal(y, y3)
+
+
 def test_output_guard_bands_untouched():
     # the kernel writes exactly [M,N]: sentinel bytes around y stay intact
     M, N, K = 3, 200, 256
