@@ -182,3 +182,48 @@ def test_full_size_block(full_bank, M):
                    shared=(wl.torch_to_bits(Ws13), wl.torch_to_bits(Ws2)), tokens=tokens)
     got = to_f64(out)
     assert_within_tol(got[tokens], r["out"][tokens], r["absref"][tokens], "full M=%d" % M)
+
+
+# ---------------------------------------------------------------- decode layer
+@pytest.mark.parametrize("M", [1, 5, 33])
+def test_decode_layer_composition(M):
+    """The layer as the benchmark composes it: one fused q|kv projection, the o
+    projection reading q in place with the residual fused, then the MoE block
+    with its residual; every stage against the oracle on the GPU's own input
+    to that stage."""
+    H, KV, E, I, k = 256, 64, 32, 128, 4
+    key = ("layer", M)
+    Wr = wl.normal_bf16((E, H), 1.0 / math.sqrt(H), *key, "Wr")
+    x, _ = gap_rows(Wr, M, H, k, *key, "x")
+    Wq = wl.normal_bf16((H, H), 0.02, *key, "Wq")
+    Wkv = wl.normal_bf16((KV, H), 0.02, *key, "Wkv")
+    Wo = wl.normal_bf16((H, H), 0.02, *key, "Wo")
+    W13 = np.stack([wl.normal_bf16((2 * I, H), 0.02, *key, "W13", e) for e in range(E)])
+    W2 = np.stack([wl.normal_bf16((H, I), 0.02, *key, "W2", e) for e in range(E)])
+    Ws = (wl.normal_bf16((2 * I, H), 0.02, *key, "Ws13"), wl.normal_bf16((H, I), 0.02, *key, "Ws2"))
+    t = wl.bits_to_torch
+    xt = t(x)
+    qkv = dg.dec_linear(xt, t(np.concatenate([Wq, Wkv])))
+    assert dg.sync_check() == dg.DEC_OK
+    ref, A = oracle.linear(x, np.concatenate([Wq, Wkv]))
+    assert_within_tol(to_f64(qkv), ref, A, "q|kv")
+    q_bits = wl.torch_to_bits(qkv)[:, :H]
+    # o projection on the q columns of the fused output, residual x
+    r = dg.dec_linear(qkv[:, :H], t(Wo), residual=xt)
+    assert dg.sync_check() == dg.DEC_OK
+    o, oA = oracle.linear(q_bits, Wo)
+    rref, rA = oracle.residual(x, o, oA)
+    assert_within_tol(to_f64(r), rref, rA, "o + residual")
+    # MoE block on r with its residual; with Wo = 0 the block's input is x
+    # exactly, whose router scores satisfy the gap rule, so the chosen experts
+    # must match the oracle's bit for bit
+    r0 = dg.dec_linear(qkv[:, :H], t(np.zeros_like(Wo)), residual=xt)
+    assert torch.equal(r0, xt)
+    idx = torch.full((M, k), -1, dtype=torch.int32, device="cuda")
+    out = dg.moe_decode(r0, t(Wr), t(W13), t(W2), t(Ws[0]), t(Ws[1]), k, topk_idx=idx,
+                        residual=r0)
+    assert dg.sync_check() == dg.DEC_OK
+    mo = oracle.moe(x, Wr, lambda e: (W13[e], W2[e]), k, I, shared=Ws)
+    assert np.array_equal(idx.cpu().numpy(), mo["idx"])
+    oref, oA2 = oracle.residual(x, mo["out"], mo["absref"])
+    assert_within_tol(to_f64(out), oref, oA2, "moe + residual")
