@@ -36,18 +36,19 @@ _TRUE = ("true", "1")
 
 def kernel_label(name):
     """Readable label for one (demangled) kernel name."""
-    m = re.search(r"wstream_kernel<(\d+), (\d+), (\d+), (\w+), (\w+), (\w+)(?:, (\d+))?"
-                  r"(?:, (\d+))?>", name)
+    m = re.search(r"wstream_kernel<([^>]*)>", name)
     if m:
-        xr, st, epi, paired, grouped, wide, role, minb = m.groups()
-        role = _ROLE.get(role or "0", role)
+        p = [v.strip() for v in m.group(1).split(",")]
+        p += ["0"] * (9 - len(p))  # defaults: projection role, 1 CTA per SM, no cluster
+        xr, st, epi, paired, grouped, wide, role, minb, cluster = p[:9]
+        role = _ROLE.get(role, role)
         part = ""
         if role in ("routed expert", "shared expert"):
             part = " gate/up" if paired in _TRUE else " down"
         tile = "256-row" if wide in _TRUE else "128-row"
-        occ = " 2/SM" if minb == "2" else ""
+        extra = (" 2/SM" if minb == "2" else "") + (" cluster" if cluster in _TRUE else "")
         return "%s%s [wstream XR=%s S=%s %s %s%s]" % (role, part, xr, st, _EPI.get(epi, epi), tile,
-                                                     occ)
+                                                     extra)
     m = re.search(r"tc_linear_kernel<(\d+)>", name)
     if m:
         return "projection [tcgen05 %s]" % _EPI.get(m.group(1), m.group(1))
