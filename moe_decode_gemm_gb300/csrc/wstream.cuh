@@ -162,37 +162,33 @@ __device__ __forceinline__ void reduce_partials(const float* ws, long long slot_
     auto add = [](float4& acc, const float4& v) {
       acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     };
-    int j = 0;
-    for (; j + JB <= nc; j += JB) {
+    // JB contributors per round, the last round predicated: every round keeps
+    // all of its loads in flight, however few contributors are left.
+    for (int j = 0; j < nc; j += JB) {
       float4 pg[JB][EB], pu[JB][EB];
 #pragma unroll
       for (int jj = 0; jj < JB; ++jj) {
-        const float* b = ws + slot_of(j + jj) * slot_floats;
+        if (j + jj < nc) {
+          const float* b = ws + slot_of(j + jj) * slot_floats;
 #pragma unroll
-        for (int q = 0; q < EB; ++q) {
-          if (ok[q]) {
-            pg[jj][q] = __ldcg(reinterpret_cast<const float4*>(b + off[q]));
-            if (PAIRED) pu[jj][q] = __ldcg(reinterpret_cast<const float4*>(b + off[q] + kTileRows));
+          for (int q = 0; q < EB; ++q) {
+            if (ok[q]) {
+              pg[jj][q] = __ldcg(reinterpret_cast<const float4*>(b + off[q]));
+              if (PAIRED) pu[jj][q] = __ldcg(reinterpret_cast<const float4*>(b + off[q] + kTileRows));
+            }
           }
         }
       }
 #pragma unroll
-      for (int jj = 0; jj < JB; ++jj)
+      for (int jj = 0; jj < JB; ++jj) {
+        if (j + jj < nc) {
 #pragma unroll
-        for (int q = 0; q < EB; ++q) {
-          if (ok[q]) {
-            add(g[q], pg[jj][q]);
-            if (PAIRED) add(u[q], pu[jj][q]);
+          for (int q = 0; q < EB; ++q) {
+            if (ok[q]) {
+              add(g[q], pg[jj][q]);
+              if (PAIRED) add(u[q], pu[jj][q]);
+            }
           }
-        }
-    }
-    for (; j < nc; ++j) {
-      const float* b = ws + slot_of(j) * slot_floats;
-#pragma unroll
-      for (int q = 0; q < EB; ++q) {
-        if (ok[q]) {
-          add(g[q], __ldcg(reinterpret_cast<const float4*>(b + off[q])));
-          if (PAIRED) add(u[q], __ldcg(reinterpret_cast<const float4*>(b + off[q] + kTileRows)));
         }
       }
     }
