@@ -219,7 +219,7 @@ long long dec_launch_count(void);
  * dec_probe_begin / dec_probe_end -- time every launch of one kernel kind with
  * CUDA events recorded on the stream the kernel is launched on.
  * kind: 0 = routed-expert gate/up kernel, 1 = routed-expert down kernel,
- *       2 = projection kernels, 3 = router/top-k kernel, 4 = combine kernel.
+ *       2 = projection kernels, 3 = router projection kernel, 4 = combine kernel.
  * dec_probe_begin arms the probe for up to `capacity` launches (0 disarms).
  * dec_probe_end synchronises those events and returns, through the
  * pointers, the summed duration in ms and the number of launches timed.

@@ -314,12 +314,12 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   if ((rc = moe_bufs(s, M, H, E, topk, I, st))) return rc;
   // partial slots: 2 per CTA, up to 256 rows (gate + up halves) x 64 tokens
   const size_t ws_bytes = (size_t)s->sms * 2 * 256 * 64 * sizeof(float);
-  const int tiles13 = (I + 127) / 128, tiles2 = (H + 127) / 128, tilesr = (E + 127) / 128;
+  const int tiles13 = (I + 127) / 128, tiles2 = (H + 127) / 128;
   int maxt = tiles13 > tiles2 ? tiles13 : tiles2;
   // an expert chosen by more than 16 tokens forms several groups: at most
   // E + M*topk/16 groups, each with its own tile counters
   const int max_groups = E + (M * topk + 15) / 16;
-  const size_t ctr_bytes = (size_t)(max_groups * (size_t)maxt + tilesr + 64) * sizeof(int);
+  const size_t ctr_bytes = (size_t)(max_groups * (size_t)maxt + 64) * sizeof(int);
   if ((rc = ensure(s->ws_main, ws_bytes, st))) return rc;
   if ((rc = ensure(s->ctr_main, ctr_bytes, st))) return rc;
   const bool shared = Ws13 != nullptr;
