@@ -13,10 +13,13 @@
 
     python -m moe_decode_gemm_gb300.profiling case moe TOKENS EXPERTS [CALLS]
     python -m moe_decode_gemm_gb300.profiling case linear M N K [CALLS]
+    python -m moe_decode_gemm_gb300.profiling case router TOKENS [CALLS]
         A small case to run under `ncu --set full` (needs a GPU): CALLS
         (default 3) MoE blocks of TOKENS tokens over a bank of EXPERTS routed
         experts (hidden 7168, intermediate 2048, top-8, no shared expert),
-        or CALLS projections alternating over two weight matrices. Inputs are
+        or CALLS projections alternating over two weight matrices, or CALLS
+        MoE blocks with the full router (384 experts x 7168) and tiny experts
+        (intermediate 16), to profile routing alone. Inputs are
         seeded and synthetic; each expert is 88 MB, so a bank of 32 (2.8 GB)
         is far larger than L2 and its DRAM counters mean what they say.
 
@@ -136,6 +139,18 @@ def case(kind, *args):
         torch.cuda.synchronize()
         active = len(set(idx.cpu().numpy().ravel().tolist()))
         print("moe tokens=%d experts=%d active=%d calls=%d" % (M, E, active, calls))
+    elif kind == "router":
+        M = int(args[0])
+        calls = int(args[1]) if len(args) > 1 else 3
+        E, H, I = 384, HIDDEN, 16
+        W13 = normal_bf16_cuda((E, 2 * I, H), WEIGHT_STD, "profile", "W13r")
+        W2 = normal_bf16_cuda((E, H, I), WEIGHT_STD, "profile", "W2r")
+        Wr = normal_bf16_cuda((E, H), ROUTER_STD, "profile", "Wr")
+        x = normal_bf16_cuda((M, H), 1.0, "profile", "xr", M)
+        for _ in range(calls):
+            dg.moe_decode(x, Wr, W13, W2, None, None, TOPK)
+        torch.cuda.synchronize()
+        print("router tokens=%d experts=%d calls=%d" % (M, E, calls))
     elif kind == "linear":
         M, N, K = int(args[0]), int(args[1]), int(args[2])
         calls = int(args[3]) if len(args) > 3 else 3
