@@ -11,8 +11,10 @@
 // tiles shared by several CTAs finished by the last arriver in CTA order.
 //
 // Warp roles: warp 0 issues TMA, warp 1 allocates tensor memory and issues
-// the MMAs (one thread), warps 2-5 drain the accumulator (each warp owns the
-// 32 tensor-memory lanes of its quarter).
+// the MMAs (one thread), warps 2-9 drain the accumulator: each warp owns the
+// 32 tensor-memory lanes of its quarter (warp % 4) and half of the token
+// columns, so the split-K reduction of a tile's partials is spread over 256
+// threads.
 //
 // "vLLM 如何用智能体辅助优化 Kimi K3 解码性能", Part 1 §1 "针对工作负载调优形状"
 // (split-K projections at larger batch).
@@ -29,8 +31,9 @@ constexpr int kTcStages = 4;
 constexpr int kTcXRows = 64;
 constexpr int kTcXSub = kTcXRows * 128;                   // 8 KB per box column
 constexpr int kTcStageBytes = kWBytes + kKSub * kTcXSub;  // 48 KB
-constexpr int kTcThreads = 192;
-constexpr int kTcEpi = 128;
+constexpr int kTcThreads = 320;
+constexpr int kTcEpi = 256;    // 8 epilogue warps: two per tensor-memory lane quarter
+constexpr int kTcCols = kTcXRows / 2;  // token columns each epilogue warp drains
 constexpr int kTmemCols = 128;  // two 64-column accumulators
 
 constexpr int tc_smem() {
@@ -186,9 +189,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else {
     // ---------------------------------------------------------------- epilogue
     griddep_wait();
-    const int et = threadIdx.x - 64;         // 0..127
+    const int et = threadIdx.x - 64;         // 0..255
     const int quarter = warp & 3;            // TMEM lanes this warp may access
+    const int half = (warp - 2) >> 2;        // which half of the token columns it drains
     const int r = quarter * 32 + lane;       // tile row = TMEM lane
+    const int t0 = half * kTcCols;           // first token column of this warp
     const GroupInfo gi{0, 0, a.M};
     if (nunits > 0) {
       const long long gfirst = u0 / KB, glast = (u1 - 1) / KB;
@@ -200,11 +205,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (!mbar_wait(&tfull[buf], (jt >> 1) & 1, a.timeout_ns, a.status)) s_flags[0] = 1;
         }
         tc_fence_after();
-        float v[kTcXRows];
+        float v[kTcCols];
 #pragma unroll
-        for (int cc = 0; cc < kTcXRows / 16; ++cc)
-          if (cc * 16 < NP)
-            tmem_ld16_sync(taddr + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * 64 + cc * 16),
+        for (int cc = 0; cc < kTcCols / 16; ++cc)
+          if (t0 + cc * 16 < NP)
+            tmem_ld16_sync(taddr + ((uint32_t)(quarter * 32) << 16) +
+                               (uint32_t)(buf * 64 + t0 + cc * 16),
                            v + cc * 16);
         tc_fence_before();
         __syncwarp();
@@ -216,16 +222,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (whole) {
           if (!aborted && n < a.nout) {
 #pragma unroll
-            for (int t = 0; t < kTcXRows; ++t)
-              if (t < gi.c) store_out<EPI, false>(a, gi, t, n, v[t]);
+            for (int t = 0; t < kTcCols; ++t)
+              if (t0 + t < gi.c) store_out<EPI, false>(a, gi, t0 + t, n, v[t]);
           }
         } else {
           constexpr long long kSlotFloats = (long long)kTileRows * kTcXRows;
           const int slot = (gt == u0 / KB) ? 0 : 1;
           float* mine = a.ws + (c * 2 + slot) * kSlotFloats;
 #pragma unroll
-          for (int t = 0; t < kTcXRows; ++t)
-            if (t < gi.c) __stcg(mine + t * kTileRows + r, v[t]);
+          for (int t = 0; t < kTcCols; ++t)
+            if (t0 + t < gi.c) __stcg(mine + (t0 + t) * kTileRows + r, v[t]);
           named_bar_sync(1, kTcEpi);
           const long long cf = cta_of(gt * KB, T, G);
           const long long cl = cta_of((gt + 1) * KB - 1, T, G);
