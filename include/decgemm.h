@@ -63,8 +63,8 @@ extern "C" {
 /* Kernel regimes reported by dec_last_choice (low 8 bits). */
 #define DEC_REGIME_NONE   0
 #define DEC_REGIME_SMALLM 1  /* CUDA-core small-matrix kernel, M <= 2 */
-#define DEC_REGIME_MMA    2  /* split-K with mma.sync tensor cores, 3 <= M <= 15 */
-#define DEC_REGIME_TC     3  /* split-K with tcgen05 tensor cores and TMEM, M >= 16 */
+#define DEC_REGIME_MMA    2  /* split-K with mma.sync tensor cores, 3 <= M <= 16 */
+#define DEC_REGIME_TC     3  /* split-K with tcgen05 tensor cores and TMEM, M >= 17 */
 
 /*
  * dec_linear -- decode projection y = x·Wᵀ. [tune-shapes]
@@ -73,10 +73,11 @@ extern "C" {
  *   y : [M,N] bf16 output               1 <= M <= 64, N >= 1, K >= 8, K % 8 == 0
  *
  * Accumulates in fp32 and rounds once to bf16 (nearest even). The kernel is
- * chosen from M: M <= 2 the small-matrix kernel; 3 <= M <= 15 split-K on
- * mma.sync; M >= 16 split-K on tcgen05. Split-K partial sums are reduced in a
- * fixed order by the last-arriving CTA of each output tile, so the result is
- * identical from run to run. The environment variable DEC_FORCE=smallm|mma|tc
+ * chosen from M: M <= 2 the small-matrix kernel; 3 <= M <= 16 split-K on
+ * mma.sync; M >= 17 split-K on tcgen05 (at exactly 16 tokens mma.sync streams
+ * faster). Split-K partial sums are reduced in a fixed order (by the
+ * last-arriving CTA of each output tile, or by the CTAs of one thread-block
+ * cluster for small projections), so the result is identical from run to run. The environment variable DEC_FORCE=smallm|mma|tc
  * overrides the choice (smallm only for M <= 2).
  * Errors: DEC_EINVAL, DEC_EUNSUPPORTED, DEC_ECUDA, DEC_ENOMEM.
  */

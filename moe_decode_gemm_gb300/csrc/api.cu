@@ -173,8 +173,12 @@ static int regime_for(int M) {
     if (!std::strcmp(f, "mma")) return DEC_REGIME_MMA;
     if (!std::strcmp(f, "tc") && M >= 16) return DEC_REGIME_TC;
   }
+  // tcgen05 from 17 tokens: at exactly 16 the mma.sync kernel with 16 token
+  // rows per stage streams faster on GB300 (N = 2048 / 8192 / 16384, K = 7168:
+  // 9.7 / 22.9 / 37.2 us against 12.7 / 24.2 / 42.4 us); from 24 tokens the
+  // tensor-memory kernel wins (13.0 against 20.5 us at N = 2048).
   if (M <= 2) return DEC_REGIME_SMALLM;
-  if (M < 16) return DEC_REGIME_MMA;
+  if (M <= 16) return DEC_REGIME_MMA;
   return DEC_REGIME_TC;
 }
 

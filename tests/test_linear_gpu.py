@@ -28,7 +28,7 @@ import moe_decode_gemm_gb300 as dg  # noqa: E402
 
 
 def _expect_regime(M):
-    return "smallm" if M <= 2 else ("mma" if M < 16 else "tc")
+    return "smallm" if M <= 2 else ("mma" if M <= 16 else "tc")
 
 
 def _gpu_linear(x_bits, W_bits, S=None, res_bits=None):
