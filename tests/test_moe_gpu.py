@@ -227,3 +227,45 @@ def test_decode_layer_composition(M):
     assert np.array_equal(idx.cpu().numpy(), mo["idx"])
     oref, oA2 = oracle.residual(x, mo["out"], mo["absref"])
     assert_within_tol(to_f64(out), oref, oA2, "moe + residual")
+
+
+def test_decode_layer_replays_from_a_cuda_graph():
+    """A decode layer captured into a CUDA graph (after one eager warm-up call,
+    so that the library's workspace exists) replays to the same bits: the
+    shared expert's side-stream fork and join, programmatic dependent launches
+    and cluster launches all capture."""
+    M, H, KV, E, I, k = 5, 256, 64, 32, 128, 4
+    key = ("graph",)
+    t = wl.bits_to_torch
+    Wr = t(wl.normal_bf16((E, H), 1.0 / math.sqrt(H), *key, "Wr"))
+    x = t(wl.normal_bf16((M, H), 1.0, *key, "x"))
+    Wqkv = t(wl.normal_bf16((H + KV, H), 0.02, *key, "Wqkv"))
+    Wo = t(wl.normal_bf16((H, H), 0.02, *key, "Wo"))
+    W13 = t(np.stack([wl.normal_bf16((2 * I, H), 0.02, *key, "W13", e) for e in range(E)]))
+    W2 = t(np.stack([wl.normal_bf16((H, I), 0.02, *key, "W2", e) for e in range(E)]))
+    Ws13 = t(wl.normal_bf16((2 * I, H), 0.02, *key, "Ws13"))
+    Ws2 = t(wl.normal_bf16((H, I), 0.02, *key, "Ws2"))
+    qkv = torch.empty((M, H + KV), dtype=torch.bfloat16, device="cuda")
+    r = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+
+    def layer():
+        dg.dec_linear(x, Wqkv, qkv, stream=s)
+        dg.dec_linear(qkv[:, :H], Wo, r, stream=s, residual=x)
+        dg.moe_decode(r, Wr, W13, W2, Ws13, Ws2, k, out=out, stream=s, residual=r)
+
+    layer()
+    torch.cuda.synchronize()
+    assert dg.sync_check() == dg.DEC_OK
+    eager = out.clone()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        layer()
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
+    assert dg.sync_check() == dg.DEC_OK
