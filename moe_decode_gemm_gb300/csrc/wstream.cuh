@@ -1,14 +1,18 @@
 // wstream.cuh -- persistent weight-streaming GEMM for decode shapes (swap-AB:
 // weight rows are the long side, the 1..64 tokens the short side).
 //
-// One producer warp streams 128-row x 64-column bf16 weight tiles (16 KB, 128B
-// swizzle) and the matching token tile into a ring of shared-memory stages
-// with TMA; eight consumer warps reduce them. The work is the list of
-// (group, output tile, 64-wide k block) units, cut into one contiguous range
-// per CTA ("stream-K"), so every CTA streams the same number of weight bytes
-// whatever the shape. An output tile whose k range spans several CTAs is
-// finished by the last CTA to arrive on the tile's counter, which sums the
-// partials in CTA order: the result does not depend on arrival order.
+// One producer warp streams weight stages -- 128 weight rows x 128 k (two
+// 128-row x 64-column bf16 TMA boxes with 128B swizzle, 32 KB), or twice that
+// for SwiGLU gate/up pairs and 256-row tiles -- and the matching token tile
+// into a ring of shared-memory stages; eight consumer warps reduce them. The
+// work is the list of (group, output tile, 128-wide k chunk) units, cut into
+// one contiguous range per CTA ("stream-K"), so every CTA streams the same
+// number of weight bytes whatever the shape. An output tile whose k range
+// spans several CTAs is finished by the last CTA to arrive on the tile's
+// counter, which sums the partials in CTA order: the result does not depend on
+// arrival order. Small projections instead split each tile over the CTAs of
+// one thread-block cluster, which sum their partials through distributed
+// shared memory.
 //
 // Consumers: a CUDA-core path for 1-2 tokens (a GEMV has no dense
 // contraction to give the tensor cores) and an mma.sync m16n8k16 path for
@@ -39,11 +43,11 @@ enum Epi : int { EPI_BF16 = 0, EPI_BF16_RES = 1, EPI_F32 = 2, EPI_SWIGLU = 3 };
 // the token rows of an expert kernel's pipeline stage.
 constexpr int kGroupTokens = 16;
 
-constexpr int kMaxSlots = 512;
+constexpr int kMaxSlots = 512;  // contributor slot table entries in shared memory
 // Weight bytes per CTA a plain projection prefetches into L2 before waiting
 // for its predecessor, beyond the ones its ring loads (152 CTAs: 39 MB, under
 // a third of L2).
-constexpr int kPrefetchBytes = 256 * 1024;             // contributor slot table entries in shared memory
+constexpr int kPrefetchBytes = 256 * 1024;
 
 // Dynamic shared memory of one wstream_kernel instantiation: 1 KB alignment
 // slack, the stage ring, full/empty barriers, flags, slot table, and `extra`.
