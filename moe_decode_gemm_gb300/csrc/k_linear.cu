@@ -1,6 +1,8 @@
 // k_linear.cu -- dense decode projections y = x·Wᵀ on the weight-streaming
 // kernel: the CUDA-core small-matrix path (M <= 2) and the mma.sync split-K
-// path (M >= 3). "vLLM 如何用智能体辅助优化 Kimi K3 解码性能", Part 1 §1.
+// path (3 <= M <= 16, and up to 64 when forced), each with stream-K, 256-row
+// (wide) or cluster-split instances. "vLLM 如何用智能体辅助优化 Kimi K3 解码性能",
+// Part 1 §1.
 #include <utility>
 
 #include "launch.h"

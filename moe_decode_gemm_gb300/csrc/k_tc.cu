@@ -1,6 +1,6 @@
 // k_tc.cu -- decode projection y = x·Wᵀ on the tcgen05 tensor cores, for
-// 16 <= M <= 64 tokens, where the projection is a real dense contraction
-// (up to 64 flops per weight byte).
+// 17 <= M <= 64 tokens (16 when forced), where the projection is a real dense
+// contraction (up to 64 flops per weight byte).
 //
 // Swap-AB: the weight tile is the MMA's A operand (128 rows x 64 k, K-major,
 // 128B swizzle, straight from TMA) and the token tile its B operand (N = M
