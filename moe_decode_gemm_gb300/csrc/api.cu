@@ -7,6 +7,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -341,10 +342,21 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   // not take SMs early and sit waiting for the gate/up kernel. The routed
   // experts take the SMs as the shared expert's CTAs leave them; the streams
   // join before the combine.
-  const int egrid = s->sms;
+  //
+  // Small batches: the routed experts read few bytes, and the shared expert,
+  // packed into the routing window, then delays the routed gate/up kernel's
+  // start on most SMs and leaves its down projection as a tail. There it gets
+  // gd dedicated SMs for the whole block instead -- its share of the block's
+  // bytes, from the expected number of distinct experts under uniform routing
+  // -- and the routed experts the others; used when gd >= 4 (M <= 4 at
+  // E = 384, k = 8).
+  const double eu = E * (1.0 - std::pow(1.0 - (double)topk / E, (double)M));
+  const int gd = (int)(s->sms / (1.0 + eu) + 0.5);
+  const bool dedicated = shared && gd >= 4 && gd < s->sms / 2;
+  const int egrid = dedicated ? s->sms - gd : s->sms;
   if (shared) {
     const int rc_ctas = router_ctas(E, H);
-    const int sgrid = s->sms - rc_ctas > 0 ? s->sms - rc_ctas : 1;
+    const int sgrid = dedicated ? gd : (s->sms - rc_ctas > 0 ? s->sms - rc_ctas : 1);
     if (cudaEventRecord(s->ev_fork, st) != cudaSuccess) return DEC_ECUDA;
     if (cudaStreamWaitEvent(s->side, s->ev_fork, 0) != cudaSuccess) return DEC_ECUDA;
     Ctx sx = make_ctx(s, s->side);
