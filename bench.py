@@ -14,6 +14,7 @@ layer's weights are its own and far exceed L2).
 Prints one JSON line (rank 0). Usage:
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--layers L] [--no-prefetch] [--no-cpu-baseline] [--cpu-seconds S]
+                  [--no-configs] [--router-skew S]
 """
 from __future__ import annotations
 
@@ -177,6 +178,79 @@ def replica_max(values, world):
 def job_tbps(world, step_bytes, steps, ms):
     """Whole-job TB/s: every rank's bytes over the slowest rank's time."""
     return world * step_bytes * steps / (ms / 1e3) / 1e12
+
+
+# ------------------------------------------------------------------ per config
+def _graph_us(torch, call, stream, reps=20, rounds=3):
+    """µs per call: `reps` calls captured into a CUDA graph, replayed `rounds`
+    times on `stream` between CUDA events; best round."""
+    for i in range(3):
+        call(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(reps):
+            call(i)
+    best = float("inf")
+    for _ in range(rounds):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        # replay() launches on torch's current stream: make it the timed one.
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1) * 1000.0 / reps)
+    del g
+    return best
+
+
+def per_config(dg, torch, dev, layer0, peak_gbs):
+    """µs per call and TB/s of algorithmic bytes for each config of the path:
+    the single projection, the batch sweep, the split-K regime (the
+    dispatcher's choice) and the MoE block of the stack's first layer. Weights
+    rotate through copies 4x the L2 size, so no call finds its weights in L2."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    s = torch.cuda.Stream(device=dev)
+    out = {}
+
+    def proj(M, N, K, key):
+        nbuf = max(2, math.ceil(4 * l2 / (2 * N * K)))
+        Ws = [wl.normal_bf16_cuda((N, K), wl.WEIGHT_STD, "cfg", key, N, K, i, device=dev)
+              for i in range(nbuf)]
+        x = wl.normal_bf16_cuda((M, K), 1.0, "cfg", key, "x", M, device=dev)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        us = _graph_us(torch, lambda i: dg.dec_linear(x, Ws[i % nbuf], y, stream=s), s)
+        regime, split = dg.last_choice()
+        tbps = linear_bytes(M, N, K) / us / 1e6
+        r = {"M": M, "N": N, "K": K, "us": round(us, 2), "TBps": round(tbps, 3),
+             "pct_of_peak": round(100 * tbps * 1e3 / peak_gbs, 1), "regime": regime,
+             "split": split, "cluster": dg.last_cluster()}
+        del Ws
+        return r
+
+    out["single_projection"] = proj(1, 4096, 4096, "single")
+    out["batch_sweep"] = [proj(M, N, 7168, "sweep") for N in (2048, 7168, 16384)
+                          for M in (1, 2, 4, 8, 16, 32, 64)]
+    out["split_k"] = [proj(M, 2048, 16384, "splitk") for M in (8, 32, 64)]
+    torch.cuda.empty_cache()
+    L = layer0
+    blocks = []
+    for M in BATCHES:
+        x = wl.bits_to_torch(wl.token_rows(M, H, "cfg-moe", M), device=dev)
+        o = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+        idx = torch.empty((M, K8), dtype=torch.int32, device=dev)
+        us = _graph_us(torch, lambda i: dg.moe_decode(x, L.Wr, L.W13, L.W2, L.Ws13, L.Ws2, K8,
+                                                      out=o, topk_idx=idx, stream=s), s, reps=10)
+        U = len(set(idx.cpu().numpy().ravel().tolist()))
+        tbps = moe_bytes(M, U) / us / 1e6
+        blocks.append({"M": M, "us": round(us, 2), "TBps": round(tbps, 3),
+                       "pct_of_peak": round(100 * tbps * 1e3 / peak_gbs, 1), "active_experts": U})
+    out["moe_block"] = blocks
+    out["timing"] = ("CUDA graph of 20 calls (10 for the MoE block), best of 3 replays; weights "
+                     "rotate through copies 4x L2 (the MoE bank is 34 GB)")
+    return out
 
 
 # ------------------------------------------------------------------ our arm
@@ -387,6 +461,8 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk,
         "generation_s": round(gen_s, 1),
     }
+    if rank == 0 and not args.no_configs:
+        line["configs"] = per_config(dg, torch, dev, layers[0], peak_gbs)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(layers[0], acts, budget_s=args.cpu_seconds)
     return line
@@ -486,6 +562,8 @@ def main():
     ap.add_argument("--no-prefetch", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-config µs/call table")
     ap.add_argument("--router-skew", type=float, default=0.0,
                     help="power-law expert popularity (0 = the uniform workload)")
     args = ap.parse_args()
