@@ -103,6 +103,26 @@ __device__ __forceinline__ GroupInfo load_group(const StreamArgs& a, int g) {
   return gi;
 }
 
+// Position of work unit u in (group, tile, k chunk) order: u = (g * TILES +
+// tile) * KB + kc. Walked one unit at a time with next().
+struct UnitPos {
+  int kc, tile, g;
+  __device__ __forceinline__ void next(int KB, int TILES) {
+    if (++kc == KB) {
+      kc = 0;
+      if (++tile == TILES) {
+        tile = 0;
+        ++g;
+      }
+    }
+  }
+};
+
+__device__ __forceinline__ UnitPos unit_pos(long long u, int KB, int TILES) {
+  const long long gt = u / KB;
+  return UnitPos{(int)(u - gt * KB), (int)(gt % TILES), (int)(gt / TILES)};
+}
+
 __device__ __forceinline__ long long cta_start(long long c, long long T, long long G) {
   return (c * T) / G;
 }
@@ -321,26 +341,24 @@ __global__ void __launch_bounds__(kThreads, MINB)
       const uint64_t pol_x = policy_evict_last();
       int gcur = -1;
       GroupInfo gi{0, 0, 0};
-      auto issue_w = [&](int s, long long u) {
-        const long long gt = u / KB;
-        const int kc = (int)(u - gt * KB);
-        const int tile = (int)(gt % TILES);
+      // Unit positions advance one unit at a time: no 64-bit division per
+      // stage on the path that refills the ring.
+      auto issue_w = [&](int s, const UnitPos& p) {
         uint8_t* wdst = smem + s * kStageBytes;
         const int rbase = gi.e * a.w_group_rows;
 #pragma unroll
         for (int sb = 0; sb < kKSub; ++sb) {
-          const int k0 = (kc * kKSub + sb) * kKBlk;
+          const int k0 = (p.kc * kKSub + sb) * kKBlk;
           uint8_t* d = wdst + sb * H2 * kWSub;
-          tma_load_2d(d, &wmap, k0, rbase + tile * kTileOut, &full[s], pol_w);
+          tma_load_2d(d, &wmap, k0, rbase + p.tile * kTileOut, &full[s], pol_w);
           if (H2 == 2)
             tma_load_2d(d + kWSub, &wmap, k0,
-                        rbase + (PAIRED ? a.w_up_offset + tile * kTileRows
-                                        : tile * kTileOut + kTileRows),
+                        rbase + (PAIRED ? a.w_up_offset + p.tile * kTileRows
+                                        : p.tile * kTileOut + kTileRows),
                         &full[s], pol_w);
         }
       };
-      auto issue_x = [&](int s, long long u, const GroupInfo& g_) {
-        const int kc = (int)(u % KB);
+      auto issue_x = [&](int s, int kc, const GroupInfo& g_) {
         uint8_t* xdst = smem + s * kStageBytes + kWStage;
 #pragma unroll
         for (int sb = 0; sb < kKSub; ++sb) {
@@ -354,43 +372,35 @@ __global__ void __launch_bounds__(kThreads, MINB)
         }
       };
       // The same weight boxes as issue_w for expert e, into L2 only.
-      auto prefetch_w = [&](long long u, int e) {
-        const long long gt = u / KB;
-        const int kc = (int)(u - gt * KB);
-        const int tile = (int)(gt % TILES);
+      auto prefetch_w = [&](const UnitPos& p, int e) {
         const int rbase = e * a.w_group_rows;
 #pragma unroll
         for (int sb = 0; sb < kKSub; ++sb) {
-          const int k0 = (kc * kKSub + sb) * kKBlk;
-          tma_prefetch_2d(&wmap, k0, rbase + tile * kTileOut);
+          const int k0 = (p.kc * kKSub + sb) * kKBlk;
+          tma_prefetch_2d(&wmap, k0, rbase + p.tile * kTileOut);
           if (H2 == 2)
             tma_prefetch_2d(&wmap, k0,
-                            rbase + (PAIRED ? a.w_up_offset + tile * kTileRows
-                                            : tile * kTileOut + kTileRows));
+                            rbase + (PAIRED ? a.w_up_offset + p.tile * kTileRows
+                                            : p.tile * kTileOut + kTileRows));
         }
       };
-      auto group_of = [&](long long u) -> int { return (int)((u / KB) / TILES); };
-      auto xbytes = [&](const GroupInfo& g_) -> uint32_t {
-        (void)g_;
-        return (uint32_t)kXBytes;
-      };
-      const uint32_t wbytes = kWStage;
+      const uint32_t tx_bytes = kWStage + kXBytes;
+      UnitPos pos = unit_pos(u0, KB, TILES);
       int i = 0;
       if (early) {
         // Weights do not depend on the previous kernel: start streaming them
         // before waiting for it, then fetch the token tiles.
         const int npre = nunits < STAGES ? nunits : STAGES;
         GroupInfo pg[STAGES];
-        for (; i < npre; ++i) {
-          const long long u = u0 + i;
-          const int g = GROUPED ? group_of(u) : 0;
-          if (g != gcur) {
-            gcur = g;
-            gi = load_group<GROUPED>(a, g);
+        const UnitPos pos0 = pos;
+        for (; i < npre; ++i, pos.next(KB, TILES)) {
+          if (pos.g != gcur) {
+            gcur = pos.g;
+            gi = load_group<GROUPED>(a, pos.g);
           }
           pg[i] = gi;
-          mbar_arrive_expect_tx(&full[i], wbytes + xbytes(gi));
-          issue_w(i, u);
+          mbar_arrive_expect_tx(&full[i], tx_bytes);
+          issue_w(i, pos);
         }
         // The units beyond the ring: pull up to kPrefetchBytes of them into
         // L2 while the previous kernel finishes, so that after the wait they
@@ -399,19 +409,19 @@ __global__ void __launch_bounds__(kThreads, MINB)
         constexpr int kPfUnits = CLUSTER ? 0 : kPrefetchBytes / kWStage;
         const int npf = nunits - npre < kPfUnits ? nunits - npre : kPfUnits;
         int pgrp = -1, pexp = 0;
-        for (int j = 0; j < npf; ++j) {
-          const long long u = u0 + npre + j;
-          const int g = GROUPED ? group_of(u) : 0;
-          if (g != pgrp) {
-            pgrp = g;
-            pexp = load_group<GROUPED>(a, g).e;
+        UnitPos pp = pos;
+        for (int j = 0; j < npf; ++j, pp.next(KB, TILES)) {
+          if (pp.g != pgrp) {
+            pgrp = pp.g;
+            pexp = load_group<GROUPED>(a, pp.g).e;
           }
-          prefetch_w(u, pexp);
+          prefetch_w(pp, pexp);
         }
         griddep_wait();
-        for (int j = 0; j < npre; ++j) issue_x(j, u0 + j, pg[j]);
+        UnitPos px = pos0;
+        for (int j = 0; j < npre; ++j, px.next(KB, TILES)) issue_x(j, px.kc, pg[j]);
       }
-      for (; i < nunits; ++i) {
+      for (; i < nunits; ++i, pos.next(KB, TILES)) {
         const int s = i % STAGES;
         if (i >= STAGES) {
           if (!mbar_wait(&empty[s], ((i / STAGES) + 1) & 1, a.timeout_ns, a.status)) {
@@ -420,18 +430,14 @@ __global__ void __launch_bounds__(kThreads, MINB)
           }
         }
         if (s_flags[0]) break;
-        const long long u = u0 + i;
-        if (GROUPED) {
-          const int g = group_of(u);
-          if (g != gcur) {
-            // new expert group: read its id and pair range once
-            gcur = g;
-            gi = load_group<GROUPED>(a, g);
-          }
+        if (GROUPED && pos.g != gcur) {
+          // new expert group: read its id and pair range once
+          gcur = pos.g;
+          gi = load_group<GROUPED>(a, pos.g);
         }
-        mbar_arrive_expect_tx(&full[s], wbytes + xbytes(gi));
-        issue_w(s, u);
-        issue_x(s, u, gi);
+        mbar_arrive_expect_tx(&full[s], tx_bytes);
+        issue_w(s, pos);
+        issue_x(s, pos.kc, gi);
       }
       // Drain: wait until every issued copy has landed before the CTA may exit.
       const int issued = i;
@@ -656,9 +662,15 @@ __global__ void __launch_bounds__(kThreads, MINB)
       named_bar_sync(1, kNCW * 32);  // partial slots and flags may be reused next tile
     };
 
+    // tile of the current unit, advanced with its k chunk (no division per stage)
+    long long gt_next = u0 / KB;
+    int kc_next = (int)(u0 - gt_next * KB);
     for (int i = 0; i < nunits; ++i) {
-      const long long u = u0 + i;
-      const long long gt = u / KB;
+      const long long gt = gt_next;
+      if (++kc_next == KB) {
+        kc_next = 0;
+        ++gt_next;
+      }
       if (gt != cur) {
         if (cur >= 0) finish_tile(cur, cur == u0 / KB);
         cur = gt;
