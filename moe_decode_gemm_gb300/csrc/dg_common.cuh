@@ -193,7 +193,23 @@ __device__ __forceinline__ float bf_bits2f(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
-// Dot of 8 bf16 weights (uint4) with 8 floats.
+// acc + w0*x0 + w1*x1 for the two bf16 halves of w and x (low half first),
+// each step one fma.rn.f32.bf16: the bf16 operands enter at full precision
+// (a bf16 x bf16 product is exact in fp32) and the sum rounds once per step,
+// as fmaf on the widened values would -- without widening them first.
+__device__ __forceinline__ float dot2_bf16(uint32_t w, uint32_t x, float acc) {
+  asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+      "mov.b32 {wl, wh}, %1;\n\t"
+      "mov.b32 {xl, xh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, wl, xl, %0;\n\t"
+      "fma.rn.f32.bf16 %0, wh, xh, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(w), "r"(x));
+  return acc;
+}
+
+// The same dot with the activations widened to fp32 beforehand (unpack8) and
+// each weight widened in the loop: bit-identical to dot8_bf16.
 __device__ __forceinline__ float dot8(const uint4& w, const float* xv, float acc) {
   acc = fmaf(bf16lo(w.x), xv[0], acc);
   acc = fmaf(bf16hi(w.x), xv[1], acc);
@@ -211,6 +227,15 @@ __device__ __forceinline__ void unpack8(const uint4& v, float* o) {
   o[2] = bf16lo(v.y); o[3] = bf16hi(v.y);
   o[4] = bf16lo(v.z); o[5] = bf16hi(v.z);
   o[6] = bf16lo(v.w); o[7] = bf16hi(v.w);
+}
+
+// Dot of 8 bf16 weights with 8 bf16 activations (one uint4 each), in order.
+__device__ __forceinline__ float dot8_bf16(const uint4& w, const uint4& x, float acc) {
+  acc = dot2_bf16(w.x, x.x, acc);
+  acc = dot2_bf16(w.y, x.y, acc);
+  acc = dot2_bf16(w.z, x.z, acc);
+  acc = dot2_bf16(w.w, x.w, acc);
+  return acc;
 }
 
 // silu(z) = z / (1 + e^-z), with CUDA's expf.

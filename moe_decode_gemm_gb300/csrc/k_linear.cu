@@ -32,10 +32,14 @@ constexpr int dense_smem() {
 
 // WIDE: 256-row output tiles, 64 KB weight stages (two 128-row halves).
 // CL > 0: cluster split, CL CTAs per output tile (grid = tiles * CL).
-template <int XR, int EPI, bool WIDE = false, bool CLUSTER = false>
-static cudaError_t run_dense(const Ctx& cx, bool mma, const void* x, const void* W, const void* res,
-                             void* y, int M, int N, int K, int grid, float* ws, int* ctr,
-                             int cl = 0) {
+// PATH: PATH_CORE (1-2 tokens, CUDA cores only) or PATH_ANY with every group
+// on mma.sync (mma_min_tokens = 1). The mma.sync instances keep the CUDA-core
+// branch: without it the compiler scheduled their loop into more spills at
+// 112 registers (M = 4 / 16, N = 2048: 8.3 / 9.1 us against 10.1 / 11.0 us).
+template <int XR, int EPI, bool WIDE, bool CLUSTER, int PATH>
+static cudaError_t run_dense_path(const Ctx& cx, const void* x, const void* W, const void* res,
+                                  void* y, int M, int N, int K, int grid, float* ws, int* ctr,
+                                  int cl) {
   constexpr int S = dense_stages<XR, WIDE>();
   constexpr int MINB = dense_minb<XR, WIDE>();
   constexpr int SMEM = dense_smem<XR, WIDE>();
@@ -43,7 +47,7 @@ static cudaError_t run_dense(const Ctx& cx, bool mma, const void* x, const void*
   static_assert(MINB == 1 || 2 * (SMEM + 1024) <= kSmemPerSm, "two CTAs per SM");
   static_assert(!CLUSTER || kTileRows * XR * 4 <= S * (kWBytes + kKSub * XR * 128),
                 "the partial tile fits in the stage ring");
-  auto kern = wstream_kernel<XR, S, EPI, false, false, WIDE, ROLE_PROJECTION, MINB, CLUSTER>;
+  auto kern = wstream_kernel<XR, S, EPI, false, false, WIDE, ROLE_PROJECTION, MINB, CLUSTER, PATH>;
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = allow_smem(kern, SMEM);
@@ -66,7 +70,7 @@ static cudaError_t run_dense(const Ctx& cx, bool mma, const void* x, const void*
   a.TILES = (N + kTile - 1) / kTile;
   a.nout = N;
   a.M = M;
-  a.mma_min_tokens = mma ? 1 : 1 << 30;
+  a.mma_min_tokens = PATH == PATH_CORE ? 1 << 30 : 1;
   a.out = y;
   a.ldo = N;
   a.res = reinterpret_cast<const uint16_t*>(res);
@@ -77,6 +81,23 @@ static cudaError_t run_dense(const Ctx& cx, bool mma, const void* x, const void*
   if (CLUSTER)
     return launch_kc(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, cl, wmap, xmap, a);
   return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
+}
+
+// The CUDA-core consumer takes at most two tokens and only runs at 8 token
+// rows per stage (the small-matrix regime); every other instance is mma.sync.
+template <int XR, int EPI, bool WIDE = false, bool CLUSTER = false>
+static cudaError_t run_dense(const Ctx& cx, bool mma, const void* x, const void* W, const void* res,
+                             void* y, int M, int N, int K, int grid, float* ws, int* ctr,
+                             int cl = 0) {
+  if (mma)
+    return run_dense_path<XR, EPI, WIDE, CLUSTER, PATH_ANY>(cx, x, W, res, y, M, N, K, grid, ws,
+                                                            ctr, cl);
+  if constexpr (XR == 8) {
+    if (M <= 2)
+      return run_dense_path<8, EPI, WIDE, CLUSTER, PATH_CORE>(cx, x, W, res, y, M, N, K, grid, ws,
+                                                              ctr, cl);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_dense_cluster(const Ctx& cx, int xr, bool mma, bool residual, const void* x,

@@ -259,12 +259,24 @@ constexpr int reduce_jb(bool paired, int eb, int loads) {
 // shared memory, in rank order, behind two cluster barriers -- no global
 // partials, counters or atomics.
 enum Role : int { ROLE_PROJECTION = 0, ROLE_ROUTER = 1, ROLE_EXPERT = 2, ROLE_SHARED = 3 };
+// PATH: which consumers the instantiation carries. PATH_ANY chooses per group
+// (CUDA cores below mma_min_tokens tokens, mma.sync from there): expert groups
+// hold 1..XR tokens each. PATH_CORE carries the CUDA-core consumer only, for
+// projections of 1-2 tokens.
+enum Path : int { PATH_ANY = 0, PATH_CORE = 1 };
 template <int XR, int STAGES, int EPI, bool PAIRED, bool GROUPED, bool WIDE = false,
-          int ROLE = ROLE_PROJECTION, int MINB = 1, bool CLUSTER = false>
+          int ROLE = ROLE_PROJECTION, int MINB = 1, bool CLUSTER = false, int PATH = PATH_ANY>
 __global__ void __launch_bounds__(kThreads, MINB)
     wstream_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const StreamArgs a) {
   constexpr int H2 = (PAIRED || WIDE) ? 2 : 1;  // 128-row weight halves per box column
+  // CUDA-core dot form. Both give the same bits. The bf16-operand form
+  // (fma.rn.f32.bf16) issues half the instructions; the widened form is kept
+  // in the two-CTA-per-SM instantiations that carry the mma.sync path too,
+  // where at 112 registers the compiler's allocation of the mma loop spilled
+  // more with the other form and that path lost 6-8 % (M = 4 / 16 tokens,
+  // N = 2048, K = 7168, same-GPU A/B).
+  constexpr bool kMixedDot = PATH == PATH_CORE || MINB == 1;
   constexpr int kTileOut = PAIRED ? kTileRows : H2 * kTileRows;  // output features per tile
   constexpr int kXSub = XR * 128;              // token rows of one box column
   constexpr int kXBytes = kXSub * kKSub;
@@ -676,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         cur = gt;
         zero_acc();
         gi = load_group<GROUPED>(a, (int)(gt / TILES));
-        use_mma = gi.c >= a.mma_min_tokens;
+        use_mma = PATH == PATH_ANY && gi.c >= a.mma_min_tokens;
       }
       const int s = i % STAGES;
       if (!s_flags[0]) {
@@ -688,27 +700,49 @@ __global__ void __launch_bounds__(kThreads, MINB)
         const uint8_t* xs_base = smem + s * kStageBytes + kWStage + sb * kXSub;
         if (!use_mma) {
           // CUDA-core path: lane reads 16-byte chunk q of rows 16w + rho + 4r
-          float xv[2][8];
+          // and multiplies it with the same chunk of each token.
+          if constexpr (kMixedDot) {
+            // bf16 operands, fp32 sums: no widening instructions
+            uint4 xq[2];
 #pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (t < gi.c) {
-              const uint4 v =
-                  *reinterpret_cast<const uint4*>(xs_base + t * 128 + ((q ^ (t & 7)) << 4));
-              unpack8(v, xv[t]);
-            } else {
+            for (int t = 0; t < 2; ++t)
+              xq[t] = t < gi.c ? *reinterpret_cast<const uint4*>(xs_base + t * 128 +
+                                                                  ((q ^ (t & 7)) << 4))
+                               : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-              for (int j = 0; j < 8; ++j) xv[t][j] = 0.f;
+            for (int r = 0; r < 4; ++r) {
+              const int row = 16 * w + rho + 4 * r;
+#pragma unroll
+              for (int h = 0; h < H2; ++h) {
+                const uint4 wv = *reinterpret_cast<const uint4*>(wbase + h * kWSub + row * 128 +
+                                                                 ((q ^ (row & 7)) << 4));
+                dacc[h][r][0] = dot8_bf16(wv, xq[0], dacc[h][r][0]);
+                if (gi.c > 1) dacc[h][r][1] = dot8_bf16(wv, xq[1], dacc[h][r][1]);
+              }
             }
-          }
+          } else {
+            float xv[2][8];
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int row = 16 * w + rho + 4 * r;
+            for (int t = 0; t < 2; ++t) {
+              if (t < gi.c) {
+                const uint4 v =
+                    *reinterpret_cast<const uint4*>(xs_base + t * 128 + ((q ^ (t & 7)) << 4));
+                unpack8(v, xv[t]);
+              } else {
 #pragma unroll
-            for (int h = 0; h < H2; ++h) {
-              const uint4 wv = *reinterpret_cast<const uint4*>(wbase + h * kWSub + row * 128 +
-                                                               ((q ^ (row & 7)) << 4));
-              dacc[h][r][0] = dot8(wv, xv[0], dacc[h][r][0]);
-              if (gi.c > 1) dacc[h][r][1] = dot8(wv, xv[1], dacc[h][r][1]);
+                for (int j = 0; j < 8; ++j) xv[t][j] = 0.f;
+              }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              const int row = 16 * w + rho + 4 * r;
+#pragma unroll
+              for (int h = 0; h < H2; ++h) {
+                const uint4 wv = *reinterpret_cast<const uint4*>(wbase + h * kWSub + row * 128 +
+                                                                 ((q ^ (row & 7)) << 4));
+                dacc[h][r][0] = dot8(wv, xv[0], dacc[h][r][0]);
+                if (gi.c > 1) dacc[h][r][1] = dot8(wv, xv[1], dacc[h][r][1]);
+              }
             }
           }
         } else {

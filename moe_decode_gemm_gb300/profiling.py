@@ -42,14 +42,16 @@ def kernel_label(name):
     m = re.search(r"wstream_kernel<([^>]*)>", name)
     if m:
         p = [v.strip() for v in m.group(1).split(",")]
-        p += ["0"] * (9 - len(p))  # defaults: projection role, 1 CTA per SM, no cluster
-        xr, st, epi, paired, grouped, wide, role, minb, cluster = p[:9]
+        # defaults: projection role, 1 CTA per SM, no cluster, consumer chosen per group
+        p += ["0"] * (10 - len(p))
+        xr, st, epi, paired, grouped, wide, role, minb, cluster, path = p[:10]
         role = _ROLE.get(role, role)
         part = ""
         if role in ("routed expert", "shared expert"):
             part = " gate/up" if paired in _TRUE else " down"
         tile = "256-row" if wide in _TRUE else "128-row"
         extra = (" 2/SM" if minb == "2" else "") + (" cluster" if cluster in _TRUE else "")
+        extra += " CUDA cores" if path == "1" else ""
         return "%s%s [wstream XR=%s S=%s %s %s%s]" % (role, part, xr, st, _EPI.get(epi, epi), tile,
                                                      extra)
     m = re.search(r"tc_linear_kernel<(\d+)>", name)
