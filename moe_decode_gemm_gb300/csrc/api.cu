@@ -231,6 +231,22 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
                                         res, y, M, N, K, cl));
   }
   long long grid = S ? tiles * S : (T < s->sms ? T : s->sms);
+  // tcgen05: a tile-aligned split -- tiles * sa CTAs, sa dividing the k chunks,
+  // so that every CTA covers whole k ranges of one tile -- when it keeps at
+  // least three quarters of the SMs busy. Its fixups sum sa equal partials
+  // (none at sa = 1) instead of the uneven ones of a split over every SM,
+  // each partial 32 KB at 64 token columns. Measured, us (stream-K over 152
+  // SMs -> aligned): M = 64, N x K = 2048 x 7168: 15.9 -> 14.0 (sa = 8);
+  // 2048 x 16384: 21.0 -> 20.0 (8); 16384 x 7168: 42.4 -> 38.6 (1). At
+  // 7168 x 7168 the only aligned split (2) leaves a quarter of the SMs idle
+  // and is slower (23.1 against 22.2).
+  if (S == 0 && regime == DEC_REGIME_TC) {
+    for (long long sa = KB < 16 ? KB : 16; sa >= 1; --sa)
+      if (tiles * sa <= s->sms && KB % sa == 0) {
+        if (tiles * sa * 4 >= 3LL * s->sms) grid = tiles * sa;
+        break;
+      }
+  }
   if (grid > T) grid = T;
   const size_t slot_rows = wide ? 256 : 128;
   if ((rc = ensure(s->ws_main, (size_t)grid * 2 * slot_rows * xr * sizeof(float), st))) return rc;

@@ -99,31 +99,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
       const uint32_t bytes = kWBytes + kKSub * NP * 128;
-      auto issue_w = [&](int s, long long u) {
-        const long long gt = u / KB;
-        const int kc = (int)(u - gt * KB);
+      // unit positions advance one unit at a time (no division per stage)
+      auto issue_w = [&](int s, const UnitPos& p) {
 #pragma unroll
         for (int sb = 0; sb < kKSub; ++sb)
-          tma_load_2d(smem + s * kTcStageBytes + sb * kWSub, &wmap, (kc * kKSub + sb) * kKBlk,
-                      (int)gt * kTileRows, &full[s], pol_w);
+          tma_load_2d(smem + s * kTcStageBytes + sb * kWSub, &wmap, (p.kc * kKSub + sb) * kKBlk,
+                      p.tile * kTileRows, &full[s], pol_w);
       };
-      auto issue_x = [&](int s, long long u) {
-        const int kc = (int)(u % KB);
+      auto issue_x = [&](int s, const UnitPos& p) {
 #pragma unroll
         for (int sb = 0; sb < kKSub; ++sb)
           tma_load_2d(smem + s * kTcStageBytes + kWBytes + sb * kTcXSub, &xmap,
-                      (kc * kKSub + sb) * kKBlk, 0, &full[s], pol_x);
+                      (p.kc * kKSub + sb) * kKBlk, 0, &full[s], pol_x);
       };
       // weights first (independent of the previous kernel), then tokens
       const int npre = nunits < kTcStages ? nunits : kTcStages;
+      const UnitPos pos0 = unit_pos(u0, KB, TILES);
+      UnitPos pos = pos0;
       int i = 0;
-      for (; i < npre; ++i) {
+      for (; i < npre; ++i, pos.next(KB, TILES)) {
         mbar_arrive_expect_tx(&full[i], bytes);
-        issue_w(i, u0 + i);
+        issue_w(i, pos);
       }
       griddep_wait();
-      for (int j = 0; j < npre; ++j) issue_x(j, u0 + j);
-      for (; i < nunits; ++i) {
+      UnitPos px = pos0;
+      for (int j = 0; j < npre; ++j, px.next(KB, TILES)) issue_x(j, px);
+      for (; i < nunits; ++i, pos.next(KB, TILES)) {
         const int s = i % kTcStages;
         if (!mbar_wait(&empty[s], ((i / kTcStages) + 1) & 1, a.timeout_ns, a.status)) {
           s_flags[0] = 1;
@@ -131,8 +132,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if (s_flags[0]) break;
         mbar_arrive_expect_tx(&full[s], bytes);
-        issue_w(s, u0 + i);
-        issue_x(s, u0 + i);
+        issue_w(s, pos);
+        issue_x(s, pos);
       }
       const int issued = i;
       for (int s = 0; s < kTcStages && s < issued; ++s) {
@@ -148,9 +149,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       long long cur = -1;
       int jt = -1;
+      long long gt_next = u0 / KB;  // tile of unit u0 + i, advanced with its k chunk
+      int kc_next = (int)(u0 - gt_next * KB);
       for (int i = 0; i < nunits; ++i) {
-        const long long u = u0 + i;
-        const long long gt = u / KB;
+        const long long gt = gt_next;
+        const bool tile_end = ++kc_next == KB;
+        if (tile_end) {
+          kc_next = 0;
+          ++gt_next;
+        }
         const bool first = gt != cur;
         if (first) {
           cur = gt;
@@ -180,7 +187,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
         }
         umma_commit(&empty[s]);
-        if (i == nunits - 1 || ((u + 1) % KB) == 0) umma_commit(&tfull[jt & 1]);
+        if (i == nunits - 1 || tile_end) umma_commit(&tfull[jt & 1]);
       }
       umma_commit(mma_done);
       mbar_wait(mma_done, 0, a.timeout_ns, nullptr);

@@ -158,6 +158,36 @@ def test_forced_regimes_agree(M, forces):
     assert np.array_equal(outs[forces[0]], outs[forces[1]])
 
 
+# ---------------------------------------------------------------- tcgen05 grid
+def _tc_aligned_split(N, K, sms):
+    # the dispatcher's tile-aligned split for the tcgen05 kernel, or 0 for a
+    # split over every SM
+    KB, tiles = (K + 127) // 128, (N + 127) // 128
+    for sa in range(min(KB, 16), 0, -1):
+        if tiles * sa <= sms and KB % sa == 0:
+            return sa if tiles * sa * 4 >= 3 * sms else 0
+    return 0
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 2048, 7168), (32, 2048, 16384), (64, 16384, 7168),
+                                   (17, 4096, 4096), (64, 7168, 7168)])
+def test_tc_tile_aligned_split(M, N, K):
+    # 17..64 tokens on the tcgen05 kernel at full size: a tile-aligned split
+    # (tiles * sa CTAs, sa dividing the k chunks; sa = 1 has no fixup at all)
+    # where it keeps three quarters of the SMs busy, else stream-K over every
+    # SM; sampled output features of every tile against the oracle
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cols = np.arange(0, N, 61)
+    y, (regime, split) = _check_random(M, N, K, ("tcgrid", M, N, K), cols=cols)
+    assert regime == "tc"
+    sa = _tc_aligned_split(N, K, sms)
+    tiles = (N + 127) // 128
+    if sa:
+        assert split == sa and dg.last_grid() == tiles * sa
+    else:
+        assert dg.last_grid() == min(sms, tiles * ((K + 127) // 128))
+
+
 # ---------------------------------------------------------------- cluster split
 # Narrow projections with few 128-row tiles (M <= 16) split each tile's k
 # chunks over the CTAs of one thread-block cluster and sum the partial tiles
