@@ -143,9 +143,9 @@ def layer_bytes(M, U):
 
 # DRAM traffic (read + write) of the routed gate/up kernel per chosen expert,
 # from one ncu capture of a small case (16 tokens over a 32-expert bank, 31
-# experts chosen: 1826.1 MB in one launch). Its traffic grows in proportion to
+# experts chosen: 1825.8 MB in one launch). Its traffic grows in proportion to
 # the experts it streams, so a full launch's traffic is this times its count.
-W13_TRAFFIC_PER_EXPERT = 1826.1e6 / 31
+W13_TRAFFIC_PER_EXPERT = 1825.8e6 / 31
 
 
 def w13_launch_bytes(M, U):
