@@ -76,8 +76,10 @@ extern "C" {
  * chosen from M: M <= 2 the small-matrix kernel; 3 <= M <= 16 split-K on
  * mma.sync; M >= 17 split-K on tcgen05 (at exactly 16 tokens mma.sync streams
  * faster). Split-K partial sums are reduced in a fixed order (by the
- * last-arriving CTA of each output tile, or by the CTAs of one thread-block
- * cluster for small projections), so the result is identical from run to run. The environment variable DEC_FORCE=smallm|mma|tc
+ * last-arriving CTA of each output tile, or -- when N has few 128-row tiles,
+ * on every kernel -- by the CTAs of one thread-block cluster per tile, in rank
+ * order), so the result is identical from run to run. The environment
+ * variable DEC_FORCE=smallm|mma|tc
  * overrides the choice (smallm only for M <= 2).
  * Errors: DEC_EINVAL, DEC_EUNSUPPORTED, DEC_ECUDA, DEC_ENOMEM.
  */

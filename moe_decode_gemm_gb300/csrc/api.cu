@@ -183,6 +183,13 @@ static int regime_for(int M) {
   return DEC_REGIME_TC;
 }
 
+// Weight bytes one CTA of the tcgen05 cluster split may stream. Measured (us,
+// tile-aligned stream-K split -> cluster split, 8 CTAs per tile): 2048 x 7168
+// at M = 64 / 32 / 17: 14.1 / 11.2 / 10.6 -> 11.4 / 9.6 / 9.2 (224 KB per
+// CTA); 2048 x 16384 at M = 64 / 32: 19.9 / 16.9 -> 18.7 / 16.9 (512 KB);
+// 4096 x 4096 at M = 64 (4 per tile): 12.6 either way.
+constexpr long long kTcClusterMaxBytes = 1024LL * 1024;
+
 static int linear_impl(const void* x, const void* W, const void* res, void* y, int M, int N, int K,
                        int S, void* stream, long long ldx = 0) {
   if (!x || !W || !y) return DEC_EINVAL;
@@ -221,12 +228,24 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
       }
     if (cl && (tiles * cl * 4 < 3LL * s->sms || 256LL * K / cl > 320LL * 1024)) cl = 0;
   }
+  // The same split for the tcgen05 kernel (17-64 tokens): its stream-K fixups
+  // sum partial tiles of 32 KB per contributor at 64 tokens through L2.
+  if (S == 0 && regime == DEC_REGIME_TC) {
+    for (int c = 8; c >= 2; c >>= 1)
+      if (tiles * c <= s->sms && c <= KB) {
+        cl = c;
+        break;
+      }
+    if (cl && (tiles * cl * 4 < 3LL * s->sms || 256LL * K / cl > kTcClusterMaxBytes)) cl = 0;
+  }
   if (cl) {
     Ctx cx = make_ctx(s, st);
     cx.ldx = ldx;
     t_last_choice = regime | (cl << 8) | (1 << 16);
     t_last_grid = (int)(tiles * cl);
     ProbeScope probe(2, st);
+    if (regime == DEC_REGIME_TC)
+      return counted(launch_dense_tc_cluster(cx, res != nullptr, x, W, res, y, M, N, K, cl));
     return counted(launch_dense_cluster(cx, xr, regime != DEC_REGIME_SMALLM, res != nullptr, x, W,
                                         res, y, M, N, K, cl));
   }

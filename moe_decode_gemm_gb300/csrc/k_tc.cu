@@ -14,7 +14,8 @@
 // the MMAs (one thread), warps 2-9 drain the accumulator: each warp owns the
 // 32 tensor-memory lanes of its quarter (warp % 4) and half of the token
 // columns, so the split-K reduction of a tile's partials is spread over 256
-// threads.
+// threads. For N with few 128-row tiles a second kernel splits each tile over
+// the CTAs of a thread-block cluster instead (below), two CTAs per SM.
 //
 // "vLLM 如何用智能体辅助优化 Kimi K3 解码性能", Part 1 §1 "针对工作负载调优形状"
 // (split-K projections at larger batch).
@@ -283,6 +284,237 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     tmem_dealloc(taddr, kTmemCols);
   }
+}
+
+// ------------------------------------------------------------------ cluster split
+// Small N: cluster i of S CTAs owns output tile i, rank r streams the r-th of
+// S equal shares of its k chunks into one tensor-memory accumulator, drains
+// it to its own shared memory, and after a cluster barrier sums rows
+// [r*128/S, (r+1)*128/S) of every token over the S partials in rank order
+// (ld.shared::cluster on mapa addresses); a second barrier keeps every CTA
+// alive while the others read it. No global partials, counters or atomics,
+// deterministic. Two 48 KB stages keep a CTA near 100 KB of shared memory, so
+// two fit on an SM: a call's CTAs load their first weight stages while the
+// previous call's CTAs on those SMs finish.
+constexpr int kTcClStages = 2;
+constexpr int kTcClCols = 64;  // one accumulator of up to 64 token columns
+
+constexpr int tc_cluster_smem() {
+  return 1024 + kTcClStages * kTcStageBytes + 8 * (2 * kTcClStages + 1) + 64;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kTcThreads, 2)
+    tc_cluster_kernel(const __grid_constant__ CUtensorMap wmap,
+                      const __grid_constant__ CUtensorMap xmap, const StreamArgs a, const int NP,
+                      const uint32_t idesc) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTcClStages * kTcStageBytes);
+  uint64_t* empty = full + kTcClStages;
+  uint64_t* tfull = empty + kTcClStages;  // [1] accumulator complete
+  volatile int* s_flags = reinterpret_cast<volatile int*>(tfull + 1);  // [0] abort
+  uint32_t* s_taddr = reinterpret_cast<uint32_t*>(const_cast<int*>(s_flags) + 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTcClStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    s_flags[0] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(s_taddr, kTcClCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&wmap);
+    prefetch_tmap(&xmap);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t taddr = *s_taddr;
+  griddep_launch_dependents();
+
+  const int KB = a.KB;
+  const int cs = (int)cluster_size(), cr = (int)cluster_rank();
+  const int tile = (int)(blockIdx.x / cs);
+  const int kc0 = cr * KB / cs;
+  const int nunits = (cr + 1) * KB / cs - kc0;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      const uint32_t bytes = kWBytes + kKSub * NP * 128;
+      auto issue_w = [&](int s, int kc) {
+#pragma unroll
+        for (int sb = 0; sb < kKSub; ++sb)
+          tma_load_2d(smem + s * kTcStageBytes + sb * kWSub, &wmap, (kc * kKSub + sb) * kKBlk,
+                      tile * kTileRows, &full[s], pol_w);
+      };
+      auto issue_x = [&](int s, int kc) {
+#pragma unroll
+        for (int sb = 0; sb < kKSub; ++sb)
+          tma_load_2d(smem + s * kTcStageBytes + kWBytes + sb * kTcXSub, &xmap,
+                      (kc * kKSub + sb) * kKBlk, 0, &full[s], pol_x);
+      };
+      // weights first (independent of the previous kernel), then tokens
+      const int npre = nunits < kTcClStages ? nunits : kTcClStages;
+      int i = 0;
+      for (; i < npre; ++i) {
+        mbar_arrive_expect_tx(&full[i], bytes);
+        issue_w(i, kc0 + i);
+      }
+      griddep_wait();
+      for (int j = 0; j < npre; ++j) issue_x(j, kc0 + j);
+      for (; i < nunits; ++i) {
+        const int s = i % kTcClStages;
+        if (!mbar_wait(&empty[s], ((i / kTcClStages) + 1) & 1, a.timeout_ns, a.status)) {
+          s_flags[0] = 1;
+          break;
+        }
+        if (s_flags[0]) break;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        issue_w(s, kc0 + i);
+        issue_x(s, kc0 + i);
+      }
+      const int issued = i;
+      for (int s = 0; s < kTcClStages && s < issued; ++s) {
+        const int uses = (issued - s + kTcClStages - 1) / kTcClStages;
+        mbar_wait(&full[s], (uses - 1) & 1, a.timeout_ns, nullptr);
+      }
+    } else {
+      griddep_wait();
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA
+    griddep_wait();
+    if (lane == 0) {
+      for (int i = 0; i < nunits; ++i) {
+        const int s = i % kTcClStages;
+        if (!s_flags[0]) {
+          if (!mbar_wait(&full[s], (i / kTcClStages) & 1, a.timeout_ns, a.status)) s_flags[0] = 1;
+        }
+        tc_fence_after();
+        if (!s_flags[0]) {
+          const uint32_t wb = smem_u32(smem + s * kTcStageBytes);
+          const uint32_t xb = wb + kWBytes;
+#pragma unroll
+          for (int sb = 0; sb < kKSub; ++sb)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = umma_desc_sw128(wb + sb * kWSub + kk * 32);
+              const uint64_t bd = umma_desc_sw128(xb + sb * kTcXSub + kk * 32);
+              umma_bf16(taddr, ad, bd, idesc, (i == 0 && sb == 0 && kk == 0) ? 0u : 1u);
+            }
+        }
+        umma_commit(&empty[s]);
+      }
+      // every MMA above is complete (and so every stage read) when this fires
+      umma_commit(tfull);
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    griddep_wait();
+    const int quarter = warp & 3;      // TMEM lanes this warp may access
+    const int half = (warp - 2) >> 2;  // which half of the token columns it drains
+    const int r = quarter * 32 + lane;
+    const int t0 = half * kTcCols;
+    if (!s_flags[0]) {
+      if (!mbar_wait(tfull, 0, a.timeout_ns, a.status)) s_flags[0] = 1;
+    }
+    tc_fence_after();
+    float v[kTcCols];
+#pragma unroll
+    for (int cc = 0; cc < kTcCols / 16; ++cc)
+      if (t0 + cc * 16 < NP)
+        tmem_ld16_sync(taddr + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(t0 + cc * 16),
+                       v + cc * 16);
+    tc_fence_before();
+    // This CTA's partial tile [token][128] at the start of its shared memory:
+    // the stages are free (every MMA, and so every copy, has completed).
+    float* part = reinterpret_cast<float*>(smem);
+#pragma unroll
+    for (int t = 0; t < kTcCols; ++t)
+      if (t0 + t < a.M) part[(t0 + t) * kTileRows + r] = v[t];
+  }
+  // Every thread of the cluster: partials written -> visible cluster-wide.
+  __syncwarp();
+  cluster_sync_all();
+  if (warp >= 2) {
+    const int et = threadIdx.x - 64;
+    const int R = kTileRows / cs;
+    const GroupInfo gi{0, 0, a.M};
+    const float* part = reinterpret_cast<const float*>(smem);
+    if (!s_flags[0]) {
+      for (int e = et; e < R * a.M; e += kTcEpi) {
+        const int t = e / R, rr = cr * R + (e - t * R);
+        float acc = 0.f;
+        for (int q = 0; q < cs; ++q) acc += ld_dsmem_f32(part + t * kTileRows + rr, (uint32_t)q);
+        const int n = tile * kTileRows + rr;
+        if (n < a.nout) store_out<EPI, false>(a, gi, t, n, acc);
+      }
+    }
+  }
+  __syncwarp();
+  cluster_sync_all();  // no CTA leaves while another still reads its partial
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(taddr, kTcClCols);
+  }
+}
+
+template <int EPI>
+static cudaError_t run_tc_cluster(const Ctx& cx, const void* x, const void* W, const void* res,
+                                  void* y, int M, int N, int K, int cl) {
+  constexpr int SMEM = tc_cluster_smem();
+  static_assert(2 * (SMEM + 1024) <= kSmemPerSm, "two CTAs per SM");
+  static_assert(kTileRows * kTcXRows * 4 <= kTcClStages * kTcStageBytes, "partial tile fits");
+  auto kern = tc_cluster_kernel<EPI>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = allow_smem(kern, SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int NP = (M + 15) / 16 * 16;
+  CUtensorMap wmap, xmap;
+  if (!make_tmap(&wmap, W, (uint64_t)N, (uint64_t)K, kTileRows, true)) return cudaErrorInvalidValue;
+  if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)K, (uint32_t)NP, false, (uint64_t)cx.ldx))
+    return cudaErrorInvalidValue;
+  StreamArgs a = {};
+  a.K = K;
+  a.KB = (K + kKChunk - 1) / kKChunk;
+  a.TILES = (N + kTileRows - 1) / kTileRows;
+  a.nout = N;
+  a.M = M;
+  a.out = y;
+  a.ldo = N;
+  a.res = reinterpret_cast<const uint16_t*>(res);
+  a.status = cx.status;
+  a.timeout_ns = cx.timeout_ns;
+  return launch_kc(kern, dim3(a.TILES * cl), dim3(kTcThreads), SMEM, cx.stream, cx.pdl, cl, wmap,
+                   xmap, a, NP, umma_idesc_bf16(128, NP));
+}
+
+cudaError_t launch_dense_tc_cluster(const Ctx& cx, bool residual, const void* x, const void* W,
+                                    const void* res, void* y, int M, int N, int K, int cl) {
+  if (M < 16 || M > kTcXRows || cl < 2 || cl > 8 || cl > (K + kKChunk - 1) / kKChunk)
+    return cudaErrorInvalidValue;
+  return residual ? run_tc_cluster<EPI_BF16_RES>(cx, x, W, res, y, M, N, K, cl)
+                  : run_tc_cluster<EPI_BF16>(cx, x, W, res, y, M, N, K, cl);
 }
 
 template <int EPI>

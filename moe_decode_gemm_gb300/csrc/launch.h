@@ -43,6 +43,9 @@ cudaError_t launch_dense_wide(const Ctx& cx, int xr, bool mma, bool residual, co
 cudaError_t launch_dense_tc(const Ctx& cx, bool residual, const void* x, const void* W,
                             const void* res, void* y, int M, int N, int K, int grid, float* ws,
                             int* ctr);
+// tcgen05 cluster split: cl CTAs per 128-row tile (grid = tiles * cl).
+cudaError_t launch_dense_tc_cluster(const Ctx& cx, bool residual, const void* x, const void* W,
+                                    const void* res, void* y, int M, int N, int K, int cl);
 
 struct MoeBufs {
   float* logits;   // [M,E]

@@ -234,9 +234,53 @@ def test_cluster_split_residual(M):
     assert_within_tol(to_f64(y), ref, Aref, "cluster residual M=%d" % M)
 
 
+# 17-64 tokens (tcgen05) take the same cluster split when N has few tiles:
+# each rank accumulates its k share in tensor memory, drains it to shared
+# memory, and the ranks sum the partials through distributed shared memory.
+@pytest.mark.parametrize("M,N,K", [(33, 1900, 904), (17, 2000, 1288), (64, 1920, 1024),
+                                   (48, 4096, 4096), (64, 2048, 7168)])
+def test_tc_cluster_split_shapes(M, N, K):
+    # ragged last tile and last k chunk, uneven k shares, token counts not a
+    # multiple of 16
+    y, (regime, cl) = _check_random(M, N, K, ("tccluster", M, N, K))
+    assert regime == "tc" and dg.last_cluster() and cl >= 2
+    y2, _ = _gpu_linear(wl.normal_bf16((M, K), 1.0, "tccluster", M, N, K, "x"),
+                        wl.normal_bf16((N, K), 0.02, "tccluster", M, N, K, "W"))
+    assert torch.equal(y, y2), "tcgen05 cluster split not deterministic"
+
+
+@pytest.mark.parametrize("M", [17, 32, 64])
+def test_tc_cluster_integer_inputs_match_stream_k(M):
+    # exact fp32 sums: the cluster split, the stream-K tcgen05 split and the
+    # oracle give the same bits
+    K, N = 2048, 2048
+    x = wl.integer_bf16((M, K), -2, 2, "tccl-int", M, "x")
+    W = wl.integer_bf16((N, K), -2, 2, "tccl-int", M, "W")
+    y, (regime, _) = _gpu_linear(x, W)
+    assert regime == "tc" and dg.last_cluster()
+    ys, (_, s_used) = _gpu_linear(x, W, S=4)
+    assert not dg.last_cluster() and s_used == 4
+    ref, _ = oracle.linear(x, W)
+    assert np.array_equal(wl.torch_to_bits(y), oracle.f64_to_bf16_bits(ref))
+    assert torch.equal(y, ys)
+
+
+@pytest.mark.parametrize("M", [17, 64])
+def test_tc_cluster_residual(M):
+    K, N = 1024, 2048
+    x = wl.normal_bf16((M, K), 1.0, "tccl-res", M, "x")
+    W = wl.normal_bf16((N, K), 0.02, "tccl-res", M, "W")
+    r = wl.normal_bf16((M, N), 1.0, "tccl-res", M, "r")
+    y, (regime, _) = _gpu_linear(x, W, res_bits=r)
+    assert regime == "tc" and dg.last_cluster()
+    f, A = oracle.linear(x, W)
+    ref, Aref = oracle.residual(r, f, A)
+    assert_within_tol(to_f64(y), ref, Aref, "tcgen05 cluster residual M=%d" % M)
+
+
 @pytest.mark.parametrize("M,N,K,ldx", [(1, 7168, 7168, 8192), (4, 4096, 2048, 2056),
                                        (16, 1024, 2048, 4096), (64, 640, 1536, 1544),
-                                       (2, 4096, 4096, 8192)])
+                                       (2, 4096, 4096, 8192), (64, 2048, 1024, 1032)])
 def test_row_strided_input_reads_a_column_slice(M, N, K, ldx):
     # x is the first K columns of a [M, ldx] activation (the q part of a fused
     # q|kv output, say): read in place, with and without a residual
