@@ -183,6 +183,13 @@ static int regime_for(int M) {
   return DEC_REGIME_TC;
 }
 
+// Weight bytes one CTA of the CUDA-core / mma.sync cluster split may stream.
+// Measured (us, stream-K over every SM -> cluster split): 2048 x 16384 at
+// M = 1 / 4 / 8 / 16: 16.0 / 17.4 / 17.5 / 18.4 -> 14.4 / 15.7 / 15.9 / 17.2
+// (512 KB per CTA); 4096 x 7168 at M = 1 / 8: 13.2 / 15.0 -> 12.8 / 14.0
+// (448 KB).
+constexpr long long kClusterMaxBytes = 1024LL * 1024;
+
 // Weight bytes one CTA of the tcgen05 cluster split may stream. Measured (us,
 // tile-aligned stream-K split -> cluster split, 8 CTAs per tile): 2048 x 7168
 // at M = 64 / 32 / 17: 14.1 / 11.2 / 10.6 -> 11.4 / 9.6 / 9.2 (224 KB per
@@ -213,12 +220,11 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
   const bool wide = S == 0 && regime != DEC_REGIME_TC && xr <= 16 && wide_units >= 10LL * s->sms;
   const long long tiles = wide ? (N + 255) / 256 : (N + 127) / 128;
   const long long T = tiles * KB;
-  // Cluster split for small narrow projections: cl CTAs per 128-row tile (a
+  // Cluster split for narrow projections: cl CTAs per 128-row tile (a
   // thread-block cluster), the largest portable size (<= 8) with
   // tiles * cl <= SMs and cl <= KB. Used when it keeps at least three quarters
-  // of the SMs busy and each CTA streams at most 320 KB of weights: there the
-  // split-K fixup's latency dominates; beyond, all SMs' bandwidth does. No
-  // split-K workspace, counters or atomics.
+  // of the SMs busy and each CTA streams at most kClusterMaxBytes of weights.
+  // No split-K workspace, counters or atomics.
   int cl = 0;
   if (S == 0 && regime != DEC_REGIME_TC && !wide && xr <= 16) {
     for (int c = 8; c >= 2; c >>= 1)
@@ -226,7 +232,7 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
         cl = c;
         break;
       }
-    if (cl && (tiles * cl * 4 < 3LL * s->sms || 256LL * K / cl > 320LL * 1024)) cl = 0;
+    if (cl && (tiles * cl * 4 < 3LL * s->sms || 256LL * K / cl > kClusterMaxBytes)) cl = 0;
   }
   // The same split for the tcgen05 kernel (17-64 tokens): its stream-K fixups
   // sum partial tiles of 32 KB per contributor at 64 tokens through L2.
