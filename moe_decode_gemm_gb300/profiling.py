@@ -57,6 +57,9 @@ def kernel_label(name):
     m = re.search(r"tc_linear_kernel<(\d+)>", name)
     if m:
         return "projection [tcgen05 %s]" % _EPI.get(m.group(1), m.group(1))
+    m = re.search(r"tc_cluster_kernel<(\d+)>", name)
+    if m:
+        return "projection [tcgen05 %s cluster]" % _EPI.get(m.group(1), m.group(1))
     for k, lab in (("topk_kernel", "top-k + gates"), ("schedule_gather_kernel", "schedule + gather"),
                    ("combine_kernel", "combine"), ("add_kernel", "residual add"),
                    ("prefetch_kernel", "l2_prefetch")):
