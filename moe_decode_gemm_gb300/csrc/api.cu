@@ -307,7 +307,9 @@ static int moe_bufs(DevState* s, int M, int H, int E, int k, int I, cudaStream_t
   size_t off = 0;
   size_t o_logits = off; off += al((size_t)Mx * Ex * 4);
   size_t o_nact = off; off += al(4);
-  const size_t Gx = (size_t)Ex + ((size_t)Mx * kx + 15) / 16;  // expert groups (16 tokens each at most)
+  // expert groups: at most one per expert plus one per 16 (token, slot) pairs
+  // (a bound for groups of 16 or more tokens)
+  const size_t Gx = (size_t)Ex + ((size_t)Mx * kx + 15) / 16;
   size_t o_gexp = off; off += al(Gx * 4);
   size_t o_goff = off; off += al((Gx + 1) * 4);
   size_t o_ptok = off; off += al((size_t)Mx * kx * 4);
@@ -362,8 +364,8 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   const size_t ws_bytes = (size_t)s->sms * 2 * 256 * 64 * sizeof(float);
   const int tiles13 = (I + 127) / 128, tiles2 = (H + 127) / 128;
   int maxt = tiles13 > tiles2 ? tiles13 : tiles2;
-  // an expert chosen by more than 16 tokens forms several groups: at most
-  // E + M*topk/16 groups, each with its own tile counters
+  // an expert chosen by more tokens than a group holds forms several groups:
+  // at most E + M*topk/16 groups, each with its own tile counters
   const int max_groups = E + (M * topk + 15) / 16;
   const size_t ctr_bytes = (size_t)(max_groups * (size_t)maxt + 64) * sizeof(int);
   if ((rc = ensure(s->ws_main, ws_bytes, st))) return rc;

@@ -13,10 +13,17 @@
 
 namespace dg {
 
-constexpr int kExpertXR = kGroupTokens;     // routed experts: one group's tokens
-constexpr int kExpertPairStages = 3;        // gate/up: 64 KB stages (gate and up halves)
+constexpr int kExpertPairStages = 3;  // gate/up: 64 KB stages (gate and up halves)
 
-constexpr int expert_pair_smem() { return wstream_smem(kExpertXR, kExpertPairStages, 0, true); }
+// Token rows per stage of the routed-expert kernels: a group's tokens. Up to
+// 16 tokens no expert can have more than 16, and the 16-row instances are
+// used; beyond, the 32-row instances, so that an expert chosen by 17-32 tokens
+// streams its weights once. Groups of at most 16 tokens load a 16-row token
+// box there (kNarrowRows).
+template <int XR>
+constexpr int expert_pair_smem() {
+  return wstream_smem(XR, kExpertPairStages, 0, true);
+}
 
 template <typename K>
 static cudaError_t smem_once(K kern, int bytes, bool& done) {
@@ -67,7 +74,7 @@ static cudaError_t run_router(const Ctx& cx, const void* x, const void* Wr, int 
   a.ldo = E;
   const int cl = router_clusters(H);
   return launch_kc(kern, dim3(a.TILES * cl), dim3(kThreads), SMEM, cx.stream, cx.pdl, cl, wmap,
-                   xmap, a);
+                   xmap, xmap, a);
 }
 
 cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E,
@@ -290,19 +297,23 @@ cudaError_t launch_gather(const Ctx& cx, const void* x, int M, int H, int E, int
                   b.pair_tok, b.pair_of);
 }
 
-cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, int M, int H, int E,
-                               int k, int I, const MoeBufs& b, int grid, float* ws, int* ctr) {
-  constexpr int SMEM = expert_pair_smem();
+template <int XR>
+static cudaError_t run_experts_w13(const Ctx& cx, const void* W13, int M, int H, int E, int k,
+                                   int I, const MoeBufs& b, int grid, float* ws, int* ctr) {
+  constexpr int SMEM = expert_pair_smem<XR>();
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
-  auto kern =
-      wstream_kernel<kExpertXR, kExpertPairStages, EPI_SWIGLU, true, true, false, ROLE_EXPERT>;
+  auto kern = wstream_kernel<XR, kExpertPairStages, EPI_SWIGLU, true, true, false, ROLE_EXPERT>;
   static bool done = false;
   cudaError_t e = smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;
   CUtensorMap wmap, xmap;
   if (!make_tmap(&wmap, W13, (uint64_t)E * 2 * I, (uint64_t)H, kTileRows, true))
     return cudaErrorInvalidValue;
-  if (!make_tmap(&xmap, b.xs, (uint64_t)M * k, (uint64_t)H, kExpertXR, false))
+  if (!make_tmap(&xmap, b.xs, (uint64_t)M * k, (uint64_t)H, XR, false))
+    return cudaErrorInvalidValue;
+  CUtensorMap xnarrow = xmap;
+  if (XR > kNarrowRows &&
+      !make_tmap(&xnarrow, b.xs, (uint64_t)M * k, (uint64_t)H, kNarrowRows, false))
     return cudaErrorInvalidValue;
   StreamArgs a = base_args(cx, ws, ctr);
   a.K = H;
@@ -317,21 +328,26 @@ cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, in
   a.w_up_offset = I;
   a.out = b.h;
   a.ldo = I;
-  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
+  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, xnarrow,
+                  a);
 }
 
-cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E, int k, int I,
-                              const MoeBufs& b, int grid, float* ws, int* ctr) {
+template <int XR>
+static cudaError_t run_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E, int k, int I,
+                                  const MoeBufs& b, int grid, float* ws, int* ctr) {
   // 256-row output tiles: two 128-row halves, 64 KB weight stages
-  constexpr int SMEM = expert_pair_smem();
-  auto kern =
-      wstream_kernel<kExpertXR, kExpertPairStages, EPI_F32, false, true, true, ROLE_EXPERT>;
+  constexpr int SMEM = expert_pair_smem<XR>();
+  auto kern = wstream_kernel<XR, kExpertPairStages, EPI_F32, false, true, true, ROLE_EXPERT>;
   static bool done = false;
   cudaError_t e = smem_once(kern, SMEM, done);
   if (e != cudaSuccess) return e;
   CUtensorMap wmap, xmap;
   if (!make_tmap(&wmap, W2, (uint64_t)E * H, (uint64_t)I, kTileRows, true)) return cudaErrorInvalidValue;
-  if (!make_tmap(&xmap, b.h, (uint64_t)M * k, (uint64_t)I, kExpertXR, false))
+  if (!make_tmap(&xmap, b.h, (uint64_t)M * k, (uint64_t)I, XR, false))
+    return cudaErrorInvalidValue;
+  CUtensorMap xnarrow = xmap;
+  if (XR > kNarrowRows &&
+      !make_tmap(&xnarrow, b.h, (uint64_t)M * k, (uint64_t)I, kNarrowRows, false))
     return cudaErrorInvalidValue;
   StreamArgs a = base_args(cx, ws, ctr);
   a.K = I;
@@ -346,7 +362,21 @@ cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E
   a.tables_ready = 1;  // the gate/up kernel lets this one launch only after its own wait
   a.out = b.o;
   a.ldo = H;
-  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
+  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, xnarrow,
+                  a);
+}
+
+cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, int M, int H, int E,
+                               int k, int I, const MoeBufs& b, int grid, float* ws, int* ctr) {
+  (void)x;
+  if (M <= kNarrowRows) return run_experts_w13<kNarrowRows>(cx, W13, M, H, E, k, I, b, grid, ws, ctr);
+  return run_experts_w13<kGroupTokens>(cx, W13, M, H, E, k, I, b, grid, ws, ctr);
+}
+
+cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E, int k, int I,
+                              const MoeBufs& b, int grid, float* ws, int* ctr) {
+  if (M <= kNarrowRows) return run_experts_w2<kNarrowRows>(cx, W2, M, H, E, k, I, b, grid, ws, ctr);
+  return run_experts_w2<kGroupTokens>(cx, W2, M, H, E, k, I, b, grid, ws, ctr);
 }
 
 // Shared expert: a dense (ungrouped) pass over every token, token rows per
@@ -377,7 +407,7 @@ static cudaError_t run_shared_w13(const Ctx& cx, const void* x, const void* Ws13
   a.ldo = I;
   const long long T = (long long)a.TILES * a.KB;
   if (grid > T) grid = (int)T;
-  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
+  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, xmap, a);
 }
 
 template <int XR>
@@ -403,7 +433,7 @@ static cudaError_t run_shared_w2(const Ctx& cx, const void* Ws2, int M, int H, i
   a.ldo = H;
   const long long T = (long long)a.TILES * a.KB;
   if (grid > T) grid = (int)T;
-  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
+  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, xmap, a);
 }
 
 cudaError_t launch_shared_w13(const Ctx& cx, const void* x, const void* Ws13, int M, int H, int I,

@@ -40,8 +40,12 @@ enum Epi : int { EPI_BF16 = 0, EPI_BF16_RES = 1, EPI_F32 = 2, EPI_SWIGLU = 3 };
 
 // An expert chosen by more tokens than this is split into several groups of
 // at most this many (its weights are then streamed once per group). It sizes
-// the token rows of an expert kernel's pipeline stage.
-constexpr int kGroupTokens = 16;
+// the token rows of an expert kernel's pipeline stage beyond 16 tokens.
+constexpr int kGroupTokens = 32;
+// Groups of at most this many tokens load a token box of this height when
+// the stage holds more rows (the smaller box fills the first rows of the
+// same shared-memory slot): the token rows a stage moves follow the group.
+constexpr int kNarrowRows = 16;
 
 constexpr int kMaxSlots = 512;  // contributor slot table entries in shared memory
 // Weight bytes per CTA a plain projection prefetches into L2 before waiting
@@ -268,7 +272,7 @@ template <int XR, int STAGES, int EPI, bool PAIRED, bool GROUPED, bool WIDE = fa
           int ROLE = ROLE_PROJECTION, int MINB = 1, bool CLUSTER = false, int PATH = PATH_ANY>
 __global__ void __launch_bounds__(kThreads, MINB)
     wstream_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
-                   const StreamArgs a) {
+                   const __grid_constant__ CUtensorMap xmap_narrow, const StreamArgs a) {
   constexpr int H2 = (PAIRED || WIDE) ? 2 : 1;  // 128-row weight halves per box column
   // CUDA-core dot form. Both give the same bits. The bf16-operand form
   // (fma.rn.f32.bf16) issues half the instructions; the widened form is kept
@@ -305,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
   if (threadIdx.x == 32) {
     prefetch_tmap(&wmap);
     prefetch_tmap(&xmap);
+    if (GROUPED && XR > kNarrowRows) prefetch_tmap(&xmap_narrow);
   }
   __syncthreads();
   // Kernels that can stream weights before their predecessor finishes let
@@ -370,6 +375,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
                         &full[s], pol_w);
         }
       };
+      auto narrow_group = [&](const GroupInfo& g_) {
+        return GROUPED && XR > kNarrowRows && g_.c <= kNarrowRows;
+      };
       auto issue_x = [&](int s, int kc, const GroupInfo& g_) {
         uint8_t* xdst = smem + s * kStageBytes + kWStage;
 #pragma unroll
@@ -380,7 +388,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
           // tensor (pairs are stored in expert order), so one box of XR rows
           // at the group's first pair covers them; rows past the group are
           // never read.
-          tma_load_2d(d, &xmap, k0, GROUPED ? g_.p0 : 0, &full[s], pol_x);
+          tma_load_2d(d, narrow_group(g_) ? &xmap_narrow : &xmap, k0, GROUPED ? g_.p0 : 0,
+                      &full[s], pol_x);
         }
       };
       // The same weight boxes as issue_w for expert e, into L2 only.
@@ -396,7 +405,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
                                             : p.tile * kTileOut + kTileRows));
         }
       };
-      const uint32_t tx_bytes = kWStage + kXBytes;
+      auto tx_bytes = [&](const GroupInfo& g_) -> uint32_t {
+        return kWStage + (narrow_group(g_) ? (uint32_t)(kKSub * kNarrowRows * 128) : (uint32_t)kXBytes);
+      };
       UnitPos pos = unit_pos(u0, KB, TILES);
       int i = 0;
       if (early) {
@@ -411,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
             gi = load_group<GROUPED>(a, pos.g);
           }
           pg[i] = gi;
-          mbar_arrive_expect_tx(&full[i], tx_bytes);
+          mbar_arrive_expect_tx(&full[i], tx_bytes(gi));
           issue_w(i, pos);
         }
         // The units beyond the ring: pull up to kPrefetchBytes of them into
@@ -447,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
           gcur = pos.g;
           gi = load_group<GROUPED>(a, pos.g);
         }
-        mbar_arrive_expect_tx(&full[s], tx_bytes);
+        mbar_arrive_expect_tx(&full[s], tx_bytes(gi));
         issue_w(s, pos);
         issue_x(s, pos.kc, gi);
       }

@@ -118,8 +118,10 @@ def test_routing_limits_topk32_of_1024_experts_64_tokens():
 
 
 def test_skewed_routing_shares_experts_across_groups():
-    # power-law expert popularity: the most popular experts serve more than
-    # 16 tokens (several token groups each) and many experts serve none
+    # power-law expert popularity at 64 tokens (32-row expert groups): experts
+    # serving 17-32 tokens (one wide group), one serving more than 32 (two
+    # groups), experts of at most 16 (the narrow token box), and many serving
+    # none
     M, H, E, I, k = 64, 256, 64, 128, 8
     key = ("moe-skew",)
     Wr = wl.skewed_router_bf16(E, H, 1.0, *key, "Wr")
@@ -129,7 +131,8 @@ def test_skewed_routing_shares_experts_across_groups():
     Ws = (wl.normal_bf16((2 * I, H), 0.02, *key, "Ws13"), wl.normal_bf16((H, I), 0.02, *key, "Ws2"))
     idx = oracle.moe(x, Wr, lambda e: (W13[e], W2[e]), k, I, shared=None)["idx"]
     counts = np.bincount(idx.ravel(), minlength=E)
-    assert counts.max() > 16 and (counts == 0).sum() > 0, counts
+    assert counts.max() > 32 and ((counts > 16) & (counts <= 32)).any(), counts
+    assert ((counts > 0) & (counts <= 16)).any() and (counts == 0).sum() > 0, counts
     _check(x, Wr, W13, W2, Ws, k, "skewed routing")
 
 
