@@ -142,10 +142,13 @@ def layer_bytes(M, U):
 
 
 # DRAM traffic (read + write) of the routed gate/up kernel per chosen expert,
-# from one ncu capture of a small case (16 tokens over a 32-expert bank, 31
-# experts chosen: 1825.8 MB in one launch). Its traffic grows in proportion to
-# the experts it streams, so a full launch's traffic is this times its count.
-W13_TRAFFIC_PER_EXPERT = 1825.8e6 / 31
+# from one ncu capture of a small case of each instance: 16 token rows per
+# stage (up to 16 tokens; 16 tokens over a 32-expert bank, 31 experts chosen:
+# 1826.0 MB in one launch) and 32 rows (beyond; 32 tokens, 32 experts:
+# 1887.6 MB). Its traffic grows in proportion to the experts it streams, so a
+# full launch's traffic is this times its count.
+def w13_traffic_per_expert(M):
+    return 1826.0e6 / 31 if M <= 16 else 1887.6e6 / 32
 
 
 def w13_launch_bytes(M, U):
@@ -335,7 +338,7 @@ def run_ours(args, rank, world, local_rank):
     step_bytes = sum(layer_bytes(M, U[M][l]) for M in BATCHES for l in range(nl))
     w13_bytes = sum(w13_launch_bytes(M, U[M][l]) for M in BATCHES for l in range(nl))
     w13_units = [U[M][l] for M in BATCHES for l in range(nl)]
-    w13_experts = sum(w13_units)
+    w13_traffic = sum(w13_traffic_per_expert(M) * U[M][l] for M in BATCHES for l in range(nl))
 
     def barrier():
         replica_barrier(world)
@@ -454,7 +457,7 @@ def run_ours(args, rank, world, local_rank):
             # the kernel's share of the timed device time (compare with the
             # share in the ncu launch list)
             "share_of_step": round(w13_ms / ms, 4) if w13_n == expect_n else None,
-            "traffic": int(W13_TRAFFIC_PER_EXPERT * w13_experts / len(w13_units)),
+            "traffic": int(w13_traffic / len(w13_units)),
             "traffic_note": "DRAM bytes per launch: small-case ncu capture scaled by chosen experts",
             "algorithmic_bytes_per_launch": int(w13_bytes / len(w13_units)),
         },
