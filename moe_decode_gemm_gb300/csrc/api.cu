@@ -193,8 +193,7 @@ constexpr long long kClusterMaxBytes = 1024LL * 1024;
 // Weight bytes one CTA of the tcgen05 cluster split may stream. Measured (us,
 // tile-aligned stream-K split -> cluster split, 8 CTAs per tile): 2048 x 7168
 // at M = 64 / 32 / 17: 14.1 / 11.2 / 10.6 -> 11.4 / 9.6 / 9.2 (224 KB per
-// CTA); 2048 x 16384 at M = 64 / 32: 19.9 / 16.9 -> 18.7 / 16.9 (512 KB);
-// 4096 x 4096 at M = 64 (4 per tile): 12.6 either way.
+// CTA); 2048 x 16384 at M = 64 / 32: 19.9 / 16.9 -> 18.7 / 16.9 (512 KB).
 constexpr long long kTcClusterMaxBytes = 1024LL * 1024;
 
 static int linear_impl(const void* x, const void* W, const void* res, void* y, int M, int N, int K,
@@ -234,16 +233,15 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
       }
     if (cl && (tiles * cl * 4 < 3LL * s->sms || 256LL * K / cl > kClusterMaxBytes)) cl = 0;
   }
-  // The same split for the tcgen05 kernel (17-64 tokens): its stream-K fixups
-  // sum partial tiles of 32 KB per contributor at 64 tokens through L2.
-  if (S == 0 && regime == DEC_REGIME_TC) {
-    for (int c = 8; c >= 2; c >>= 1)
-      if (tiles * c <= s->sms && c <= KB) {
-        cl = c;
-        break;
-      }
-    if (cl && (tiles * cl * 4 < 3LL * s->sms || 256LL * K / cl > kTcClusterMaxBytes)) cl = 0;
-  }
+  // The same split for the tcgen05 kernel (17-64 tokens), whose stream-K
+  // fixups sum partial tiles of 32 KB per contributor at 64 tokens, but only
+  // with 8 ranks per tile: with 2-4 partials per tile the tile-aligned split
+  // below sums them cheaply and its 4-stage ring streams a large share faster
+  // than the cluster kernel's 2-stage one (M = 64, us, cluster -> aligned:
+  // 4096 x 7168 17.8 -> 16.2 at 4 ranks, 8192 x 7168 31.9 -> 24.9 at 2).
+  if (S == 0 && regime == DEC_REGIME_TC && tiles * 8 <= s->sms && KB >= 8 &&
+      tiles * 8 * 4 >= 3LL * s->sms && 256LL * K / 8 <= kTcClusterMaxBytes)
+    cl = 8;
   if (cl) {
     Ctx cx = make_ctx(s, st);
     cx.ldx = ldx;

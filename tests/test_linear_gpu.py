@@ -238,7 +238,7 @@ def test_cluster_split_residual(M):
 # each rank accumulates its k share in tensor memory, drains it to shared
 # memory, and the ranks sum the partials through distributed shared memory.
 @pytest.mark.parametrize("M,N,K", [(33, 1900, 904), (17, 2000, 1288), (64, 1920, 1024),
-                                   (48, 4096, 4096), (64, 2048, 7168)])
+                                   (48, 2304, 4096), (64, 2048, 7168)])
 def test_tc_cluster_split_shapes(M, N, K):
     # ragged last tile and last k chunk, uneven k shares, token counts not a
     # multiple of 16
