@@ -319,6 +319,7 @@ static int moe_bufs(DevState* s, int M, int H, int E, int k, int I, cudaStream_t
   size_t o_o = off; off += al((size_t)Mx * kx * Hx * 4);
   size_t o_hs = off; off += al((size_t)Mx * Ix * 2);
   size_t o_s = off; off += al((size_t)Mx * Hx * 4);
+  size_t o_rctr = off; off += al(4);
   int rc = ensure(s->moe, off, st);
   if (rc) return rc;
   uint8_t* b = (uint8_t*)s->moe.p;
@@ -335,6 +336,7 @@ static int moe_bufs(DevState* s, int M, int H, int E, int k, int I, cudaStream_t
   s->mb.o = (float*)(b + o_o);
   s->mb.hs = (uint16_t*)(b + o_hs);
   s->mb.s = (float*)(b + o_s);
+  s->mb.route_ctr = (int*)(b + o_rctr);
   s->moe_M = Mx;
   s->moe_E = Ex;
   s->moe_k = kx;
@@ -412,9 +414,8 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   }
   {
     ProbeScope p(3, st);
-    if ((rc = counted(launch_router(cx, x, Wr, M, H, E, s->mb)))) return rc;
+    if ((rc = counted(launch_router(cx, x, Wr, M, H, E, topk, topk_idx, topk_w, s->mb)))) return rc;
   }
-  if ((rc = counted(launch_topk(cx, M, E, topk, topk_idx, topk_w, s->mb)))) return rc;
   if ((rc = counted(launch_gather(cx, x, M, H, E, topk, s->mb)))) return rc;
   {
     ProbeScope p(0, st);

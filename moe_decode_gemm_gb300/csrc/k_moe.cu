@@ -1,5 +1,6 @@
-// k_moe.cu -- the MoE decode block's kernels: router scoring, top-k with
-// renormalised gates, the expert-gather schedule and token gather, the routed
+// k_moe.cu -- the MoE decode block's kernels: router scoring with the top-k
+// and renormalised gates in the same kernel (routing.cuh), the expert-gather
+// schedule and token gather, the routed
 // experts' gate-up (SwiGLU) and down projections over the selected experts
 // only, the shared expert, and the gate-weighted combine. Plus the residual
 // add, the L2 prefetch kernel and the failure-detection self test.
@@ -50,10 +51,12 @@ static StreamArgs base_args(const Ctx& cx, float* ws, int* ctr) {
 // cluster split, router_clusters(H) CTAs per 128-row tile of experts summing
 // their partial tiles through distributed shared memory, so no split-K fixup
 // through L2 sits on the routing path; the shared expert streams on the
-// other SMs meanwhile.
+// other SMs meanwhile. The last cluster to write its logits then selects
+// every token's top-k experts and gates (one warp per token), so no separate
+// top-k kernel and launch sits between the scores and the schedule.
 template <int XR>
 static cudaError_t run_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E,
-                              const MoeBufs& b) {
+                              int k, int32_t* idx_user, float* w_user, const MoeBufs& b) {
   constexpr int STAGES = XR == 64 ? 4 : 6;
   constexpr int SMEM = wstream_smem(XR, STAGES, 0);
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
@@ -72,99 +75,23 @@ static cudaError_t run_router(const Ctx& cx, const void* x, const void* Wr, int 
   a.M = M;
   a.out = b.logits;
   a.ldo = E;
+  a.route_k = k;
+  a.route_ctr = b.route_ctr;
+  a.route_idx = b.topk;
+  a.route_gate = b.gate;
+  a.route_idx_user = idx_user;
+  a.route_w_user = w_user;
   const int cl = router_clusters(H);
   return launch_kc(kern, dim3(a.TILES * cl), dim3(kThreads), SMEM, cx.stream, cx.pdl, cl, wmap,
                    xmap, xmap, a);
 }
 
-cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E,
-                          const MoeBufs& b) {
-  if (M <= 8) return run_router<8>(cx, x, Wr, M, H, E, b);
-  if (M <= 16) return run_router<16>(cx, x, Wr, M, H, E, b);
-  return run_router<64>(cx, x, Wr, M, H, E, b);
-}
-
-// ------------------------------------------------------------------ top-k
-// Order-preserving map of a float to uint32 (larger float, larger key); 0 is
-// below every float's key.
-__device__ __forceinline__ uint32_t float_key(float f) {
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ float key_float(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
-}
-
-// One warp per token: the topk largest scores, ordered by (value desc,
-// index asc), and gates g_j = exp(l_j - l_max) / sum_j' exp(l_j' - l_max)
-// summed j = 0..topk-1. A lane holds scores e = lane + 32 j, j < PER, as keys
-// in registers; each round takes the lane's best, the warp's maximum key and,
-// among lanes holding it, the smallest index.
-template <int PER>
-__global__ void __launch_bounds__(32) topk_kernel(const float* __restrict__ logits, int E, int K,
-                                                  int* __restrict__ idx, float* __restrict__ gate,
-                                                  int32_t* idx_user, float* w_user) {
-  griddep_launch_dependents();
-  griddep_wait();
-  const int m = blockIdx.x, lane = threadIdx.x;
-  const float* row = logits + (long long)m * E;
-  uint32_t kv[PER];
-#pragma unroll
-  for (int j = 0; j < PER; ++j) {
-    const int e = lane + 32 * j;
-    kv[j] = e < E ? float_key(__ldcg(row + e)) : 0u;
-  }
-  float selv0 = 0.f, myv = 0.f;
-  int mye = 0;
-  for (int j = 0; j < K; ++j) {
-    uint32_t bk = kv[0];
-    int bj = 0;
-#pragma unroll
-    for (int jj = 1; jj < PER; ++jj)
-      if (kv[jj] > bk) {  // strict: the smallest jj (smallest index) on ties
-        bk = kv[jj];
-        bj = jj;
-      }
-    const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
-    const uint32_t cand = (bk == kmax && kmax != 0u) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
-    const uint32_t emin = __reduce_min_sync(0xffffffffu, cand);
-    if ((int)(emin & 31) == lane) {
-#pragma unroll
-      for (int jj = 0; jj < PER; ++jj)
-        if (jj == bj) kv[jj] = 0u;
-    }
-    const float wv = key_float(kmax);
-    if (j == 0) selv0 = wv;
-    if (lane == j) {
-      myv = wv;
-      mye = (int)emin;
-    }
-  }
-  const float w = (lane < K) ? expf(myv - selv0) : 0.f;
-  float denom = 0.f;
-  for (int j = 0; j < K; ++j) denom += __shfl_sync(0xffffffffu, w, j);
-  if (lane < K) {
-    const float g = w / denom;
-    idx[m * K + lane] = mye;
-    gate[m * K + lane] = g;
-    if (idx_user) idx_user[m * K + lane] = mye;
-    if (w_user) w_user[m * K + lane] = g;
-  }
-}
-
-cudaError_t launch_topk(const Ctx& cx, int M, int E, int k, int32_t* idx_user, float* w_user,
-                        const MoeBufs& b) {
-  const int per = (E + 31) / 32;
-  auto go = [&](auto kern) {
-    return launch_k(kern, dim3(M), dim3(32), 0, cx.stream, cx.pdl, (const float*)b.logits, E, k,
-                    b.topk, b.gate, idx_user, w_user);
-  };
-  if (per <= 4) return go(topk_kernel<4>);
-  if (per <= 8) return go(topk_kernel<8>);
-  if (per <= 12) return go(topk_kernel<12>);
-  if (per <= 16) return go(topk_kernel<16>);
-  return go(topk_kernel<32>);
+cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E, int k,
+                          int32_t* idx_user, float* w_user, const MoeBufs& b) {
+  if (k < 1 || k > 32 || k > E || E > 1024) return cudaErrorInvalidValue;
+  if (M <= 8) return run_router<8>(cx, x, Wr, M, H, E, k, idx_user, w_user, b);
+  if (M <= 16) return run_router<16>(cx, x, Wr, M, H, E, k, idx_user, w_user, b);
+  return run_router<64>(cx, x, Wr, M, H, E, k, idx_user, w_user, b);
 }
 
 // ------------------------------------------------------------------ schedule + gather

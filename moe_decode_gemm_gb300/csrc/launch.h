@@ -61,6 +61,7 @@ struct MoeBufs {
   float* o;        // [M*k, H]
   uint16_t* hs;    // [M, I]
   float* s;        // [M, H]
+  int* route_ctr;  // router clusters arrived (zero at rest)
 };
 
 // Router: CTAs per 128-row tile of experts (one thread-block cluster each),
@@ -71,10 +72,9 @@ inline int router_clusters(int H) {
 }
 inline int router_ctas(int E, int H) { return (E + 127) / 128 * router_clusters(H); }
 
-cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E,
-                          const MoeBufs& b);
-cudaError_t launch_topk(const Ctx& cx, int M, int E, int k, int32_t* idx_user, float* w_user,
-                        const MoeBufs& b);
+// Router scores and, in the same kernel, the top-k experts and gates.
+cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E, int k,
+                          int32_t* idx_user, float* w_user, const MoeBufs& b);
 cudaError_t launch_gather(const Ctx& cx, const void* x, int M, int H, int E, int k,
                           const MoeBufs& b);
 // grid: CTAs (the expert kernels split their work statically over them).

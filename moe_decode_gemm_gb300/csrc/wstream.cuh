@@ -24,6 +24,7 @@
 #pragma once
 
 #include "dg_common.cuh"
+#include "routing.cuh"
 
 namespace dg {
 
@@ -84,6 +85,14 @@ struct StreamArgs {
   int* ctr;                  // per output tile arrival counters (zero at rest)
   int* status;
   long long timeout_ns;
+  // router role: with route_k > 0 the last cluster to finish its logits
+  // selects every token's top route_k experts and their gates
+  int route_k;
+  int* route_ctr;            // arrival counter (zero at rest)
+  int* route_idx;            // [M][route_k]
+  float* route_gate;         // [M][route_k]
+  int32_t* route_idx_user;   // optional copies for the caller
+  float* route_w_user;
 };
 
 struct GroupInfo {
@@ -291,7 +300,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
                                              ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * kStageBytes);
   uint64_t* empty = full + STAGES;
-  volatile int* s_flags = reinterpret_cast<volatile int*>(empty + STAGES);  // [0] abort [1] last
+  // [0] abort [1] last arriver of a split tile [2] last cluster of the router
+  volatile int* s_flags = reinterpret_cast<volatile int*>(empty + STAGES);
   int* s_slot = const_cast<int*>(s_flags) + 8;                                 // [kMaxSlots]
 
   const int warp = threadIdx.x >> 5;
@@ -304,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     }
     s_flags[0] = 0;
     s_flags[1] = 0;
+    s_flags[2] = 0;
     fence_mbar_init();
   }
   if (threadIdx.x == 32) {
@@ -471,10 +482,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
     }
     if (early && lane != 0) griddep_wait();
     if (CLUSTER) {
-      // the producer warp takes part in the consumers' two cluster barriers
+      // the producer warp takes part in the consumers' cluster barriers
       __syncwarp();
       cluster_sync_all();
       cluster_sync_all();
+      if (ROLE == ROLE_ROUTER && a.route_k > 0) cluster_sync_all();
     }
   } else {
     // ---------------------------------------------------------------- consumers
@@ -815,6 +827,28 @@ __global__ void __launch_bounds__(kThreads, MINB)
         }
       }
       cluster_sync_all();  // no CTA leaves while another still reads its partial
+      if (ROLE == ROLE_ROUTER && a.route_k > 0) {
+        // This cluster's logits are written (the barrier orders every
+        // thread's stores before the release of the arrival below). The last
+        // of the TILES clusters to arrive acquires them all and selects the
+        // experts: its consumer warps take the tokens in turn.
+        if (cr == 0 && ct == 0) {
+          const int old = atomic_add_acq_rel_gpu(a.route_ctr, 1);
+          const int last = old == TILES - 1 ? 1 : 0;
+          if (last) *a.route_ctr = 0;
+          for (int qr = 0; qr < cs; ++qr)
+            st_dsmem_s32(const_cast<int*>(&s_flags[2]), (uint32_t)qr, last);
+        }
+        cluster_sync_all();
+        if (s_flags[2]) {
+          const int K = a.route_k;
+          for (int m = cr * kNCW + w; m < a.M; m += cs * kNCW)
+            warp_topk_gates(reinterpret_cast<const float*>(a.out) + (long long)m * a.ldo, a.nout,
+                            K, lane, a.route_idx + m * K, a.route_gate + m * K,
+                            a.route_idx_user ? a.route_idx_user + m * K : nullptr,
+                            a.route_w_user ? a.route_w_user + m * K : nullptr);
+        }
+      }
     } else if (cur >= 0) {
       finish_tile(cur, false);
     }

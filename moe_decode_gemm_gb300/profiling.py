@@ -33,7 +33,7 @@ import re
 import sys
 
 _EPI = {"0": "bf16", "1": "bf16+residual", "2": "fp32", "3": "SwiGLU"}
-_ROLE = {"0": "projection", "1": "router", "2": "routed expert", "3": "shared expert"}
+_ROLE = {"0": "projection", "1": "router + top-k", "2": "routed expert", "3": "shared expert"}
 _TRUE = ("true", "1")
 
 
@@ -60,7 +60,7 @@ def kernel_label(name):
     m = re.search(r"tc_cluster_kernel<(\d+)>", name)
     if m:
         return "projection [tcgen05 %s cluster]" % _EPI.get(m.group(1), m.group(1))
-    for k, lab in (("topk_kernel", "top-k + gates"), ("schedule_gather_kernel", "schedule + gather"),
+    for k, lab in (("schedule_gather_kernel", "schedule + gather"),
                    ("combine_kernel", "combine"), ("add_kernel", "residual add"),
                    ("prefetch_kernel", "l2_prefetch")):
         if k in name:
