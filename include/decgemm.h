@@ -133,9 +133,10 @@ int dec_linear_splitk(const void* x, const void* W, void* y, int M, int N, int K
  *   g_j    = exp(l_j - l_max) / sum_{j' < topk} exp(l_j' - l_max);
  *   h      = silu(x·W1ᵀ) * (x·W3ᵀ) per chosen expert (rounded to bf16);
  *   out    = bf16( sum_{j=0..topk-1} g_j · h_j·W2ᵀ  +  shared(x) ).
- * Only the chosen experts' weights are read, each once per call however many
- * tokens chose it. Kernels on `stream`: router projection, top-k (one warp per
- * token), schedule + token gather, expert gate/up with SwiGLU, expert down,
+ * Only the chosen experts' weights are read: each once per call, or once per
+ * group of 32 tokens if more than 32 tokens chose it. Kernels on `stream`:
+ * router projection with the top-k (one warp per token, in the router's last
+ * cluster), schedule + token gather, expert gate/up with SwiGLU, expert down,
  * combine. The shared expert runs on a library-owned side stream of the
  * lowest priority that waits on `stream` at entry: its kernels take the SMs
  * the router leaves free and stream their weights while routing runs;
