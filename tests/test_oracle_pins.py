@@ -333,6 +333,58 @@ def test_decoder_layer_identity_and_doubling():
     assert np.array_equal(_dec(r["out"]), 2.0 * _dec(x))
 
 
+def test_decoder_layer_o_projection_reads_q_not_x():
+    # Wq = 2I, Wo = I: q = 2x and r = bf16(x + 2x) = bf16(3x). An o projection
+    # wired to x would give 2x; one that skipped the residual would give 2x too.
+    H, I, E, M = 32, 8, 4, 3
+    x = wl.normal_bf16((M, H), 1.0, "pin", "layer-q", "x")
+    Wr = wl.normal_bf16((E, H), 0.2, "pin", "layer-q", "Wr")
+    W13 = np.stack([wl.normal_bf16((2 * I, H), 0.1, "pin", "layer-q", "W13", e) for e in range(E)])
+    zW2 = np.zeros((E, H, I), dtype=np.uint16)
+    Wkv = wl.normal_bf16((16, H), 0.1, "pin", "layer-q", "Wkv")
+    r = oracle.decoder_layer(x, _bits(2 * np.eye(H)), Wkv, _bits(np.eye(H)), Wr,
+                             _bank_fetch(W13, zW2), 2, I, None)
+    three_x = wl.f32_to_bf16_bits(np.float32(3) * _dec(x).astype(np.float32))  # exact in fp32
+    assert np.array_equal(r["q"], _bits(2 * _dec(x)))
+    assert np.array_equal(r["r"], three_x)
+    assert np.array_equal(r["out"], three_x)          # zero expert outputs: x' = r
+    # A permutation for Wq (row n picks column perm[n]) and Wo = 2I:
+    # r = bf16(x + 2 x[:, perm]); a transposed Wq would pick the inverse permutation.
+    perm = np.random.default_rng(5).permutation(H)
+    P = np.zeros((H, H))
+    P[np.arange(H), perm] = 1.0
+    assert not np.array_equal(perm, np.argsort(perm))
+    r = oracle.decoder_layer(x, _bits(P), Wkv, _bits(2 * np.eye(H)), Wr,
+                             _bank_fetch(W13, zW2), 2, I, None)
+    xv = _dec(x).astype(np.float32)
+    assert np.array_equal(r["q"], x[:, perm])
+    assert np.array_equal(r["r"], wl.f32_to_bf16_bits(xv + np.float32(2) * xv[:, perm]))
+
+
+def test_decoder_layer_moe_reads_r_and_adds_r():
+    # With r = bf16(3x) != x and nonzero experts, the block's input and its
+    # residual must both be r: x' = bf16(r + moe(r)), routed on r's scores.
+    H, I, E, M, k = 32, 8, 6, 4, 2
+    x = wl.normal_bf16((M, H), 1.0, "pin", "layer-m", "x")
+    Wr = wl.normal_bf16((E, H), 0.3, "pin", "layer-m", "Wr")
+    W13 = np.stack([wl.normal_bf16((2 * I, H), 0.2, "pin", "layer-m", "W13", e) for e in range(E)])
+    W2 = np.stack([wl.normal_bf16((H, I), 0.2, "pin", "layer-m", "W2", e) for e in range(E)])
+    Ws = (wl.normal_bf16((2 * I, H), 0.2, "pin", "layer-m", "Ws13"),
+          wl.normal_bf16((H, I), 0.2, "pin", "layer-m", "Ws2"))
+    Wkv = wl.normal_bf16((16, H), 0.1, "pin", "layer-m", "Wkv")
+    lay = oracle.decoder_layer(x, _bits(2 * np.eye(H)), Wkv, _bits(np.eye(H)), Wr,
+                               _bank_fetch(W13, W2), k, I, Ws)
+    r = wl.f32_to_bf16_bits(np.float32(3) * _dec(x).astype(np.float32))
+    on_r = oracle.moe(r, Wr, _bank_fetch(W13, W2), k, I, shared=Ws)
+    on_x = oracle.moe(x, Wr, _bank_fetch(W13, W2), k, I, shared=Ws)
+    assert np.array_equal(lay["idx"], on_r["idx"])
+    want = oracle.f64_to_bf16_bits(_dec(r) + on_r["out"])
+    assert np.array_equal(lay["out"], want)
+    # the pin has teeth: feeding x to the block, or adding x, changes the result
+    assert not np.array_equal(want, oracle.f64_to_bf16_bits(_dec(r) + on_x["out"]))
+    assert not np.array_equal(want, oracle.f64_to_bf16_bits(_dec(x) + on_r["out"]))
+
+
 # ------------------------------------------------------------------ generators
 def test_generators_are_deterministic_and_scaled():
     a = wl.normal_bf16((64, 512), 0.02, "gen", 1)
