@@ -178,12 +178,14 @@ int dec_add(const void* a, const void* b, void* out, size_t n, void* stream);
 
 /*
  * dec_last_choice -- regime and split of this thread's last dec_linear* call.
- * [trace-path] Returns regime | (S << 8) | (C << 16) where regime is a
- * DEC_REGIME_* value, S the number of CTAs that share each output tile's K
- * range (1 = none), rounded up, and C is 1 when those S CTAs form one
+ * [trace-path] Returns regime | (S << 8) | (C << 16) | (Wd << 17) where regime
+ * is a DEC_REGIME_* value, S the number of CTAs that share each output tile's
+ * K range (1 = none), rounded up, C is 1 when those S CTAs form one
  * thread-block cluster and sum their partial tiles through distributed shared
  * memory (small projections: few 128-row tiles, M <= 16), 0 when the split is
- * the stream-K one with a last-arriver fixup. DEC_REGIME_NONE before any call.
+ * the stream-K one with a last-arriver fixup, and Wd is 1 when the output
+ * tiles are 256 rows high (large projections at M <= 16). DEC_REGIME_NONE
+ * before any call.
  */
 int dec_last_choice(void);
 
@@ -194,9 +196,12 @@ int dec_last_grid(void);
 const char* dec_strerror(int code);
 
 /*
- * dec_sync_check -- synchronise `stream`, then read and clear the device
- * status word that kernels set when a bounded wait gives up. Returns DEC_OK,
- * DEC_ETIMEOUT, or DEC_ECUDA if the synchronisation itself failed.
+ * dec_sync_check -- synchronise `stream` (and the library's side stream),
+ * then read and clear the device status words that kernels set when a bounded
+ * wait gives up: the library's own and the one in dec_linear_noalloc's fixed
+ * array. Returns DEC_OK, DEC_ETIMEOUT, or DEC_ECUDA if the synchronisation
+ * itself failed. Allocates nothing: in a process that has only called
+ * dec_linear_noalloc it sets up no workspace, stream or event.
  */
 int dec_sync_check(void* stream);
 
@@ -263,8 +268,12 @@ int dec_probe_end(double* total_ms, int* launches);
  * last call's contents (each call clears the counters it uses): calls that can
  * overlap on the GPU -- on unordered streams or from several host threads --
  * race and corrupt each other's results. A bounded device-side wait that
- * gives up ends the kernel as in dec_linear, but is not reported through
- * dec_sync_check. Does not update dec_last_choice or dec_launch_count.
+ * gives up ends the kernel as in dec_linear (y is then incomplete) and sets a
+ * status word in the fixed array; the word is not cleared by later calls, and
+ * dec_sync_check reports it as DEC_ETIMEOUT (and clears it) -- call it before
+ * trusting y where a give-up must not pass unseen. A first call made while
+ * `stream` is being captured returns DEC_EINVAL (the set-up above cannot run
+ * inside a capture). Does not update dec_last_choice or dec_launch_count.
  */
 int dec_linear_noalloc(const void* x, const void* W, void* y, int M, int N, int K, void* stream);
 

@@ -96,6 +96,38 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _need(t, name, shape=None, dtype="bf16", contiguous=True):
+    """Reject a tensor the C ABI would misread: the ABI sees only pointers
+    and sizes, so dtype, shape and layout are checked here (the device by
+    ``_on_one_gpu`` once every operand has passed)."""
+    import torch
+
+    want = {"bf16": torch.bfloat16, "i32": torch.int32, "f32": torch.float32}[dtype]
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s: expected a torch tensor, got %s" % (name, type(t).__name__))
+    if t.dtype != want:
+        raise TypeError("%s: expected %s, got %s" % (name, want, t.dtype))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s: expected shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    if contiguous and not t.is_contiguous():
+        raise ValueError("%s: must be contiguous (row-major)" % name)
+    return t
+
+
+def _on_one_gpu(**tensors):
+    """Every given tensor (None entries skipped) lives on one CUDA device."""
+    dev = None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if t.device.type != "cuda":
+            raise ValueError("%s: expected a CUDA tensor, got one on %s" % (name, t.device))
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError("%s: on %s, the other operands on %s" % (name, t.device, dev))
+
+
 def _stream(stream):
     import torch
 
@@ -114,13 +146,23 @@ def dec_linear(x, W, y=None, stream=None, residual=None):
     """
     import torch
 
+    _need(x, "x", contiguous=False)
+    if x.dim() != 2:
+        raise ValueError("x: expected [M, K], got shape %s" % (tuple(x.shape),))
     M, K = x.shape
+    _need(W, "W")
+    if W.dim() != 2 or W.shape[1] != K:
+        raise ValueError("W: expected [N, %d], got shape %s" % (K, tuple(W.shape)))
     N = W.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _need(y, "y", shape=(M, N))
+    if residual is not None:
+        _need(residual, "residual", shape=(M, N))
     ldx = x.stride(0) if M > 1 else K
     if x.stride(1) != 1:
         raise ValueError("dec_linear: x needs unit column stride")
+    _on_one_gpu(x=x, W=W, y=y, residual=residual)
     if ldx != K:
         rc = lib().dec_linear_ex(_ptr(x), ldx, _ptr(W), _ptr(residual), _ptr(y), M, N, K,
                                  _stream(stream))
@@ -137,8 +179,14 @@ def dec_linear_noalloc(x, W, y, stream=None):
     """dec_linear that allocates nothing: its split-K scratch is a fixed array
     inside the library (for callers that cannot allocate device memory).
     ``y`` must be given. Calls that may overlap on the GPU race."""
+    _need(x, "x")
     M, K = x.shape
+    _need(W, "W")
+    if W.dim() != 2 or W.shape[1] != K:
+        raise ValueError("W: expected [N, %d], got shape %s" % (K, tuple(W.shape)))
     N = W.shape[0]
+    _need(y, "y", shape=(M, N))
+    _on_one_gpu(x=x, W=W, y=y)
     _check(lib().dec_linear_noalloc(_ptr(x), _ptr(W), _ptr(y), M, N, K, _stream(stream)),
            "dec_linear_noalloc")
     return y
@@ -148,10 +196,16 @@ def dec_linear_splitk(x, W, S, y=None, stream=None):
     """dec_linear with the split factor forced to S (test/tuning hook)."""
     import torch
 
+    _need(x, "x")
     M, K = x.shape
+    _need(W, "W")
+    if W.dim() != 2 or W.shape[1] != K:
+        raise ValueError("W: expected [N, %d], got shape %s" % (K, tuple(W.shape)))
     N = W.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _need(y, "y", shape=(M, N))
+    _on_one_gpu(x=x, W=W, y=y)
     _check(lib().dec_linear_splitk(_ptr(x), _ptr(W), _ptr(y), M, N, K, int(S), _stream(stream)),
            "dec_linear_splitk")
     return y
@@ -164,11 +218,35 @@ def moe_decode(x, Wr, W13, W2, Ws13, Ws2, topk, out=None, topk_idx=None, topk_w=
     residual when given)."""
     import torch
 
+    _need(x, "x")
+    if x.dim() != 2:
+        raise ValueError("x: expected [M, H], got shape %s" % (tuple(x.shape),))
     M, H = x.shape
+    _need(Wr, "Wr")
+    if Wr.dim() != 2 or Wr.shape[1] != H:
+        raise ValueError("Wr: expected [E, %d], got shape %s" % (H, tuple(Wr.shape)))
     E = Wr.shape[0]
+    _need(W13, "W13")
+    if W13.dim() != 3 or W13.shape[0] != E or W13.shape[2] != H or W13.shape[1] % 2:
+        raise ValueError("W13: expected [%d, 2I, %d], got shape %s" % (E, H, tuple(W13.shape)))
     I = W13.shape[1] // 2
+    _need(W2, "W2", shape=(E, H, I))
+    if (Ws13 is None) != (Ws2 is None):
+        raise ValueError("Ws13 and Ws2: give both or neither")
+    if Ws13 is not None:
+        _need(Ws13, "Ws13", shape=(2 * I, H))
+        _need(Ws2, "Ws2", shape=(H, I))
     if out is None:
         out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    _need(out, "out", shape=(M, H))
+    if residual is not None:
+        _need(residual, "residual", shape=(M, H))
+    if topk_idx is not None:
+        _need(topk_idx, "topk_idx", shape=(M, int(topk)), dtype="i32")
+    if topk_w is not None:
+        _need(topk_w, "topk_w", shape=(M, int(topk)), dtype="f32")
+    _on_one_gpu(x=x, Wr=Wr, W13=W13, W2=W2, Ws13=Ws13, Ws2=Ws2, out=out, residual=residual,
+                topk_idx=topk_idx, topk_w=topk_w)
     args = [_ptr(x), _ptr(Wr), _ptr(W13), _ptr(W2), _ptr(Ws13), _ptr(Ws2)]
     tail = [M, H, E, int(topk), I, _ptr(topk_idx), _ptr(topk_w), _stream(stream)]
     if residual is None:
@@ -182,6 +260,8 @@ def moe_decode(x, Wr, W13, W2, Ws13, Ws2, topk, out=None, topk_idx=None, topk_w=
 def l2_prefetch(t_or_ptr, nbytes=None, stream=None):
     """Warm L2 with a tensor's bytes (or a raw device pointer and byte count)."""
     if nbytes is None:
+        if t_or_ptr.device.type != "cuda":
+            raise ValueError("l2_prefetch: expected a CUDA tensor")
         ptr, nbytes = t_or_ptr.data_ptr(), t_or_ptr.numel() * t_or_ptr.element_size()
     else:
         ptr = int(t_or_ptr)
@@ -192,8 +272,12 @@ def dec_add(a, b, out=None, stream=None):
     """out = bf16(a + b) elementwise."""
     import torch
 
+    _need(a, "a")
+    _need(b, "b", shape=a.shape)
     if out is None:
         out = torch.empty_like(a)
+    _need(out, "out", shape=a.shape)
+    _on_one_gpu(a=a, b=b, out=out)
     _check(lib().dec_add(_ptr(a), _ptr(b), _ptr(out), a.numel(), _stream(stream)), "dec_add")
     return out
 
@@ -208,6 +292,11 @@ def last_choice():
 def last_cluster() -> bool:
     """Whether this thread's last projection call used the cluster split."""
     return bool((lib().dec_last_choice() >> 16) & 1)
+
+
+def last_wide() -> bool:
+    """Whether this thread's last projection call used 256-row output tiles."""
+    return bool((lib().dec_last_choice() >> 17) & 1)
 
 
 def last_grid() -> int:

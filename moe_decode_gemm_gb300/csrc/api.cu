@@ -278,7 +278,7 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
   cx.ldx = ldx;
   long long seff = (KB * grid + T - 1) / T;
   if (seff < 1) seff = 1;
-  t_last_choice = regime | ((int)seff << 8);
+  t_last_choice = regime | ((int)seff << 8) | ((wide ? 1 : 0) << 17);
   t_last_grid = (int)grid;
   ProbeScope probe(2, st);
   if (regime == DEC_REGIME_TC)
@@ -520,14 +520,28 @@ const char* dec_strerror(int code) {
   }
 }
 
+// The device state of the current device if it has been set up, else null
+// (sets up nothing).
+static DevState* peek_dev() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if ((int)g_dev.size() <= d || !g_dev[d].init) return nullptr;
+  return &g_dev[d];
+}
+
 int dec_sync_check(void* stream) {
-  DevState* s = nullptr;
-  int rc = get_dev(&s);
-  if (rc) return rc;
+  // Allocates nothing: a device whose state was never set up (a process that
+  // only calls dec_linear_noalloc) is not set up here.
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return DEC_ECUDA;
+  const int nst = noalloc_take_status();
+  if (nst < 0) return DEC_ECUDA;
+  DevState* s = peek_dev();
+  if (!s) return nst ? DEC_ETIMEOUT : DEC_OK;
   if (cudaStreamSynchronize(s->side) != cudaSuccess) return DEC_ECUDA;
   int st = 0;
   if (cudaMemcpy(&st, s->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DEC_ECUDA;
+  if (st == 0 && nst != 0) return DEC_ETIMEOUT;
   if (st != 0) {
     // Reset the status word and every arrival counter a timed-out kernel may
     // have left behind.

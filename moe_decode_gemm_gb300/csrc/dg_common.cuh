@@ -74,6 +74,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
   }
 }
 
+// Bound of a drain: the wait, after a kernel has given up, for its own copies
+// and MMAs still in flight, so that no copy lands in (and no MMA writes to) a
+// CTA's shared or tensor memory after the CTA has released it. Issued copies
+// always complete, so this bound is never reached in practice; it is at least
+// one second whatever the caller's wait bound, which may be far shorter.
+__device__ __forceinline__ long long drain_ns(long long timeout_ns) {
+  return timeout_ns > 1000000000LL ? timeout_ns : 1000000000LL;
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;

@@ -48,17 +48,8 @@ static cudaError_t run_dense_path(const Ctx& cx, const void* x, const void* W, c
   static_assert(!CLUSTER || kTileRows * XR * 4 <= S * (kWBytes + kKSub * XR * 128),
                 "the partial tile fits in the stage ring");
   auto kern = wstream_kernel<XR, S, EPI, false, false, WIDE, ROLE_PROJECTION, MINB, CLUSTER, PATH>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = allow_smem(kern, SMEM);
-    if (e != cudaSuccess) return e;
-    if (MINB > 1) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                               (int)cudaSharedmemCarveoutMaxShared);
-      if (e != cudaSuccess) return e;
-    }
-    attr_done = true;
-  }
+  static DevOnce once;
+  if (cudaError_t e = setup_smem(once, kern, SMEM, MINB > 1); e != cudaSuccess) return e;
   constexpr int kTile = WIDE ? 2 * kTileRows : kTileRows;
   CUtensorMap wmap, xmap;
   if (!make_tmap(&wmap, W, (uint64_t)N, (uint64_t)K, kTileRows, true)) return cudaErrorInvalidValue;

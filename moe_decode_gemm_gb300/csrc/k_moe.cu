@@ -26,13 +26,6 @@ constexpr int expert_pair_smem() {
   return wstream_smem(XR, kExpertPairStages, 0, true);
 }
 
-template <typename K>
-static cudaError_t smem_once(K kern, int bytes, bool& done) {
-  if (done) return cudaSuccess;
-  cudaError_t e = allow_smem(kern, bytes);
-  if (e == cudaSuccess) done = true;
-  return e;
-}
 
 static StreamArgs base_args(const Ctx& cx, float* ws, int* ctr) {
   StreamArgs a = {};
@@ -61,9 +54,8 @@ static cudaError_t run_router(const Ctx& cx, const void* x, const void* Wr, int 
   constexpr int SMEM = wstream_smem(XR, STAGES, 0);
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
   auto kern = wstream_kernel<XR, STAGES, EPI_F32, false, false, false, ROLE_ROUTER, 1, true>;
-  static bool done = false;
-  cudaError_t e = smem_once(kern, SMEM, done);
-  if (e != cudaSuccess) return e;
+  static DevOnce once;
+  if (cudaError_t e = setup_smem(once, kern, SMEM); e != cudaSuccess) return e;
   CUtensorMap wmap, xmap;
   if (!make_tmap(&wmap, Wr, (uint64_t)E, (uint64_t)H, kTileRows, true)) return cudaErrorInvalidValue;
   if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)H, XR, false)) return cudaErrorInvalidValue;
@@ -230,9 +222,8 @@ static cudaError_t run_experts_w13(const Ctx& cx, const void* W13, int M, int H,
   constexpr int SMEM = expert_pair_smem<XR>();
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
   auto kern = wstream_kernel<XR, kExpertPairStages, EPI_SWIGLU, true, true, false, ROLE_EXPERT>;
-  static bool done = false;
-  cudaError_t e = smem_once(kern, SMEM, done);
-  if (e != cudaSuccess) return e;
+  static DevOnce once;
+  if (cudaError_t e = setup_smem(once, kern, SMEM); e != cudaSuccess) return e;
   CUtensorMap wmap, xmap;
   if (!make_tmap(&wmap, W13, (uint64_t)E * 2 * I, (uint64_t)H, kTileRows, true))
     return cudaErrorInvalidValue;
@@ -265,9 +256,8 @@ static cudaError_t run_experts_w2(const Ctx& cx, const void* W2, int M, int H, i
   // 256-row output tiles: two 128-row halves, 64 KB weight stages
   constexpr int SMEM = expert_pair_smem<XR>();
   auto kern = wstream_kernel<XR, kExpertPairStages, EPI_F32, false, true, true, ROLE_EXPERT>;
-  static bool done = false;
-  cudaError_t e = smem_once(kern, SMEM, done);
-  if (e != cudaSuccess) return e;
+  static DevOnce once;
+  if (cudaError_t e = setup_smem(once, kern, SMEM); e != cudaSuccess) return e;
   CUtensorMap wmap, xmap;
   if (!make_tmap(&wmap, W2, (uint64_t)E * H, (uint64_t)I, kTileRows, true)) return cudaErrorInvalidValue;
   if (!make_tmap(&xmap, b.h, (uint64_t)M * k, (uint64_t)I, XR, false))
@@ -316,9 +306,8 @@ static cudaError_t run_shared_w13(const Ctx& cx, const void* x, const void* Ws13
   constexpr int SMEM = wstream_smem(XR, STAGES, 0, true);
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
   auto kern = wstream_kernel<XR, STAGES, EPI_SWIGLU, true, false, false, ROLE_SHARED>;
-  static bool done = false;
-  cudaError_t e = smem_once(kern, SMEM, done);
-  if (e != cudaSuccess) return e;
+  static DevOnce once;
+  if (cudaError_t e = setup_smem(once, kern, SMEM); e != cudaSuccess) return e;
   CUtensorMap wmap, xmap;
   if (!make_tmap(&wmap, Ws13, (uint64_t)2 * I, (uint64_t)H, kTileRows, true))
     return cudaErrorInvalidValue;
@@ -344,9 +333,8 @@ static cudaError_t run_shared_w2(const Ctx& cx, const void* Ws2, int M, int H, i
   constexpr int SMEM = wstream_smem(XR, STAGES, 0);
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
   auto kern = wstream_kernel<XR, STAGES, EPI_F32, false, false, false, ROLE_SHARED>;
-  static bool done = false;
-  cudaError_t e = smem_once(kern, SMEM, done);
-  if (e != cudaSuccess) return e;
+  static DevOnce once;
+  if (cudaError_t e = setup_smem(once, kern, SMEM); e != cudaSuccess) return e;
   CUtensorMap wmap, xmap;
   if (!make_tmap(&wmap, Ws2, (uint64_t)H, (uint64_t)I, kTileRows, true)) return cudaErrorInvalidValue;
   if (!make_tmap(&xmap, b.hs, (uint64_t)M, (uint64_t)I, XR, false)) return cudaErrorInvalidValue;

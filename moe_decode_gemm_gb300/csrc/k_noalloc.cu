@@ -68,9 +68,51 @@ int noalloc_setup(NoAllocDevice** out) {
   return DEC_OK;
 }
 
+// As noalloc_setup, but a device that is not set up yet is not set up inside a
+// stream capture: the set-up's runtime calls have to run outside it.
+int noalloc_setup_checked(void* stream, NoAllocDevice** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DEC_ENODEV;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return DEC_ENODEV;
+  bool ready = false;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    ready = g_noalloc_dev[dev].ready;
+  }
+  if (!ready) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(reinterpret_cast<cudaStream_t>(stream), &cs) != cudaSuccess ||
+        cs != cudaStreamCaptureStatusNone) {
+      cudaGetLastError();  // a query refused during capture leaves no sticky error
+      return DEC_EINVAL;
+    }
+  }
+  return noalloc_setup(out);
+}
+
 bool is_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+// Read and clear the status word of the array on the current device: the
+// bits a bounded wait of an earlier call set when it gave up. Synchronous
+// (callers synchronise the streams first); allocates nothing; 0 when the
+// entry point has not run on this device.
+int noalloc_take_status() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return 0;
+  unsigned char* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_dev[dev].ready) return 0;
+    base = g_noalloc_dev[dev].base;
+  }
+  int st = 0;
+  if (cudaMemcpy(&st, base, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+  if (st != 0 && cudaMemset(base, 0, sizeof(int)) != cudaSuccess) return -1;
+  return st;
+}
+
 }  // namespace dg
 
 extern "C" int dec_linear_noalloc(const void* x, const void* W, void* y, int M, int N, int K,
@@ -81,7 +123,7 @@ extern "C" int dec_linear_noalloc(const void* x, const void* W, void* y, int M, 
   if (!is_aligned16(x) || !is_aligned16(W) || !is_aligned16(y)) return DEC_EINVAL;
   if (M > kNoAllocMaxM) return DEC_EUNSUPPORTED;
   NoAllocDevice* d = nullptr;
-  int rc = noalloc_setup(&d);
+  int rc = noalloc_setup_checked(stream, &d);
   if (rc) return rc;
   const int xr = M <= 2 ? 8 : 16;  // token rows per pipeline stage
   const long long tiles = (N + 127) / 128;
@@ -95,9 +137,11 @@ extern "C" int dec_linear_noalloc(const void* x, const void* W, void* y, int M, 
   int* status = reinterpret_cast<int*>(d->base);
   int* ctr = reinterpret_cast<int*>(d->base + kNoAllocStatusBytes);
   float* ws = reinterpret_cast<float*>(d->base + kNoAllocStatusBytes + kNoAllocCtrBytes);
-  // The array keeps whatever the last call left: the status word and the
-  // counters this launch uses must start at zero.
-  if (cudaMemsetAsync(d->base, 0, kNoAllocStatusBytes + ctr_bytes, st) != cudaSuccess)
+  // The array keeps whatever the last call left: the counters this launch
+  // uses must start at zero (a launch that gave up may have left some set).
+  // The status word is not cleared here: it keeps a give-up until
+  // dec_sync_check reads it.
+  if (cudaMemsetAsync(d->base + kNoAllocStatusBytes, 0, ctr_bytes, st) != cudaSuccess)
     return DEC_ECUDA;
   Ctx cx;
   cx.sms = d->sms;

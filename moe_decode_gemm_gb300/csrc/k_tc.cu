@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int issued = i;
       for (int s = 0; s < kTcStages && s < issued; ++s) {
         const int uses = (issued - s + kTcStages - 1) / kTcStages;
-        mbar_wait(&full[s], (uses - 1) & 1, a.timeout_ns, nullptr);
+        mbar_wait(&full[s], (uses - 1) & 1, drain_ns(a.timeout_ns), nullptr);
       }
     } else {
       griddep_wait();
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (i == nunits - 1 || tile_end) umma_commit(&tfull[jt & 1]);
       }
       umma_commit(mma_done);
-      mbar_wait(mma_done, 0, a.timeout_ns, nullptr);
+      mbar_wait(mma_done, 0, drain_ns(a.timeout_ns), nullptr);
     }
     __syncwarp();
   } else {
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       const int issued = i;
       for (int s = 0; s < kTcClStages && s < issued; ++s) {
         const int uses = (issued - s + kTcClStages - 1) / kTcClStages;
-        mbar_wait(&full[s], (uses - 1) & 1, a.timeout_ns, nullptr);
+        mbar_wait(&full[s], (uses - 1) & 1, drain_ns(a.timeout_ns), nullptr);
       }
     } else {
       griddep_wait();
@@ -419,6 +419,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       }
       // every MMA above is complete (and so every stage read) when this fires
       umma_commit(tfull);
+      // The epilogue waits for it too, but gives up with the caller's bound:
+      // the tensor memory is freed only once every MMA has completed.
+      mbar_wait(tfull, 0, drain_ns(a.timeout_ns), nullptr);
     }
   } else {
     // ---------------------------------------------------------------- epilogue
@@ -480,15 +483,8 @@ static cudaError_t run_tc_cluster(const Ctx& cx, const void* x, const void* W, c
   static_assert(2 * (SMEM + 1024) <= kSmemPerSm, "two CTAs per SM");
   static_assert(kTileRows * kTcXRows * 4 <= kTcClStages * kTcStageBytes, "partial tile fits");
   auto kern = tc_cluster_kernel<EPI>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = allow_smem(kern, SMEM);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static DevOnce once;
+  if (cudaError_t e = setup_smem(once, kern, SMEM, true); e != cudaSuccess) return e;
   const int NP = (M + 15) / 16 * 16;
   CUtensorMap wmap, xmap;
   if (!make_tmap(&wmap, W, (uint64_t)N, (uint64_t)K, kTileRows, true)) return cudaErrorInvalidValue;
@@ -523,12 +519,8 @@ static cudaError_t run_tc(const Ctx& cx, const void* x, const void* W, const voi
   constexpr int SMEM = tc_smem();
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
   auto kern = tc_linear_kernel<EPI>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = allow_smem(kern, SMEM);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static DevOnce once;
+  if (cudaError_t e = setup_smem(once, kern, SMEM); e != cudaSuccess) return e;
   const int NP = (M + 15) / 16 * 16;
   CUtensorMap wmap, xmap;
   if (!make_tmap(&wmap, W, (uint64_t)N, (uint64_t)K, kTileRows, true)) return cudaErrorInvalidValue;

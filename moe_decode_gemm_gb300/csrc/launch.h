@@ -92,6 +92,10 @@ cudaError_t launch_add(const Ctx& cx, const void* a, const void* b, void* out, s
 cudaError_t launch_prefetch(const Ctx& cx, const void* ptr, size_t bytes);
 cudaError_t launch_selftest_timeout(const Ctx& cx, long long ns);
 
+// Status bits of the allocation-free projection's fixed array on the current
+// device, read and cleared (0 if none or never used; -1 if the read failed).
+int noalloc_take_status();
+
 // Shared memory each dense/MoE kernel needs (bytes), for cudaFuncSetAttribute.
 constexpr int kMaxDynSmem = 232448;
 constexpr int kSmemPerSm = 233472;  // per SM; each resident CTA also reserves 1 KB

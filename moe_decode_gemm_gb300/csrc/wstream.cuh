@@ -477,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
       const int issued = i;
       for (int s = 0; s < STAGES && s < issued; ++s) {
         const int uses = (issued - s + STAGES - 1) / STAGES;
-        mbar_wait(&full[s], (uses - 1) & 1, a.timeout_ns, nullptr);
+        mbar_wait(&full[s], (uses - 1) & 1, drain_ns(a.timeout_ns), nullptr);
       }
     }
     if (early && lane != 0) griddep_wait();

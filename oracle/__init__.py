@@ -230,8 +230,20 @@ def expert_mlp(x_bits, W13_bits, W2_bits, I: int, round_h: bool = False):
     return linear_f64act(h, W2_bits)
 
 
+def gates_for(logits, idx) -> np.ndarray:
+    """Renormalised softmax gates of a given choice of experts, in fp64:
+    g[m,j] = exp(l[m,idx[m,j]] - l_max) / sum_j' exp(l[m,idx[m,j']] - l_max),
+    l_max the largest chosen score of token m (the same closed form the top-k
+    routine returns for its own choice)."""
+    l = _f64(logits)
+    idx = np.asarray(idx)
+    chosen = np.take_along_axis(l, idx.astype(np.int64), axis=1)
+    w = np.exp(chosen - chosen.max(axis=1, keepdims=True))
+    return w / w.sum(axis=1, keepdims=True)
+
+
 def moe(x_bits, Wr_bits, fetch_expert, topk_k: int, I: int, shared=None,
-        round_h: bool = False, tokens=None):
+        round_h: bool = False, tokens=None, route=None):
     """MoE decode block, "vLLM 如何用智能体辅助优化 Kimi K3 解码性能" Part 1 §3.
 
     logits = x·Wrᵀ (fp64); (idx, g) = top-k with renormalised softmax gates;
@@ -241,6 +253,11 @@ def moe(x_bits, Wr_bits, fetch_expert, topk_k: int, I: int, shared=None,
     fetch_expert(e) -> (W13_e [2I,H] bits, W2_e [H,I] bits); only the experts
     that the oracle itself selects are fetched. shared is (Ws13, Ws2) or None.
     tokens: optional list of token rows to compute (the others stay NaN).
+    route: optional [M,k] choice of experts to use instead of the oracle's own
+    top-k (gates from ``gates_for`` on the oracle's scores). Where two scores
+    are closer than fp32 can separate, an implementation that scores in fp32
+    may legitimately choose the other expert; its output is then checked for
+    the choice it made.
 
     Returns dict(out, absref, idx, gates, logits), where
     absref[m,n] = sum_j g_j sum_i |h_ji W2[e_j,n,i]| + sum_i |hs_i Ws2[n,i]|.
@@ -248,7 +265,13 @@ def moe(x_bits, Wr_bits, fetch_expert, topk_k: int, I: int, shared=None,
     x = _u16(x_bits)
     M, H = x.shape
     logits, _ = linear(x, Wr_bits)
-    idx, gates = topk(logits, topk_k)
+    if route is None:
+        idx, gates = topk(logits, topk_k)
+    else:
+        idx = np.ascontiguousarray(route, dtype=np.int32)
+        if idx.shape != (M, topk_k) or idx.min() < 0 or idx.max() >= logits.shape[1]:
+            raise ValueError("route must be [M, k] expert indices")
+        gates = gates_for(logits, idx)
     rows = list(range(M)) if tokens is None else sorted(set(int(t) for t in tokens))
     o = {}
     oabs = {}

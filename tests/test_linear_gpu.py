@@ -313,3 +313,21 @@ def test_output_guard_bands_untouched():
     dg.dec_linear(x, W, y)
     assert dg.sync_check() == dg.DEC_OK
     assert torch.all(buf[:pad] == 12345) and torch.all(buf[pad + M * N:] == 12345)
+
+
+@pytest.mark.parametrize("M", [4, 16])
+@pytest.mark.parametrize("residual", [True, False])
+def test_wide_tiles_full_size_7168(M, residual):
+    # N = K = 7168 at 4 and 16 tokens takes the 256-row-tile instance (the
+    # layer stack's o projection, with the residual fused): every element
+    # against the oracle
+    N = K = 7168
+    x = wl.normal_bf16((M, K), 1.0, "wide", M, "x")
+    W = wl.normal_bf16((N, K), 0.02, "wide", M, "W")
+    r = wl.normal_bf16((M, N), 1.0, "wide", M, "r") if residual else None
+    y, (regime, _) = _gpu_linear(x, W, res_bits=r)
+    assert regime == "mma" and dg.last_wide() and not dg.last_cluster()
+    f, A = oracle.linear(x, W)
+    if residual:
+        f, A = oracle.residual(r, f, A)
+    assert_within_tol(to_f64(y), f, A, "wide tiles M=%d residual=%s" % (M, residual))

@@ -405,3 +405,32 @@ def test_skewed_router_scales():
     W = _dec(wl.skewed_router_bf16(8, 4096, 1.0, "gen", "Wr"))
     sd = W.std(axis=1) / wl.ROUTER_STD
     assert np.allclose(sd, wl.router_scales(8, 1.0), rtol=0.05)
+
+
+def test_gates_for_a_given_choice():
+    # the gates of the oracle's own choice equal the top-k routine's, and a
+    # given route reproduces the unrouted block exactly when it is that choice
+    l = oracle.bf16_to_f64(wl.normal_bf16((5, 24), 1.0, "pin", "gates-for"))
+    idx, g = oracle.topk(l, 4)
+    np.testing.assert_allclose(oracle.gates_for(l, idx), g, rtol=1e-14)
+    # a permuted choice permutes the gates; sum is 1; ratio is exp(l_a - l_b)
+    gp = oracle.gates_for(l, idx[:, ::-1])
+    np.testing.assert_allclose(gp, g[:, ::-1], rtol=1e-14)
+    H, I, E, M, k = 16, 8, 6, 3, 2
+    x = wl.normal_bf16((M, H), 1.0, "pin", "route", "x")
+    Wr = wl.normal_bf16((E, H), 0.3, "pin", "route", "Wr")
+    W13 = np.stack([wl.normal_bf16((2 * I, H), 0.2, "pin", "route", "W13", e) for e in range(E)])
+    W2 = np.stack([wl.normal_bf16((H, I), 0.2, "pin", "route", "W2", e) for e in range(E)])
+    a = oracle.moe(x, Wr, _bank_fetch(W13, W2), k, I)
+    b = oracle.moe(x, Wr, _bank_fetch(W13, W2), k, I, route=a["idx"])
+    assert np.array_equal(a["idx"], b["idx"])
+    np.testing.assert_allclose(b["out"], a["out"], rtol=1e-13, atol=1e-15)
+    # another choice: each token's output is the gate-weighted sum of exactly
+    # the experts named, with gates from the given scores
+    alt = np.array([[0, 1], [2, 3], [5, 4]], dtype=np.int32)
+    c = oracle.moe(x, Wr, _bank_fetch(W13, W2), k, I, route=alt)
+    gl = oracle.gates_for(c["logits"], alt)
+    for m in range(M):
+        want = sum(gl[m, j] * oracle.expert_mlp(x[m:m + 1], W13[alt[m, j]], W2[alt[m, j]], I)[0][0]
+                   for j in range(k))
+        np.testing.assert_allclose(c["out"][m], want, rtol=1e-13, atol=1e-15)

@@ -134,3 +134,37 @@ def torch_to_bits(t) -> np.ndarray:
     import torch
 
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+# ----------------------------------------------------------------- layer stack
+class LayerWeights:
+    """Seeded weights of one synthetic decode layer, on the device.
+
+    Wqkv [H + KV, H] holds Wq (rows 0..H-1) and Wkv (rows H..H+KV-1) as one
+    matrix, so q and kv are one fused projection; Wq and Wkv are views of it.
+    Wo [H, H]; router Wr [E, H] ~N(0, 1/sqrt(H)) (row e scaled by c_e for a
+    skewed-routing workload, ``router_scales``); routed experts W13 [E, 2I, H]
+    and W2 [E, H, I]; shared expert Ws13 [2I, H] and Ws2 [H, I]; all other
+    weights ~N(0, 0.02).
+    """
+
+    def __init__(self, l, device="cuda", skew=0.0, H=HIDDEN, KV=KV_WIDTH, E=EXPERTS, I=INTER):
+        import torch
+
+        g = lambda shape, *key: normal_bf16_cuda(shape, WEIGHT_STD, "stack", l, *key,
+                                                 device=device)
+        self.Wqkv = torch.empty((H + KV, H), dtype=torch.bfloat16, device=device)
+        normal_bf16_cuda((H, H), WEIGHT_STD, "stack", l, "Wq", device=device, out=self.Wqkv[:H])
+        normal_bf16_cuda((KV, H), WEIGHT_STD, "stack", l, "Wkv", device=device,
+                         out=self.Wqkv[H:])
+        self.Wq, self.Wkv = self.Wqkv[:H], self.Wqkv[H:]
+        self.Wo = g((H, H), "Wo")
+        self.Wr = normal_bf16_cuda((E, H), ROUTER_STD, "stack", l, "Wr", device=device)
+        if skew > 0:
+            c = torch.tensor(router_scales(E, skew), dtype=torch.float32, device=device)
+            self.Wr.copy_((self.Wr.float() * c[:, None]).to(torch.bfloat16))
+        self.W13 = g((E, 2 * I, H), "W13")
+        self.W2 = g((E, H, I), "W2")
+        self.Ws13 = g((2 * I, H), "Ws13")
+        self.Ws2 = g((H, I), "Ws2")
+        self.H, self.KV, self.E, self.I = H, KV, E, I
