@@ -242,6 +242,44 @@ def gates_for(logits, idx) -> np.ndarray:
     return w / w.sum(axis=1, keepdims=True)
 
 
+def _routed_sum(rows_bits, rows, idx, gates, fetch_expert, topk_k: int, I: int, round_h: bool):
+    """acc[r] = sum_{j=0..k-1} g[m,j] * expert_{idx[m,j]}(rows_bits[m]) for m = rows[r],
+    summed in the order j = 0..k-1, and accabs[r] = sum_j g[m,j] * absref of
+    that expert's output. Only the experts the given rows chose are fetched."""
+    width = None
+    o, oabs = {}, {}
+    needed = sorted(set(int(e) for m in rows for e in idx[m]))
+    for e in needed:
+        W13_e, W2_e = fetch_expert(e)
+        pairs = [(m, j) for m in rows for j in range(topk_k) if idx[m, j] == e]
+        xs = rows_bits[[m for m, _ in pairs]]
+        oe, ae = expert_mlp(xs, W13_e, W2_e, I, round_h)
+        width = oe.shape[1]
+        for r, (m, j) in enumerate(pairs):
+            o[(m, j)] = oe[r]
+            oabs[(m, j)] = ae[r]
+    acc = np.zeros((len(rows), width or 0))
+    accabs = np.zeros((len(rows), width or 0))
+    for r, m in enumerate(rows):
+        a = np.zeros(width)
+        aa = np.zeros(width)
+        for j in range(topk_k):
+            a = a + gates[m, j] * o[(m, j)]
+            aa = aa + gates[m, j] * oabs[(m, j)]
+        acc[r] = a
+        accabs[r] = aa
+    return acc, accabs
+
+
+def _route(logits, topk_k, route):
+    if route is None:
+        return topk(logits, topk_k)
+    idx = np.ascontiguousarray(route, dtype=np.int32)
+    if idx.shape != (logits.shape[0], topk_k) or idx.min() < 0 or idx.max() >= logits.shape[1]:
+        raise ValueError("route must be [M, k] expert indices")
+    return idx, gates_for(logits, idx)
+
+
 def moe(x_bits, Wr_bits, fetch_expert, topk_k: int, I: int, shared=None,
         round_h: bool = False, tokens=None, route=None):
     """MoE decode block, "vLLM 如何用智能体辅助优化 Kimi K3 解码性能" Part 1 §3.
@@ -265,43 +303,67 @@ def moe(x_bits, Wr_bits, fetch_expert, topk_k: int, I: int, shared=None,
     x = _u16(x_bits)
     M, H = x.shape
     logits, _ = linear(x, Wr_bits)
-    if route is None:
-        idx, gates = topk(logits, topk_k)
-    else:
-        idx = np.ascontiguousarray(route, dtype=np.int32)
-        if idx.shape != (M, topk_k) or idx.min() < 0 or idx.max() >= logits.shape[1]:
-            raise ValueError("route must be [M, k] expert indices")
-        gates = gates_for(logits, idx)
+    idx, gates = _route(logits, topk_k, route)
     rows = list(range(M)) if tokens is None else sorted(set(int(t) for t in tokens))
-    o = {}
-    oabs = {}
-    needed = sorted(set(int(e) for m in rows for e in idx[m]))
-    for e in needed:
-        W13_e, W2_e = fetch_expert(e)
-        pairs = [(m, j) for m in rows for j in range(topk_k) if idx[m, j] == e]
-        xs = x[[m for m, _ in pairs]]
-        oe, ae = expert_mlp(xs, W13_e, W2_e, I, round_h)
-        for r, (m, j) in enumerate(pairs):
-            o[(m, j)] = oe[r]
-            oabs[(m, j)] = ae[r]
+    acc, accabs = _routed_sum(x, rows, idx, gates, fetch_expert, topk_k, I, round_h)
     out = np.full((M, H), np.nan)
     absref = np.full((M, H), np.nan)
-    s = sabs = None
     if shared is not None:
         Ws13, Ws2 = shared
         s, sabs = expert_mlp(x[rows], Ws13, Ws2, I, round_h)
-    for r, m in enumerate(rows):
-        acc = np.zeros(H)
-        accabs = np.zeros(H)
-        for j in range(topk_k):
-            acc = acc + gates[m, j] * o[(m, j)]
-            accabs = accabs + gates[m, j] * oabs[(m, j)]
-        if s is not None:
-            acc = acc + s[r]
-            accabs = accabs + sabs[r]
-        out[m] = acc
-        absref[m] = accabs
+        acc = acc + s
+        accabs = accabs + sabs
+    out[rows] = acc
+    absref[rows] = accabs
     return dict(out=out, absref=absref, idx=idx, gates=gates, logits=logits)
+
+
+def moe_latent(x_bits, Wrl_bits, E: int, fetch_expert, topk_k: int, I: int, Wup_bits,
+               shared=None, round_h: bool = False, tokens=None, route=None):
+    """MoE decode block whose routed experts work on a latent width L.
+
+    "vLLM 如何用智能体辅助优化 Kimi K3 解码性能", Part 1 §3: the router scores and
+    the latent input projection are computed as one matrix product. The
+    reading taken here (the pages name the two projections and nothing else):
+      sc     = x·Wrlᵀ in fp64, Wrl [E + L, H] = the router's E rows stacked on
+               the latent input projection's L rows;
+      logits = sc[:, :E] (the router scores, not rounded);
+      lat    = bf16(sc[:, E:]) (the latent input, rounded: the experts' operand);
+      (idx, g) = top-k of logits with renormalised softmax gates;
+      z      = bf16(sum_{j=0..k-1} g_j * expert_{idx_j}(lat)) -- experts map
+               L -> I -> L (W13_e [2I, L], W2_e [L, I]); z rounded once, as the
+               next product's operand;
+      out    = z·Wupᵀ + shared(x), Wup [H, L] the up-projection back to the
+               hidden width, the shared expert on x as in ``moe``.
+    Returns dict(out, absref, idx, gates, logits, lat, z), with
+    absref[m,n] = sum_l |z_l Wup[n,l]| + sum_i |hs_i Ws2[n,i]| (the block's last
+    contractions) and z the bf16 bits of the rows computed (others 0).
+    """
+    x = _u16(x_bits)
+    Wrl = _u16(Wrl_bits)
+    M, H = x.shape
+    L = Wrl.shape[0] - E
+    if L < 1:
+        raise ValueError("Wrl must stack E router rows on L >= 1 latent rows")
+    sc, _ = linear(x, Wrl)
+    logits = np.ascontiguousarray(sc[:, :E])
+    lat = f64_to_bf16_bits(sc[:, E:])
+    idx, gates = _route(logits, topk_k, route)
+    rows = list(range(M)) if tokens is None else sorted(set(int(t) for t in tokens))
+    acc, _ = _routed_sum(lat, rows, idx, gates, fetch_expert, topk_k, I, round_h)
+    z = np.zeros((M, L), dtype=np.uint16)
+    z[rows] = f64_to_bf16_bits(acc)
+    u, uabs = linear(z[rows], Wup_bits)
+    out = np.full((M, H), np.nan)
+    absref = np.full((M, H), np.nan)
+    if shared is not None:
+        Ws13, Ws2 = shared
+        s, sabs = expert_mlp(x[rows], Ws13, Ws2, I, round_h)
+        u = u + s
+        uabs = uabs + sabs
+    out[rows] = u
+    absref[rows] = uabs
+    return dict(out=out, absref=absref, idx=idx, gates=gates, logits=logits, lat=lat, z=z)
 
 
 def residual(x_bits, f, f_absref):

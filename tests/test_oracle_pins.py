@@ -434,3 +434,86 @@ def test_gates_for_a_given_choice():
         want = sum(gl[m, j] * oracle.expert_mlp(x[m:m + 1], W13[alt[m, j]], W2[alt[m, j]], I)[0][0]
                    for j in range(k))
         np.testing.assert_allclose(c["out"][m], want, rtol=1e-13, atol=1e-15)
+
+
+# ------------------------------------------------------------------ latent block
+def _latent_case(H, L, E, I, M, key):
+    x = wl.normal_bf16((M, H), 1.0, "pin", key, "x")
+    Wr = wl.normal_bf16((E, H), 0.3, "pin", key, "Wr")
+    Ws = (wl.normal_bf16((2 * I, H), 0.2, "pin", key, "Ws13"),
+          wl.normal_bf16((H, I), 0.2, "pin", key, "Ws2"))
+    W13 = np.stack([wl.normal_bf16((2 * I, L), 0.2, "pin", key, "W13", e) for e in range(E)])
+    W2 = np.stack([wl.normal_bf16((L, I), 0.2, "pin", key, "W2", e) for e in range(E)])
+    return x, Wr, Ws, W13, W2
+
+
+def test_latent_with_identity_projections_is_the_plain_block_with_z_rounded():
+    # L = H, latent rows = I, Wup = I: lat = x exactly, so the routed part is
+    # the plain block's routed sum, rounded once to bf16 (z), plus the shared
+    # expert on x
+    H, I, E, M, k = 24, 8, 6, 4, 2
+    x, Wr, Ws, W13, W2 = _latent_case(H, H, E, I, M, "lat-id")
+    eye = _bits(np.eye(H))
+    r = oracle.moe_latent(x, np.concatenate([Wr, eye]), E, _bank_fetch(W13, W2), k, I, eye,
+                          shared=Ws)
+    plain = oracle.moe(x, Wr, _bank_fetch(W13, W2), k, I, shared=None)
+    s, sA = oracle.expert_mlp(x, Ws[0], Ws[1], I)
+    assert np.array_equal(r["idx"], plain["idx"])
+    assert np.array_equal(r["lat"], x)
+    assert np.array_equal(r["z"], oracle.f64_to_bf16_bits(plain["out"]))
+    np.testing.assert_allclose(r["out"], oracle.round_bf16(plain["out"]) + s, rtol=1e-14,
+                               atol=1e-15)
+    # the pin has teeth: an unrounded z differs
+    assert not np.allclose(r["out"], plain["out"] + s, rtol=1e-9, atol=0)
+
+
+def test_latent_input_is_projected_and_output_projected_back():
+    # latent rows 2I (lat = 2x exactly) and Wup = I/2: the block equals the
+    # plain routed block on 2x, routed on x's scores, rounded, halved, plus the
+    # shared expert. lat = x, or an ignored Wup, would give another result.
+    H, I, E, M, k = 24, 8, 6, 4, 2
+    x, Wr, Ws, W13, W2 = _latent_case(H, H, E, I, M, "lat-scale")
+    r = oracle.moe_latent(x, np.concatenate([Wr, _bits(2 * np.eye(H))]), E,
+                          _bank_fetch(W13, W2), k, I, _bits(0.5 * np.eye(H)), shared=Ws)
+    x2 = _bits(2 * _dec(x))
+    half_Wr = _bits(0.5 * _dec(Wr))                    # (2x)·(Wr/2)ᵀ = x·Wrᵀ exactly
+    on2x = oracle.moe(x2, half_Wr, _bank_fetch(W13, W2), k, I, shared=None, route=r["idx"])
+    s, _ = oracle.expert_mlp(x, Ws[0], Ws[1], I)
+    np.testing.assert_allclose(on2x["gates"], r["gates"], rtol=1e-14)
+    want = 0.5 * oracle.round_bf16(on2x["out"]) + s
+    np.testing.assert_allclose(r["out"], want, rtol=1e-14, atol=1e-15)
+    on1x = oracle.moe(x, Wr, _bank_fetch(W13, W2), k, I, shared=None, route=r["idx"])
+    assert not np.allclose(r["out"], 0.5 * oracle.round_bf16(on1x["out"]) + s, rtol=1e-6)
+
+
+def test_latent_special_cases():
+    H, L, I, E, M, k = 32, 12, 8, 5, 3, 2
+    x, Wr, Ws, W13, W2 = _latent_case(H, L, E, I, M, "lat-special")
+    Wd = wl.normal_bf16((L, H), 0.2, "pin", "lat-special", "Wd")
+    Wup = wl.normal_bf16((H, L), 0.2, "pin", "lat-special", "Wup")
+    f = _bank_fetch(W13, W2)
+    base = oracle.moe_latent(x, np.concatenate([Wr, Wd]), E, f, k, I, Wup, shared=Ws)
+    assert base["out"].shape == (M, H) and base["lat"].shape == (M, L)
+    s, sA = oracle.expert_mlp(x, Ws[0], Ws[1], I)
+    # routing comes from the router rows alone
+    other = oracle.moe_latent(x, np.concatenate([Wr, np.zeros_like(Wd)]), E, f, k, I, Wup,
+                              shared=Ws)
+    assert np.array_equal(other["idx"], base["idx"])
+    assert np.array_equal(other["idx"], oracle.topk(oracle.linear(x, Wr)[0], k)[0])
+    np.testing.assert_array_equal(other["gates"], base["gates"])
+    # the latent input is the rounded latent projection of x
+    assert np.array_equal(base["lat"], oracle.f64_to_bf16_bits(oracle.linear(x, Wd)[0]))
+    # Wup = 0: the shared expert alone
+    z0 = oracle.moe_latent(x, np.concatenate([Wr, Wd]), E, f, k, I, np.zeros_like(Wup),
+                           shared=Ws)
+    assert np.array_equal(z0["out"], s) and np.array_equal(z0["absref"], sA)
+    # no shared expert: the up-projection of z, and linear in Wup
+    a = oracle.moe_latent(x, np.concatenate([Wr, Wd]), E, f, k, I, Wup, shared=None)
+    b = oracle.moe_latent(x, np.concatenate([Wr, Wd]), E, f, k, I, _bits(2 * _dec(Wup)),
+                          shared=None)
+    assert np.array_equal(b["out"], 2 * a["out"])
+    np.testing.assert_allclose(base["out"], a["out"] + s, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(a["out"], _dec(a["z"]) @ _dec(Wup).T, rtol=1e-12, atol=1e-14)
+    # token independence
+    t = oracle.moe_latent(x, np.concatenate([Wr, Wd]), E, f, k, I, Wup, shared=Ws, tokens=[1])
+    assert np.array_equal(t["out"][1], base["out"][1]) and np.isnan(t["out"][0]).all()
