@@ -230,6 +230,22 @@ def expert_mlp(x_bits, W13_bits, W2_bits, I: int, round_h: bool = False):
     return linear_f64act(h, W2_bits)
 
 
+def expert_mlp_f64act(a, W13_bits, W2_bits, I: int, round_h: bool = False):
+    """One SwiGLU expert on fp64 activations a [c, L]: g = a·W1ᵀ, u = a·W3ᵀ,
+    h = silu(g) * u with silu(z) = z / (1 + e^-z), o = h·W2ᵀ; the same
+    definition as ``expert_mlp``, for an input that is not a bf16 tensor.
+    Returns (o, absref) with absref_n = sum_i |h_i W2_ni|."""
+    W13 = _u16(W13_bits)
+    if W13.shape[0] != 2 * I:
+        raise ValueError("W13 must be [2I, L]")
+    g, _ = linear_f64act(a, W13[:I])
+    u, _ = linear_f64act(a, W13[I:])
+    h = g / (1.0 + np.exp(-g)) * u
+    if round_h:
+        h = round_bf16(h)
+    return linear_f64act(h, W2_bits)
+
+
 def gates_for(logits, idx) -> np.ndarray:
     """Renormalised softmax gates of a given choice of experts, in fp64:
     g[m,j] = exp(l[m,idx[m,j]] - l_max) / sum_j' exp(l[m,idx[m,j']] - l_max),
@@ -242,18 +258,22 @@ def gates_for(logits, idx) -> np.ndarray:
     return w / w.sum(axis=1, keepdims=True)
 
 
-def _routed_sum(rows_bits, rows, idx, gates, fetch_expert, topk_k: int, I: int, round_h: bool):
-    """acc[r] = sum_{j=0..k-1} g[m,j] * expert_{idx[m,j]}(rows_bits[m]) for m = rows[r],
+def _routed_sum(rows_in, rows, idx, gates, fetch_expert, topk_k: int, I: int, round_h: bool):
+    """acc[r] = sum_{j=0..k-1} g[m,j] * expert_{idx[m,j]}(rows_in[m]) for m = rows[r],
     summed in the order j = 0..k-1, and accabs[r] = sum_j g[m,j] * absref of
-    that expert's output. Only the experts the given rows chose are fetched."""
+    that expert's output. rows_in: bf16 bits, or fp64 activations. Only the
+    experts the given rows chose are fetched."""
     width = None
     o, oabs = {}, {}
     needed = sorted(set(int(e) for m in rows for e in idx[m]))
     for e in needed:
         W13_e, W2_e = fetch_expert(e)
         pairs = [(m, j) for m in rows for j in range(topk_k) if idx[m, j] == e]
-        xs = rows_bits[[m for m, _ in pairs]]
-        oe, ae = expert_mlp(xs, W13_e, W2_e, I, round_h)
+        xs = rows_in[[m for m, _ in pairs]]
+        if xs.dtype == np.uint16:
+            oe, ae = expert_mlp(xs, W13_e, W2_e, I, round_h)
+        else:
+            oe, ae = expert_mlp_f64act(xs, W13_e, W2_e, I, round_h)
         width = oe.shape[1]
         for r, (m, j) in enumerate(pairs):
             o[(m, j)] = oe[r]
@@ -319,7 +339,7 @@ def moe(x_bits, Wr_bits, fetch_expert, topk_k: int, I: int, shared=None,
 
 
 def moe_latent(x_bits, Wrl_bits, E: int, fetch_expert, topk_k: int, I: int, Wup_bits,
-               shared=None, round_h: bool = False, tokens=None, route=None):
+               shared=None, round_inter: bool = False, tokens=None, route=None):
     """MoE decode block whose routed experts work on a latent width L.
 
     "vLLM 如何用智能体辅助优化 Kimi K3 解码性能", Part 1 §3: the router scores and
@@ -327,17 +347,20 @@ def moe_latent(x_bits, Wrl_bits, E: int, fetch_expert, topk_k: int, I: int, Wup_
     reading taken here (the pages name the two projections and nothing else):
       sc     = x·Wrlᵀ in fp64, Wrl [E + L, H] = the router's E rows stacked on
                the latent input projection's L rows;
-      logits = sc[:, :E] (the router scores, not rounded);
-      lat    = bf16(sc[:, E:]) (the latent input, rounded: the experts' operand);
+      logits = sc[:, :E] (the router scores);
+      lat    = sc[:, E:] (the latent input);
       (idx, g) = top-k of logits with renormalised softmax gates;
-      z      = bf16(sum_{j=0..k-1} g_j * expert_{idx_j}(lat)) -- experts map
-               L -> I -> L (W13_e [2I, L], W2_e [L, I]); z rounded once, as the
-               next product's operand;
+      z      = sum_{j=0..k-1} g_j * expert_{idx_j}(lat) -- experts map
+               L -> I -> L (W13_e [2I, L], W2_e [L, I]);
       out    = z·Wupᵀ + shared(x), Wup [H, L] the up-projection back to the
                hidden width, the shared expert on x as in ``moe``.
+    Everything stays in fp64, as in the plain block: an implementation rounds
+    lat, h and z to bf16 where they become a product's operand, and the
+    tolerance absorbs those roundings. round_inter rounds lat and z to bf16
+    here too (a diagnostic, to tell rounding-point effects from bugs).
     Returns dict(out, absref, idx, gates, logits, lat, z), with
     absref[m,n] = sum_l |z_l Wup[n,l]| + sum_i |hs_i Ws2[n,i]| (the block's last
-    contractions) and z the bf16 bits of the rows computed (others 0).
+    contractions); lat and z are fp64 ([M, L], rows not computed are NaN in z).
     """
     x = _u16(x_bits)
     Wrl = _u16(Wrl_bits)
@@ -347,18 +370,22 @@ def moe_latent(x_bits, Wrl_bits, E: int, fetch_expert, topk_k: int, I: int, Wup_
         raise ValueError("Wrl must stack E router rows on L >= 1 latent rows")
     sc, _ = linear(x, Wrl)
     logits = np.ascontiguousarray(sc[:, :E])
-    lat = f64_to_bf16_bits(sc[:, E:])
+    lat = np.ascontiguousarray(sc[:, E:])
+    if round_inter:
+        lat = round_bf16(lat)
     idx, gates = _route(logits, topk_k, route)
     rows = list(range(M)) if tokens is None else sorted(set(int(t) for t in tokens))
-    acc, _ = _routed_sum(lat, rows, idx, gates, fetch_expert, topk_k, I, round_h)
-    z = np.zeros((M, L), dtype=np.uint16)
-    z[rows] = f64_to_bf16_bits(acc)
-    u, uabs = linear(z[rows], Wup_bits)
+    acc, _ = _routed_sum(lat, rows, idx, gates, fetch_expert, topk_k, I, round_inter)
+    if round_inter:
+        acc = round_bf16(acc)
+    z = np.full((M, L), np.nan)
+    z[rows] = acc
+    u, uabs = linear_f64act(acc, Wup_bits)
     out = np.full((M, H), np.nan)
     absref = np.full((M, H), np.nan)
     if shared is not None:
         Ws13, Ws2 = shared
-        s, sabs = expert_mlp(x[rows], Ws13, Ws2, I, round_h)
+        s, sabs = expert_mlp(x[rows], Ws13, Ws2, I, round_inter)
         u = u + s
         uabs = uabs + sabs
     out[rows] = u

@@ -447,24 +447,40 @@ def _latent_case(H, L, E, I, M, key):
     return x, Wr, Ws, W13, W2
 
 
-def test_latent_with_identity_projections_is_the_plain_block_with_z_rounded():
-    # L = H, latent rows = I, Wup = I: lat = x exactly, so the routed part is
-    # the plain block's routed sum, rounded once to bf16 (z), plus the shared
-    # expert on x
+def test_latent_with_identity_projections_is_the_plain_block():
+    # L = H, latent rows = I, Wup = I: lat = x and z·Iᵀ = z exactly, so the
+    # block is the plain block; with the diagnostic rounding of lat, h and z,
+    # z is the plain block's routed sum (h rounded) rounded once more
     H, I, E, M, k = 24, 8, 6, 4, 2
     x, Wr, Ws, W13, W2 = _latent_case(H, H, E, I, M, "lat-id")
     eye = _bits(np.eye(H))
-    r = oracle.moe_latent(x, np.concatenate([Wr, eye]), E, _bank_fetch(W13, W2), k, I, eye,
-                          shared=Ws)
-    plain = oracle.moe(x, Wr, _bank_fetch(W13, W2), k, I, shared=None)
-    s, sA = oracle.expert_mlp(x, Ws[0], Ws[1], I)
+    Wrl = np.concatenate([Wr, eye])
+    r = oracle.moe_latent(x, Wrl, E, _bank_fetch(W13, W2), k, I, eye, shared=Ws)
+    plain = oracle.moe(x, Wr, _bank_fetch(W13, W2), k, I, shared=Ws)
+    routed = oracle.moe(x, Wr, _bank_fetch(W13, W2), k, I, shared=None)
     assert np.array_equal(r["idx"], plain["idx"])
-    assert np.array_equal(r["lat"], x)
-    assert np.array_equal(r["z"], oracle.f64_to_bf16_bits(plain["out"]))
-    np.testing.assert_allclose(r["out"], oracle.round_bf16(plain["out"]) + s, rtol=1e-14,
+    assert np.array_equal(r["lat"], _dec(x))
+    np.testing.assert_allclose(r["z"], routed["out"], rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(r["out"], plain["out"], rtol=1e-14, atol=1e-15)
+    rr = oracle.moe_latent(x, Wrl, E, _bank_fetch(W13, W2), k, I, eye, shared=Ws,
+                           round_inter=True)
+    routed_h = oracle.moe(x, Wr, _bank_fetch(W13, W2), k, I, shared=None, round_h=True)
+    s_h, _ = oracle.expert_mlp(x, Ws[0], Ws[1], I, round_h=True)
+    np.testing.assert_allclose(rr["out"], oracle.round_bf16(routed_h["out"]) + s_h, rtol=1e-14,
                                atol=1e-15)
-    # the pin has teeth: an unrounded z differs
-    assert not np.allclose(r["out"], plain["out"] + s, rtol=1e-9, atol=0)
+    assert not np.allclose(rr["out"], r["out"], rtol=1e-9, atol=0)
+
+
+def test_expert_on_fp64_activations_matches_bf16_expert():
+    H, I = 40, 16
+    x = wl.normal_bf16((3, H), 1.0, "pin", "f64act", "x")
+    W13 = wl.normal_bf16((2 * I, H), 0.2, "pin", "f64act", "W13")
+    W2 = wl.normal_bf16((H, I), 0.2, "pin", "f64act", "W2")
+    for rh in (False, True):
+        a, aA = oracle.expert_mlp(x, W13, W2, I, round_h=rh)
+        b, bA = oracle.expert_mlp_f64act(_dec(x), W13, W2, I, round_h=rh)
+        np.testing.assert_allclose(b, a, rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(bA, aA, rtol=1e-13, atol=1e-15)
 
 
 def test_latent_input_is_projected_and_output_projected_back():
@@ -480,10 +496,10 @@ def test_latent_input_is_projected_and_output_projected_back():
     on2x = oracle.moe(x2, half_Wr, _bank_fetch(W13, W2), k, I, shared=None, route=r["idx"])
     s, _ = oracle.expert_mlp(x, Ws[0], Ws[1], I)
     np.testing.assert_allclose(on2x["gates"], r["gates"], rtol=1e-14)
-    want = 0.5 * oracle.round_bf16(on2x["out"]) + s
+    want = 0.5 * on2x["out"] + s
     np.testing.assert_allclose(r["out"], want, rtol=1e-14, atol=1e-15)
     on1x = oracle.moe(x, Wr, _bank_fetch(W13, W2), k, I, shared=None, route=r["idx"])
-    assert not np.allclose(r["out"], 0.5 * oracle.round_bf16(on1x["out"]) + s, rtol=1e-6)
+    assert not np.allclose(r["out"], 0.5 * on1x["out"] + s, rtol=1e-6)
 
 
 def test_latent_special_cases():
@@ -501,8 +517,8 @@ def test_latent_special_cases():
     assert np.array_equal(other["idx"], base["idx"])
     assert np.array_equal(other["idx"], oracle.topk(oracle.linear(x, Wr)[0], k)[0])
     np.testing.assert_array_equal(other["gates"], base["gates"])
-    # the latent input is the rounded latent projection of x
-    assert np.array_equal(base["lat"], oracle.f64_to_bf16_bits(oracle.linear(x, Wd)[0]))
+    # the latent input is the latent projection of x
+    assert np.array_equal(base["lat"], oracle.linear(x, Wd)[0])
     # Wup = 0: the shared expert alone
     z0 = oracle.moe_latent(x, np.concatenate([Wr, Wd]), E, f, k, I, np.zeros_like(Wup),
                            shared=Ws)
@@ -513,7 +529,7 @@ def test_latent_special_cases():
                           shared=None)
     assert np.array_equal(b["out"], 2 * a["out"])
     np.testing.assert_allclose(base["out"], a["out"] + s, rtol=1e-14, atol=1e-15)
-    np.testing.assert_allclose(a["out"], _dec(a["z"]) @ _dec(Wup).T, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(a["out"], a["z"] @ _dec(Wup).T, rtol=1e-12, atol=1e-14)
     # token independence
     t = oracle.moe_latent(x, np.concatenate([Wr, Wd]), E, f, k, I, Wup, shared=Ws, tokens=[1])
     assert np.array_equal(t["out"][1], base["out"][1]) and np.isnan(t["out"][0]).all()
