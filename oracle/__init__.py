@@ -358,9 +358,13 @@ def moe_latent(x_bits, Wrl_bits, E: int, fetch_expert, topk_k: int, I: int, Wup_
     lat, h and z to bf16 where they become a product's operand, and the
     tolerance absorbs those roundings. round_inter rounds lat and z to bf16
     here too (a diagnostic, to tell rounding-point effects from bugs).
-    Returns dict(out, absref, idx, gates, logits, lat, z), with
-    absref[m,n] = sum_l |z_l Wup[n,l]| + sum_i |hs_i Ws2[n,i]| (the block's last
-    contractions); lat and z are fp64 ([M, L], rows not computed are NaN in z).
+    Returns dict(out, absref, idx, gates, logits, lat, z), with the reference
+    scale carried through the block's linear steps after the experts:
+      absref[m,n] = sum_l |Wup[n,l]| * Az[m,l] + sum_i |hs_i Ws2[n,i]|,
+      Az[m,l]     = sum_j g_j sum_i |h_ji W2[e_j,l,i]|
+    (the plain block's scale, in the latent space, expanded through the
+    up-projection: every product of the expression taken in absolute value).
+    lat and z are fp64 ([M, L], rows not computed are NaN in z).
     """
     x = _u16(x_bits)
     Wrl = _u16(Wrl_bits)
@@ -375,12 +379,14 @@ def moe_latent(x_bits, Wrl_bits, E: int, fetch_expert, topk_k: int, I: int, Wup_
         lat = round_bf16(lat)
     idx, gates = _route(logits, topk_k, route)
     rows = list(range(M)) if tokens is None else sorted(set(int(t) for t in tokens))
-    acc, _ = _routed_sum(lat, rows, idx, gates, fetch_expert, topk_k, I, round_inter)
+    acc, acc_abs = _routed_sum(lat, rows, idx, gates, fetch_expert, topk_k, I, round_inter)
     if round_inter:
         acc = round_bf16(acc)
     z = np.full((M, L), np.nan)
     z[rows] = acc
-    u, uabs = linear_f64act(acc, Wup_bits)
+    u, _ = linear_f64act(acc, Wup_bits)
+    Wup_abs = _u16(Wup_bits) & np.uint16(0x7FFF)       # |w| of a bf16 value: its sign bit cleared
+    uabs, _ = linear_f64act(acc_abs, Wup_abs)
     out = np.full((M, H), np.nan)
     absref = np.full((M, H), np.nan)
     if shared is not None:

@@ -462,6 +462,7 @@ def test_latent_with_identity_projections_is_the_plain_block():
     assert np.array_equal(r["lat"], _dec(x))
     np.testing.assert_allclose(r["z"], routed["out"], rtol=1e-14, atol=1e-15)
     np.testing.assert_allclose(r["out"], plain["out"], rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(r["absref"], plain["absref"], rtol=1e-14, atol=1e-15)
     rr = oracle.moe_latent(x, Wrl, E, _bank_fetch(W13, W2), k, I, eye, shared=Ws,
                            round_inter=True)
     routed_h = oracle.moe(x, Wr, _bank_fetch(W13, W2), k, I, shared=None, round_h=True)
@@ -528,6 +529,15 @@ def test_latent_special_cases():
     b = oracle.moe_latent(x, np.concatenate([Wr, Wd]), E, f, k, I, _bits(2 * _dec(Wup)),
                           shared=None)
     assert np.array_equal(b["out"], 2 * a["out"])
+    assert np.array_equal(b["absref"], 2 * a["absref"])
+    assert np.all(a["absref"] >= np.abs(a["out"]) * (1 - 1e-12))
+    # the scale is the whole expression in absolute values: with every weight
+    # and activation replaced by its magnitude the block's value equals it
+    absb = lambda w: w & np.uint16(0x7FFF)
+    pos = oracle.moe_latent(x, np.concatenate([Wr, Wd]), E,
+                            lambda e: (W13[e], absb(W2[e])), k, I, absb(Wup), shared=None,
+                            route=a["idx"])
+    np.testing.assert_allclose(pos["absref"], a["absref"], rtol=1e-12)
     np.testing.assert_allclose(base["out"], a["out"] + s, rtol=1e-14, atol=1e-15)
     np.testing.assert_allclose(a["out"], a["z"] @ _dec(Wup).T, rtol=1e-12, atol=1e-14)
     # token independence
