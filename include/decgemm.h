@@ -59,6 +59,7 @@ extern "C" {
 #define DEC_ETIMEOUT     -4  /* a bounded device-side wait gave up */
 #define DEC_ENOMEM       -5  /* the workspace could not be allocated */
 #define DEC_ENODEV       -6  /* no sm_103 device is current */
+#define DEC_EBOUNDS      -7  /* a device-side index check failed (DEC_DEBUG builds only) */
 
 /* Kernel regimes reported by dec_last_choice (low 8 bits). */
 #define DEC_REGIME_NONE   0
@@ -162,6 +163,36 @@ int moe_decode_residual(const void* x, const void* Wr, const void* W13, const vo
                         int32_t* topk_idx, float* topk_w, void* stream);
 
 /*
+ * moe_decode_latent -- an MoE decode block whose routed experts work on a
+ * latent width L. [moe-overlap] The router scores and the latent input
+ * projection are computed as one product over a stacked weight (the pages
+ * merge the two into one matrix multiplication); the steps after it are the
+ * library's reading of the block, the pages naming only that product:
+ *
+ *   x    : [M,H] bf16               Wrl : [E+L,H] bf16, rows 0..E-1 the router,
+ *                                         rows E..E+L-1 the latent input projection
+ *   W13  : [E,2I,L] bf16 (gate rows 0..I-1, up rows I..2I-1)   W2 : [E,L,I] bf16
+ *   Wup  : [H,L] bf16 up-projection     Ws13 [2I,H] / Ws2 [H,I]: shared expert on x
+ *   res  : optional [M,H] bf16 residual (may alias x or out)   out : [M,H] bf16
+ *
+ *   sc     = x·Wrlᵀ (fp32);  logits = sc[:, :E];  lat = bf16(sc[:, E:])
+ *   idx, g = top-k of logits, renormalised softmax gates (as moe_decode)
+ *   z      = bf16( sum_{j=0..topk-1} g_j · expert_{idx_j}(lat) )   (width L)
+ *   out    = bf16( res + (z·Wupᵀ + shared(x)) )   (fp32 sum, one rounding)
+ *
+ * Kernels on `stream`: the router over E+L rows with the top-k, schedule +
+ * gather of the latent rows (rounded to bf16 as they are copied), expert
+ * gate/up, expert down, the gate-weighted sum z, the up-projection, and the
+ * final sum; the shared expert on the library's side stream as in
+ * moe_decode. Limits as moe_decode; L >= 8, L % 8 == 0.
+ * Errors: DEC_EINVAL, DEC_EUNSUPPORTED, DEC_ECUDA, DEC_ENOMEM.
+ */
+int moe_decode_latent(const void* x, const void* Wrl, const void* W13, const void* W2,
+                      const void* Wup, const void* Ws13, const void* Ws2, const void* res,
+                      void* out, int M, int H, int L, int E, int topk, int I,
+                      int32_t* topk_idx, float* topk_w, void* stream);
+
+/*
  * l2_prefetch -- enqueue a light kernel on `stream` that pulls
  * [ptr, ptr + bytes) into L2, so that a later kernel reading the range hits
  * in cache. [prefetch] It has no data dependency and changes no memory;
@@ -220,6 +251,20 @@ long long dec_set_wait_timeout_ns(long long ns);
  * Exercises failure detection without faulting or hanging the GPU.
  */
 int dec_selftest_timeout(long long ns, void* stream);
+
+/*
+ * dec_debug_build -- 1 for the index-checking build of this library
+ * (libdecgemm_debug.so, compiled with DEC_DEBUG), 0 otherwise. In that build
+ * every index a kernel computes into a global buffer (output rows and
+ * columns, split-K slots and counters, expert group tables, pair positions,
+ * gathered token rows) is checked against the buffer's extent; an access out
+ * of range is skipped, and dec_sync_check returns DEC_EBOUNDS.
+ * dec_debug_check_site -- the source line of the first failed check and the
+ * offending index, as read by the dec_sync_check that returned DEC_EBOUNDS;
+ * returns 1 if there was one, 0 if not.
+ */
+int dec_debug_build(void);
+int dec_debug_check_site(int* line, long long* index);
 
 /* dec_launch_count -- kernels launched by this library since load (all threads). */
 long long dec_launch_count(void);

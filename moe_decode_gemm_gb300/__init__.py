@@ -14,6 +14,7 @@ import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdecgemm.so")
+DEBUG_LIB_PATH = os.path.join(_HERE, "libdecgemm_debug.so")
 
 DEC_OK = 0
 DEC_EINVAL = -1
@@ -22,6 +23,7 @@ DEC_ECUDA = -3
 DEC_ETIMEOUT = -4
 DEC_ENOMEM = -5
 DEC_ENODEV = -6
+DEC_EBOUNDS = -7
 
 REGIME_NONE, REGIME_SMALLM, REGIME_MMA, REGIME_TC = 0, 1, 2, 3
 REGIME_NAMES = {0: "none", 1: "smallm", 2: "mma", 3: "tc"}
@@ -29,10 +31,10 @@ REGIME_NAMES = {0: "none", 1: "smallm", 2: "mma", 3: "tc"}
 # Names the header declares; the ABI tests check every one is exported.
 EXPORTS = [
     "dec_linear", "dec_linear_residual", "dec_linear_ex", "dec_linear_splitk", "moe_decode",
-    "moe_decode_residual", "l2_prefetch", "dec_add", "dec_last_choice", "dec_last_grid",
+    "moe_decode_residual", "moe_decode_latent", "l2_prefetch", "dec_add", "dec_last_choice", "dec_last_grid",
     "dec_strerror", "dec_sync_check", "dec_set_wait_timeout_ns", "dec_selftest_timeout",
     "dec_launch_count", "dec_probe_begin", "dec_probe_end", "dec_shutdown", "dec_version",
-    "dec_linear_noalloc",
+    "dec_linear_noalloc", "dec_debug_build", "dec_debug_check_site",
 ]
 
 _lib = None
@@ -44,43 +46,74 @@ class DecError(RuntimeError):
         super().__init__("%s failed: %s (%d)" % (what, strerror(code), code))
 
 
+def _load(path):
+    if not os.path.exists(path):
+        raise RuntimeError("%s is not built; run `python -m moe_decode_gemm_gb300.build` "
+                           "(no fallback exists)" % os.path.basename(path))
+    return _configure(ctypes.CDLL(path))
+
+
 def lib():
     """The loaded library. Raises if it has not been built."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError("libdecgemm.so is not built; run "
-                               "`python -m moe_decode_gemm_gb300.build` (no fallback exists)")
-        L = ctypes.CDLL(LIB_PATH)
-        P, I, SZ, LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_longlong
-        sig = {
-            "dec_linear": (I, [P, P, P, I, I, I, P]),
-            "dec_linear_residual": (I, [P, P, P, P, I, I, I, P]),
-            "dec_linear_ex": (I, [P, I, P, P, P, I, I, I, P]),
-            "dec_linear_splitk": (I, [P, P, P, I, I, I, I, P]),
-            "moe_decode": (I, [P, P, P, P, P, P, P, I, I, I, I, I, P, P, P]),
-            "moe_decode_residual": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, P]),
-            "l2_prefetch": (I, [P, SZ, P]),
-            "dec_add": (I, [P, P, P, SZ, P]),
-            "dec_last_choice": (I, []),
-            "dec_last_grid": (I, []),
-            "dec_strerror": (ctypes.c_char_p, [I]),
-            "dec_sync_check": (I, [P]),
-            "dec_set_wait_timeout_ns": (LL, [LL]),
-            "dec_selftest_timeout": (I, [LL, P]),
-            "dec_launch_count": (LL, []),
-            "dec_probe_begin": (I, [I, I]),
-            "dec_probe_end": (I, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
-            "dec_shutdown": (None, []),
-            "dec_version": (I, []),
-            "dec_linear_noalloc": (I, [P, P, P, I, I, I, P]),
-        }
-        for name, (res, args) in sig.items():
-            f = getattr(L, name)
-            f.restype = res
-            f.argtypes = args
-        _lib = L
+        _lib = _load(LIB_PATH)
     return _lib
+
+
+def use_library(path):
+    """Route every call of this binding to another build of the library (the
+    index-checking one, DEBUG_LIB_PATH) and return the previous handle; give
+    the handle back to restore it."""
+    global _lib
+    old = _lib
+    _lib = path if not isinstance(path, str) else _load(path)
+    return old
+
+
+def _configure(L):
+    """Declare the C signatures of every exported function on a loaded library."""
+    P, I, SZ, LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_longlong
+    sig = {
+        "dec_linear": (I, [P, P, P, I, I, I, P]),
+        "dec_linear_residual": (I, [P, P, P, P, I, I, I, P]),
+        "dec_linear_ex": (I, [P, I, P, P, P, I, I, I, P]),
+        "dec_linear_splitk": (I, [P, P, P, I, I, I, I, P]),
+        "moe_decode": (I, [P, P, P, P, P, P, P, I, I, I, I, I, P, P, P]),
+        "moe_decode_residual": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, P]),
+        "moe_decode_latent": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P]),
+        "l2_prefetch": (I, [P, SZ, P]),
+        "dec_add": (I, [P, P, P, SZ, P]),
+        "dec_last_choice": (I, []),
+        "dec_last_grid": (I, []),
+        "dec_strerror": (ctypes.c_char_p, [I]),
+        "dec_sync_check": (I, [P]),
+        "dec_set_wait_timeout_ns": (LL, [LL]),
+        "dec_selftest_timeout": (I, [LL, P]),
+        "dec_launch_count": (LL, []),
+        "dec_probe_begin": (I, [I, I]),
+        "dec_probe_end": (I, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
+        "dec_shutdown": (None, []),
+        "dec_version": (I, []),
+        "dec_linear_noalloc": (I, [P, P, P, I, I, I, P]),
+        "dec_debug_build": (I, []),
+        "dec_debug_check_site": (I, [ctypes.POINTER(ctypes.c_int),
+                                     ctypes.POINTER(ctypes.c_longlong)]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    return L
+
+
+def check_site():
+    """(line, index) of the first failed index check of the debug build, as
+    read by the last sync_check that returned DEC_EBOUNDS, or None."""
+    line, idx = ctypes.c_int(0), ctypes.c_longlong(0)
+    if lib().dec_debug_check_site(ctypes.byref(line), ctypes.byref(idx)):
+        return line.value, idx.value
+    return None
 
 
 def strerror(code: int) -> str:
@@ -254,6 +287,48 @@ def moe_decode(x, Wr, W13, W2, Ws13, Ws2, topk, out=None, topk_idx=None, topk_w=
     else:
         rc = lib().moe_decode_residual(*args, _ptr(residual), _ptr(out), *tail)
     _check(rc, "moe_decode")
+    return out
+
+
+def moe_decode_latent(x, Wrl, W13, W2, Wup, Ws13, Ws2, topk, out=None, topk_idx=None,
+                      topk_w=None, stream=None, residual=None):
+    """MoE block with the routed experts on a latent width L. Shapes: x [M,H],
+    Wrl [E+L,H] (router rows, then the latent input projection), W13 [E,2I,L],
+    W2 [E,L,I], Wup [H,L], Ws13 [2I,H] / Ws2 [H,I] or both None. Returns out
+    [M,H] bf16 (plus the residual when given)."""
+    import torch
+
+    _need(x, "x")
+    if x.dim() != 2:
+        raise ValueError("x: expected [M, H], got shape %s" % (tuple(x.shape),))
+    M, H = x.shape
+    _need(W13, "W13")
+    if W13.dim() != 3 or W13.shape[1] % 2:
+        raise ValueError("W13: expected [E, 2I, L], got shape %s" % (tuple(W13.shape),))
+    E, I, L = W13.shape[0], W13.shape[1] // 2, W13.shape[2]
+    _need(Wrl, "Wrl", shape=(E + L, H))
+    _need(W2, "W2", shape=(E, L, I))
+    _need(Wup, "Wup", shape=(H, L))
+    if (Ws13 is None) != (Ws2 is None):
+        raise ValueError("Ws13 and Ws2: give both or neither")
+    if Ws13 is not None:
+        _need(Ws13, "Ws13", shape=(2 * I, H))
+        _need(Ws2, "Ws2", shape=(H, I))
+    if out is None:
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    _need(out, "out", shape=(M, H))
+    if residual is not None:
+        _need(residual, "residual", shape=(M, H))
+    if topk_idx is not None:
+        _need(topk_idx, "topk_idx", shape=(M, int(topk)), dtype="i32")
+    if topk_w is not None:
+        _need(topk_w, "topk_w", shape=(M, int(topk)), dtype="f32")
+    _on_one_gpu(x=x, Wrl=Wrl, W13=W13, W2=W2, Wup=Wup, Ws13=Ws13, Ws2=Ws2, out=out,
+                residual=residual, topk_idx=topk_idx, topk_w=topk_w)
+    rc = lib().moe_decode_latent(_ptr(x), _ptr(Wrl), _ptr(W13), _ptr(W2), _ptr(Wup), _ptr(Ws13),
+                                 _ptr(Ws2), _ptr(residual), _ptr(out), M, H, L, E, int(topk), I,
+                                 _ptr(topk_idx), _ptr(topk_w), _stream(stream))
+    _check(rc, "moe_decode_latent")
     return out
 
 

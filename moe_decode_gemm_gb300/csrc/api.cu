@@ -63,7 +63,7 @@ struct DevState {
   int* status = nullptr;                  // device status word
   Buf ws_main, ctr_main, ws_side, ctr_side;
   Buf moe;                                // routing tables + intermediates
-  int moe_M = 0, moe_E = 0, moe_k = 0, moe_I = 0, moe_H = 0;
+  int moe_M = 0, moe_E = 0, moe_k = 0, moe_I = 0, moe_H = 0, moe_L = 0;
   MoeBufs mb = {};
 };
 
@@ -82,6 +82,10 @@ static std::vector<cudaEvent_t> g_probe_ev;  // start/end pairs
 static int g_probe_n = 0;
 
 static int to_err(cudaError_t e) { return e == cudaSuccess ? DEC_OK : DEC_ECUDA; }
+
+// The status word's bit for a failed index check (the device-side
+// kStatusBounds of the kernels).
+constexpr int kStatusBoundsBit = 2;
 
 static int get_dev(DevState** out) {
   int d = 0;
@@ -276,6 +280,8 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
   if ((rc = ensure(s->ctr_main, (size_t)tiles * sizeof(int), st))) return rc;
   Ctx cx = make_ctx(s, st);
   cx.ldx = ldx;
+  cx.ws_len = (long long)(s->ws_main.bytes / sizeof(float));
+  cx.ctr_len = (long long)(s->ctr_main.bytes / sizeof(int));
   long long seff = (KB * grid + T - 1) / T;
   if (seff < 1) seff = 1;
   t_last_choice = regime | ((int)seff << 8) | ((wide ? 1 : 0) << 17);
@@ -294,16 +300,21 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
 }
 
 // ------------------------------------------------------------------ MoE
-static int moe_bufs(DevState* s, int M, int H, int E, int k, int I, cudaStream_t st) {
-  if (M <= s->moe_M && H <= s->moe_H && E <= s->moe_E && k <= s->moe_k && I <= s->moe_I) return DEC_OK;
+// L: the latent width of a latent block (0 for the plain block).
+static int moe_bufs(DevState* s, int M, int H, int E, int k, int I, int L, cudaStream_t st) {
+  if (M <= s->moe_M && H <= s->moe_H && E <= s->moe_E && k <= s->moe_k && I <= s->moe_I &&
+      L <= s->moe_L)
+    return DEC_OK;
   const int Mx = 64;  // sized for the whole decode envelope at once
   const int Ex = E > s->moe_E ? E : s->moe_E;
   const int kx = k > s->moe_k ? k : s->moe_k;
   const int Ix = I > s->moe_I ? I : s->moe_I;
   const int Hx = H > s->moe_H ? H : s->moe_H;
+  const int Lx = L > s->moe_L ? L : s->moe_L;
+  const int Wx = Hx > Lx ? Hx : Lx;  // expert model width: H, or L in a latent block
   auto al = [](size_t v) { return (v + 255) & ~size_t(255); };
   size_t off = 0;
-  size_t o_logits = off; off += al((size_t)Mx * Ex * 4);
+  size_t o_logits = off; off += al((size_t)Mx * (Ex + Lx) * 4);
   size_t o_nact = off; off += al(4);
   // expert groups: at most one per expert plus one per 16 (token, slot) pairs
   // (a bound for groups of 16 or more tokens)
@@ -314,14 +325,23 @@ static int moe_bufs(DevState* s, int M, int H, int E, int k, int I, cudaStream_t
   size_t o_pof = off; off += al((size_t)Mx * kx * 4);
   size_t o_gate = off; off += al((size_t)Mx * kx * 4);
   size_t o_topk = off; off += al((size_t)Mx * kx * 4);
-  size_t o_xs = off; off += al((size_t)Mx * kx * Hx * 2);
+  size_t o_xs = off; off += al((size_t)Mx * kx * Wx * 2);
   size_t o_h = off; off += al((size_t)Mx * kx * Ix * 2);
-  size_t o_o = off; off += al((size_t)Mx * kx * Hx * 4);
+  size_t o_o = off; off += al((size_t)Mx * kx * Wx * 4);
   size_t o_hs = off; off += al((size_t)Mx * Ix * 2);
   size_t o_s = off; off += al((size_t)Mx * Hx * 4);
   size_t o_rctr = off; off += al(4);
+  size_t o_z = off; off += al((size_t)Mx * (Lx > 0 ? Lx : 1) * 2);
+  size_t o_u = off; off += al((size_t)Mx * Hx * 4);
+  const size_t comb_bytes = (size_t)Mx * ((Wx + 255) / 256) * 4;
+  size_t o_comb = off; off += al(comb_bytes);
   int rc = ensure(s->moe, off, st);
   if (rc) return rc;
+  // The layout has changed even when the buffer did not have to grow (its
+  // slack held the larger shapes): the arrival counters that must be zero at
+  // rest now sit on bytes of the old layout. Clear it, on the stream that
+  // orders every earlier use of the buffer.
+  if (cudaMemsetAsync(s->moe.p, 0, off, st) != cudaSuccess) return DEC_ECUDA;
   uint8_t* b = (uint8_t*)s->moe.p;
   s->mb.logits = (float*)(b + o_logits);
   s->mb.nact = (int*)(b + o_nact);
@@ -337,7 +357,13 @@ static int moe_bufs(DevState* s, int M, int H, int E, int k, int I, cudaStream_t
   s->mb.hs = (uint16_t*)(b + o_hs);
   s->mb.s = (float*)(b + o_s);
   s->mb.route_ctr = (int*)(b + o_rctr);
+  s->mb.z = (uint16_t*)(b + o_z);
+  s->mb.u = (float*)(b + o_u);
+  s->mb.comb_ctr = (int*)(b + o_comb);
+  s->mb.comb_ctr_bytes = comb_bytes;
+  s->mb.groups_cap = (int)Gx;
   s->moe_M = Mx;
+  s->moe_L = Lx;
   s->moe_E = Ex;
   s->moe_k = kx;
   s->moe_I = Ix;
@@ -345,13 +371,18 @@ static int moe_bufs(DevState* s, int M, int H, int E, int k, int I, cudaStream_t
   return DEC_OK;
 }
 
+// The MoE block; with L > 0 the latent block: Wr stacks the E router rows on
+// the latent input projection's L rows, the experts work on width L, and Wup
+// [H, L] projects their gate-weighted sum back to the hidden width.
 static int moe_impl(const void* x, const void* Wr, const void* W13, const void* W2, const void* Ws13,
                     const void* Ws2, const void* res, void* out, int M, int H, int E, int topk,
-                    int I, int32_t* topk_idx, float* topk_w, void* stream) {
+                    int I, int32_t* topk_idx, float* topk_w, void* stream, int L = 0,
+                    const void* Wup = nullptr) {
   if (!x || !Wr || !W13 || !W2 || !out) return DEC_EINVAL;
   if ((Ws13 == nullptr) != (Ws2 == nullptr)) return DEC_EINVAL;
   if (M < 1 || H < 8 || E < 1 || topk < 1 || I < 8 || (H % 8) || (I % 8)) return DEC_EINVAL;
-  const void* ptrs[] = {x, Wr, W13, W2, Ws13, Ws2, res, out, topk_idx, topk_w};
+  if (L < 0 || (L > 0 && (L < 8 || (L % 8) || !Wup))) return DEC_EINVAL;
+  const void* ptrs[] = {x, Wr, W13, W2, Ws13, Ws2, res, out, topk_idx, topk_w, Wup};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return DEC_EINVAL;
   if (M > 64 || E > 1024 || topk > 32 || topk > E) return DEC_EUNSUPPORTED;
@@ -359,14 +390,15 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   int rc = get_dev(&s);
   if (rc) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if ((rc = moe_bufs(s, M, H, E, topk, I, st))) return rc;
+  if ((rc = moe_bufs(s, M, H, E, topk, I, L, st))) return rc;
+  const int Wd = L > 0 ? L : H;  // the experts' model width
   // partial slots: 2 per CTA, up to 256 rows (gate + up halves) x 64 tokens
   const size_t ws_bytes = (size_t)s->sms * 2 * 256 * 64 * sizeof(float);
-  const int tiles13 = (I + 127) / 128, tiles2 = (H + 127) / 128;
+  const int tiles13 = (I + 127) / 128, tiles2 = ((Wd > H ? Wd : H) + 127) / 128;
   int maxt = tiles13 > tiles2 ? tiles13 : tiles2;
   // an expert chosen by more tokens than a group holds forms several groups:
   // at most E + M*topk/16 groups, each with its own tile counters
-  const int max_groups = E + (M * topk + 15) / 16;
+  const int max_groups = E + (M * topk + 15) / 16 + (M + 15) / 16;  // + the shared expert's
   const size_t ctr_bytes = (size_t)(max_groups * (size_t)maxt + 64) * sizeof(int);
   if ((rc = ensure(s->ws_main, ws_bytes, st))) return rc;
   if ((rc = ensure(s->ctr_main, ctr_bytes, st))) return rc;
@@ -376,15 +408,19 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
     if ((rc = ensure(s->ctr_side, (size_t)(maxt + 64) * sizeof(int), st))) return rc;
   }
   Ctx cx = make_ctx(s, st);
+  cx.ws_len = (long long)(s->ws_main.bytes / sizeof(float));
+  cx.ctr_len = (long long)(s->ctr_main.bytes / sizeof(int));
   float* ws = (float*)s->ws_main.p;
   int* ctr = (int*)s->ctr_main.p;
   // Shared expert, forked first to the side stream (lowest priority), one CTA
-  // on each SM the router leaves free, so its weights stream while the
-  // latency-bound router, top-k and gather run on the other SMs. Its down
-  // projection is launched without the early-start dependency, so its CTAs do
-  // not take SMs early and sit waiting for the gate/up kernel. The routed
-  // experts take the SMs as the shared expert's CTAs leave them; the streams
-  // join before the combine.
+  // on each SM the router leaves free, so its gate/up weights stream while
+  // the latency-bound router, top-k and gather run on the other SMs. The
+  // routed experts take the SMs as the shared expert's CTAs leave them. Its
+  // down projection runs inside the routed down projection, as extra groups,
+  // so the streams join before that kernel; the combine is that kernel's
+  // epilogue. (In the latent block the down projection stays on the side
+  // stream -- its output width is H, the routed one's L -- and the streams
+  // join before the final sum.)
   //
   // Small batches: the routed experts read few bytes, and the shared expert,
   // packed into the routing window, then delays the routed gate/up kernel's
@@ -398,43 +434,68 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   const bool dedicated = shared && gd >= 4 && gd < s->sms / 2;
   const int egrid = dedicated ? s->sms - gd : s->sms;
   if (shared) {
-    const int rc_ctas = router_ctas(E, H);
+    const int rc_ctas = router_ctas(E + L, H);
     const int sgrid = dedicated ? gd : (s->sms - rc_ctas > 0 ? s->sms - rc_ctas : 1);
     if (cudaEventRecord(s->ev_fork, st) != cudaSuccess) return DEC_ECUDA;
     if (cudaStreamWaitEvent(s->side, s->ev_fork, 0) != cudaSuccess) return DEC_ECUDA;
     Ctx sx = make_ctx(s, s->side);
     sx.pdl = false;
+    sx.ws_len = (long long)(s->ws_side.bytes / sizeof(float));
+    sx.ctr_len = (long long)(s->ctr_side.bytes / sizeof(int));
     if ((rc = counted(launch_shared_w13(sx, x, Ws13, M, H, I, s->mb, sgrid, (float*)s->ws_side.p,
                                         (int*)s->ctr_side.p))))
       return rc;
-    if ((rc = counted(launch_shared_w2(sx, Ws2, M, H, I, s->mb, sgrid, (float*)s->ws_side.p,
-                                       (int*)s->ctr_side.p))))
+    if (L > 0 && (rc = counted(launch_shared_w2(sx, Ws2, M, H, I, s->mb, sgrid,
+                                                (float*)s->ws_side.p, (int*)s->ctr_side.p))))
       return rc;
     if (cudaEventRecord(s->ev_join, s->side) != cudaSuccess) return DEC_ECUDA;
   }
   {
     ProbeScope p(3, st);
-    if ((rc = counted(launch_router(cx, x, Wr, M, H, E, topk, topk_idx, topk_w, s->mb)))) return rc;
+    if ((rc = counted(launch_router(cx, x, Wr, M, H, E, topk, topk_idx, topk_w, s->mb, L))))
+      return rc;
   }
-  if ((rc = counted(launch_gather(cx, x, M, H, E, topk, s->mb)))) return rc;
+  if ((rc = counted(launch_gather(cx, x, M, H, E, topk, s->mb, L)))) return rc;
   {
     ProbeScope p(0, st);
-    if ((rc = counted(launch_experts_w13(cx, x, W13, M, H, E, topk, I, s->mb, egrid, ws, ctr))))
+    if ((rc = counted(launch_experts_w13(cx, x, W13, M, Wd, E, topk, I, s->mb, egrid, ws, ctr))))
       return rc;
+  }
+  DownExtras dx;
+  if (L > 0) {
+    dx.comb_out = s->mb.z;  // z = bf16(sum_j g_j o_j) on width L
+  } else {
+    dx.Ws2 = Ws2;           // null without a shared expert
+    dx.comb_out = out;
+    dx.comb_res = res;
+    // the shared expert's hidden rows must be complete before the down
+    // projection starts
+    if (shared && cudaStreamWaitEvent(st, s->ev_join, 0) != cudaSuccess) return DEC_ECUDA;
   }
   {
     ProbeScope p(1, st);
-    if ((rc = counted(launch_experts_w2(cx, W2, M, H, E, topk, I, s->mb, egrid, ws, ctr))))
+    if ((rc = counted(launch_experts_w2(cx, W2, M, Wd, E, topk, I, s->mb, L > 0 ? egrid : s->sms,
+                                        ws, ctr, dx))))
+      return rc;
+  }
+  if (L == 0) return DEC_OK;
+  {
+    // u = z·Wupᵀ in fp32 (stream-K over every SM), then out = bf16(res + (u + s)).
+    const int xr = M <= 2 ? 8 : (M <= 16 ? 16 : 64);
+    const long long T = (long long)((H + 127) / 128) * ((L + 127) / 128);
+    const int ugrid = (int)(T < s->sms ? T : s->sms);
+    if ((rc = counted(launch_dense_f32(cx, xr, M > 2, s->mb.z, Wup, s->mb.u, M, H, L, ugrid, ws,
+                                       ctr))))
       return rc;
   }
   if (shared) {
     if (cudaStreamWaitEvent(st, s->ev_join, 0) != cudaSuccess) return DEC_ECUDA;
   }
-  // After the join the combine depends on two streams: launch it without the
-  // programmatic (early-start) dependency so both are complete ones.
+  // After the join the final sum depends on two streams: launch it without
+  // the programmatic (early-start) dependency so both are complete ones.
   cx.pdl = !shared;
   ProbeScope p(4, st);
-  return counted(launch_combine(cx, s->mb, shared, res, out, M, H, topk));
+  return counted(launch_combine_up(cx, s->mb, shared, res, out, M, H));
 }
 
 }  // namespace dg
@@ -481,6 +542,15 @@ int moe_decode_residual(const void* x, const void* Wr, const void* W13, const vo
   return moe_impl(x, Wr, W13, W2, Ws13, Ws2, res, out, M, H, E, topk, I, topk_idx, topk_w, stream);
 }
 
+int moe_decode_latent(const void* x, const void* Wrl, const void* W13, const void* W2,
+                      const void* Wup, const void* Ws13, const void* Ws2, const void* res,
+                      void* out, int M, int H, int L, int E, int topk, int I, int32_t* topk_idx,
+                      float* topk_w, void* stream) {
+  if (L < 1) return DEC_EINVAL;
+  return moe_impl(x, Wrl, W13, W2, Ws13, Ws2, res, out, M, H, E, topk, I, topk_idx, topk_w, stream,
+                  L, Wup);
+}
+
 int l2_prefetch(const void* ptr, size_t bytes, void* stream) {
   if (!ptr || !aligned16(ptr)) return DEC_EINVAL;
   bytes &= ~size_t(15);
@@ -516,6 +586,7 @@ const char* dec_strerror(int code) {
     case DEC_ETIMEOUT: return "a bounded device-side wait gave up";
     case DEC_ENOMEM: return "workspace allocation failed";
     case DEC_ENODEV: return "no sm_103 (GB300) device is current";
+    case DEC_EBOUNDS: return "a device-side index check failed (DEC_DEBUG build)";
     default: return "unknown error code";
   }
 }
@@ -530,6 +601,11 @@ static DevState* peek_dev() {
   return &g_dev[d];
 }
 
+// Where the first failed index check of a DEC_DEBUG build was, as read by the
+// last dec_sync_check that reported DEC_EBOUNDS.
+static int g_check_line = 0;
+static long long g_check_index = 0;
+
 int dec_sync_check(void* stream) {
   // Allocates nothing: a device whose state was never set up (a process that
   // only calls dec_linear_noalloc) is not set up here.
@@ -539,19 +615,42 @@ int dec_sync_check(void* stream) {
   DevState* s = peek_dev();
   if (!s) return nst ? DEC_ETIMEOUT : DEC_OK;
   if (cudaStreamSynchronize(s->side) != cudaSuccess) return DEC_ECUDA;
-  int st = 0;
-  if (cudaMemcpy(&st, s->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DEC_ECUDA;
+  int words[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(words, s->status, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DEC_ECUDA;
+  const int st = words[0];
   if (st == 0 && nst != 0) return DEC_ETIMEOUT;
   if (st != 0) {
+    if (st & kStatusBoundsBit) {
+      g_check_line = words[1];
+      g_check_index = (long long)(unsigned)words[2] | ((long long)words[3] << 32);
+    }
     // Reset the status word and every arrival counter a timed-out kernel may
     // have left behind.
     cudaMemset(s->status, 0, sizeof(int));
     if (s->ctr_main.p) cudaMemset(s->ctr_main.p, 0, s->ctr_main.bytes);
     if (s->ctr_side.p) cudaMemset(s->ctr_side.p, 0, s->ctr_side.bytes);
+    if (s->mb.comb_ctr) cudaMemset(s->mb.comb_ctr, 0, s->mb.comb_ctr_bytes);
+    if (s->mb.route_ctr) cudaMemset(s->mb.route_ctr, 0, sizeof(int));
+    cudaMemset(s->status, 0, sizeof(words));
     cudaDeviceSynchronize();
-    return DEC_ETIMEOUT;
+    return (st & kStatusBoundsBit) ? DEC_EBOUNDS : DEC_ETIMEOUT;
   }
   return DEC_OK;
+}
+
+int dec_debug_check_site(int* line, long long* index) {
+  if (line) *line = g_check_line;
+  if (index) *index = g_check_index;
+  return g_check_line != 0 ? 1 : 0;
+}
+
+int dec_debug_build(void) {
+#ifdef DEC_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
 }
 
 long long dec_set_wait_timeout_ns(long long ns) {

@@ -11,7 +11,44 @@
 namespace dg {
 
 // Status word bits set by device code (read and cleared by dec_sync_check).
-enum : int { kStatusTimeout = 1 };
+// kStatusBounds: an index check of a DEC_DEBUG build failed; the status words
+// after the first then hold the source line of the first failed check and
+// the offending index (low and high 32 bits).
+enum : int { kStatusTimeout = 1, kStatusBounds = 2 };
+
+// ------------------------------------------------------------------ index checks
+// DG_AT(status, base, idx, len) is base + idx. In a DEC_DEBUG build an index
+// outside [0, len) is not accessed: the first failure records its line and
+// index in the status words (status[1..3]), sets kStatusBounds, and the
+// access goes to a scratch word of this translation unit instead, so the
+// kernel runs on (with wrong results, reported) rather than faulting.
+#ifdef DEC_DEBUG
+static __device__ __align__(16) unsigned char g_dbg_sink[64];
+
+static __device__ __noinline__ void dbg_check_failed(int* status, int line, long long idx) {
+  if (!status) return;
+  if (atomicCAS(status + 1, 0, line) == 0) {
+    status[2] = (int)(idx & 0xFFFFFFFFLL);
+    status[3] = (int)(idx >> 32);
+  }
+  atomicOr(status, kStatusBounds);
+}
+
+template <typename T>
+__device__ __forceinline__ T* dbg_at(T* base, long long idx, long long len, int* status,
+                                     int line) {
+  if (idx >= 0 && idx < len) return base + idx;
+  dbg_check_failed(status, line, idx);
+  return reinterpret_cast<T*>(const_cast<unsigned char*>(g_dbg_sink));
+}
+#define DG_AT(status, base, idx, len) \
+  ::dg::dbg_at((base), (long long)(idx), (long long)(len), (status), __LINE__)
+#define DG_OK(status, cond, v) \
+  ((cond) ? true : (::dg::dbg_check_failed((status), __LINE__, (long long)(v)), false))
+#else
+#define DG_AT(status, base, idx, len) ((base) + (idx))
+#define DG_OK(status, cond, v) true
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -68,11 +68,16 @@ static cudaError_t run_dense_path(const Ctx& cx, const void* x, const void* W, c
   a.ws = ws;
   a.ctr = ctr;
   a.status = cx.status;
+  a.out_len = (long long)M * N;
+  a.res_len = res ? (long long)M * N : 0;
+  a.ws_len = cx.ws_len;
+  a.ctr_len = cx.ctr_len;
   a.timeout_ns = cx.timeout_ns;
   if (CLUSTER)
     return launch_kc(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, cl, wmap, xmap, xmap,
-                     a);
-  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, xmap, a);
+                     wmap, xmap, a);
+  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, xmap, wmap,
+                  xmap, a);
 }
 
 // The CUDA-core consumer takes at most two tokens and only runs at 8 token
@@ -121,6 +126,13 @@ cudaError_t launch_dense_wide(const Ctx& cx, int xr, bool mma, bool residual, co
                ? run_dense<16, EPI_BF16_RES, true>(cx, mma, x, W, res, y, M, N, K, grid, ws, ctr)
                : run_dense<16, EPI_BF16, true>(cx, mma, x, W, res, y, M, N, K, grid, ws, ctr);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_dense_f32(const Ctx& cx, int xr, bool mma, const void* x, const void* W,
+                             float* y, int M, int N, int K, int grid, float* ws, int* ctr) {
+  if (xr == 8) return run_dense<8, EPI_F32>(cx, mma, x, W, nullptr, y, M, N, K, grid, ws, ctr);
+  if (xr == 16) return run_dense<16, EPI_F32>(cx, mma, x, W, nullptr, y, M, N, K, grid, ws, ctr);
+  return run_dense<64, EPI_F32>(cx, mma, x, W, nullptr, y, M, N, K, grid, ws, ctr);
 }
 
 cudaError_t launch_dense(const Ctx& cx, int xr, bool mma, bool residual, const void* x,

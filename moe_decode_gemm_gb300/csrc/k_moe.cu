@@ -34,6 +34,8 @@ static StreamArgs base_args(const Ctx& cx, float* ws, int* ctr) {
   a.ctr = ctr;
   a.status = cx.status;
   a.timeout_ns = cx.timeout_ns;
+  a.ws_len = cx.ws_len;
+  a.ctr_len = cx.ctr_len;
   return a;
 }
 
@@ -49,7 +51,7 @@ static StreamArgs base_args(const Ctx& cx, float* ws, int* ctr) {
 // top-k kernel and launch sits between the scores and the schedule.
 template <int XR>
 static cudaError_t run_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E,
-                              int k, int32_t* idx_user, float* w_user, const MoeBufs& b) {
+                              int k, int32_t* idx_user, float* w_user, const MoeBufs& b, int L) {
   constexpr int STAGES = XR == 64 ? 4 : 6;
   constexpr int SMEM = wstream_smem(XR, STAGES, 0);
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
@@ -57,33 +59,37 @@ static cudaError_t run_router(const Ctx& cx, const void* x, const void* Wr, int 
   static DevOnce once;
   if (cudaError_t e = setup_smem(once, kern, SMEM); e != cudaSuccess) return e;
   CUtensorMap wmap, xmap;
-  if (!make_tmap(&wmap, Wr, (uint64_t)E, (uint64_t)H, kTileRows, true)) return cudaErrorInvalidValue;
+  if (!make_tmap(&wmap, Wr, (uint64_t)(E + L), (uint64_t)H, kTileRows, true))
+    return cudaErrorInvalidValue;
   if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)H, XR, false)) return cudaErrorInvalidValue;
   StreamArgs a = base_args(cx, nullptr, nullptr);
   a.K = H;
   a.KB = (H + kKChunk - 1) / kKChunk;
-  a.TILES = (E + kTileRows - 1) / kTileRows;
-  a.nout = E;
+  a.TILES = (E + L + kTileRows - 1) / kTileRows;
+  a.nout = E + L;
   a.M = M;
   a.out = b.logits;
-  a.ldo = E;
+  a.ldo = E + L;
   a.route_k = k;
+  a.route_E = E;
   a.route_ctr = b.route_ctr;
   a.route_idx = b.topk;
   a.route_gate = b.gate;
   a.route_idx_user = idx_user;
   a.route_w_user = w_user;
+  a.out_len = (long long)M * (E + L);
+  a.pairs = M * k;
   const int cl = router_clusters(H);
   return launch_kc(kern, dim3(a.TILES * cl), dim3(kThreads), SMEM, cx.stream, cx.pdl, cl, wmap,
-                   xmap, xmap, a);
+                   xmap, xmap, wmap, xmap, a);
 }
 
 cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E, int k,
-                          int32_t* idx_user, float* w_user, const MoeBufs& b) {
-  if (k < 1 || k > 32 || k > E || E > 1024) return cudaErrorInvalidValue;
-  if (M <= 8) return run_router<8>(cx, x, Wr, M, H, E, k, idx_user, w_user, b);
-  if (M <= 16) return run_router<16>(cx, x, Wr, M, H, E, k, idx_user, w_user, b);
-  return run_router<64>(cx, x, Wr, M, H, E, k, idx_user, w_user, b);
+                          int32_t* idx_user, float* w_user, const MoeBufs& b, int L) {
+  if (k < 1 || k > 32 || k > E || E > 1024 || L < 0) return cudaErrorInvalidValue;
+  if (M <= 8) return run_router<8>(cx, x, Wr, M, H, E, k, idx_user, w_user, b, L);
+  if (M <= 16) return run_router<16>(cx, x, Wr, M, H, E, k, idx_user, w_user, b, L);
+  return run_router<64>(cx, x, Wr, M, H, E, k, idx_user, w_user, b, L);
 }
 
 // ------------------------------------------------------------------ schedule + gather
@@ -99,9 +105,16 @@ constexpr int kSchedThreads = 256;
 constexpr int kMaxE = 1024;
 constexpr int kMaxPairs = 64 * 32;
 
+// LATENT: the rows copied are the latent inputs, fp32 scores at columns
+// E..E+row_vecs*8-1 of rows of src_ld floats, rounded to bf16 on the way;
+// otherwise bf16 token rows of x.
+// status / src_len / groups_cap: for the index checks of a DEC_DEBUG build
+// (src_len in floats for LATENT, else in 16-byte vectors).
+template <bool LATENT>
 __global__ void __launch_bounds__(kSchedThreads) schedule_gather_kernel(
-    const uint4* __restrict__ x, const int* __restrict__ topk, int M, int E, int K, int row_vecs,
-    uint4* __restrict__ xs, int* nact, int* grp_exp, int* grp_off, int* pair_tok, int* pair_of) {
+    const void* __restrict__ src, long long src_ld, const int* __restrict__ topk, int M, int E,
+    int K, int row_vecs, uint4* __restrict__ xs, int* nact, int* grp_exp, int* grp_off,
+    int* pair_tok, int* pair_of, int* status, long long src_len, int groups_cap) {
   // Dynamic shared memory sized to E and M*k (about 9 KB at E = 384, M = 64,
   // k = 8), so a CTA fits on an SM beside a weight-streaming CTA:
   // [E] token masks, [E] pair offsets, [M*k] chosen experts, [M*k] pair tokens.
@@ -118,7 +131,10 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_gather_kernel(
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int P = M * K;
   const bool publish = blockIdx.x == 0;
-  for (int p = t; p < P; p += kSchedThreads) s_idx[p] = topk[p];
+  for (int p = t; p < P; p += kSchedThreads) {
+    const int e = topk[p];
+    s_idx[p] = DG_OK(status, e >= 0 && e < E, e) ? e : 0;
+  }
   for (int e = t; e < E; e += kSchedThreads) s_mask[e] = 0ull;
   __syncthreads();
   for (int p = t; p < P; p += kSchedThreads) atomicOr(&s_mask[s_idx[p]], 1ull << (p / K));
@@ -163,8 +179,8 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_gather_kernel(
       s_off[e] = cpre;
       if (publish)
         for (int j = 0; j < grp[q]; ++j) {
-          grp_exp[gpre + j] = e;
-          grp_off[gpre + j] = cpre + j * kGroupTokens;
+          *DG_AT(status, grp_exp, gpre + j, groups_cap) = e;
+          *DG_AT(status, grp_off, gpre + j, groups_cap + 1) = cpre + j * kGroupTokens;
         }
     }
     cpre += cnt[q];
@@ -173,7 +189,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_gather_kernel(
   if (publish && t == kSchedThreads - 1) {
     int total = 0;
     for (int w2 = 0; w2 < kSchedThreads / 32; ++w2) total += s_warp[32 + w2];
-    grp_off[total] = P;
+    *DG_AT(status, grp_off, total, groups_cap + 1) = P;
     *nact = total;
   }
   __syncthreads();
@@ -183,9 +199,9 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_gather_kernel(
     const int e = s_idx[p];
     const unsigned long long below = (m == 0) ? 0ull : (s_mask[e] & ((1ull << m) - 1ull));
     const int pos = s_off[e] + __popcll(below);
-    s_tok[pos] = m;
+    *DG_AT(status, s_tok, pos, P) = m;
     if (publish) {
-      pair_tok[pos] = m;
+      *DG_AT(status, pair_tok, pos, P) = m;
       pair_of[p] = pos;
     }
   }
@@ -196,24 +212,43 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_gather_kernel(
        v += (long long)gridDim.x * kSchedThreads) {
     const int p = (int)(v / row_vecs);
     const int c = (int)(v - (long long)p * row_vecs);
-    xs[v] = x[(long long)s_tok[p] * row_vecs + c];
+    const int m = s_tok[p];
+    if constexpr (LATENT) {
+      const long long f0 = (long long)m * src_ld + E + (long long)c * 8;
+      const float* f = DG_AT(status, reinterpret_cast<const float*>(src), f0, src_len - 7);
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        w[q] = (uint32_t)f2bf_bits(__ldcg(f + 2 * q)) |
+               ((uint32_t)f2bf_bits(__ldcg(f + 2 * q + 1)) << 16);
+      xs[v] = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      xs[v] = *DG_AT(status, reinterpret_cast<const uint4*>(src), (long long)m * row_vecs + c,
+                     src_len);
+    }
   }
   griddep_launch_dependents();
 }
 
 cudaError_t launch_gather(const Ctx& cx, const void* x, int M, int H, int E, int k,
-                          const MoeBufs& b) {
+                          const MoeBufs& b, int L) {
   if (E > kMaxE || M * k > kMaxPairs) return cudaErrorInvalidValue;
-  const int row_vecs = H / 8;
+  const int row_vecs = (L > 0 ? L : H) / 8;
   const long long total = (long long)M * k * row_vecs;
   long long grid = (total + kSchedThreads - 1) / kSchedThreads;
   if (grid > cx.sms) grid = cx.sms;
   if (grid < 1) grid = 1;
   const int smem = E * 8 + E * 4 + 2 * M * k * 4;
-  return launch_k(schedule_gather_kernel, dim3((unsigned)grid), dim3(kSchedThreads), smem, cx.stream,
-                  cx.pdl, reinterpret_cast<const uint4*>(x), (const int*)b.topk, M, E, k,
-                  row_vecs, reinterpret_cast<uint4*>(b.xs), b.nact, b.grp_exp, b.grp_off,
-                  b.pair_tok, b.pair_of);
+  if (L > 0)
+    return launch_k(schedule_gather_kernel<true>, dim3((unsigned)grid), dim3(kSchedThreads), smem,
+                    cx.stream, cx.pdl, (const void*)b.logits, (long long)(E + L),
+                    (const int*)b.topk, M, E, k, row_vecs, reinterpret_cast<uint4*>(b.xs), b.nact,
+                    b.grp_exp, b.grp_off, b.pair_tok, b.pair_of, cx.status,
+                    (long long)M * (E + L), b.groups_cap);
+  return launch_k(schedule_gather_kernel<false>, dim3((unsigned)grid), dim3(kSchedThreads), smem,
+                  cx.stream, cx.pdl, x, (long long)0, (const int*)b.topk, M, E, k, row_vecs,
+                  reinterpret_cast<uint4*>(b.xs), b.nact, b.grp_exp, b.grp_off, b.pair_tok,
+                  b.pair_of, cx.status, (long long)M * row_vecs, b.groups_cap);
 }
 
 template <int XR>
@@ -246,13 +281,17 @@ static cudaError_t run_experts_w13(const Ctx& cx, const void* W13, int M, int H,
   a.w_up_offset = I;
   a.out = b.h;
   a.ldo = I;
+  a.out_len = (long long)M * k * I;
+  a.pairs = M * k;
+  a.groups_len = b.groups_cap;
   return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, xnarrow,
-                  a);
+                  wmap, xmap, a);
 }
 
 template <int XR>
 static cudaError_t run_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E, int k, int I,
-                                  const MoeBufs& b, int grid, float* ws, int* ctr) {
+                                  const MoeBufs& b, int grid, float* ws, int* ctr,
+                                  const DownExtras& dx) {
   // 256-row output tiles: two 128-row halves, 64 KB weight stages
   constexpr int SMEM = expert_pair_smem<XR>();
   auto kern = wstream_kernel<XR, kExpertPairStages, EPI_F32, false, true, true, ROLE_EXPERT>;
@@ -279,8 +318,35 @@ static cudaError_t run_experts_w2(const Ctx& cx, const void* W2, int M, int H, i
   a.tables_ready = 1;  // the gate/up kernel lets this one launch only after its own wait
   a.out = b.o;
   a.ldo = H;
+  a.out_len = (long long)M * k * H;
+  a.pairs = M * k;
+  a.groups_len = b.groups_cap;
+  // The shared expert's down projection as groups of at most XR tokens after
+  // the routed ones (its hidden rows b.hs, its output b.s).
+  CUtensorMap wmap2 = wmap, xmap2 = xmap;
+  if (dx.Ws2) {
+    if (!make_tmap(&wmap2, dx.Ws2, (uint64_t)H, (uint64_t)I, kTileRows, true) ||
+        !make_tmap(&xmap2, b.hs, (uint64_t)M, (uint64_t)I, XR, false))
+      return cudaErrorInvalidValue;
+    a.sh_groups = (M + XR - 1) / XR;
+    a.out2 = b.s;
+    a.out2_len = (long long)M * H;
+  }
+  if (dx.comb_out) {
+    a.comb_out = reinterpret_cast<uint16_t*>(dx.comb_out);
+    a.comb_res = reinterpret_cast<const uint16_t*>(dx.comb_res);
+    a.comb_gate = b.gate;
+    a.comb_pair_of = b.pair_of;
+    a.pair_tok = b.pair_tok;
+    a.comb_k = k;
+    a.comb_shared = dx.Ws2 ? 1 : 0;
+    a.comb_need = k + a.comb_shared;
+    a.comb_ctr = b.comb_ctr;
+    a.comb_len = (long long)M * H;
+    a.comb_ctr_len = (long long)(b.comb_ctr_bytes / sizeof(int));
+  }
   return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, xnarrow,
-                  a);
+                  wmap2, xmap2, a);
 }
 
 cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, int M, int H, int E,
@@ -291,9 +357,11 @@ cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, in
 }
 
 cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E, int k, int I,
-                              const MoeBufs& b, int grid, float* ws, int* ctr) {
-  if (M <= kNarrowRows) return run_experts_w2<kNarrowRows>(cx, W2, M, H, E, k, I, b, grid, ws, ctr);
-  return run_experts_w2<kGroupTokens>(cx, W2, M, H, E, k, I, b, grid, ws, ctr);
+                              const MoeBufs& b, int grid, float* ws, int* ctr,
+                              const DownExtras& dx) {
+  if (M <= kNarrowRows)
+    return run_experts_w2<kNarrowRows>(cx, W2, M, H, E, k, I, b, grid, ws, ctr, dx);
+  return run_experts_w2<kGroupTokens>(cx, W2, M, H, E, k, I, b, grid, ws, ctr, dx);
 }
 
 // Shared expert: a dense (ungrouped) pass over every token, token rows per
@@ -321,9 +389,11 @@ static cudaError_t run_shared_w13(const Ctx& cx, const void* x, const void* Ws13
   a.w_up_offset = I;
   a.out = b.hs;
   a.ldo = I;
+  a.out_len = (long long)M * I;
   const long long T = (long long)a.TILES * a.KB;
   if (grid > T) grid = (int)T;
-  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, xmap, a);
+  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, xmap, wmap,
+                  xmap, a);
 }
 
 template <int XR>
@@ -346,9 +416,11 @@ static cudaError_t run_shared_w2(const Ctx& cx, const void* Ws2, int M, int H, i
   a.M = M;
   a.out = b.s;
   a.ldo = H;
+  a.out_len = (long long)M * H;
   const long long T = (long long)a.TILES * a.KB;
   if (grid > T) grid = (int)T;
-  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, xmap, a);
+  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, xmap, wmap,
+                  xmap, a);
 }
 
 cudaError_t launch_shared_w13(const Ctx& cx, const void* x, const void* Ws13, int M, int H, int I,
@@ -367,14 +439,16 @@ cudaError_t launch_shared_w2(const Ctx& cx, const void* Ws2, int M, int H, int I
 
 // ------------------------------------------------------------------ combine
 // out[m,n] = bf16( res[m,n] + (sum_{j<k} g[m,j] * o[pair(m,j), n] + s[m,n]) ),
-// j summed in order 0..k-1, then the shared term, then the residual.
+// j summed in order 0..k-1, then the shared term, then the residual. Without
+// gates (gate == nullptr, k = 1) the sum is o[m, n] itself: the latent
+// block's up-projection plus the shared expert and the residual.
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ o,
                                                       const float* __restrict__ s,
                                                       const float* __restrict__ gate,
                                                       const int* __restrict__ pair_of,
                                                       const uint16_t* res,  // may alias out
                                                       uint16_t* out, int M, int H,
-                                                      int k) {
+                                                      int k, int* status, long long o_len) {
   griddep_launch_dependents();
   griddep_wait();
   const int per_row = H / 4;
@@ -385,9 +459,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     const int n = (int)(v - (long long)m * per_row) * 4;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < k; ++j) {
-      const float g = gate[m * k + j];
-      const int p = pair_of[m * k + j];
-      const float4 ov = *reinterpret_cast<const float4*>(o + (long long)p * H + n);
+      const float g = gate ? gate[m * k + j] : 1.0f;
+      const int p = gate ? pair_of[m * k + j] : m;
+      const float4 ov =
+          *reinterpret_cast<const float4*>(DG_AT(status, o, (long long)p * H + n, o_len - 3));
       acc[0] = fmaf(g, ov.x, acc[0]);
       acc[1] = fmaf(g, ov.y, acc[1]);
       acc[2] = fmaf(g, ov.z, acc[2]);
@@ -409,16 +484,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   }
 }
 
-cudaError_t launch_combine(const Ctx& cx, const MoeBufs& b, bool with_shared, const void* res,
-                           void* out, int M, int H, int k) {
+cudaError_t launch_combine_up(const Ctx& cx, const MoeBufs& b, bool with_shared, const void* res,
+                              void* out, int M, int H) {
   const long long total = (long long)M * (H / 4);
   int grid = (int)((total + 255) / 256);
   if (grid > 4 * cx.sms) grid = 4 * cx.sms;
   if (grid < 1) grid = 1;
-  return launch_k(combine_kernel, dim3(grid), dim3(256), 0, cx.stream, cx.pdl, (const float*)b.o,
-                  (const float*)(with_shared ? b.s : nullptr), (const float*)b.gate,
-                  (const int*)b.pair_of, reinterpret_cast<const uint16_t*>(res),
-                  reinterpret_cast<uint16_t*>(out), M, H, k);
+  return launch_k(combine_kernel, dim3(grid), dim3(256), 0, cx.stream, cx.pdl, (const float*)b.u,
+                  (const float*)(with_shared ? b.s : nullptr), (const float*)nullptr,
+                  (const int*)nullptr, reinterpret_cast<const uint16_t*>(res),
+                  reinterpret_cast<uint16_t*>(out), M, H, 1, cx.status, (long long)M * H);
 }
 
 // ------------------------------------------------------------------ residual add

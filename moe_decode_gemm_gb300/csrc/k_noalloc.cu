@@ -149,6 +149,8 @@ extern "C" int dec_linear_noalloc(const void* x, const void* W, void* y, int M, 
   cx.status = status;
   cx.stream = st;
   cx.pdl = true;
+  cx.ws_len = (long long)(kNoAllocPartBytes / sizeof(float));
+  cx.ctr_len = (long long)(kNoAllocCtrBytes / sizeof(int));
   const cudaError_t e = launch_dense(cx, xr, M > 2, false, x, W, nullptr, y, M, N, K, (int)grid,
                                      ws, ctr);
   return e == cudaSuccess ? DEC_OK : DEC_ECUDA;

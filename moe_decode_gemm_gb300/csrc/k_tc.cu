@@ -236,19 +236,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         } else {
           constexpr long long kSlotFloats = (long long)kTileRows * kTcXRows;
           const int slot = (gt == u0 / KB) ? 0 : 1;
-          float* mine = a.ws + (c * 2 + slot) * kSlotFloats;
+          const long long mine = (c * 2 + slot) * kSlotFloats;
 #pragma unroll
           for (int t = 0; t < kTcCols; ++t)
-            if (t0 + t < gi.c) __stcg(mine + (t0 + t) * kTileRows + r, v[t]);
+            if (t0 + t < gi.c)
+              __stcg(DG_AT(a.status, a.ws, mine + (t0 + t) * kTileRows + r, a.ws_len), v[t]);
           named_bar_sync(1, kTcEpi);
           const long long cf = cta_of(gt * KB, T, G);
           const long long cl = cta_of((gt + 1) * KB - 1, T, G);
           // barrier + release (and acquire + barrier on the last arriver)
           // order the partial slots; no separate fence needed
           if (et == 0) {
-            const int old = atomic_add_acq_rel_gpu(&a.ctr[gt], 1);
+            int* cp = DG_AT(a.status, a.ctr, gt, a.ctr_len);
+            const int old = atomic_add_acq_rel_gpu(cp, 1);
             const int is_last = (old == (int)(cl - cf)) ? 1 : 0;
-            if (is_last) a.ctr[gt] = 0;
+            if (is_last) *cp = 0;
             s_flags[1] = is_last;
           }
           named_bar_sync(1, kTcEpi);
@@ -270,7 +272,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               };
               // 4 items x 4 contributors: 16 loads in flight per thread
               reduce_partials<kTcEpi, false, kTileRows, 4, 4>(a.ws, kSlotFloats, nc, gi.c, et,
-                                                              slot_at, store);
+                                                              slot_at, store, a.ws_len, a.status);
             }
           }
           named_bar_sync(1, kTcEpi);
@@ -500,6 +502,8 @@ static cudaError_t run_tc_cluster(const Ctx& cx, const void* x, const void* W, c
   a.ldo = N;
   a.res = reinterpret_cast<const uint16_t*>(res);
   a.status = cx.status;
+  a.out_len = (long long)M * N;
+  a.res_len = res ? (long long)M * N : 0;
   a.timeout_ns = cx.timeout_ns;
   return launch_kc(kern, dim3(a.TILES * cl), dim3(kTcThreads), SMEM, cx.stream, cx.pdl, cl, wmap,
                    xmap, a, NP, umma_idesc_bf16(128, NP));
@@ -538,6 +542,10 @@ static cudaError_t run_tc(const Ctx& cx, const void* x, const void* W, const voi
   a.ws = ws;
   a.ctr = ctr;
   a.status = cx.status;
+  a.out_len = (long long)M * N;
+  a.res_len = res ? (long long)M * N : 0;
+  a.ws_len = cx.ws_len;
+  a.ctr_len = cx.ctr_len;
   a.timeout_ns = cx.timeout_ns;
   return launch_k(kern, dim3(grid), dim3(kTcThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a, NP,
                   umma_idesc_bf16(128, NP));

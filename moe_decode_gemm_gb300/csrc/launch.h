@@ -19,6 +19,9 @@ struct Ctx {
   cudaStream_t stream;
   bool pdl;
   long long ldx = 0;  // dense projections: elements between rows of x (0: K)
+  // extents of the split-K workspace given to a launch (floats, ints): the
+  // index checks of a DEC_DEBUG build test against them
+  long long ws_len = 0, ctr_len = 0;
 };
 
 // Dense projection: y = x·Wᵀ (+ res), XR in {8, 16, 64} token rows per stage.
@@ -62,6 +65,22 @@ struct MoeBufs {
   uint16_t* hs;    // [M, I]
   float* s;        // [M, H]
   int* route_ctr;  // router clusters arrived (zero at rest)
+  uint16_t* z;     // latent block: [M, L] gate-weighted sum of the experts, bf16
+  float* u;        // latent block: [M, H] its up-projection, fp32
+  int* comb_ctr;   // [M][tiles of the down projection] combine arrivals (zero at rest)
+  size_t comb_ctr_bytes;
+  int groups_cap;  // entries of grp_exp (grp_off has one more)
+};
+
+// What the routed down projection does besides its own groups: the shared
+// expert's down projection folded in as extra groups (Ws2 non-null; its
+// hidden rows b.hs must be complete when the kernel starts), and the combine
+// fused into its epilogue (comb_out non-null: out = bf16(res + (sum_j g_j o_j
+// (+ the shared expert's output))), res nullable).
+struct DownExtras {
+  const void* Ws2 = nullptr;
+  void* comb_out = nullptr;
+  const void* comb_res = nullptr;
 };
 
 // Router: CTAs per 128-row tile of experts (one thread-block cluster each),
@@ -72,22 +91,34 @@ inline int router_clusters(int H) {
 }
 inline int router_ctas(int E, int H) { return (E + 127) / 128 * router_clusters(H); }
 
-// Router scores and, in the same kernel, the top-k experts and gates.
+// Router scores and, in the same kernel, the top-k experts and gates. With
+// L > 0 the weight stacks the E router rows on the latent input projection's
+// L rows (one product, [M, E + L] fp32 into b.logits); the top-k ranks the
+// first E columns.
 cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E, int k,
-                          int32_t* idx_user, float* w_user, const MoeBufs& b);
+                          int32_t* idx_user, float* w_user, const MoeBufs& b, int L = 0);
+// Schedule + gather of the token rows (width H, bf16 from x); with L > 0 the
+// rows are the latent inputs instead: columns E..E+L-1 of b.logits rounded to
+// bf16 (width L).
 cudaError_t launch_gather(const Ctx& cx, const void* x, int M, int H, int E, int k,
-                          const MoeBufs& b);
+                          const MoeBufs& b, int L = 0);
 // grid: CTAs (the expert kernels split their work statically over them).
 cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, int M, int H, int E,
                                int k, int I, const MoeBufs& b, int grid, float* ws, int* ctr);
 cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E, int k, int I,
-                              const MoeBufs& b, int grid, float* ws, int* ctr);
+                              const MoeBufs& b, int grid, float* ws, int* ctr,
+                              const DownExtras& dx = DownExtras());
 cudaError_t launch_shared_w13(const Ctx& cx, const void* x, const void* Ws13, int M, int H, int I,
                               const MoeBufs& b, int grid, float* ws, int* ctr);
 cudaError_t launch_shared_w2(const Ctx& cx, const void* Ws2, int M, int H, int I,
                              const MoeBufs& b, int grid, float* ws, int* ctr);
-cudaError_t launch_combine(const Ctx& cx, const MoeBufs& b, bool with_shared, const void* res,
-                           void* out, int M, int H, int k);
+// out = bf16(res + (u + s)) over [M, H]: the latent block's last step (s the
+// shared expert's output when with_shared, res nullable).
+cudaError_t launch_combine_up(const Ctx& cx, const MoeBufs& b, bool with_shared, const void* res,
+                              void* out, int M, int H);
+// Dense projection with an fp32 output (no residual): stream-K over `grid` CTAs.
+cudaError_t launch_dense_f32(const Ctx& cx, int xr, bool mma, const void* x, const void* W,
+                             float* y, int M, int N, int K, int grid, float* ws, int* ctr);
 cudaError_t launch_add(const Ctx& cx, const void* a, const void* b, void* out, size_t n);
 cudaError_t launch_prefetch(const Ctx& cx, const void* ptr, size_t bytes);
 cudaError_t launch_selftest_timeout(const Ctx& cx, long long ns);

@@ -58,7 +58,7 @@ constexpr int kPrefetchBytes = 256 * 1024;
 // slack, the stage ring, full/empty barriers, flags, slot table, and `extra`.
 constexpr int wstream_smem(int xr, int stages, int extra, bool paired = false) {
   return 1024 + stages * ((paired ? 2 : 1) * kWBytes + kKSub * xr * 128) + 2 * 8 * stages + 32 +
-         4 * kMaxSlots + extra;
+         4 * kMaxSlots + 4 * kGroupTokens + extra;
 }
 
 struct StreamArgs {
@@ -85,33 +85,80 @@ struct StreamArgs {
   int* ctr;                  // per output tile arrival counters (zero at rest)
   int* status;
   long long timeout_ns;
+  // grouped mode: sh_groups more groups after the routed ones -- the shared
+  // expert's down projection, groups of at most XR tokens (token t of group i
+  // is token i*XR + t) -- whose weights come through wmap2, whose token rows
+  // through xmap2, and whose output goes to out2 ([M, ldo] fp32)
+  int sh_groups;
+  float* out2;
+  // combine fused into a grouped down projection (comb_out non-null): when the
+  // last of comb_need contributions to (token m, output tile) is written --
+  // one per routed (token, slot) pair, plus the shared expert's -- the CTA
+  // that wrote it computes, for that token's tile,
+  //   comb_out[m, n] = bf16(comb_res[m, n] + (sum_{j<comb_k} g[m,j] * out[pair_of[m,j], n]
+  //                                          + out2[m, n]))
+  // in that order (the shared and residual terms only when present).
+  uint16_t* comb_out;
+  const uint16_t* comb_res;
+  const float* comb_gate;    // [M][comb_k]
+  const int* comb_pair_of;   // [M][comb_k]
+  const int* pair_tok;       // pair -> token
+  int comb_k;
+  int comb_need;
+  int comb_shared;           // out2 holds the shared expert's output
+  int* comb_ctr;             // [M][TILES] arrivals (zero at rest)
   // router role: with route_k > 0 the last cluster to finish its logits
   // selects every token's top route_k experts and their gates
   int route_k;
+  int route_E;               // scores the top-k ranks: columns 0..route_E-1 of each row
   int* route_ctr;            // arrival counter (zero at rest)
   int* route_idx;            // [M][route_k]
   float* route_gate;         // [M][route_k]
   int32_t* route_idx_user;   // optional copies for the caller
   float* route_w_user;
+  // extents (elements) of the buffers above, checked by the index checks of
+  // a DEC_DEBUG build: out, out2, res, ws (floats), ctr, comb_out/comb_res,
+  // comb_ctr; pairs = rows of the pair tables (grouped: M*k; router: M*k of
+  // route_idx); groups_len = entries of grp_exp (grp_off has one more)
+  long long out_len, out2_len, res_len, ws_len, ctr_len, comb_len, comb_ctr_len;
+  int pairs, groups_len;
 };
 
 struct GroupInfo {
-  int e;       // expert id (0 in dense mode)
-  int p0;      // first output row (pair) of the group
+  int e;       // expert id (0 in dense mode and for the shared expert)
+  int p0;      // first output row (pair, or token for the shared expert) of the group
   int c;       // tokens in the group
+  int sh;      // the shared expert's down projection (grouped mode)
 };
 
+// Group g of nr routed groups; groups nr.. are the shared expert's, gsz
+// tokens each.
 template <bool GROUPED>
-__device__ __forceinline__ GroupInfo load_group(const StreamArgs& a, int g) {
+__device__ __forceinline__ GroupInfo load_group(const StreamArgs& a, int g, int nr = 0,
+                                                int gsz = 0) {
   GroupInfo gi;
   if (GROUPED) {
-    gi.e = a.grp_exp[g];
-    gi.p0 = a.grp_off[g];
-    gi.c = a.grp_off[g + 1] - gi.p0;
+    if (g >= nr) {
+      gi.e = 0;
+      gi.p0 = (g - nr) * gsz;
+      gi.c = a.M - gi.p0 < gsz ? a.M - gi.p0 : gsz;
+      gi.sh = 1;
+    } else {
+      gi.e = *DG_AT(a.status, a.grp_exp, g, a.groups_len);
+      gi.p0 = *DG_AT(a.status, a.grp_off, g, a.groups_len + 1);
+      gi.c = *DG_AT(a.status, a.grp_off, g + 1, a.groups_len + 1) - gi.p0;
+      gi.sh = 0;
+      if (!DG_OK(a.status, gi.p0 >= 0 && gi.c >= 0 && gi.p0 + gi.c <= a.pairs && gi.c <= gsz,
+                 (long long)gi.c * 1000000 + gi.p0)) {
+        gi.p0 = 0;
+        gi.c = 0;
+      }
+    }
   } else {
     gi.e = 0;
     gi.p0 = 0;
     gi.c = a.M;
+    gi.sh = 0;
   }
   return gi;
 }
@@ -150,13 +197,15 @@ template <int EPI, bool GROUPED>
 __device__ __forceinline__ void store_out(const StreamArgs& a, const GroupInfo& gi, int t, int n,
                                           float v) {
   const long long row = (long long)gi.p0 + t;
+  const long long i = row * a.ldo + n;
   if (EPI == EPI_F32) {
-    reinterpret_cast<float*>(a.out)[row * a.ldo + n] = v;
+    if (GROUPED && gi.sh) *DG_AT(a.status, a.out2, i, a.out2_len) = v;
+    else *DG_AT(a.status, reinterpret_cast<float*>(a.out), i, a.out_len) = v;
   } else if (EPI == EPI_BF16_RES) {
-    const float r = bf_bits2f(a.res[row * a.ldo + n]);
-    reinterpret_cast<uint16_t*>(a.out)[row * a.ldo + n] = f2bf_bits(r + v);
+    const float r = bf_bits2f(*DG_AT(a.status, a.res, i, a.res_len));
+    *DG_AT(a.status, reinterpret_cast<uint16_t*>(a.out), i, a.out_len) = f2bf_bits(r + v);
   } else {
-    reinterpret_cast<uint16_t*>(a.out)[row * a.ldo + n] = f2bf_bits(v);
+    *DG_AT(a.status, reinterpret_cast<uint16_t*>(a.out), i, a.out_len) = f2bf_bits(v);
   }
 }
 
@@ -164,7 +213,7 @@ __device__ __forceinline__ void store_swiglu(const StreamArgs& a, const GroupInf
                                              float gate, float up) {
   const long long row = (long long)gi.p0 + t;
   const float h = silu_f(gate) * up;
-  reinterpret_cast<uint16_t*>(a.out)[row * a.ldo + i] = f2bf_bits(h);
+  *DG_AT(a.status, reinterpret_cast<uint16_t*>(a.out), row * a.ldo + i, a.out_len) = f2bf_bits(h);
 }
 
 // ------------------------------------------------------------------ routing tail
@@ -178,9 +227,12 @@ __device__ __forceinline__ void store_swiglu(const StreamArgs& a, const GroupInf
 // A round loads EB items from JB contributors at once, so each thread keeps
 // EB x JB loads in flight (twice that for SwiGLU tiles); each item's
 // contributions are still added in contributor order.
+// ws_len and st: the workspace's extent in floats and the status word, for
+// the index checks of a DEC_DEBUG build.
 template <int NT, bool PAIRED, int STRIDE, int EB, int JB, typename Slot, typename Store>
 __device__ __forceinline__ void reduce_partials(const float* ws, long long slot_floats, int nc,
-                                                int c, int tid, Slot slot_of, Store store) {
+                                                int c, int tid, Slot slot_of, Store store,
+                                                long long ws_len, int* st) {
   constexpr int R4 = (PAIRED ? kTileRows : STRIDE) / 4;  // output rows per token, in fours
   const int nel4 = R4 * c;
   for (int base = 0; base < nel4; base += NT * EB) {
@@ -206,12 +258,14 @@ __device__ __forceinline__ void reduce_partials(const float* ws, long long slot_
 #pragma unroll
       for (int jj = 0; jj < JB; ++jj) {
         if (j + jj < nc) {
-          const float* b = ws + slot_of(j + jj) * slot_floats;
+          const long long b = slot_of(j + jj) * slot_floats;
 #pragma unroll
           for (int q = 0; q < EB; ++q) {
             if (ok[q]) {
-              pg[jj][q] = __ldcg(reinterpret_cast<const float4*>(b + off[q]));
-              if (PAIRED) pu[jj][q] = __ldcg(reinterpret_cast<const float4*>(b + off[q] + kTileRows));
+              pg[jj][q] = __ldcg(reinterpret_cast<const float4*>(DG_AT(st, ws, b + off[q], ws_len - 3)));
+              if (PAIRED)
+                pu[jj][q] = __ldcg(reinterpret_cast<const float4*>(
+                    DG_AT(st, ws, b + off[q] + kTileRows, ws_len - 3)));
             }
           }
         }
@@ -281,7 +335,10 @@ template <int XR, int STAGES, int EPI, bool PAIRED, bool GROUPED, bool WIDE = fa
           int ROLE = ROLE_PROJECTION, int MINB = 1, bool CLUSTER = false, int PATH = PATH_ANY>
 __global__ void __launch_bounds__(kThreads, MINB)
     wstream_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
-                   const __grid_constant__ CUtensorMap xmap_narrow, const StreamArgs a) {
+                   const __grid_constant__ CUtensorMap xmap_narrow,
+                   const __grid_constant__ CUtensorMap wmap2,
+                   const __grid_constant__ CUtensorMap xmap2, const StreamArgs a) {
+  static_assert(!GROUPED || XR <= kGroupTokens, "a group's tokens fit the fused-combine table");
   constexpr int H2 = (PAIRED || WIDE) ? 2 : 1;  // 128-row weight halves per box column
   // CUDA-core dot form. Both give the same bits. The bf16-operand form
   // (fma.rn.f32.bf16) issues half the instructions; the widened form is kept
@@ -303,6 +360,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
   // [0] abort [1] last arriver of a split tile [2] last cluster of the router
   volatile int* s_flags = reinterpret_cast<volatile int*>(empty + STAGES);
   int* s_slot = const_cast<int*>(s_flags) + 8;                                 // [kMaxSlots]
+  int* s_comb = s_slot + kMaxSlots;                                            // [kGroupTokens]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -321,6 +379,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
     prefetch_tmap(&wmap);
     prefetch_tmap(&xmap);
     if (GROUPED && XR > kNarrowRows) prefetch_tmap(&xmap_narrow);
+    if (GROUPED && a.sh_groups > 0) {
+      prefetch_tmap(&wmap2);
+      prefetch_tmap(&xmap2);
+    }
   }
   __syncthreads();
   // Kernels that can stream weights before their predecessor finishes let
@@ -335,12 +397,14 @@ __global__ void __launch_bounds__(kThreads, MINB)
   const int KB = a.KB, TILES = a.TILES;
 
   long long T;
+  int nr = 0;  // routed groups (grouped mode)
   if (GROUPED) {
     if (!early) {
       griddep_wait();
       griddep_launch_dependents();
     }
-    T = (long long)(*a.nact) * TILES * KB;
+    nr = *a.nact;
+    T = (long long)(nr + a.sh_groups) * TILES * KB;
   } else {
     T = (long long)TILES * KB;
   }
@@ -368,26 +432,27 @@ __global__ void __launch_bounds__(kThreads, MINB)
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
       int gcur = -1;
-      GroupInfo gi{0, 0, 0};
+      GroupInfo gi{0, 0, 0, 0};
       // Unit positions advance one unit at a time: no 64-bit division per
       // stage on the path that refills the ring.
       auto issue_w = [&](int s, const UnitPos& p) {
         uint8_t* wdst = smem + s * kStageBytes;
+        const CUtensorMap* wm = GROUPED && gi.sh ? &wmap2 : &wmap;
         const int rbase = gi.e * a.w_group_rows;
 #pragma unroll
         for (int sb = 0; sb < kKSub; ++sb) {
           const int k0 = (p.kc * kKSub + sb) * kKBlk;
           uint8_t* d = wdst + sb * H2 * kWSub;
-          tma_load_2d(d, &wmap, k0, rbase + p.tile * kTileOut, &full[s], pol_w);
+          tma_load_2d(d, wm, k0, rbase + p.tile * kTileOut, &full[s], pol_w);
           if (H2 == 2)
-            tma_load_2d(d + kWSub, &wmap, k0,
+            tma_load_2d(d + kWSub, wm, k0,
                         rbase + (PAIRED ? a.w_up_offset + p.tile * kTileRows
                                         : p.tile * kTileOut + kTileRows),
                         &full[s], pol_w);
         }
       };
       auto narrow_group = [&](const GroupInfo& g_) {
-        return GROUPED && XR > kNarrowRows && g_.c <= kNarrowRows;
+        return GROUPED && XR > kNarrowRows && g_.c <= kNarrowRows && !g_.sh;
       };
       auto issue_x = [&](int s, int kc, const GroupInfo& g_) {
         uint8_t* xdst = smem + s * kStageBytes + kWStage;
@@ -399,19 +464,20 @@ __global__ void __launch_bounds__(kThreads, MINB)
           // tensor (pairs are stored in expert order), so one box of XR rows
           // at the group's first pair covers them; rows past the group are
           // never read.
-          tma_load_2d(d, narrow_group(g_) ? &xmap_narrow : &xmap, k0, GROUPED ? g_.p0 : 0,
-                      &full[s], pol_x);
+          tma_load_2d(d, GROUPED && g_.sh ? &xmap2 : narrow_group(g_) ? &xmap_narrow : &xmap, k0,
+                      GROUPED ? g_.p0 : 0, &full[s], pol_x);
         }
       };
-      // The same weight boxes as issue_w for expert e, into L2 only.
-      auto prefetch_w = [&](const UnitPos& p, int e) {
-        const int rbase = e * a.w_group_rows;
+      // The same weight boxes as issue_w for group g_, into L2 only.
+      auto prefetch_w = [&](const UnitPos& p, const GroupInfo& g_) {
+        const CUtensorMap* wm = GROUPED && g_.sh ? &wmap2 : &wmap;
+        const int rbase = g_.e * a.w_group_rows;
 #pragma unroll
         for (int sb = 0; sb < kKSub; ++sb) {
           const int k0 = (p.kc * kKSub + sb) * kKBlk;
-          tma_prefetch_2d(&wmap, k0, rbase + p.tile * kTileOut);
+          tma_prefetch_2d(wm, k0, rbase + p.tile * kTileOut);
           if (H2 == 2)
-            tma_prefetch_2d(&wmap, k0,
+            tma_prefetch_2d(wm, k0,
                             rbase + (PAIRED ? a.w_up_offset + p.tile * kTileRows
                                             : p.tile * kTileOut + kTileRows));
         }
@@ -430,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         for (; i < npre; ++i, pos.next(KB, TILES)) {
           if (pos.g != gcur) {
             gcur = pos.g;
-            gi = load_group<GROUPED>(a, pos.g);
+            gi = load_group<GROUPED>(a, pos.g, nr, XR);
           }
           pg[i] = gi;
           mbar_arrive_expect_tx(&full[i], tx_bytes(gi));
@@ -442,14 +508,15 @@ __global__ void __launch_bounds__(kThreads, MINB)
         // (not in cluster mode: there the shares are small and it did not pay)
         constexpr int kPfUnits = CLUSTER ? 0 : kPrefetchBytes / kWStage;
         const int npf = nunits - npre < kPfUnits ? nunits - npre : kPfUnits;
-        int pgrp = -1, pexp = 0;
+        int pgrp = -1;
+        GroupInfo pgi{0, 0, 0, 0};
         UnitPos pp = pos;
         for (int j = 0; j < npf; ++j, pp.next(KB, TILES)) {
           if (pp.g != pgrp) {
             pgrp = pp.g;
-            pexp = load_group<GROUPED>(a, pp.g).e;
+            pgi = load_group<GROUPED>(a, pp.g, nr, XR);
           }
-          prefetch_w(pp, pexp);
+          prefetch_w(pp, pgi);
         }
         griddep_wait();
         UnitPos px = pos0;
@@ -467,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         if (GROUPED && pos.g != gcur) {
           // new expert group: read its id and pair range once
           gcur = pos.g;
-          gi = load_group<GROUPED>(a, pos.g);
+          gi = load_group<GROUPED>(a, pos.g, nr, XR);
         }
         mbar_arrive_expect_tx(&full[s], tx_bytes(gi));
         issue_w(s, pos);
@@ -504,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     float dacc[H2][4][2];
     float macc[H2][XR / 8][4];
     long long cur = -1;
-    GroupInfo gi{0, 0, 0};
+    GroupInfo gi{0, 0, 0, 0};
     bool use_mma = false;
 
     auto zero_acc = [&]() {
@@ -587,9 +654,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
     // to its workspace slot as [token][kSlotStride] fp32.
     // Partial tiles go to global memory (L2) for the split-K fixup, or to
     // this CTA's shared memory in cluster mode.
-    auto put = [](float* p, float v) {
+    auto put = [&](float* p, float v) {
       if (CLUSTER) *p = v;
-      else __stcg(p, v);
+      else __stcg(DG_AT(a.status, a.ws, p - a.ws, a.ws_len), v);
     };
     auto write_partial = [&](float* mine) {
       if (!use_mma) {
@@ -648,7 +715,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
         constexpr int kEB = reduce_eb(kNCW * 32, PAIRED, kSlotStride, XR, kLoads);
         constexpr int kJB = reduce_jb(PAIRED, kEB, kLoads);
         reduce_partials<kNCW * 32, PAIRED, kSlotStride, kEB, kJB>(a.ws, kSlotFloats, nc, gi.c, ct,
-                                                                  slot_at, store);
+                                                                  slot_at, store, a.ws_len,
+                                                                  a.status);
       }
     };
 
@@ -657,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     // the counter for the next call.
     auto settle = [&](long long gt, int old) {
       const int is_last = (old == (int)(last_cta(gt) - first_cta(gt))) ? 1 : 0;
-      if (is_last) a.ctr[gt] = 0;
+      if (is_last) *DG_AT(a.status, a.ctr, gt, a.ctr_len) = 0;
       s_flags[1] = is_last;
     };
 
@@ -667,7 +735,49 @@ __global__ void __launch_bounds__(kThreads, MINB)
     // read, and the tile reduced if this CTA arrived last, after the range.
     long long dgt = -1;  // deferred tile
     int dold = 0;        // its counter's value before this CTA's increment (thread 0)
-    GroupInfo dgi{0, 0, 0};
+    GroupInfo dgi{0, 0, 0, 0};
+
+    // Fused combine (grouped down projection with comb_out): called by every
+    // consumer thread once the final values of tile gt of group g_ are
+    // written. Each token of the group arrives on its (token, tile) counter;
+    // the CTA whose arrival completes a counter sums that token's tile.
+    auto combine_tile = [&](long long gt, const GroupInfo& g_) {
+      if (!GROUPED || a.comb_out == nullptr) return;
+      const int tile = (int)(gt % TILES);
+      // every thread's output stores of the tile are ordered before the
+      // arrivals' release (barrier, then acq_rel atomics); the acquire side
+      // plus the next barrier order the reads below after the other CTAs'
+      named_bar_sync(1, kNCW * 32);
+      if (ct < g_.c) {
+        const int m = g_.sh ? g_.p0 + ct : *DG_AT(a.status, a.pair_tok, g_.p0 + ct, a.pairs);
+        int* cp = DG_AT(a.status, a.comb_ctr, (long long)m * TILES + tile, a.comb_ctr_len);
+        const int old = atomic_add_acq_rel_gpu(cp, 1);
+        const bool last = old == a.comb_need - 1;
+        if (last) *cp = 0;
+        s_comb[ct] = last ? m : -1;
+      }
+      named_bar_sync(1, kNCW * 32);
+      const float* o = reinterpret_cast<const float*>(a.out);
+      for (int t = 0; t < g_.c; ++t) {
+        const int m = s_comb[t];
+        if (m < 0) continue;
+        for (int r = ct; r < kTileOut; r += kNCW * 32) {
+          const int n = tile * kTileOut + r;
+          if (n >= a.nout) continue;
+          float acc = 0.f;
+          for (int j = 0; j < a.comb_k; ++j) {
+            const float gj = __ldg(DG_AT(a.status, a.comb_gate, m * a.comb_k + j, a.pairs));
+            const int p = __ldg(DG_AT(a.status, a.comb_pair_of, m * a.comb_k + j, a.pairs));
+            acc = fmaf(gj, __ldcg(DG_AT(a.status, o, (long long)p * a.ldo + n, a.out_len)), acc);
+          }
+          const long long i = (long long)m * a.ldo + n;
+          if (a.comb_shared) acc += __ldcg(DG_AT(a.status, a.out2, i, a.out2_len));
+          if (a.comb_res) acc = bf_bits2f(*DG_AT(a.status, a.comb_res, i, a.comb_len)) + acc;
+          *DG_AT(a.status, a.comb_out, i, a.comb_len) = f2bf_bits(acc);
+        }
+      }
+      named_bar_sync(1, kNCW * 32);  // s_comb is reused by the next tile
+    };
 
     auto finish_tile = [&](long long gt, bool defer) {
       const int tile = (int)(gt % TILES);
@@ -676,6 +786,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
       const bool whole = (u0 <= gt * KB) && ((gt + 1) * KB <= u1);
       if (whole) {
         if (!aborted) reg_epilogue(tile);
+        combine_tile(gt, gi);
       } else {
         const int slot = (gt == u0 / KB) ? 0 : 1;
         write_partial(a.ws + (c * 2 + slot) * kSlotFloats);
@@ -685,14 +796,17 @@ __global__ void __launch_bounds__(kThreads, MINB)
         // every contributor's release. No separate fence needed.
         named_bar_sync(1, kNCW * 32);
         if (defer) {
-          if (ct == 0) dold = atomic_add_acq_rel_gpu(&a.ctr[gt], 1);
+          if (ct == 0) dold = atomic_add_acq_rel_gpu(DG_AT(a.status, a.ctr, gt, a.ctr_len), 1);
           dgt = gt;
           dgi = gi;
           return;
         }
-        if (ct == 0) settle(gt, atomic_add_acq_rel_gpu(&a.ctr[gt], 1));
+        if (ct == 0) settle(gt, atomic_add_acq_rel_gpu(DG_AT(a.status, a.ctr, gt, a.ctr_len), 1));
         named_bar_sync(1, kNCW * 32);
-        if (s_flags[1]) reduce_tile(gt, aborted);
+        if (s_flags[1]) {
+          reduce_tile(gt, aborted);
+          combine_tile(gt, gi);
+        }
       }
       named_bar_sync(1, kNCW * 32);  // partial slots and flags may be reused next tile
     };
@@ -710,7 +824,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         if (cur >= 0) finish_tile(cur, cur == u0 / KB);
         cur = gt;
         zero_acc();
-        gi = load_group<GROUPED>(a, (int)(gt / TILES));
+        gi = load_group<GROUPED>(a, (int)(gt / TILES), nr, XR);
         use_mma = PATH == PATH_ANY && gi.c >= a.mma_min_tokens;
       }
       const int s = i % STAGES;
@@ -843,7 +957,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
         if (s_flags[2]) {
           const int K = a.route_k;
           for (int m = cr * kNCW + w; m < a.M; m += cs * kNCW)
-            warp_topk_gates(reinterpret_cast<const float*>(a.out) + (long long)m * a.ldo, a.nout,
+            if (DG_OK(a.status, (long long)(m + 1) * K <= a.pairs &&
+                                    (long long)m * a.ldo + a.route_E <= a.out_len, m))
+              warp_topk_gates(reinterpret_cast<const float*>(a.out) + (long long)m * a.ldo, a.route_E,
                             K, lane, a.route_idx + m * K, a.route_gate + m * K,
                             a.route_idx_user ? a.route_idx_user + m * K : nullptr,
                             a.route_w_user ? a.route_w_user + m * K : nullptr);
@@ -858,6 +974,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
       if (s_flags[1]) {
         gi = dgi;
         reduce_tile(dgt, s_flags[0] != 0);
+        combine_tile(dgt, gi);
       }
     }
   }

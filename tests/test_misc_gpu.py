@@ -64,3 +64,44 @@ def test_probe_times_projection_launches():
         dg.dec_linear(x, W)
     ms, n = dg.probe_end()
     assert n == 5 and ms > 0.0
+
+
+def test_kernels_per_moe_block_and_per_layer():
+    # the MoE block with a shared expert is five launches: the shared expert's
+    # gate/up (side stream), the router with the top-k, schedule + gather, the
+    # routed gate/up, and the routed down projection with the shared expert's
+    # down projection and the combine in its epilogue; four without a shared
+    # expert. A decode layer adds the fused q|kv and the o projection and the
+    # L2 prefetch: eight.
+    import math
+    from moe_decode_gemm_gb300.stack import decode_layer
+
+    M, H, KV, E, I, k = 4, 256, 64, 32, 128, 4
+    t = wl.bits_to_torch
+    g = lambda *s, std=0.02, key="": t(wl.normal_bf16(s, std, "count", key, *s))
+    x = g(M, H, std=1.0, key="x")
+    Wr = g(E, H, std=1.0 / math.sqrt(H), key="Wr")
+    W13, W2 = g(E, 2 * I, H, key="W13"), g(E, H, I, key="W2")
+    Ws13, Ws2 = g(2 * I, H, key="Ws13"), g(H, I, key="Ws2")
+    dg.moe_decode(x, Wr, W13, W2, Ws13, Ws2, k)        # workspace set up
+    assert dg.sync_check() == dg.DEC_OK
+    n0 = dg.launch_count()
+    dg.moe_decode(x, Wr, W13, W2, Ws13, Ws2, k)
+    assert dg.launch_count() - n0 == 5
+    n0 = dg.launch_count()
+    dg.moe_decode(x, Wr, W13, W2, None, None, k)
+    assert dg.launch_count() - n0 == 4
+
+    class L:
+        pass
+    L.Wqkv, L.Wo, L.Wr, L.W13, L.W2, L.Ws13, L.Ws2 = g(H + KV, H, key="qkv"), g(H, H, key="o"), \
+        Wr, W13, W2, Ws13, Ws2
+    bufs = [torch.empty((M, n), dtype=torch.bfloat16, device="cuda") for n in (H + KV, H, H)]
+    side, ev = torch.cuda.Stream(), torch.cuda.Event()
+    decode_layer(L, x, *bufs, k, prefetch=(side, ev, L.Wqkv.data_ptr(), 1 << 20))
+    torch.cuda.synchronize()
+    n0 = dg.launch_count()
+    decode_layer(L, x, *bufs, k, prefetch=(side, ev, L.Wqkv.data_ptr(), 1 << 20))
+    torch.cuda.synchronize()
+    assert dg.launch_count() - n0 == 8
+    assert dg.sync_check() == dg.DEC_OK

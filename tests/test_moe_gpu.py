@@ -272,3 +272,16 @@ def test_decode_layer_replays_from_a_cuda_graph():
         torch.cuda.synchronize()
         assert torch.equal(out, eager)
     assert dg.sync_check() == dg.DEC_OK
+
+
+def test_workspace_relayout_within_its_capacity():
+    # A larger block that still fits the workspace allocated for a smaller one
+    # (it is allocated with slack) changes the workspace's layout without a
+    # new allocation: the arrival counters must still start at zero. Three
+    # blocks of growing E, each checked against the oracle. The workspace is
+    # freed first, so that the first block sizes it.
+    torch.cuda.synchronize()
+    dg.shutdown()
+    for E in (40, 44, 48):
+        blk = _small_block(6, 192, E, 96, 4, ("moe-relayout", E))
+        _check(*blk, 4, "E=%d after a smaller block" % E)
