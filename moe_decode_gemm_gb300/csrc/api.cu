@@ -333,8 +333,6 @@ static int moe_bufs(DevState* s, int M, int H, int E, int k, int I, int L, cudaS
   size_t o_rctr = off; off += al(4);
   size_t o_z = off; off += al((size_t)Mx * (Lx > 0 ? Lx : 1) * 2);
   size_t o_u = off; off += al((size_t)Mx * Hx * 4);
-  const size_t comb_bytes = (size_t)Mx * ((Wx + 255) / 256) * 4;
-  size_t o_comb = off; off += al(comb_bytes);
   int rc = ensure(s->moe, off, st);
   if (rc) return rc;
   // The layout has changed even when the buffer did not have to grow (its
@@ -359,8 +357,6 @@ static int moe_bufs(DevState* s, int M, int H, int E, int k, int I, int L, cudaS
   s->mb.route_ctr = (int*)(b + o_rctr);
   s->mb.z = (uint16_t*)(b + o_z);
   s->mb.u = (float*)(b + o_u);
-  s->mb.comb_ctr = (int*)(b + o_comb);
-  s->mb.comb_ctr_bytes = comb_bytes;
   s->mb.groups_cap = (int)Gx;
   s->moe_M = Mx;
   s->moe_L = Lx;
@@ -398,7 +394,7 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   int maxt = tiles13 > tiles2 ? tiles13 : tiles2;
   // an expert chosen by more tokens than a group holds forms several groups:
   // at most E + M*topk/16 groups, each with its own tile counters
-  const int max_groups = E + (M * topk + 15) / 16 + (M + 15) / 16;  // + the shared expert's
+  const int max_groups = E + (M * topk + 15) / 16;
   const size_t ctr_bytes = (size_t)(max_groups * (size_t)maxt + 64) * sizeof(int);
   if ((rc = ensure(s->ws_main, ws_bytes, st))) return rc;
   if ((rc = ensure(s->ctr_main, ctr_bytes, st))) return rc;
@@ -413,14 +409,12 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   float* ws = (float*)s->ws_main.p;
   int* ctr = (int*)s->ctr_main.p;
   // Shared expert, forked first to the side stream (lowest priority), one CTA
-  // on each SM the router leaves free, so its gate/up weights stream while
-  // the latency-bound router, top-k and gather run on the other SMs. The
-  // routed experts take the SMs as the shared expert's CTAs leave them. Its
-  // down projection runs inside the routed down projection, as extra groups,
-  // so the streams join before that kernel; the combine is that kernel's
-  // epilogue. (In the latent block the down projection stays on the side
-  // stream -- its output width is H, the routed one's L -- and the streams
-  // join before the final sum.)
+  // on each SM the router leaves free, so its weights stream while the
+  // latency-bound router, top-k and gather run on the other SMs. Its down
+  // projection is launched without the early-start dependency, so its CTAs do
+  // not take SMs early and sit waiting for the gate/up kernel. The routed
+  // experts take the SMs as the shared expert's CTAs leave them; the streams
+  // join before the combine.
   //
   // Small batches: the routed experts read few bytes, and the shared expert,
   // packed into the routing window, then delays the routed gate/up kernel's
@@ -445,8 +439,8 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
     if ((rc = counted(launch_shared_w13(sx, x, Ws13, M, H, I, s->mb, sgrid, (float*)s->ws_side.p,
                                         (int*)s->ctr_side.p))))
       return rc;
-    if (L > 0 && (rc = counted(launch_shared_w2(sx, Ws2, M, H, I, s->mb, sgrid,
-                                                (float*)s->ws_side.p, (int*)s->ctr_side.p))))
+    if ((rc = counted(launch_shared_w2(sx, Ws2, M, H, I, s->mb, sgrid, (float*)s->ws_side.p,
+                                       (int*)s->ctr_side.p))))
       return rc;
     if (cudaEventRecord(s->ev_join, s->side) != cudaSuccess) return DEC_ECUDA;
   }
@@ -461,26 +455,15 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
     if ((rc = counted(launch_experts_w13(cx, x, W13, M, Wd, E, topk, I, s->mb, egrid, ws, ctr))))
       return rc;
   }
-  DownExtras dx;
-  if (L > 0) {
-    dx.comb_out = s->mb.z;  // z = bf16(sum_j g_j o_j) on width L
-  } else {
-    dx.Ws2 = Ws2;           // null without a shared expert
-    dx.comb_out = out;
-    dx.comb_res = res;
-    // the shared expert's hidden rows must be complete before the down
-    // projection starts
-    if (shared && cudaStreamWaitEvent(st, s->ev_join, 0) != cudaSuccess) return DEC_ECUDA;
-  }
   {
     ProbeScope p(1, st);
-    if ((rc = counted(launch_experts_w2(cx, W2, M, Wd, E, topk, I, s->mb, L > 0 ? egrid : s->sms,
-                                        ws, ctr, dx))))
+    if ((rc = counted(launch_experts_w2(cx, W2, M, Wd, E, topk, I, s->mb, egrid, ws, ctr))))
       return rc;
   }
-  if (L == 0) return DEC_OK;
-  {
-    // u = z·Wupᵀ in fp32 (stream-K over every SM), then out = bf16(res + (u + s)).
+  if (L > 0) {
+    // z = bf16(sum_j g_j o_j) on width L, then u = z·Wupᵀ in fp32 (stream-K
+    // over every SM), then out = bf16(res + (u + s)) below.
+    if ((rc = counted(launch_combine(cx, s->mb, false, nullptr, s->mb.z, M, L, topk)))) return rc;
     const int xr = M <= 2 ? 8 : (M <= 16 ? 16 : 64);
     const long long T = (long long)((H + 127) / 128) * ((L + 127) / 128);
     const int ugrid = (int)(T < s->sms ? T : s->sms);
@@ -495,7 +478,8 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   // the programmatic (early-start) dependency so both are complete ones.
   cx.pdl = !shared;
   ProbeScope p(4, st);
-  return counted(launch_combine_up(cx, s->mb, shared, res, out, M, H));
+  if (L > 0) return counted(launch_combine_up(cx, s->mb, shared, res, out, M, H));
+  return counted(launch_combine(cx, s->mb, shared, res, out, M, H, topk));
 }
 
 }  // namespace dg
@@ -630,7 +614,6 @@ int dec_sync_check(void* stream) {
     cudaMemset(s->status, 0, sizeof(int));
     if (s->ctr_main.p) cudaMemset(s->ctr_main.p, 0, s->ctr_main.bytes);
     if (s->ctr_side.p) cudaMemset(s->ctr_side.p, 0, s->ctr_side.bytes);
-    if (s->mb.comb_ctr) cudaMemset(s->mb.comb_ctr, 0, s->mb.comb_ctr_bytes);
     if (s->mb.route_ctr) cudaMemset(s->mb.route_ctr, 0, sizeof(int));
     cudaMemset(s->status, 0, sizeof(words));
     cudaDeviceSynchronize();

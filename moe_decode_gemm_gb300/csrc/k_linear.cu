@@ -75,9 +75,8 @@ static cudaError_t run_dense_path(const Ctx& cx, const void* x, const void* W, c
   a.timeout_ns = cx.timeout_ns;
   if (CLUSTER)
     return launch_kc(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, cl, wmap, xmap, xmap,
-                     wmap, xmap, a);
-  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, xmap, wmap,
-                  xmap, a);
+                     a);
+  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, xmap, a);
 }
 
 // The CUDA-core consumer takes at most two tokens and only runs at 8 token

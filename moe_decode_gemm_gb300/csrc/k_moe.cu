@@ -81,7 +81,7 @@ static cudaError_t run_router(const Ctx& cx, const void* x, const void* Wr, int 
   a.pairs = M * k;
   const int cl = router_clusters(H);
   return launch_kc(kern, dim3(a.TILES * cl), dim3(kThreads), SMEM, cx.stream, cx.pdl, cl, wmap,
-                   xmap, xmap, wmap, xmap, a);
+                   xmap, xmap, a);
 }
 
 cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E, int k,
@@ -285,13 +285,12 @@ static cudaError_t run_experts_w13(const Ctx& cx, const void* W13, int M, int H,
   a.pairs = M * k;
   a.groups_len = b.groups_cap;
   return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, xnarrow,
-                  wmap, xmap, a);
+                  a);
 }
 
 template <int XR>
 static cudaError_t run_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E, int k, int I,
-                                  const MoeBufs& b, int grid, float* ws, int* ctr,
-                                  const DownExtras& dx) {
+                                  const MoeBufs& b, int grid, float* ws, int* ctr) {
   // 256-row output tiles: two 128-row halves, 64 KB weight stages
   constexpr int SMEM = expert_pair_smem<XR>();
   auto kern = wstream_kernel<XR, kExpertPairStages, EPI_F32, false, true, true, ROLE_EXPERT>;
@@ -321,32 +320,8 @@ static cudaError_t run_experts_w2(const Ctx& cx, const void* W2, int M, int H, i
   a.out_len = (long long)M * k * H;
   a.pairs = M * k;
   a.groups_len = b.groups_cap;
-  // The shared expert's down projection as groups of at most XR tokens after
-  // the routed ones (its hidden rows b.hs, its output b.s).
-  CUtensorMap wmap2 = wmap, xmap2 = xmap;
-  if (dx.Ws2) {
-    if (!make_tmap(&wmap2, dx.Ws2, (uint64_t)H, (uint64_t)I, kTileRows, true) ||
-        !make_tmap(&xmap2, b.hs, (uint64_t)M, (uint64_t)I, XR, false))
-      return cudaErrorInvalidValue;
-    a.sh_groups = (M + XR - 1) / XR;
-    a.out2 = b.s;
-    a.out2_len = (long long)M * H;
-  }
-  if (dx.comb_out) {
-    a.comb_out = reinterpret_cast<uint16_t*>(dx.comb_out);
-    a.comb_res = reinterpret_cast<const uint16_t*>(dx.comb_res);
-    a.comb_gate = b.gate;
-    a.comb_pair_of = b.pair_of;
-    a.pair_tok = b.pair_tok;
-    a.comb_k = k;
-    a.comb_shared = dx.Ws2 ? 1 : 0;
-    a.comb_need = k + a.comb_shared;
-    a.comb_ctr = b.comb_ctr;
-    a.comb_len = (long long)M * H;
-    a.comb_ctr_len = (long long)(b.comb_ctr_bytes / sizeof(int));
-  }
   return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, xnarrow,
-                  wmap2, xmap2, a);
+                  a);
 }
 
 cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, int M, int H, int E,
@@ -357,11 +332,9 @@ cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, in
 }
 
 cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E, int k, int I,
-                              const MoeBufs& b, int grid, float* ws, int* ctr,
-                              const DownExtras& dx) {
-  if (M <= kNarrowRows)
-    return run_experts_w2<kNarrowRows>(cx, W2, M, H, E, k, I, b, grid, ws, ctr, dx);
-  return run_experts_w2<kGroupTokens>(cx, W2, M, H, E, k, I, b, grid, ws, ctr, dx);
+                              const MoeBufs& b, int grid, float* ws, int* ctr) {
+  if (M <= kNarrowRows) return run_experts_w2<kNarrowRows>(cx, W2, M, H, E, k, I, b, grid, ws, ctr);
+  return run_experts_w2<kGroupTokens>(cx, W2, M, H, E, k, I, b, grid, ws, ctr);
 }
 
 // Shared expert: a dense (ungrouped) pass over every token, token rows per
@@ -392,8 +365,7 @@ static cudaError_t run_shared_w13(const Ctx& cx, const void* x, const void* Ws13
   a.out_len = (long long)M * I;
   const long long T = (long long)a.TILES * a.KB;
   if (grid > T) grid = (int)T;
-  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, xmap, wmap,
-                  xmap, a);
+  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, xmap, a);
 }
 
 template <int XR>
@@ -419,8 +391,7 @@ static cudaError_t run_shared_w2(const Ctx& cx, const void* Ws2, int M, int H, i
   a.out_len = (long long)M * H;
   const long long T = (long long)a.TILES * a.KB;
   if (grid > T) grid = (int)T;
-  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, xmap, wmap,
-                  xmap, a);
+  return launch_k(kern, dim3(grid), dim3(kThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, xmap, a);
 }
 
 cudaError_t launch_shared_w13(const Ctx& cx, const void* x, const void* Ws13, int M, int H, int I,
@@ -482,6 +453,18 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 #pragma unroll
     for (int q = 0; q < 4; ++q) out[(long long)m * H + n + q] = f2bf_bits(acc[q]);
   }
+}
+
+cudaError_t launch_combine(const Ctx& cx, const MoeBufs& b, bool with_shared, const void* res,
+                           void* out, int M, int H, int k) {
+  const long long total = (long long)M * (H / 4);
+  int grid = (int)((total + 255) / 256);
+  if (grid > 4 * cx.sms) grid = 4 * cx.sms;
+  if (grid < 1) grid = 1;
+  return launch_k(combine_kernel, dim3(grid), dim3(256), 0, cx.stream, cx.pdl, (const float*)b.o,
+                  (const float*)(with_shared ? b.s : nullptr), (const float*)b.gate,
+                  (const int*)b.pair_of, reinterpret_cast<const uint16_t*>(res),
+                  reinterpret_cast<uint16_t*>(out), M, H, k, cx.status, (long long)M * k * H);
 }
 
 cudaError_t launch_combine_up(const Ctx& cx, const MoeBufs& b, bool with_shared, const void* res,

@@ -67,20 +67,7 @@ struct MoeBufs {
   int* route_ctr;  // router clusters arrived (zero at rest)
   uint16_t* z;     // latent block: [M, L] gate-weighted sum of the experts, bf16
   float* u;        // latent block: [M, H] its up-projection, fp32
-  int* comb_ctr;   // [M][tiles of the down projection] combine arrivals (zero at rest)
-  size_t comb_ctr_bytes;
   int groups_cap;  // entries of grp_exp (grp_off has one more)
-};
-
-// What the routed down projection does besides its own groups: the shared
-// expert's down projection folded in as extra groups (Ws2 non-null; its
-// hidden rows b.hs must be complete when the kernel starts), and the combine
-// fused into its epilogue (comb_out non-null: out = bf16(res + (sum_j g_j o_j
-// (+ the shared expert's output))), res nullable).
-struct DownExtras {
-  const void* Ws2 = nullptr;
-  void* comb_out = nullptr;
-  const void* comb_res = nullptr;
 };
 
 // Router: CTAs per 128-row tile of experts (one thread-block cluster each),
@@ -106,8 +93,11 @@ cudaError_t launch_gather(const Ctx& cx, const void* x, int M, int H, int E, int
 cudaError_t launch_experts_w13(const Ctx& cx, const void* x, const void* W13, int M, int H, int E,
                                int k, int I, const MoeBufs& b, int grid, float* ws, int* ctr);
 cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E, int k, int I,
-                              const MoeBufs& b, int grid, float* ws, int* ctr,
-                              const DownExtras& dx = DownExtras());
+                              const MoeBufs& b, int grid, float* ws, int* ctr);
+// out = bf16(res + (sum_{j<k} g_j o_j + s)) over [M, H] (s when with_shared,
+// res nullable); o in expert-sorted pair order.
+cudaError_t launch_combine(const Ctx& cx, const MoeBufs& b, bool with_shared, const void* res,
+                           void* out, int M, int H, int k);
 cudaError_t launch_shared_w13(const Ctx& cx, const void* x, const void* Ws13, int M, int H, int I,
                               const MoeBufs& b, int grid, float* ws, int* ctr);
 cudaError_t launch_shared_w2(const Ctx& cx, const void* Ws2, int M, int H, int I,

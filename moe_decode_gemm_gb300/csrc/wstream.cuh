@@ -58,7 +58,7 @@ constexpr int kPrefetchBytes = 256 * 1024;
 // slack, the stage ring, full/empty barriers, flags, slot table, and `extra`.
 constexpr int wstream_smem(int xr, int stages, int extra, bool paired = false) {
   return 1024 + stages * ((paired ? 2 : 1) * kWBytes + kKSub * xr * 128) + 2 * 8 * stages + 32 +
-         4 * kMaxSlots + 4 * kGroupTokens + extra;
+         4 * kMaxSlots + extra;
 }
 
 struct StreamArgs {
@@ -85,28 +85,6 @@ struct StreamArgs {
   int* ctr;                  // per output tile arrival counters (zero at rest)
   int* status;
   long long timeout_ns;
-  // grouped mode: sh_groups more groups after the routed ones -- the shared
-  // expert's down projection, groups of at most XR tokens (token t of group i
-  // is token i*XR + t) -- whose weights come through wmap2, whose token rows
-  // through xmap2, and whose output goes to out2 ([M, ldo] fp32)
-  int sh_groups;
-  float* out2;
-  // combine fused into a grouped down projection (comb_out non-null): when the
-  // last of comb_need contributions to (token m, output tile) is written --
-  // one per routed (token, slot) pair, plus the shared expert's -- the CTA
-  // that wrote it computes, for that token's tile,
-  //   comb_out[m, n] = bf16(comb_res[m, n] + (sum_{j<comb_k} g[m,j] * out[pair_of[m,j], n]
-  //                                          + out2[m, n]))
-  // in that order (the shared and residual terms only when present).
-  uint16_t* comb_out;
-  const uint16_t* comb_res;
-  const float* comb_gate;    // [M][comb_k]
-  const int* comb_pair_of;   // [M][comb_k]
-  const int* pair_tok;       // pair -> token
-  int comb_k;
-  int comb_need;
-  int comb_shared;           // out2 holds the shared expert's output
-  int* comb_ctr;             // [M][TILES] arrivals (zero at rest)
   // router role: with route_k > 0 the last cluster to finish its logits
   // selects every token's top route_k experts and their gates
   int route_k;
@@ -117,48 +95,36 @@ struct StreamArgs {
   int32_t* route_idx_user;   // optional copies for the caller
   float* route_w_user;
   // extents (elements) of the buffers above, checked by the index checks of
-  // a DEC_DEBUG build: out, out2, res, ws (floats), ctr, comb_out/comb_res,
-  // comb_ctr; pairs = rows of the pair tables (grouped: M*k; router: M*k of
-  // route_idx); groups_len = entries of grp_exp (grp_off has one more)
-  long long out_len, out2_len, res_len, ws_len, ctr_len, comb_len, comb_ctr_len;
+  // a DEC_DEBUG build: out, res, ws (floats), ctr; pairs = rows of the pair
+  // tables (grouped: M*k; router: M*k of route_idx); groups_len = entries of
+  // grp_exp (grp_off has one more)
+  long long out_len, res_len, ws_len, ctr_len;
   int pairs, groups_len;
 };
 
 struct GroupInfo {
-  int e;       // expert id (0 in dense mode and for the shared expert)
-  int p0;      // first output row (pair, or token for the shared expert) of the group
+  int e;       // expert id (0 in dense mode)
+  int p0;      // first output row (pair) of the group
   int c;       // tokens in the group
-  int sh;      // the shared expert's down projection (grouped mode)
 };
 
-// Group g of nr routed groups; groups nr.. are the shared expert's, gsz
-// tokens each.
+// Group g; gsz is the most tokens a group of this instantiation may hold.
 template <bool GROUPED>
-__device__ __forceinline__ GroupInfo load_group(const StreamArgs& a, int g, int nr = 0,
-                                                int gsz = 0) {
+__device__ __forceinline__ GroupInfo load_group(const StreamArgs& a, int g, int gsz = 0) {
   GroupInfo gi;
   if (GROUPED) {
-    if (g >= nr) {
-      gi.e = 0;
-      gi.p0 = (g - nr) * gsz;
-      gi.c = a.M - gi.p0 < gsz ? a.M - gi.p0 : gsz;
-      gi.sh = 1;
-    } else {
-      gi.e = *DG_AT(a.status, a.grp_exp, g, a.groups_len);
-      gi.p0 = *DG_AT(a.status, a.grp_off, g, a.groups_len + 1);
-      gi.c = *DG_AT(a.status, a.grp_off, g + 1, a.groups_len + 1) - gi.p0;
-      gi.sh = 0;
-      if (!DG_OK(a.status, gi.p0 >= 0 && gi.c >= 0 && gi.p0 + gi.c <= a.pairs && gi.c <= gsz,
-                 (long long)gi.c * 1000000 + gi.p0)) {
-        gi.p0 = 0;
-        gi.c = 0;
-      }
+    gi.e = *DG_AT(a.status, a.grp_exp, g, a.groups_len);
+    gi.p0 = *DG_AT(a.status, a.grp_off, g, a.groups_len + 1);
+    gi.c = *DG_AT(a.status, a.grp_off, g + 1, a.groups_len + 1) - gi.p0;
+    if (!DG_OK(a.status, gi.p0 >= 0 && gi.c >= 0 && gi.p0 + gi.c <= a.pairs && gi.c <= gsz,
+               (long long)gi.c * 1000000 + gi.p0)) {
+      gi.p0 = 0;
+      gi.c = 0;
     }
   } else {
     gi.e = 0;
     gi.p0 = 0;
     gi.c = a.M;
-    gi.sh = 0;
   }
   return gi;
 }
@@ -199,8 +165,7 @@ __device__ __forceinline__ void store_out(const StreamArgs& a, const GroupInfo& 
   const long long row = (long long)gi.p0 + t;
   const long long i = row * a.ldo + n;
   if (EPI == EPI_F32) {
-    if (GROUPED && gi.sh) *DG_AT(a.status, a.out2, i, a.out2_len) = v;
-    else *DG_AT(a.status, reinterpret_cast<float*>(a.out), i, a.out_len) = v;
+    *DG_AT(a.status, reinterpret_cast<float*>(a.out), i, a.out_len) = v;
   } else if (EPI == EPI_BF16_RES) {
     const float r = bf_bits2f(*DG_AT(a.status, a.res, i, a.res_len));
     *DG_AT(a.status, reinterpret_cast<uint16_t*>(a.out), i, a.out_len) = f2bf_bits(r + v);
@@ -335,10 +300,7 @@ template <int XR, int STAGES, int EPI, bool PAIRED, bool GROUPED, bool WIDE = fa
           int ROLE = ROLE_PROJECTION, int MINB = 1, bool CLUSTER = false, int PATH = PATH_ANY>
 __global__ void __launch_bounds__(kThreads, MINB)
     wstream_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
-                   const __grid_constant__ CUtensorMap xmap_narrow,
-                   const __grid_constant__ CUtensorMap wmap2,
-                   const __grid_constant__ CUtensorMap xmap2, const StreamArgs a) {
-  static_assert(!GROUPED || XR <= kGroupTokens, "a group's tokens fit the fused-combine table");
+                   const __grid_constant__ CUtensorMap xmap_narrow, const StreamArgs a) {
   constexpr int H2 = (PAIRED || WIDE) ? 2 : 1;  // 128-row weight halves per box column
   // CUDA-core dot form. Both give the same bits. The bf16-operand form
   // (fma.rn.f32.bf16) issues half the instructions; the widened form is kept
@@ -360,7 +322,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
   // [0] abort [1] last arriver of a split tile [2] last cluster of the router
   volatile int* s_flags = reinterpret_cast<volatile int*>(empty + STAGES);
   int* s_slot = const_cast<int*>(s_flags) + 8;                                 // [kMaxSlots]
-  int* s_comb = s_slot + kMaxSlots;                                            // [kGroupTokens]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -379,10 +340,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
     prefetch_tmap(&wmap);
     prefetch_tmap(&xmap);
     if (GROUPED && XR > kNarrowRows) prefetch_tmap(&xmap_narrow);
-    if (GROUPED && a.sh_groups > 0) {
-      prefetch_tmap(&wmap2);
-      prefetch_tmap(&xmap2);
-    }
   }
   __syncthreads();
   // Kernels that can stream weights before their predecessor finishes let
@@ -397,14 +354,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
   const int KB = a.KB, TILES = a.TILES;
 
   long long T;
-  int nr = 0;  // routed groups (grouped mode)
   if (GROUPED) {
     if (!early) {
       griddep_wait();
       griddep_launch_dependents();
     }
-    nr = *a.nact;
-    T = (long long)(nr + a.sh_groups) * TILES * KB;
+    T = (long long)(*a.nact) * TILES * KB;
   } else {
     T = (long long)TILES * KB;
   }
@@ -432,12 +387,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
       int gcur = -1;
-      GroupInfo gi{0, 0, 0, 0};
+      GroupInfo gi{0, 0, 0};
       // Unit positions advance one unit at a time: no 64-bit division per
       // stage on the path that refills the ring.
       auto issue_w = [&](int s, const UnitPos& p) {
         uint8_t* wdst = smem + s * kStageBytes;
-        const CUtensorMap* wm = GROUPED && gi.sh ? &wmap2 : &wmap;
+        const CUtensorMap* wm = &wmap;
         const int rbase = gi.e * a.w_group_rows;
 #pragma unroll
         for (int sb = 0; sb < kKSub; ++sb) {
@@ -452,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         }
       };
       auto narrow_group = [&](const GroupInfo& g_) {
-        return GROUPED && XR > kNarrowRows && g_.c <= kNarrowRows && !g_.sh;
+        return GROUPED && XR > kNarrowRows && g_.c <= kNarrowRows;
       };
       auto issue_x = [&](int s, int kc, const GroupInfo& g_) {
         uint8_t* xdst = smem + s * kStageBytes + kWStage;
@@ -464,13 +419,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
           // tensor (pairs are stored in expert order), so one box of XR rows
           // at the group's first pair covers them; rows past the group are
           // never read.
-          tma_load_2d(d, GROUPED && g_.sh ? &xmap2 : narrow_group(g_) ? &xmap_narrow : &xmap, k0,
-                      GROUPED ? g_.p0 : 0, &full[s], pol_x);
+          tma_load_2d(d, narrow_group(g_) ? &xmap_narrow : &xmap, k0, GROUPED ? g_.p0 : 0,
+                      &full[s], pol_x);
         }
       };
       // The same weight boxes as issue_w for group g_, into L2 only.
       auto prefetch_w = [&](const UnitPos& p, const GroupInfo& g_) {
-        const CUtensorMap* wm = GROUPED && g_.sh ? &wmap2 : &wmap;
+        const CUtensorMap* wm = &wmap;
         const int rbase = g_.e * a.w_group_rows;
 #pragma unroll
         for (int sb = 0; sb < kKSub; ++sb) {
@@ -496,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         for (; i < npre; ++i, pos.next(KB, TILES)) {
           if (pos.g != gcur) {
             gcur = pos.g;
-            gi = load_group<GROUPED>(a, pos.g, nr, XR);
+            gi = load_group<GROUPED>(a, pos.g, XR);
           }
           pg[i] = gi;
           mbar_arrive_expect_tx(&full[i], tx_bytes(gi));
@@ -509,12 +464,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
         constexpr int kPfUnits = CLUSTER ? 0 : kPrefetchBytes / kWStage;
         const int npf = nunits - npre < kPfUnits ? nunits - npre : kPfUnits;
         int pgrp = -1;
-        GroupInfo pgi{0, 0, 0, 0};
+        GroupInfo pgi{0, 0, 0};
         UnitPos pp = pos;
         for (int j = 0; j < npf; ++j, pp.next(KB, TILES)) {
           if (pp.g != pgrp) {
             pgrp = pp.g;
-            pgi = load_group<GROUPED>(a, pp.g, nr, XR);
+            pgi = load_group<GROUPED>(a, pp.g, XR);
           }
           prefetch_w(pp, pgi);
         }
@@ -534,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         if (GROUPED && pos.g != gcur) {
           // new expert group: read its id and pair range once
           gcur = pos.g;
-          gi = load_group<GROUPED>(a, pos.g, nr, XR);
+          gi = load_group<GROUPED>(a, pos.g, XR);
         }
         mbar_arrive_expect_tx(&full[s], tx_bytes(gi));
         issue_w(s, pos);
@@ -571,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     float dacc[H2][4][2];
     float macc[H2][XR / 8][4];
     long long cur = -1;
-    GroupInfo gi{0, 0, 0, 0};
+    GroupInfo gi{0, 0, 0};
     bool use_mma = false;
 
     auto zero_acc = [&]() {
@@ -735,49 +690,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     // read, and the tile reduced if this CTA arrived last, after the range.
     long long dgt = -1;  // deferred tile
     int dold = 0;        // its counter's value before this CTA's increment (thread 0)
-    GroupInfo dgi{0, 0, 0, 0};
-
-    // Fused combine (grouped down projection with comb_out): called by every
-    // consumer thread once the final values of tile gt of group g_ are
-    // written. Each token of the group arrives on its (token, tile) counter;
-    // the CTA whose arrival completes a counter sums that token's tile.
-    auto combine_tile = [&](long long gt, const GroupInfo& g_) {
-      if (!GROUPED || a.comb_out == nullptr) return;
-      const int tile = (int)(gt % TILES);
-      // every thread's output stores of the tile are ordered before the
-      // arrivals' release (barrier, then acq_rel atomics); the acquire side
-      // plus the next barrier order the reads below after the other CTAs'
-      named_bar_sync(1, kNCW * 32);
-      if (ct < g_.c) {
-        const int m = g_.sh ? g_.p0 + ct : *DG_AT(a.status, a.pair_tok, g_.p0 + ct, a.pairs);
-        int* cp = DG_AT(a.status, a.comb_ctr, (long long)m * TILES + tile, a.comb_ctr_len);
-        const int old = atomic_add_acq_rel_gpu(cp, 1);
-        const bool last = old == a.comb_need - 1;
-        if (last) *cp = 0;
-        s_comb[ct] = last ? m : -1;
-      }
-      named_bar_sync(1, kNCW * 32);
-      const float* o = reinterpret_cast<const float*>(a.out);
-      for (int t = 0; t < g_.c; ++t) {
-        const int m = s_comb[t];
-        if (m < 0) continue;
-        for (int r = ct; r < kTileOut; r += kNCW * 32) {
-          const int n = tile * kTileOut + r;
-          if (n >= a.nout) continue;
-          float acc = 0.f;
-          for (int j = 0; j < a.comb_k; ++j) {
-            const float gj = __ldg(DG_AT(a.status, a.comb_gate, m * a.comb_k + j, a.pairs));
-            const int p = __ldg(DG_AT(a.status, a.comb_pair_of, m * a.comb_k + j, a.pairs));
-            acc = fmaf(gj, __ldcg(DG_AT(a.status, o, (long long)p * a.ldo + n, a.out_len)), acc);
-          }
-          const long long i = (long long)m * a.ldo + n;
-          if (a.comb_shared) acc += __ldcg(DG_AT(a.status, a.out2, i, a.out2_len));
-          if (a.comb_res) acc = bf_bits2f(*DG_AT(a.status, a.comb_res, i, a.comb_len)) + acc;
-          *DG_AT(a.status, a.comb_out, i, a.comb_len) = f2bf_bits(acc);
-        }
-      }
-      named_bar_sync(1, kNCW * 32);  // s_comb is reused by the next tile
-    };
+    GroupInfo dgi{0, 0, 0};
 
     auto finish_tile = [&](long long gt, bool defer) {
       const int tile = (int)(gt % TILES);
@@ -786,7 +699,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
       const bool whole = (u0 <= gt * KB) && ((gt + 1) * KB <= u1);
       if (whole) {
         if (!aborted) reg_epilogue(tile);
-        combine_tile(gt, gi);
       } else {
         const int slot = (gt == u0 / KB) ? 0 : 1;
         write_partial(a.ws + (c * 2 + slot) * kSlotFloats);
@@ -803,10 +715,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         }
         if (ct == 0) settle(gt, atomic_add_acq_rel_gpu(DG_AT(a.status, a.ctr, gt, a.ctr_len), 1));
         named_bar_sync(1, kNCW * 32);
-        if (s_flags[1]) {
-          reduce_tile(gt, aborted);
-          combine_tile(gt, gi);
-        }
+        if (s_flags[1]) reduce_tile(gt, aborted);
       }
       named_bar_sync(1, kNCW * 32);  // partial slots and flags may be reused next tile
     };
@@ -824,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         if (cur >= 0) finish_tile(cur, cur == u0 / KB);
         cur = gt;
         zero_acc();
-        gi = load_group<GROUPED>(a, (int)(gt / TILES), nr, XR);
+        gi = load_group<GROUPED>(a, (int)(gt / TILES), XR);
         use_mma = PATH == PATH_ANY && gi.c >= a.mma_min_tokens;
       }
       const int s = i % STAGES;
@@ -974,7 +883,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
       if (s_flags[1]) {
         gi = dgi;
         reduce_tile(dgt, s_flags[0] != 0);
-        combine_tile(dgt, gi);
       }
     }
   }
