@@ -337,13 +337,16 @@ cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E
   return run_experts_w2<kGroupTokens>(cx, W2, M, H, E, k, I, b, grid, ws, ctr);
 }
 
-// Shared expert: a dense (ungrouped) pass over every token, token rows per
-// stage sized to M like the dense projections: 8 rows for 1-2 tokens (CUDA-core
-// dots), 16 for up to 16 tokens, 64 beyond (mma.sync).
+// Shared expert: a dense (ungrouped) pass over every token. Up to 16 tokens
+// the weight-streaming kernel, token rows per stage sized to M like the dense
+// projections (8 rows for 1-2 tokens on CUDA cores, 16 on mma.sync); from 17
+// tokens the gate/up and down projections are dense contractions for the
+// tcgen05 tensor cores (the SwiGLU gate/up kernel with both accumulators in
+// tensor memory, and the fp32-output projection).
 template <int XR>
 static cudaError_t run_shared_w13(const Ctx& cx, const void* x, const void* Ws13, int M, int H,
                                   int I, const MoeBufs& b, int grid, float* ws, int* ctr) {
-  constexpr int STAGES = XR == 64 ? 2 : 3;  // 64 KB of gate + up weights per stage
+  constexpr int STAGES = 3;  // 64 KB of gate + up weights per stage
   constexpr int SMEM = wstream_smem(XR, STAGES, 0, true);
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
   auto kern = wstream_kernel<XR, STAGES, EPI_SWIGLU, true, false, false, ROLE_SHARED>;
@@ -371,7 +374,7 @@ static cudaError_t run_shared_w13(const Ctx& cx, const void* x, const void* Ws13
 template <int XR>
 static cudaError_t run_shared_w2(const Ctx& cx, const void* Ws2, int M, int H, int I,
                                  const MoeBufs& b, int grid, float* ws, int* ctr) {
-  constexpr int STAGES = XR == 64 ? 4 : 6;
+  constexpr int STAGES = 6;
   constexpr int SMEM = wstream_smem(XR, STAGES, 0);
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
   auto kern = wstream_kernel<XR, STAGES, EPI_F32, false, false, false, ROLE_SHARED>;
@@ -398,14 +401,14 @@ cudaError_t launch_shared_w13(const Ctx& cx, const void* x, const void* Ws13, in
                               const MoeBufs& b, int grid, float* ws, int* ctr) {
   if (M <= 2) return run_shared_w13<8>(cx, x, Ws13, M, H, I, b, grid, ws, ctr);
   if (M <= 16) return run_shared_w13<16>(cx, x, Ws13, M, H, I, b, grid, ws, ctr);
-  return run_shared_w13<64>(cx, x, Ws13, M, H, I, b, grid, ws, ctr);
+  return launch_swiglu_tc(cx, x, Ws13, b.hs, M, I, H, grid, ws, ctr);
 }
 
 cudaError_t launch_shared_w2(const Ctx& cx, const void* Ws2, int M, int H, int I, const MoeBufs& b,
                              int grid, float* ws, int* ctr) {
   if (M <= 2) return run_shared_w2<8>(cx, Ws2, M, H, I, b, grid, ws, ctr);
   if (M <= 16) return run_shared_w2<16>(cx, Ws2, M, H, I, b, grid, ws, ctr);
-  return run_shared_w2<64>(cx, Ws2, M, H, I, b, grid, ws, ctr);
+  return launch_dense_tc_f32(cx, b.hs, Ws2, b.s, M, H, I, grid, ws, ctr);
 }
 
 // ------------------------------------------------------------------ combine

@@ -35,22 +35,39 @@ constexpr int kTcStageBytes = kWBytes + kKSub * kTcXSub;  // 48 KB
 constexpr int kTcThreads = 320;
 constexpr int kTcEpi = 256;    // 8 epilogue warps: two per tensor-memory lane quarter
 constexpr int kTcCols = kTcXRows / 2;  // token columns each epilogue warp drains
-constexpr int kTmemCols = 128;  // two 64-column accumulators
 
+// PAIRED (SwiGLU gate/up): each stage holds the 128 gate rows of a tile and
+// the 128 matching up rows (a.w_up_offset further down the weight); two MMAs
+// per k step fill a gate and an up accumulator, and the epilogue writes
+// bf16(silu(gate) * up). Two 80 KB stages; 256 tensor-memory columns.
+template <bool PAIRED>
+struct TcShape {
+  static constexpr int kWB = (PAIRED ? 2 : 1) * kWBytes;       // weight bytes per stage
+  static constexpr int kStage = kWB + kKSub * kTcXSub;         // stage bytes
+  static constexpr int kStages = PAIRED ? 2 : kTcStages;
+  static constexpr int kAcc = PAIRED ? 128 : 64;               // tensor-memory columns per tile
+  static constexpr int kCols = 2 * kAcc;                       // double-buffered
+  static constexpr int kStride = PAIRED ? 2 * kTileRows : kTileRows;  // floats per token in a slot
+};
+
+template <bool PAIRED = false>
 constexpr int tc_smem() {
-  return 1024 + kTcStages * kTcStageBytes + 8 * (2 * kTcStages + 5) + 64 + 4 * kMaxSlots;
+  return 1024 + TcShape<PAIRED>::kStages * TcShape<PAIRED>::kStage +
+         8 * (2 * TcShape<PAIRED>::kStages + 5) + 64 + 4 * kMaxSlots;
 }
 
-template <int EPI>
+template <int EPI, bool PAIRED = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_linear_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                      const StreamArgs a, const int NP, const uint32_t idesc) {
+  using Sh = TcShape<PAIRED>;
+  constexpr int kStages = Sh::kStages, kStage = Sh::kStage, kWB = Sh::kWB;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTcStages * kTcStageBytes);
-  uint64_t* empty = full + kTcStages;
-  uint64_t* tfull = empty + kTcStages;   // [2] accumulator ready
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStage);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;     // [2] accumulator ready
   uint64_t* tempty = tfull + 2;          // [2] accumulator drained
   uint64_t* mma_done = tempty + 2;       // [1]
   volatile int* s_flags = reinterpret_cast<volatile int*>(mma_done + 1);  // [0] abort [1] last
@@ -59,7 +76,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kTcStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -73,7 +90,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(s_taddr, kTmemCols);
+    tmem_alloc(s_taddr, Sh::kCols);
     tmem_relinquish();
   }
   if (threadIdx.x == 32) {
@@ -99,22 +116,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      const uint32_t bytes = kWBytes + kKSub * NP * 128;
+      const uint32_t bytes = kWB + kKSub * NP * 128;
       // unit positions advance one unit at a time (no division per stage)
       auto issue_w = [&](int s, const UnitPos& p) {
 #pragma unroll
-        for (int sb = 0; sb < kKSub; ++sb)
-          tma_load_2d(smem + s * kTcStageBytes + sb * kWSub, &wmap, (p.kc * kKSub + sb) * kKBlk,
+        for (int sb = 0; sb < kKSub; ++sb) {
+          tma_load_2d(smem + s * kStage + sb * kWSub, &wmap, (p.kc * kKSub + sb) * kKBlk,
                       p.tile * kTileRows, &full[s], pol_w);
+          if (PAIRED)  // the matching up rows
+            tma_load_2d(smem + s * kStage + kWBytes + sb * kWSub, &wmap,
+                        (p.kc * kKSub + sb) * kKBlk, a.w_up_offset + p.tile * kTileRows, &full[s],
+                        pol_w);
+        }
       };
       auto issue_x = [&](int s, const UnitPos& p) {
 #pragma unroll
         for (int sb = 0; sb < kKSub; ++sb)
-          tma_load_2d(smem + s * kTcStageBytes + kWBytes + sb * kTcXSub, &xmap,
+          tma_load_2d(smem + s * kStage + kWB + sb * kTcXSub, &xmap,
                       (p.kc * kKSub + sb) * kKBlk, 0, &full[s], pol_x);
       };
       // weights first (independent of the previous kernel), then tokens
-      const int npre = nunits < kTcStages ? nunits : kTcStages;
+      const int npre = nunits < kStages ? nunits : kStages;
       const UnitPos pos0 = unit_pos(u0, KB, TILES);
       UnitPos pos = pos0;
       int i = 0;
@@ -126,8 +148,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       UnitPos px = pos0;
       for (int j = 0; j < npre; ++j, px.next(KB, TILES)) issue_x(j, px);
       for (; i < nunits; ++i, pos.next(KB, TILES)) {
-        const int s = i % kTcStages;
-        if (!mbar_wait(&empty[s], ((i / kTcStages) + 1) & 1, a.timeout_ns, a.status)) {
+        const int s = i % kStages;
+        if (!mbar_wait(&empty[s], ((i / kStages) + 1) & 1, a.timeout_ns, a.status)) {
           s_flags[0] = 1;
           break;
         }
@@ -137,8 +159,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         issue_x(s, pos);
       }
       const int issued = i;
-      for (int s = 0; s < kTcStages && s < issued; ++s) {
-        const int uses = (issued - s + kTcStages - 1) / kTcStages;
+      for (int s = 0; s < kStages && s < issued; ++s) {
+        const int uses = (issued - s + kStages - 1) / kStages;
         mbar_wait(&full[s], (uses - 1) & 1, drain_ns(a.timeout_ns), nullptr);
       }
     } else {
@@ -169,22 +191,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           tc_fence_after();
         }
-        const int s = i % kTcStages;
+        const int s = i % kStages;
         if (!s_flags[0]) {
-          if (!mbar_wait(&full[s], (i / kTcStages) & 1, a.timeout_ns, a.status)) s_flags[0] = 1;
+          if (!mbar_wait(&full[s], (i / kStages) & 1, a.timeout_ns, a.status)) s_flags[0] = 1;
         }
         tc_fence_after();
-        const uint32_t d = taddr + (uint32_t)((jt & 1) * 64);
+        const uint32_t d = taddr + (uint32_t)((jt & 1) * Sh::kAcc);
         if (!s_flags[0]) {
-          const uint32_t wb = smem_u32(smem + s * kTcStageBytes);
-          const uint32_t xb = wb + kWBytes;
+          const uint32_t wb = smem_u32(smem + s * kStage);
+          const uint32_t xb = wb + kWB;
 #pragma unroll
           for (int sb = 0; sb < kKSub; ++sb)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = umma_desc_sw128(wb + sb * kWSub + kk * 32);
+              const uint32_t acc = (first && sb == 0 && kk == 0) ? 0u : 1u;
               const uint64_t bd = umma_desc_sw128(xb + sb * kTcXSub + kk * 32);
-              umma_bf16(d, ad, bd, idesc, (first && sb == 0 && kk == 0) ? 0u : 1u);
+              umma_bf16(d, umma_desc_sw128(wb + sb * kWSub + kk * 32), bd, idesc, acc);
+              if (PAIRED)  // up rows into the second accumulator of the tile
+                umma_bf16(d + 64, umma_desc_sw128(wb + kWBytes + sb * kWSub + kk * 32), bd, idesc,
+                          acc);
             }
         }
         umma_commit(&empty[s]);
@@ -214,12 +239,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc_fence_after();
         float v[kTcCols];
+        float vu[PAIRED ? kTcCols : 1];  // up sums (SwiGLU tiles)
 #pragma unroll
         for (int cc = 0; cc < kTcCols / 16; ++cc)
-          if (t0 + cc * 16 < NP)
-            tmem_ld16_sync(taddr + ((uint32_t)(quarter * 32) << 16) +
-                               (uint32_t)(buf * 64 + t0 + cc * 16),
-                           v + cc * 16);
+          if (t0 + cc * 16 < NP) {
+            const uint32_t ta = taddr + ((uint32_t)(quarter * 32) << 16) +
+                                (uint32_t)(buf * Sh::kAcc + t0 + cc * 16);
+            tmem_ld16_sync(ta, v + cc * 16);
+            if constexpr (PAIRED) tmem_ld16_sync(ta + 64, vu + cc * 16);
+          }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
@@ -231,16 +259,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (!aborted && n < a.nout) {
 #pragma unroll
             for (int t = 0; t < kTcCols; ++t)
-              if (t0 + t < gi.c) store_out<EPI, false>(a, gi, t0 + t, n, v[t]);
+              if (t0 + t < gi.c) {
+                if constexpr (PAIRED) store_swiglu(a, gi, t0 + t, n, v[t], vu[t]);
+                else store_out<EPI, false>(a, gi, t0 + t, n, v[t]);
+              }
           }
         } else {
-          constexpr long long kSlotFloats = (long long)kTileRows * kTcXRows;
+          // slot [token][kStride]: the tile's rows, then (SwiGLU) its up rows
+          constexpr long long kSlotFloats = (long long)Sh::kStride * kTcXRows;
           const int slot = (gt == u0 / KB) ? 0 : 1;
           const long long mine = (c * 2 + slot) * kSlotFloats;
 #pragma unroll
           for (int t = 0; t < kTcCols; ++t)
-            if (t0 + t < gi.c)
-              __stcg(DG_AT(a.status, a.ws, mine + (t0 + t) * kTileRows + r, a.ws_len), v[t]);
+            if (t0 + t < gi.c) {
+              const long long o = mine + (t0 + t) * Sh::kStride + r;
+              __stcg(DG_AT(a.status, a.ws, o, a.ws_len), v[t]);
+              if constexpr (PAIRED) __stcg(DG_AT(a.status, a.ws, o + kTileRows, a.ws_len), vu[t]);
+            }
           named_bar_sync(1, kTcEpi);
           const long long cf = cta_of(gt * KB, T, G);
           const long long cl = cta_of((gt + 1) * KB - 1, T, G);
@@ -266,13 +301,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               auto slot_at = [&](int j) -> long long {
                 return j < kMaxSlots ? (long long)s_slot[j] : slot_of(j);
               };
-              auto store = [&](int t, int rr, float v0, float) {
+              auto store = [&](int t, int rr, float v0, float v1) {
                 const int nn = tile * kTileRows + rr;
-                if (nn < a.nout) store_out<EPI, false>(a, gi, t, nn, v0);
+                if (nn >= a.nout) return;
+                if constexpr (PAIRED) store_swiglu(a, gi, t, nn, v0, v1);
+                else store_out<EPI, false>(a, gi, t, nn, v0);
               };
-              // 4 items x 4 contributors: 16 loads in flight per thread
-              reduce_partials<kTcEpi, false, kTileRows, 4, 4>(a.ws, kSlotFloats, nc, gi.c, et,
-                                                              slot_at, store, a.ws_len, a.status);
+              // 16 loads in flight per thread (4 items x 4 contributors), or
+              // 8 for SwiGLU tiles (2 items x 2 contributors x (gate, up)),
+              // whose 64 gate and up sums take most of the registers
+              reduce_partials<kTcEpi, PAIRED, Sh::kStride, PAIRED ? 2 : 4, PAIRED ? 2 : 4>(
+                  a.ws, kSlotFloats, nc, gi.c, et, slot_at, store, a.ws_len, a.status);
             }
           }
           named_bar_sync(1, kTcEpi);
@@ -284,7 +323,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(taddr, kTmemCols);
+    tmem_dealloc(taddr, Sh::kCols);
   }
 }
 
@@ -517,17 +556,20 @@ cudaError_t launch_dense_tc_cluster(const Ctx& cx, bool residual, const void* x,
                   : run_tc_cluster<EPI_BF16>(cx, x, W, res, y, M, N, K, cl);
 }
 
-template <int EPI>
+// PAIRED: W is [2I, K] (gate rows, then up rows) and N = I; y = bf16(silu(x·W1ᵀ)
+// * (x·W3ᵀ)) is [M, I].
+template <int EPI, bool PAIRED = false>
 static cudaError_t run_tc(const Ctx& cx, const void* x, const void* W, const void* res, void* y,
                           int M, int N, int K, int grid, float* ws, int* ctr) {
-  constexpr int SMEM = tc_smem();
+  constexpr int SMEM = tc_smem<PAIRED>();
   static_assert(SMEM <= kMaxDynSmem, "shared memory");
-  auto kern = tc_linear_kernel<EPI>;
+  auto kern = tc_linear_kernel<EPI, PAIRED>;
   static DevOnce once;
   if (cudaError_t e = setup_smem(once, kern, SMEM); e != cudaSuccess) return e;
   const int NP = (M + 15) / 16 * 16;
   CUtensorMap wmap, xmap;
-  if (!make_tmap(&wmap, W, (uint64_t)N, (uint64_t)K, kTileRows, true)) return cudaErrorInvalidValue;
+  if (!make_tmap(&wmap, W, (uint64_t)(PAIRED ? 2 * N : N), (uint64_t)K, kTileRows, true))
+    return cudaErrorInvalidValue;
   if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)K, (uint32_t)NP, false, (uint64_t)cx.ldx))
     return cudaErrorInvalidValue;
   StreamArgs a = {};
@@ -547,8 +589,23 @@ static cudaError_t run_tc(const Ctx& cx, const void* x, const void* W, const voi
   a.ws_len = cx.ws_len;
   a.ctr_len = cx.ctr_len;
   a.timeout_ns = cx.timeout_ns;
+  a.w_up_offset = PAIRED ? N : 0;
+  const long long T = (long long)a.TILES * a.KB;
+  if (grid > T) grid = (int)T;
   return launch_k(kern, dim3(grid), dim3(kTcThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a, NP,
                   umma_idesc_bf16(128, NP));
+}
+
+cudaError_t launch_dense_tc_f32(const Ctx& cx, const void* x, const void* W, float* y, int M, int N,
+                                int K, int grid, float* ws, int* ctr) {
+  if (M < 16 || M > kTcXRows) return cudaErrorInvalidValue;
+  return run_tc<EPI_F32>(cx, x, W, nullptr, y, M, N, K, grid, ws, ctr);
+}
+
+cudaError_t launch_swiglu_tc(const Ctx& cx, const void* x, const void* W13, void* h, int M, int I,
+                             int K, int grid, float* ws, int* ctr) {
+  if (M < 16 || M > kTcXRows) return cudaErrorInvalidValue;
+  return run_tc<EPI_SWIGLU, true>(cx, x, W13, nullptr, h, M, I, K, grid, ws, ctr);
 }
 
 cudaError_t launch_dense_tc(const Ctx& cx, bool residual, const void* x, const void* W,

@@ -46,6 +46,13 @@ cudaError_t launch_dense_wide(const Ctx& cx, int xr, bool mma, bool residual, co
 cudaError_t launch_dense_tc(const Ctx& cx, bool residual, const void* x, const void* W,
                             const void* res, void* y, int M, int N, int K, int grid, float* ws,
                             int* ctr);
+// tcgen05 projection with an fp32 output (no residual), 16 <= M <= 64.
+cudaError_t launch_dense_tc_f32(const Ctx& cx, const void* x, const void* W, float* y, int M, int N,
+                                int K, int grid, float* ws, int* ctr);
+// tcgen05 SwiGLU gate/up: W13 [2I, K] (gate rows, then up rows), h = bf16(silu(x·W1ᵀ) *
+// (x·W3ᵀ)) [M, I], 16 <= M <= 64; stream-K over `grid` CTAs.
+cudaError_t launch_swiglu_tc(const Ctx& cx, const void* x, const void* W13, void* h, int M, int I,
+                             int K, int grid, float* ws, int* ctr);
 // tcgen05 cluster split: cl CTAs per 128-row tile (grid = tiles * cl).
 cudaError_t launch_dense_tc_cluster(const Ctx& cx, bool residual, const void* x, const void* W,
                                     const void* res, void* y, int M, int N, int K, int cl);

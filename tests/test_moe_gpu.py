@@ -285,3 +285,29 @@ def test_workspace_relayout_within_its_capacity():
     for E in (40, 44, 48):
         blk = _small_block(6, 192, E, 96, 4, ("moe-relayout", E))
         _check(*blk, 4, "E=%d after a smaller block" % E)
+
+
+@pytest.mark.parametrize("M,H,I", [(17, 7168, 2048), (33, 7168, 2048), (64, 7168, 2048),
+                                   (20, 520, 328), (48, 1032, 584)])
+def test_shared_expert_on_tensor_cores(M, H, I):
+    # From 17 tokens the shared expert's gate/up (SwiGLU, gate and up
+    # accumulators in tensor memory) and down projections run on tcgen05. With
+    # the routed down projections zero the block is the shared expert alone:
+    # every element against the oracle, at the full hidden and intermediate
+    # sizes and at ragged ones (tiles and k chunks overhanging). The ragged
+    # intermediate widths are a few hundred: below about 200 the bf16 rounding
+    # of the hidden vector alone (the oracle with that rounding applied)
+    # exceeds the 1e-3 * A term on some elements.
+    E, k = 8, 2
+    key = ("shared-tc", M, H, I)
+    Wr = wl.normal_bf16((E, H), 1.0 / math.sqrt(H), *key, "Wr")
+    x = wl.normal_bf16((M, H), 1.0, *key, "x")
+    t = wl.bits_to_torch
+    W13 = torch.zeros((E, 2 * I, H), dtype=torch.bfloat16, device="cuda")
+    W2 = torch.zeros((E, H, I), dtype=torch.bfloat16, device="cuda")
+    Ws13 = wl.normal_bf16((2 * I, H), 0.02, *key, "Ws13")
+    Ws2 = wl.normal_bf16((H, I), 0.02, *key, "Ws2")
+    out = dg.moe_decode(t(x), t(Wr), W13, W2, t(Ws13), t(Ws2), k)
+    assert dg.sync_check() == dg.DEC_OK
+    s, sA = oracle.expert_mlp(x, Ws13, Ws2, I)
+    assert_within_tol(to_f64(out), s, sA, "shared expert M=%d H=%d I=%d" % (M, H, I))
