@@ -63,7 +63,7 @@ extern "C" {
 
 /* Kernel regimes reported by dec_last_choice (low 8 bits). */
 #define DEC_REGIME_NONE   0
-#define DEC_REGIME_SMALLM 1  /* CUDA-core small-matrix kernel, M <= 2 */
+#define DEC_REGIME_SMALLM 1  /* CUDA-core small-matrix kernels, M <= 2 */
 #define DEC_REGIME_MMA    2  /* split-K with mma.sync tensor cores, 3 <= M <= 16 */
 #define DEC_REGIME_TC     3  /* split-K with tcgen05 tensor cores and TMEM, M >= 17 */
 
@@ -74,14 +74,17 @@ extern "C" {
  *   y : [M,N] bf16 output               1 <= M <= 64, N >= 1, K >= 8, K % 8 == 0
  *
  * Accumulates in fp32 and rounds once to bf16 (nearest even). The kernel is
- * chosen from M: M <= 2 the small-matrix kernel; 3 <= M <= 16 split-K on
+ * chosen from M: M <= 2 the small-matrix kernels; 3 <= M <= 16 split-K on
  * mma.sync; M >= 17 split-K on tcgen05 (at exactly 16 tokens mma.sync streams
- * faster). Split-K partial sums are reduced in a fixed order (by the
- * last-arriving CTA of each output tile, or -- when N has few 128-row tiles,
- * on every kernel -- by the CTAs of one thread-block cluster per tile, in rank
- * order), so the result is identical from run to run. The environment
- * variable DEC_FORCE=smallm|mma|tc
- * overrides the choice (smallm only for M <= 2).
+ * faster). For 1-2 tokens, when K % 64 == 0 and slabs of 8, 16 or 32 whole
+ * weight rows per CTA fill between three quarters of the SMs and all of them,
+ * no CTA splits K (the sum over K stays inside the CTA); otherwise split-K.
+ * Split-K partial sums are reduced in a fixed order (by the last-arriving CTA
+ * of each output tile, or -- when N has few 128-row tiles, on every kernel --
+ * by the CTAs of one thread-block cluster per tile, in rank order), so the
+ * result is identical from run to run. The environment variable
+ * DEC_FORCE=smallm|mma|tc overrides the choice (smallm only for M <= 2);
+ * DEC_FORCE=splitk keeps 1-2 tokens on the split-K kernels.
  * Errors: DEC_EINVAL, DEC_EUNSUPPORTED, DEC_ECUDA, DEC_ENOMEM.
  */
 int dec_linear(const void* x, const void* W, void* y, int M, int N, int K, void* stream);
@@ -209,14 +212,16 @@ int dec_add(const void* a, const void* b, void* out, size_t n, void* stream);
 
 /*
  * dec_last_choice -- regime and split of this thread's last dec_linear* call.
- * [trace-path] Returns regime | (S << 8) | (C << 16) | (Wd << 17) where regime
+ * [trace-path] Returns regime | (S << 8) | (C << 16) | (Wd << 17) | (Sl << 18)
+ * where regime
  * is a DEC_REGIME_* value, S the number of CTAs that share each output tile's
  * K range (1 = none), rounded up, C is 1 when those S CTAs form one
  * thread-block cluster and sum their partial tiles through distributed shared
  * memory (small projections: few 128-row tiles, M <= 16), 0 when the split is
  * the stream-K one with a last-arriver fixup, and Wd is 1 when the output
- * tiles are 256 rows high (large projections at M <= 16). DEC_REGIME_NONE
- * before any call.
+ * tiles are 256 rows high (large projections at M <= 16), and Sl is 1 when
+ * each CTA owned whole weight rows (1-2 tokens, S = 1). DEC_REGIME_NONE before
+ * any call.
  */
 int dec_last_choice(void);
 

@@ -374,6 +374,12 @@ def last_wide() -> bool:
     return bool((lib().dec_last_choice() >> 17) & 1)
 
 
+def last_slab() -> bool:
+    """Whether this thread's last projection call gave each CTA whole weight
+    rows (1-2 tokens, no split over K)."""
+    return bool((lib().dec_last_choice() >> 18) & 1)
+
+
 def last_grid() -> int:
     return lib().dec_last_grid()
 

@@ -23,7 +23,7 @@ LIB = os.path.join(HERE, "libdecgemm.so")
 DEBUG_LIB = os.path.join(HERE, "libdecgemm_debug.so")
 ROOT = os.path.dirname(HERE)
 
-SOURCES = ["api.cu", "k_linear.cu", "k_moe.cu", "k_tc.cu", "k_noalloc.cu"]
+SOURCES = ["api.cu", "k_linear.cu", "k_moe.cu", "k_tc.cu", "k_gemv.cu", "k_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]

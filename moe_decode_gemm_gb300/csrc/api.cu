@@ -47,6 +47,32 @@ bool make_tmap(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, 
   return r == CUDA_SUCCESS;
 }
 
+// Weight rows [N, K] (K % 64 == 0) as a 3-D tensor: element (x, n, j) is
+// W[n][64 j + x]. A box of `rows` rows and `kboxes` 64-wide k blocks lands in
+// shared memory as kboxes x rows lines of 128 bytes (128-byte swizzle), one
+// TMA instruction for what would take `kboxes` 2-D boxes.
+bool make_tmap_slab(CUtensorMap* map, const void* W, uint64_t N, uint64_t K, uint32_t rows,
+                    uint32_t kboxes) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode || N == 0 || K == 0 || (K % 64) != 0) return false;
+  cuuint64_t dims[3] = {64, N, K / 64};
+  cuuint64_t strides[2] = {K * 2, 128};  // bytes: next row, next 64-wide k block
+  cuuint32_t box[3] = {64, rows, kboxes};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(W), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------ device state
 struct Buf {
   void* p = nullptr;
@@ -171,6 +197,11 @@ static int counted(cudaError_t e) {
 }
 
 // ------------------------------------------------------------------ projections
+static bool force_splitk() {
+  const char* f = std::getenv("DEC_FORCE");
+  return f && !std::strcmp(f, "splitk");
+}
+
 static int regime_for(int M) {
   const char* f = std::getenv("DEC_FORCE");
   if (f) {
@@ -214,6 +245,19 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
   if (rc) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int regime = regime_for(M);
+  // 1-2 tokens: R whole weight rows per CTA, no split over K, when the shape
+  // fills the SMs with such slabs (DEC_FORCE=splitk keeps the split-K kernels).
+  if (S == 0 && regime == DEC_REGIME_SMALLM && !force_splitk()) {
+    const int R = gemv_slab_rows(M, N, K, s->sms);
+    if (R) {
+      Ctx cx = make_ctx(s, st);
+      cx.ldx = ldx;
+      t_last_choice = regime | (1 << 8) | (1 << 18);
+      t_last_grid = (N + R - 1) / R;
+      ProbeScope probe(2, st);
+      return counted(launch_gemv_slab(cx, res != nullptr, x, W, res, y, M, N, K, R));
+    }
+  }
   // token rows per stage of the CUDA-core / mma.sync kernel; the tcgen05
   // kernel's partial tiles always hold 64 token columns
   const int xr = regime == DEC_REGIME_TC ? 64 : regime == DEC_REGIME_SMALLM ? 8 : (M <= 16 ? 16 : 64);

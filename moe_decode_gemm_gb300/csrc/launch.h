@@ -12,6 +12,11 @@ namespace dg {
 bool make_tmap(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
                bool l2_promote_256, uint64_t ld = 0);
 
+// Weight rows [N, K] (K % 64 == 0) read in boxes of `rows` rows x `kboxes`
+// 64-wide k blocks (a 3-D view), 128-byte swizzle. Returns false on failure.
+bool make_tmap_slab(CUtensorMap* map, const void* W, uint64_t N, uint64_t K, uint32_t rows,
+                    uint32_t kboxes);
+
 struct Ctx {
   int sms;
   long long timeout_ns;
@@ -41,6 +46,12 @@ cudaError_t launch_dense_cluster(const Ctx& cx, int xr, bool mma, bool residual,
 cudaError_t launch_dense_wide(const Ctx& cx, int xr, bool mma, bool residual, const void* x,
                               const void* W, const void* res, void* y, int M, int N, int K,
                               int grid, float* ws, int* ctr);
+
+// Projection for 1-2 tokens without a split over K: R rows per CTA (R from
+// gemv_slab_rows; 0 there means the shape does not suit it).
+int gemv_slab_rows(int M, int N, int K, int sms);
+cudaError_t launch_gemv_slab(const Ctx& cx, bool residual, const void* x, const void* W,
+                             const void* res, void* y, int M, int N, int K, int R);
 
 // tcgen05 projection for 16 <= M <= 64.
 cudaError_t launch_dense_tc(const Ctx& cx, bool residual, const void* x, const void* W,

@@ -194,9 +194,16 @@ def test_tc_tile_aligned_split(M, N, K):
 # through distributed shared memory.
 
 
+@pytest.fixture
+def split_k_only(monkeypatch):
+    """1-2 tokens on the split-K kernels (the slab kernel would take some of
+    these shapes)."""
+    monkeypatch.setenv("DEC_FORCE", "splitk")
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 4000, 1000), (3, 4000, 1288), (8, 2048, 1160),
                                    (15, 1900, 904), (2, 4096, 4096)])
-def test_cluster_split_shapes(M, N, K):
+def test_cluster_split_shapes(split_k_only, M, N, K):
     # ragged last tile and last k chunk; uneven k shares between the ranks
     y, (regime, cl) = _check_random(M, N, K, ("cluster", M, N, K))
     assert dg.last_cluster() and cl >= 2 and regime == _expect_regime(M)
@@ -206,7 +213,7 @@ def test_cluster_split_shapes(M, N, K):
 
 
 @pytest.mark.parametrize("M", [1, 4, 15])
-def test_cluster_split_integer_inputs_match_stream_k(M):
+def test_cluster_split_integer_inputs_match_stream_k(split_k_only, M):
     # exact fp32 sums: the cluster split, the stream-K split and the oracle
     # give the same bits
     K, N = 2048, 4096
@@ -222,7 +229,7 @@ def test_cluster_split_integer_inputs_match_stream_k(M):
 
 
 @pytest.mark.parametrize("M", [1, 4])
-def test_cluster_split_residual(M):
+def test_cluster_split_residual(split_k_only, M):
     K, N = 1024, 4096
     x = wl.normal_bf16((M, K), 1.0, "cl-res", M, "x")
     W = wl.normal_bf16((N, K), 0.02, "cl-res", M, "W")
@@ -331,3 +338,57 @@ def test_wide_tiles_full_size_7168(M, residual):
     if residual:
         f, A = oracle.residual(r, f, A)
     assert_within_tol(to_f64(y), f, A, "wide tiles M=%d residual=%s" % (M, residual))
+
+
+# ---------------------------------------------------------------- whole-row slabs
+# 1-2 tokens: each CTA owns 8, 16 or 32 whole weight rows over all of K (no
+# split over K, no partial sums leave the CTA) when such slabs fill the SMs.
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 2048, 7168), (2, 2048, 7168), (1, 4096, 4096),
+                                   (2, 1024, 1024), (2, 1100, 4096), (1, 4000, 16384),
+                                   (1, 3700, 2048), (2, 2048, 16384)])
+def test_slab_shapes(M, N, K):
+    # rows per CTA 8 / 16 / 32, a ragged last slab, K up to 16384
+    y, (regime, split) = _check_random(M, N, K, ("slab", M, N, K))
+    assert regime == "smallm" and dg.last_slab() and split == 1 and not dg.last_cluster()
+    y2, _ = _gpu_linear(wl.normal_bf16((M, K), 1.0, "slab", M, N, K, "x"),
+                        wl.normal_bf16((N, K), 0.02, "slab", M, N, K, "W"))
+    assert torch.equal(y, y2), "slab kernel not deterministic"
+
+
+@pytest.mark.parametrize("M", [1, 2])
+def test_slab_integer_inputs_match_oracle_and_split_k(M, monkeypatch):
+    K, N = 4096, 2048
+    x = wl.integer_bf16((M, K), -2, 2, "slab-int", M, "x")
+    W = wl.integer_bf16((N, K), -2, 2, "slab-int", M, "W")
+    y, _ = _gpu_linear(x, W)
+    assert dg.last_slab()
+    ref, _ = oracle.linear(x, W)
+    assert np.array_equal(wl.torch_to_bits(y), oracle.f64_to_bf16_bits(ref))
+    monkeypatch.setenv("DEC_FORCE", "splitk")
+    ys, _ = _gpu_linear(x, W)
+    assert not dg.last_slab()
+    assert torch.equal(y, ys)
+
+
+@pytest.mark.parametrize("M", [1, 2])
+def test_slab_residual_and_row_strided_input(M):
+    K, N, ldx = 4096, 2048, 4160
+    wide = wl.normal_bf16((M, ldx), 1.0, "slab-res", M, "x")
+    W = wl.normal_bf16((N, K), 0.02, "slab-res", M, "W")
+    r = wl.normal_bf16((M, N), 1.0, "slab-res", M, "r")
+    xt = wl.bits_to_torch(wide)[:, :K]
+    y = dg.dec_linear(xt, wl.bits_to_torch(W), residual=wl.bits_to_torch(r))
+    assert dg.last_slab()
+    assert dg.sync_check() == dg.DEC_OK
+    f, A = oracle.linear(wide[:, :K], W)
+    ref, Aref = oracle.residual(r, f, A)
+    assert_within_tol(to_f64(y), ref, Aref, "slab residual M=%d" % M)
+
+
+def test_slab_declines_shapes_it_does_not_fill():
+    # too few rows for three quarters of the SMs, or K not a multiple of 64
+    for M, N, K in [(1, 384, 2048), (1, 4096, 1000), (2, 6000, 2048)]:
+        _check_random(M, N, K, ("slab-no", M, N, K))
+        assert not dg.last_slab(), (M, N, K)
