@@ -14,12 +14,19 @@
     python -m moe_decode_gemm_gb300.profiling case moe TOKENS EXPERTS [CALLS]
     python -m moe_decode_gemm_gb300.profiling case linear M N K [CALLS]
     python -m moe_decode_gemm_gb300.profiling case router TOKENS [CALLS]
+    python -m moe_decode_gemm_gb300.profiling case shared TOKENS [CALLS]
+    python -m moe_decode_gemm_gb300.profiling case prefetch M ON [CALLS]
         A small case to run under `ncu --set full` (needs a GPU): CALLS
         (default 3) MoE blocks of TOKENS tokens over a bank of EXPERTS routed
         experts (hidden 7168, intermediate 2048, top-8, no shared expert),
         or CALLS projections alternating over two weight matrices, or CALLS
         MoE blocks with the full router (384 experts x 7168) and tiny experts
-        (intermediate 16), to profile routing alone. Inputs are
+        (intermediate 16), to profile routing alone, or CALLS MoE blocks with
+        the full-size shared expert over a bank of 8 routed experts (the
+        shared expert's kernels), or CALLS 7168 x 7168 projections of M
+        tokens, each after a write of 256 MB that evicts L2 and -- with ON = 1
+        -- an l2_prefetch of the weight's first half-L2 bytes (for the L2 hit
+        rate of the projection under `ncu --cache-control none`). Inputs are
         seeded and synthetic; each expert is 88 MB, so a bank of 32 (2.8 GB)
         is far larger than L2 and its DRAM counters mean what they say.
 
@@ -54,9 +61,17 @@ def kernel_label(name):
         extra += " CUDA cores" if path == "1" else ""
         return "%s%s [wstream XR=%s S=%s %s %s%s]" % (role, part, xr, st, _EPI.get(epi, epi), tile,
                                                      extra)
-    m = re.search(r"tc_linear_kernel<(\d+)>", name)
+    m = re.search(r"tc_linear_kernel<(\d+)(?:,\s*(\w+))?>", name)
     if m:
+        if m.group(2) in _TRUE:
+            return "shared expert gate/up [tcgen05 SwiGLU]"
+        if m.group(1) == "2":  # the fp32-output instance runs the shared expert's down projection
+            return "shared expert down [tcgen05 fp32]"
         return "projection [tcgen05 %s]" % _EPI.get(m.group(1), m.group(1))
+    m = re.search(r"gemv_slab_kernel<(\d+),\s*(\d+)>", name)
+    if m:
+        return "projection [slab %s rows/CTA %s, CUDA cores]" % (m.group(1),
+                                                                _EPI.get(m.group(2), m.group(2)))
     m = re.search(r"tc_cluster_kernel<(\d+)>", name)
     if m:
         return "projection [tcgen05 %s cluster]" % _EPI.get(m.group(1), m.group(1))
@@ -166,6 +181,37 @@ def case(kind, *args):
             dg.dec_linear(x, Ws[i % 2], y)
         torch.cuda.synchronize()
         print("linear M=%d N=%d K=%d regime=%s calls=%d" % (M, N, K, dg.last_choice(), calls))
+    elif kind == "shared":
+        M = int(args[0])
+        calls = int(args[1]) if len(args) > 1 else 3
+        E, H, I = 8, HIDDEN, INTER
+        W13 = normal_bf16_cuda((E, 2 * I, H), WEIGHT_STD, "profile", "W13s")
+        W2 = normal_bf16_cuda((E, H, I), WEIGHT_STD, "profile", "W2s")
+        Wr = normal_bf16_cuda((E, H), ROUTER_STD, "profile", "Wrs")
+        Ws13 = normal_bf16_cuda((2 * I, H), WEIGHT_STD, "profile", "Ws13")
+        Ws2 = normal_bf16_cuda((H, I), WEIGHT_STD, "profile", "Ws2")
+        x = normal_bf16_cuda((M, H), 1.0, "profile", "xs", M)
+        for _ in range(calls):
+            dg.moe_decode(x, Wr, W13, W2, Ws13, Ws2, 2)
+        torch.cuda.synchronize()
+        print("shared expert tokens=%d calls=%d" % (M, calls))
+    elif kind == "prefetch":
+        M, on = int(args[0]), int(args[1])
+        calls = int(args[2]) if len(args) > 2 else 3
+        H = HIDDEN
+        W = normal_bf16_cuda((H, H), WEIGHT_STD, "profile", "Wq")
+        x = normal_bf16_cuda((M, H), 1.0, "profile", "xq", M)
+        y = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        half_l2 = torch.cuda.get_device_properties(0).L2_cache_size // 2
+        for _ in range(calls):
+            flush.fill_(1)                    # evicts L2
+            if on:
+                dg.l2_prefetch(W.data_ptr(), min(half_l2, W.numel() * 2))
+            torch.cuda.synchronize()
+            dg.dec_linear(x, W, y)
+            torch.cuda.synchronize()
+        print("prefetch M=%d on=%d calls=%d regime=%s" % (M, on, calls, dg.last_choice()))
     else:
         sys.exit(__doc__)
     if dg.sync_check() != 0:
