@@ -22,8 +22,8 @@
         or CALLS projections alternating over two weight matrices, or CALLS
         MoE blocks with the full router (384 experts x 7168) and tiny experts
         (intermediate 16), to profile routing alone, or CALLS MoE blocks with
-        the full-size shared expert over a bank of 8 routed experts (the
-        shared expert's kernels), or CALLS 7168 x 7168 projections of M
+        the full-size shared expert over a bank of 48 routed experts (4.2 GB;
+        the shared expert's kernels), or CALLS 7168 x 7168 projections of M
         tokens, each after a write of 256 MB that evicts L2 and -- with ON = 1
         -- an l2_prefetch of the weight's first half-L2 bytes (for the L2 hit
         rate of the projection under `ncu --cache-control none`). Inputs are
@@ -184,7 +184,8 @@ def case(kind, *args):
     elif kind == "shared":
         M = int(args[0])
         calls = int(args[1]) if len(args) > 1 else 3
-        E, H, I = 8, HIDDEN, INTER
+        E, H, I = 48, HIDDEN, INTER   # enough distinct experts that the shared expert is not
+        #                               given dedicated SMs, as at 16-64 tokens over 384 experts
         W13 = normal_bf16_cuda((E, 2 * I, H), WEIGHT_STD, "profile", "W13s")
         W2 = normal_bf16_cuda((E, H, I), WEIGHT_STD, "profile", "W2s")
         Wr = normal_bf16_cuda((E, H), ROUTER_STD, "profile", "Wrs")
@@ -192,7 +193,7 @@ def case(kind, *args):
         Ws2 = normal_bf16_cuda((H, I), WEIGHT_STD, "profile", "Ws2")
         x = normal_bf16_cuda((M, H), 1.0, "profile", "xs", M)
         for _ in range(calls):
-            dg.moe_decode(x, Wr, W13, W2, Ws13, Ws2, 2)
+            dg.moe_decode(x, Wr, W13, W2, Ws13, Ws2, TOPK)
         torch.cuda.synchronize()
         print("shared expert tokens=%d calls=%d" % (M, calls))
     elif kind == "prefetch":
