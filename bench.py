@@ -118,6 +118,13 @@ def moe_bytes(M, U):
     return 2 * E * H + U * (2 * 2 * I * H + 2 * H * I) + 3 * 2 * I * H + 2 * 2 * M * H
 
 
+def latent_bytes(M, U, Lw):
+    # router rows and latent input rows (one [E + L, H] weight), experts on the
+    # latent width, the up-projection L -> H, the shared expert, x in and out
+    return (2 * (E + Lw) * H + U * (2 * 2 * I * Lw + 2 * Lw * I) + 2 * H * Lw + 3 * 2 * I * H
+            + 2 * 2 * M * H)
+
+
 def layer_bytes(M, U):
     # fused q|kv projection (x read once), o projection, residual add fused
     return linear_bytes(M, H + KV, H) + linear_bytes(M, H, H) + 2 * M * H + moe_bytes(M, U)
@@ -276,8 +283,38 @@ def per_config(dg, torch, dev, layer0, peak_gbs, cpu=True):
             row["gpu_over_cpu"] = round(cus / us, 1)
         blocks.append(row)
     out["moe_block"] = blocks
-    out["timing"] = ("CUDA graph of 20 calls (10 for the MoE block), best of 3 replays; weights "
-                     "rotate through copies 4x L2 (the MoE bank is 34 GB)")
+    # The latent MoE block: layer 0's router and shared expert, the routed
+    # experts on a 512-wide latent (a bank of its own, 2.4 GB), the latent
+    # input projection stacked under the router rows, the up-projection back to
+    # the hidden width.
+    LAT = 512
+    W13l = wl.normal_bf16_cuda((E, 2 * I, LAT), wl.WEIGHT_STD, "cfg-latent", "W13", device=dev)
+    W2l = wl.normal_bf16_cuda((E, LAT, I), wl.WEIGHT_STD, "cfg-latent", "W2", device=dev)
+    Wup = wl.normal_bf16_cuda((H, LAT), wl.WEIGHT_STD, "cfg-latent", "Wup", device=dev)
+    Wd = wl.normal_bf16_cuda((LAT, H), wl.ROUTER_STD, "cfg-latent", "Wd", device=dev)
+    Wrl = torch.cat([L.Wr, Wd]).contiguous()
+    lat = []
+    for M in BATCHES:
+        # four token sets in turn, so that consecutive calls choose different
+        # experts and the bank (2.4 GB) is not read back from L2
+        xs = [wl.bits_to_torch(wl.token_rows(M, H, "cfg-latent", M, j), device=dev)
+              for j in range(4)]
+        o = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+        idxs = [torch.empty((M, K8), dtype=torch.int32, device=dev) for _ in range(4)]
+        us = _graph_us(torch, lambda i: dg.moe_decode_latent(
+            xs[i % 4], Wrl, W13l, W2l, Wup, L.Ws13, L.Ws2, K8, out=o, topk_idx=idxs[i % 4],
+            stream=s), s, reps=12)
+        U = sum(len(set(t.cpu().numpy().ravel().tolist())) for t in idxs) / 4.0
+        tbps = latent_bytes(M, U, LAT) / us / 1e6
+        lat.append({"M": M, "latent": LAT, "us": round(us, 2), "TBps": round(tbps, 3),
+                    "pct_of_peak": round(100 * tbps * 1e3 / peak_gbs, 1),
+                    "active_experts": round(U, 1)})
+    out["latent_block"] = lat
+    del W13l, W2l, Wup, Wd, Wrl
+    torch.cuda.empty_cache()
+    out["timing"] = ("CUDA graph of 20 calls (10 for the MoE block, 12 for the latent one), best of 3 "
+                     "replays; weights rotate through copies 4x L2 (the MoE bank is 34 GB, the "
+                     "latent one 2.4 GB)")
     if cpu:
         out["cpu_oracle"] = ("fp64 oracle on %d host threads, same input bits, wall µs per call "
                              "(mean over ~2 s; expert weights copied before timing)"

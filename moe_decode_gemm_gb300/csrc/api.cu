@@ -197,10 +197,15 @@ static int counted(cudaError_t e) {
 }
 
 // ------------------------------------------------------------------ projections
-static bool force_splitk() {
+static bool forced(const char* what) {
   const char* f = std::getenv("DEC_FORCE");
-  return f && !std::strcmp(f, "splitk");
+  return f && !std::strcmp(f, what);
 }
+
+static bool force_splitk() { return forced("splitk"); }
+
+// Most tokens the whole-row slabs take (see linear_impl).
+constexpr int kMmaSlabMaxM = 4;
 
 static int regime_for(int M) {
   const char* f = std::getenv("DEC_FORCE");
@@ -245,17 +250,30 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
   if (rc) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int regime = regime_for(M);
-  // 1-2 tokens: R whole weight rows per CTA, no split over K, when the shape
-  // fills the SMs with such slabs (DEC_FORCE=splitk keeps the split-K kernels).
-  if (S == 0 && regime == DEC_REGIME_SMALLM && !force_splitk()) {
-    const int R = gemv_slab_rows(M, N, K, s->sms);
-    if (R) {
+  // Whole-row slabs (R weight rows per CTA, no split over K) when such slabs
+  // fill between three quarters of the SMs and all of them: up to 4 tokens on
+  // the tensor cores (16 or 32 rows per CTA), 1-2 tokens on the CUDA cores
+  // where only 8 rows per CTA fill the SMs (or under DEC_FORCE=smallm).
+  // Same-GPU A/B, us per call in a CUDA graph, N x K = 2048 x 7168, split-K ->
+  // slab: M = 1 8.0 -> 6.7 (CUDA cores 6.8), M = 2 8.3 -> 6.7 (7.8), M = 3
+  // 8.6 -> 6.9, M = 4 8.7 -> 7.1; 4096 x 4096 at M = 1 8.6 -> 7.1 (7.5); M = 8
+  // gains nothing (8.9 both) and 16 tokens lose (9.6 -> 13.8): every CTA reads
+  // every token row, and at 16 tokens those reads match the weight bytes.
+  // DEC_FORCE=splitk keeps the split-K kernels.
+  if (S == 0 && !force_splitk()) {
+    const bool core_only = forced("smallm");
+    const int Rm = (M <= kMmaSlabMaxM && regime != DEC_REGIME_TC && !core_only)
+                       ? gemv_mma_rows(M, N, K, s->sms) : 0;
+    const int Rc = (!Rm && regime == DEC_REGIME_SMALLM) ? gemv_slab_rows(M, N, K, s->sms) : 0;
+    if (Rm || Rc) {
       Ctx cx = make_ctx(s, st);
       cx.ldx = ldx;
-      t_last_choice = regime | (1 << 8) | (1 << 18);
+      const int R = Rm ? Rm : Rc;
+      t_last_choice = (Rm ? DEC_REGIME_MMA : DEC_REGIME_SMALLM) | (1 << 8) | (1 << 18);
       t_last_grid = (N + R - 1) / R;
       ProbeScope probe(2, st);
-      return counted(launch_gemv_slab(cx, res != nullptr, x, W, res, y, M, N, K, R));
+      return counted(Rm ? launch_gemv_mma(cx, res != nullptr, x, W, res, y, M, N, K, Rm)
+                        : launch_gemv_slab(cx, res != nullptr, x, W, res, y, M, N, K, Rc));
     }
   }
   // token rows per stage of the CUDA-core / mma.sync kernel; the tcgen05

@@ -1,4 +1,4 @@
-// k_gemv.cu -- decode projection y = x·Wᵀ for 1-2 tokens without splitting K
+// k_gemv.cu -- decode projection y = x·Wᵀ for 1-4 tokens without splitting K
 // across CTAs: each CTA owns R consecutive weight rows (R = 8, 16 or 32) over
 // the whole K, so no partial sums leave the CTA -- no workspace, counters,
 // atomics or cluster barriers. What split-K spends after the last weight
@@ -6,15 +6,19 @@
 // partial tiles and the barrier that keeps partials alive) is gone; the sum
 // over K ends with a reduction inside the CTA.
 //
-// One producer thread streams stages of 32 KB of weights, each R rows x
-// 16384/R k, with one 3-D TMA box (rows x k blocks of 64, 128-byte swizzle),
+// Two kernels share that plan. In both, one producer thread streams stages
+// of weights with one 3-D TMA box (R rows x k blocks of 64, 128-byte swizzle)
 // and the tokens' matching k range (a bulk copy per token, issued once the
 // previous kernel has finished; the weights of the first stages are in
-// flight before that). Eight consumer warps split each stage by k block:
-// lane l of warp w takes row l % R of k block w*(32/R) + l/R and its 8 chunks
-// of 16 bytes, multiplying them with the tokens' matching chunks
+// flight before that), and eight consumer warps split each stage by k block.
+//
+// gemv_slab_kernel (1-2 tokens, CUDA cores): 32 KB stages of R rows x 16384/R
+// k; lane l of warp w takes row l % R of k block w*(32/R) + l/R and its 8
+// chunks of 16 bytes, multiplying them with the tokens' matching chunks
 // (fma.rn.f32.bf16, fp32 sums). The 32/R lanes of a row and then the 8 warps
 // are summed in a fixed order, so results do not vary from run to run.
+//
+// gemv_mma_kernel (1-4 tokens, mma.sync): see its own comment below.
 //
 // "vLLM 如何用智能体辅助优化 Kimi K3 解码性能", Part 1 §1 "针对工作负载调优形状"
 // (a small-matrix kernel for batch 1-2).
@@ -28,7 +32,8 @@ namespace dg {
 
 constexpr int kGvStage = 32768;         // weight bytes per stage
 constexpr int kGvThreads = 9 * 32;      // producer warp + 8 consumer warps
-constexpr int kGvMaxTokens = 2;
+constexpr int kGvMaxTokens = 2;        // CUDA-core slabs
+constexpr int kMmaMaxTokens = 4;       // tensor-core slabs
 
 // Bytes of one stage: the weights, then each token's k range (16384/R k).
 constexpr int gemv_stage_bytes(int R) { return kGvStage + kGvMaxTokens * (kGvStage / R); }
@@ -177,6 +182,214 @@ __global__ void __launch_bounds__(kGvThreads, 2)
   __syncthreads();
 }
 
+// ---------------------------------------------------------------- mma slabs
+// The same whole-row slabs for up to 4 tokens with the dot products on the
+// tensor cores (mma.sync.m16n8k16: the weights are the 16-row operand, the
+// tokens the 8-column one, columns past M zero). On the CUDA cores the
+// multiply-adds of a stage cost more than its copies once the dependency has
+// resolved (~0.5 us per 32 KB stage of one token; a copy of the kernel with
+// them left out was 1-2 us faster per call), while a stage here is 32 MMAs.
+// A stage is KBS k blocks of 64 of the CTA's R rows (16 KB of weights: one
+// 3-D TMA box, 128-byte swizzle) and the tokens' matching k range, one bulk
+// copy per token into rows padded by 16 bytes, so that the token rows of a B
+// fragment fall in distinct banks. Task j of a stage (row group j % (R/16),
+// k block j / (R/16)) goes to warp j % 8; a warp keeps one accumulator tile
+// over all its tasks, and the warps of a row group are summed in order at the
+// end, so results do not vary from run to run. Every CTA reads every token
+// row: at 16 tokens those reads match the weight bytes and the slabs lose to
+// the split-K kernels, which is why they stop at 4.
+template <int R, int XR, int KBS>
+struct MmaSlab {
+  static constexpr int RG = R / 16;                     // 16-row groups
+  static constexpr int XN = (XR + 7) / 8;               // 8-token column tiles
+  static constexpr int KS = KBS * 64;                   // k per stage
+  static constexpr int WB = R * KS * 2;                 // weight bytes per stage
+  static constexpr int XS = KS + 8;                     // token row stride (elements)
+  static constexpr int SB = (WB + XR * XS * 2 + 1023) / 1024 * 1024;
+  static constexpr int RED = kNCW * 16 * XN * 8 * 4;    // per-warp tiles for the final sum
+  static constexpr int FIXED = 1024 + RED + 256;        // alignment, tiles, barriers, flags
+  static constexpr int STAGES = (115712 - FIXED) / SB;  // two CTAs per SM
+  static constexpr int SMEM = FIXED + STAGES * SB;
+  static_assert((RG * KBS) % kNCW == 0, "whole tasks per warp");
+  static_assert(STAGES >= 2, "ring depth");
+};
+
+template <int R, int XR, int KBS, int EPI>
+__global__ void __launch_bounds__(kGvThreads, 2)
+    gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const uint16_t* x, long long ldx,
+                    const StreamArgs a) {
+  using P = MmaSlab<R, XR, KBS>;
+  constexpr int STAGES = P::STAGES, KS = P::KS, SB = P::SB, XS = P::XS, RG = P::RG;
+  constexpr int XN = P::XN, XM = XN * 8;               // token columns of the tiles
+  constexpr int TPW = RG * KBS / kNCW;                 // tasks per warp per stage
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int M = a.M, K = a.K;
+  float* red = reinterpret_cast<float*>(smem + STAGES * SB);     // [warp][16][XM]
+  // (M <= XR token rows are copied; columns from M on are zero)
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * SB + P::RED);
+  uint64_t* empty = full + STAGES;
+  volatile int* s_flags = reinterpret_cast<volatile int*>(empty + STAGES);  // [0] abort
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kNCW);
+    }
+    s_flags[0] = 0;
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 32) prefetch_tmap(&wmap);
+  __syncthreads();
+  griddep_launch_dependents();
+
+  const int row0 = blockIdx.x * R;
+  const int nst = (K + KS - 1) / KS;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      auto xbytes = [&](int i) -> uint32_t {
+        const int n = K - i * KS;
+        return (uint32_t)((n < KS ? n : KS) * 2);
+      };
+      auto issue_x = [&](int s, int i) {
+        uint16_t* xs = reinterpret_cast<uint16_t*>(smem + s * SB + P::WB);
+        for (int m = 0; m < M; ++m)
+          bulk_copy_g2s(xs + m * XS, x + m * ldx + (long long)i * KS, xbytes(i), &full[s]);
+      };
+      const int npre = nst < STAGES ? nst : STAGES;
+      int i = 0;
+      for (; i < npre; ++i) {
+        mbar_arrive_expect_tx(&full[i], P::WB + M * xbytes(i));
+        tma_load_3d(smem + i * SB, &wmap, 0, row0, i * KBS, &full[i], pol_w);
+      }
+      griddep_wait();
+      for (int j = 0; j < npre; ++j) issue_x(j, j);
+      for (; i < nst; ++i) {
+        const int s = i % STAGES;
+        if (!mbar_wait(&empty[s], ((i / STAGES) + 1) & 1, a.timeout_ns, a.status)) {
+          s_flags[0] = 1;
+          break;
+        }
+        if (s_flags[0]) break;
+        mbar_arrive_expect_tx(&full[s], P::WB + M * xbytes(i));
+        tma_load_3d(smem + s * SB, &wmap, 0, row0, i * KBS, &full[s], pol_w);
+        issue_x(s, i);
+      }
+      // Drain: every issued copy has landed before the CTA may exit.
+      const int issued = i;
+      for (int s = 0; s < STAGES && s < issued; ++s) {
+        const int uses = (issued - s + STAGES - 1) / STAGES;
+        mbar_wait(&full[s], (uses - 1) & 1, drain_ns(a.timeout_ns), nullptr);
+      }
+    } else {
+      griddep_wait();
+    }
+  } else {
+    // ---------------------------------------------------------------- consumers
+    griddep_wait();
+    const int w = warp - 1;
+    const int rg = w % RG;                   // this warp's row group (every task of it)
+    const int mi = lane >> 3, r8 = lane & 7;
+    const int a_row = rg * 16 + (mi & 1) * 8 + r8;
+    const int bn = lane >> 2, bk = (lane & 3) * 2;  // B fragment: token, k pair
+    float d[XN][4];
+#pragma unroll
+    for (int nt = 0; nt < XN; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) d[nt][e] = 0.f;
+    for (int i = 0; i < nst; ++i) {
+      const int s = i % STAGES;
+      if (!s_flags[0]) {
+        if (!mbar_wait(&full[s], (i / STAGES) & 1, a.timeout_ns, a.status)) s_flags[0] = 1;
+      }
+      if (!s_flags[0]) {
+        const uint32_t wst = smem_u32(smem + s * SB);
+        const uint16_t* xs = reinterpret_cast<const uint16_t*>(smem + s * SB + P::WB);
+#pragma unroll
+        for (int q = 0; q < TPW; ++q) {
+          const int kb = (w + q * kNCW) / RG;         // k block of this task within the stage
+          if ((i * KBS + kb) * 64 < K) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              uint32_t af[4];
+              const int ach = kk * 2 + (mi >> 1);
+              ldmatrix_x4(af[0], af[1], af[2], af[3],
+                          wst + (kb * R + a_row) * 128 + ((ach ^ r8) << 4));
+              const int kx = kb * 64 + kk * 16 + bk;  // k of this lane's B pair in the stage
+#pragma unroll
+              for (int nt = 0; nt < XN; ++nt) {
+                const int t = nt * 8 + bn;
+                uint32_t b0 = 0u, b1 = 0u;
+                if (t < M) {
+                  b0 = *reinterpret_cast<const uint32_t*>(xs + t * XS + kx);
+                  b1 = *reinterpret_cast<const uint32_t*>(xs + t * XS + kx + 8);
+                }
+                if (nt * 8 < M) mma_bf16_16816(d[nt], af, b0, b1);
+              }
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    // this warp's tile of its row group: rows g, g + 8; tokens 2(l%4), +1
+    const int g = lane >> 2, tc = (lane & 3) * 2;
+#pragma unroll
+    for (int nt = 0; nt < XN; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int rr = g + (e >> 1) * 8, t = nt * 8 + tc + (e & 1);
+        red[(w * 16 + rr) * XM + t] = d[nt][e];
+      }
+    named_bar_sync(1, kNCW * 32);
+    const int ct = threadIdx.x - 32;
+    if (!s_flags[0])
+      for (int e = ct; e < R * M; e += kNCW * 32) {
+        const int r = e % R, t = e / R;
+        const int grp = r / 16, rr = r % 16;
+        float v = 0.f;
+#pragma unroll
+        for (int q = grp; q < kNCW; q += RG) v += red[(q * 16 + rr) * XM + t];
+        const int n = row0 + r;
+        if (n < a.nout) store_out<EPI, false>(a, GroupInfo{0, 0, M}, t, n, v);
+      }
+  }
+  __syncthreads();
+}
+
+template <int R, int XR, int KBS, int EPI>
+static cudaError_t run_gemv_mma(const Ctx& cx, const void* x, long long ldx, const void* W,
+                                const void* res, void* y, int M, int N, int K) {
+  if (M > XR) return cudaErrorInvalidValue;
+  auto kern = gemv_mma_kernel<R, XR, KBS, EPI>;
+  constexpr int SMEM = MmaSlab<R, XR, KBS>::SMEM;
+  static_assert(2 * (SMEM + 1024) <= kSmemPerSm, "two CTAs per SM");
+  static DevOnce once;
+  if (cudaError_t e = setup_smem(once, kern, SMEM, true); e != cudaSuccess) return e;
+  CUtensorMap wmap;
+  if (!make_tmap_slab(&wmap, W, (uint64_t)N, (uint64_t)K, R, KBS)) return cudaErrorInvalidValue;
+  StreamArgs a = {};
+  a.K = K;
+  a.nout = N;
+  a.M = M;
+  a.out = y;
+  a.ldo = N;
+  a.res = reinterpret_cast<const uint16_t*>(res);
+  a.status = cx.status;
+  a.timeout_ns = cx.timeout_ns;
+  a.out_len = (long long)M * N;
+  a.res_len = res ? (long long)M * N : 0;
+  const int grid = (N + R - 1) / R;
+  return launch_k(kern, dim3(grid), dim3(kGvThreads), SMEM, cx.stream, cx.pdl, wmap,
+                  reinterpret_cast<const uint16_t*>(x), ldx, a);
+}
+
 template <int R, int EPI>
 static cudaError_t run_gemv(const Ctx& cx, const void* x, long long ldx, const void* W,
                             const void* res, void* y, int M, int N, int K) {
@@ -214,6 +427,32 @@ int gemv_slab_rows(int M, int N, int K, int sms) {
     if (grid <= sms) return grid * 4 < 3LL * sms ? 0 : R;
   }
   return 0;
+}
+
+// Rows per CTA for the mma slabs: 16 or 32 (one or two 16-row groups), by the
+// same rule; up to kMmaMaxTokens tokens.
+int gemv_mma_rows(int M, int N, int K, int sms) {
+  if (M < 1 || M > kMmaMaxTokens || (K % 64) != 0) return 0;
+  for (int R = 16; R <= 32; R <<= 1) {
+    const long long grid = ((long long)N + R - 1) / R;
+    if (grid <= sms) return grid * 4 < 3LL * sms ? 0 : R;
+  }
+  return 0;
+}
+
+template <int R, int XR, int KBS>
+static cudaError_t mma_epi(const Ctx& cx, bool residual, const void* x, long long ldx,
+                           const void* W, const void* res, void* y, int M, int N, int K) {
+  return residual ? run_gemv_mma<R, XR, KBS, EPI_BF16_RES>(cx, x, ldx, W, res, y, M, N, K)
+                  : run_gemv_mma<R, XR, KBS, EPI_BF16>(cx, x, ldx, W, res, y, M, N, K);
+}
+
+cudaError_t launch_gemv_mma(const Ctx& cx, bool residual, const void* x, const void* W,
+                            const void* res, void* y, int M, int N, int K, int R) {
+  const long long ldx = cx.ldx ? cx.ldx : K;
+  if (R == 16) return mma_epi<16, kMmaMaxTokens, 8>(cx, residual, x, ldx, W, res, y, M, N, K);
+  if (R == 32) return mma_epi<32, kMmaMaxTokens, 4>(cx, residual, x, ldx, W, res, y, M, N, K);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gemv_slab(const Ctx& cx, bool residual, const void* x, const void* W,

@@ -53,6 +53,12 @@ int gemv_slab_rows(int M, int N, int K, int sms);
 cudaError_t launch_gemv_slab(const Ctx& cx, bool residual, const void* x, const void* W,
                              const void* res, void* y, int M, int N, int K, int R);
 
+// The same slabs for up to 4 tokens with mma.sync dot products: R = 16 or 32
+// rows per CTA (R from gemv_mma_rows; 0 means the shape does not suit it).
+int gemv_mma_rows(int M, int N, int K, int sms);
+cudaError_t launch_gemv_mma(const Ctx& cx, bool residual, const void* x, const void* W,
+                            const void* res, void* y, int M, int N, int K, int R);
+
 // tcgen05 projection for 16 <= M <= 64.
 cudaError_t launch_dense_tc(const Ctx& cx, bool residual, const void* x, const void* W,
                             const void* res, void* y, int M, int N, int K, int grid, float* ws,

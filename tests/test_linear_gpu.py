@@ -28,7 +28,13 @@ import moe_decode_gemm_gb300 as dg  # noqa: E402
 
 
 def _expect_regime(M):
+    """The split-K kernels' regime for M tokens."""
     return "smallm" if M <= 2 else ("mma" if M <= 16 else "tc")
+
+
+def _expect_path(M):
+    """The regime of the last call: 1-4 tokens on whole-row slabs run on mma.sync."""
+    return "mma" if dg.last_slab() and M <= 4 else _expect_regime(M)
 
 
 def _gpu_linear(x_bits, W_bits, S=None, res_bits=None):
@@ -60,8 +66,8 @@ def _check_random(M, N, K, key, cols=None, S=None):
 
 def test_single_projection_m1_4096():
     # M=1, K=N=4096, x ~N(0,1), W ~N(0,0.02), seed 0
-    _, (regime, _) = _check_random(1, 4096, 4096, ("cfg1", 0))
-    assert regime == "smallm"
+    _, (regime, split) = _check_random(1, 4096, 4096, ("cfg1", 0))
+    assert regime == "mma" and dg.last_slab() and split == 1   # 32-row tensor-core slabs
 
 
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 8, 15, 16, 17, 32, 33, 64])
@@ -124,7 +130,8 @@ def test_batch_sweep_k7168(M, N):
     # sample of 384 output columns
     cols = np.random.default_rng(N + M).choice(N, 384, replace=False)
     _, (regime, _) = _check_random(M, N, 7168, ("cfg2", M, N), cols=cols)
-    assert regime == _expect_regime(M)
+    assert regime == _expect_path(M)
+    assert dg.last_slab() == (N == 2048 and M <= 4)
 
 
 @pytest.mark.parametrize("M", [1, 4, 16, 64])
@@ -341,14 +348,22 @@ def test_wide_tiles_full_size_7168(M, residual):
 
 
 # ---------------------------------------------------------------- whole-row slabs
-# 1-2 tokens: each CTA owns 8, 16 or 32 whole weight rows over all of K (no
-# split over K, no partial sums leave the CTA) when such slabs fill the SMs.
+# 1-2 tokens on the CUDA cores: each CTA owns 8, 16 or 32 whole weight rows
+# over all of K (no split over K, no partial sums leave the CTA) when such
+# slabs fill the SMs. The dispatcher takes them where only 8-row slabs fill
+# the SMs (else the tensor-core slabs below); DEC_FORCE=smallm takes them
+# wherever they fit.
+
+
+@pytest.fixture
+def core_slabs(monkeypatch):
+    monkeypatch.setenv("DEC_FORCE", "smallm")
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 2048, 7168), (2, 2048, 7168), (1, 4096, 4096),
                                    (2, 1024, 1024), (2, 1100, 4096), (1, 4000, 16384),
                                    (1, 3700, 2048), (2, 2048, 16384)])
-def test_slab_shapes(M, N, K):
+def test_slab_shapes(core_slabs, M, N, K):
     # rows per CTA 8 / 16 / 32, a ragged last slab, K up to 16384
     y, (regime, split) = _check_random(M, N, K, ("slab", M, N, K))
     assert regime == "smallm" and dg.last_slab() and split == 1 and not dg.last_cluster()
@@ -359,6 +374,7 @@ def test_slab_shapes(M, N, K):
 
 @pytest.mark.parametrize("M", [1, 2])
 def test_slab_integer_inputs_match_oracle_and_split_k(M, monkeypatch):
+    monkeypatch.setenv("DEC_FORCE", "smallm")
     K, N = 4096, 2048
     x = wl.integer_bf16((M, K), -2, 2, "slab-int", M, "x")
     W = wl.integer_bf16((N, K), -2, 2, "slab-int", M, "W")
@@ -373,7 +389,7 @@ def test_slab_integer_inputs_match_oracle_and_split_k(M, monkeypatch):
 
 
 @pytest.mark.parametrize("M", [1, 2])
-def test_slab_residual_and_row_strided_input(M):
+def test_slab_residual_and_row_strided_input(core_slabs, M):
     K, N, ldx = 4096, 2048, 4160
     wide = wl.normal_bf16((M, ldx), 1.0, "slab-res", M, "x")
     W = wl.normal_bf16((N, K), 0.02, "slab-res", M, "W")
@@ -387,8 +403,85 @@ def test_slab_residual_and_row_strided_input(M):
     assert_within_tol(to_f64(y), ref, Aref, "slab residual M=%d" % M)
 
 
-def test_slab_declines_shapes_it_does_not_fill():
+@pytest.mark.parametrize("M,N", [(1, 1024), (2, 1100)])
+def test_dispatcher_takes_cuda_core_slabs_of_8_rows(M, N):
+    # 16-row slabs would leave half the SMs idle: 8-row ones on the CUDA cores
+    y, (regime, split) = _check_random(M, N, 4096, ("slab8", M, N))
+    assert regime == "smallm" and dg.last_slab() and split == 1
+
+
+def test_slab_declines_shapes_it_does_not_fill(core_slabs):
     # too few rows for three quarters of the SMs, or K not a multiple of 64
     for M, N, K in [(1, 384, 2048), (1, 4096, 1000), (2, 6000, 2048)]:
         _check_random(M, N, K, ("slab-no", M, N, K))
+        assert not dg.last_slab(), (M, N, K)
+
+
+# ---------------------------------------------------------------- tensor-core slabs
+# 1-4 tokens: the same whole-row slabs (16 or 32 rows per CTA), with the dot
+# products on the tensor cores (mma.sync).
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 2048, 7168), (2, 2048, 7168), (3, 2048, 7168),
+                                   (4, 4096, 4096), (1, 4096, 4096), (3, 3700, 2048),
+                                   (4, 2000, 1024), (2, 2048, 16384), (4, 4096, 1088)])
+def test_mma_slab_shapes(M, N, K):
+    # 16 / 32 rows per CTA, ragged last slab, K from 1024 to 16384 (1088: a
+    # last stage with one k block of 64)
+    y, (regime, split) = _check_random(M, N, K, ("mslab", M, N, K))
+    assert regime == "mma" and dg.last_slab() and split == 1 and not dg.last_cluster()
+    y2, _ = _gpu_linear(wl.normal_bf16((M, K), 1.0, "mslab", M, N, K, "x"),
+                        wl.normal_bf16((N, K), 0.02, "mslab", M, N, K, "W"))
+    assert torch.equal(y, y2), "mma slab kernel not deterministic"
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+def test_mma_slab_integer_inputs_match_oracle_and_split_k(M, monkeypatch):
+    K, N = 4096, 2048
+    x = wl.integer_bf16((M, K), -2, 2, "mslab-int", M, "x")
+    W = wl.integer_bf16((N, K), -2, 2, "mslab-int", M, "W")
+    y, _ = _gpu_linear(x, W)
+    assert dg.last_slab()
+    ref, _ = oracle.linear(x, W)
+    assert np.array_equal(wl.torch_to_bits(y), oracle.f64_to_bf16_bits(ref))
+    monkeypatch.setenv("DEC_FORCE", "splitk")
+    ys, _ = _gpu_linear(x, W)
+    assert not dg.last_slab()
+    assert torch.equal(y, ys)
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_mma_slab_residual_and_row_strided_input(M):
+    K, N, ldx = 4096, 2048, 4160
+    wide = wl.normal_bf16((M, ldx), 1.0, "mslab-res", M, "x")
+    W = wl.normal_bf16((N, K), 0.02, "mslab-res", M, "W")
+    r = wl.normal_bf16((M, N), 1.0, "mslab-res", M, "r")
+    xt = wl.bits_to_torch(wide)[:, :K]
+    y = dg.dec_linear(xt, wl.bits_to_torch(W), residual=wl.bits_to_torch(r))
+    assert dg.last_slab() and dg.last_choice()[0] == "mma"
+    assert dg.sync_check() == dg.DEC_OK
+    f, A = oracle.linear(wide[:, :K], W)
+    ref, Aref = oracle.residual(r, f, A)
+    assert_within_tol(to_f64(y), ref, Aref, "mma slab residual M=%d" % M)
+
+
+@pytest.mark.parametrize("M", [1, 2])
+def test_mma_slab_for_one_or_two_tokens_matches_the_cuda_core_slab(M, monkeypatch):
+    K, N = 7168, 2048
+    x = wl.integer_bf16((M, K), -2, 2, "mslab-12", M, "x")
+    W = wl.integer_bf16((N, K), -2, 2, "mslab-12", M, "W")
+    ym, (regime, _) = _gpu_linear(x, W)
+    assert regime == "mma" and dg.last_slab()
+    monkeypatch.setenv("DEC_FORCE", "smallm")
+    y, (regime, _) = _gpu_linear(x, W)
+    assert regime == "smallm" and dg.last_slab()
+    assert torch.equal(y, ym)
+
+
+def test_mma_slab_declines_shapes_it_does_not_fill():
+    # too few rows for three quarters of the SMs, K not a multiple of 64,
+    # too many rows for 32 per CTA, more than 4 tokens
+    for M, N, K in [(4, 1024, 4096), (3, 4096, 1000), (4, 6000, 2048), (5, 2048, 7168),
+                    (16, 2048, 7168)]:
+        _check_random(M, N, K, ("mslab-no", M, N, K))
         assert not dg.last_slab(), (M, N, K)

@@ -25,6 +25,14 @@ def test_labels_of_every_kernel_family():
             "projection [tcgen05 bf16+residual]",
         "void dg::tc_cluster_kernel<0>(CUtensorMap_st, CUtensorMap_st, dg::StreamArgs, int, unsigned int)":
             "projection [tcgen05 bf16 cluster]",
+        "void dg::tc_linear_kernel<3, true>(CUtensorMap_st, CUtensorMap_st, dg::StreamArgs, int, unsigned int)":
+            "shared expert gate/up [tcgen05 SwiGLU]",
+        "void dg::tc_linear_kernel<2, false>(CUtensorMap_st, CUtensorMap_st, dg::StreamArgs, int, unsigned int)":
+            "shared expert down [tcgen05 fp32]",
+        "void dg::gemv_slab_kernel<8, 0>(CUtensorMap_st, const unsigned short *, long long, dg::StreamArgs)":
+            "projection [slab 8 rows/CTA bf16, CUDA cores]",
+        "void dg::gemv_mma_kernel<32, 4, 4, 1>(CUtensorMap_st, const unsigned short *, long long, dg::StreamArgs)":
+            "projection [slab 32 rows/CTA bf16+residual, mma.sync]",
         "dg::schedule_gather_kernel(const uint4 *, const int *, int, int, int, int, uint4 *, int *)":
             "schedule + gather",
         "dg::combine_kernel(const float *, const float *, const float *)": "combine",
