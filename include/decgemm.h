@@ -64,7 +64,7 @@ extern "C" {
 /* Kernel regimes reported by dec_last_choice (low 8 bits). */
 #define DEC_REGIME_NONE   0
 #define DEC_REGIME_SMALLM 1  /* CUDA-core small-matrix kernels, M <= 2 */
-#define DEC_REGIME_MMA    2  /* mma.sync: split-K at 3 <= M <= 16, whole-row slabs at M <= 4 */
+#define DEC_REGIME_MMA    2  /* mma.sync: split-K at 3 <= M <= 16, whole-row slabs at M <= 16 */
 #define DEC_REGIME_TC     3  /* split-K with tcgen05 tensor cores and TMEM, M >= 17 */
 
 /*
@@ -76,7 +76,7 @@ extern "C" {
  * Accumulates in fp32 and rounds once to bf16 (nearest even). The kernel is
  * chosen from M: M <= 2 the small-matrix kernels; 3 <= M <= 16 split-K on
  * mma.sync; M >= 17 split-K on tcgen05 (at exactly 16 tokens mma.sync streams
- * faster). For 1-4 tokens, when K % 64 == 0 and slabs of 16 or 32 whole
+ * faster). For 1-16 tokens, when K % 64 == 0 and slabs of 16 or 32 whole
  * weight rows per CTA fill between three quarters of the SMs and all of them,
  * no CTA splits K (the sum over K stays inside the CTA; dot products on
  * mma.sync, reported as DEC_REGIME_MMA); for 1-2 tokens where only slabs of 8
@@ -87,7 +87,7 @@ extern "C" {
  * result is identical from run to run. The environment variable
  * DEC_FORCE=smallm|mma|tc overrides the choice (smallm only for M <= 2: the
  * CUDA-core kernels, slabs of 8, 16 or 32 rows included); DEC_FORCE=splitk
- * keeps 1-4 tokens on the split-K kernels.
+ * keeps 1-16 tokens on the split-K kernels.
  * Errors: DEC_EINVAL, DEC_EUNSUPPORTED, DEC_ECUDA, DEC_ENOMEM.
  */
 int dec_linear(const void* x, const void* W, void* y, int M, int N, int K, void* stream);
@@ -223,7 +223,7 @@ int dec_add(const void* a, const void* b, void* out, size_t n, void* stream);
  * memory (small projections: few 128-row tiles, M <= 16), 0 when the split is
  * the stream-K one with a last-arriver fixup, and Wd is 1 when the output
  * tiles are 256 rows high (large projections at M <= 16), and Sl is 1 when
- * each CTA owned whole weight rows (1-4 tokens, S = 1). DEC_REGIME_NONE before
+ * each CTA owned whole weight rows (1-16 tokens, S = 1). DEC_REGIME_NONE before
  * any call.
  */
 int dec_last_choice(void);

@@ -376,7 +376,7 @@ def last_wide() -> bool:
 
 def last_slab() -> bool:
     """Whether this thread's last projection call gave each CTA whole weight
-    rows (1-4 tokens, no split over K)."""
+    rows (1-16 tokens, no split over K)."""
     return bool((lib().dec_last_choice() >> 18) & 1)
 
 

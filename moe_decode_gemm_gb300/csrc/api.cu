@@ -52,7 +52,7 @@ bool make_tmap(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, 
 // shared memory as kboxes x rows lines of 128 bytes (128-byte swizzle), one
 // TMA instruction for what would take `kboxes` 2-D boxes.
 bool make_tmap_slab(CUtensorMap* map, const void* W, uint64_t N, uint64_t K, uint32_t rows,
-                    uint32_t kboxes) {
+                    uint32_t kboxes, uint64_t ld) {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -62,8 +62,10 @@ bool make_tmap_slab(CUtensorMap* map, const void* W, uint64_t N, uint64_t K, uin
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   });
   if (!g_encode || N == 0 || K == 0 || (K % 64) != 0) return false;
+  if (ld == 0) ld = K;
+  if (ld < K || (ld % 8) != 0) return false;
   cuuint64_t dims[3] = {64, N, K / 64};
-  cuuint64_t strides[2] = {K * 2, 128};  // bytes: next row, next 64-wide k block
+  cuuint64_t strides[2] = {ld * 2, 128};  // bytes: next row, next 64-wide k block
   cuuint32_t box[3] = {64, rows, kboxes};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(W), dims,
@@ -204,8 +206,6 @@ static bool forced(const char* what) {
 
 static bool force_splitk() { return forced("splitk"); }
 
-// Most tokens the whole-row slabs take (see linear_impl).
-constexpr int kMmaSlabMaxM = 4;
 
 static int regime_for(int M) {
   const char* f = std::getenv("DEC_FORCE");
@@ -251,19 +251,19 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int regime = regime_for(M);
   // Whole-row slabs (R weight rows per CTA, no split over K) when such slabs
-  // fill between three quarters of the SMs and all of them: up to 4 tokens on
-  // the tensor cores (16 or 32 rows per CTA), 1-2 tokens on the CUDA cores
+  // fill between three quarters of the SMs and all of them: up to 16 tokens
+  // on the tensor cores (16 or 32 rows per CTA), 1-2 tokens on the CUDA cores
   // where only 8 rows per CTA fill the SMs (or under DEC_FORCE=smallm).
-  // Same-GPU A/B, us per call in a CUDA graph, N x K = 2048 x 7168, split-K ->
-  // slab: M = 1 8.0 -> 6.7 (CUDA cores 6.8), M = 2 8.3 -> 6.7 (7.8), M = 3
-  // 8.6 -> 6.9, M = 4 8.7 -> 7.1; 4096 x 4096 at M = 1 8.6 -> 7.1 (7.5); M = 8
-  // gains nothing (8.9 both) and 16 tokens lose (9.6 -> 13.8): every CTA reads
-  // every token row, and at 16 tokens those reads match the weight bytes.
-  // DEC_FORCE=splitk keeps the split-K kernels.
+  // Same-GPU A/B, us per call in a CUDA graph, split-K -> slab: N x K =
+  // 2048 x 7168 at M = 1 / 2 / 4 / 5 / 8 / 12 / 16: 8.0 / 8.3 / 8.7 / 8.7 /
+  // 8.9 / 9.3 / 9.5 -> 6.4 / 6.4 / 6.4 / 7.0 / 6.9 / 8.8 / 8.9; 2048 x 16384
+  // at M = 8: 16.6 -> 14.0; 4096 x 4096 at M = 1 / 8: 8.6 / 9.6 -> 7.2 / 7.4;
+  // 4096 x 7168 at M = 8 / 16: 14.6 / 15.9 -> 11.6 / 14.4 (the CUDA-core
+  // slabs: 6.8 / 7.8 at M = 1 / 2 of 2048 x 7168). DEC_FORCE=splitk keeps
+  // the split-K kernels.
   if (S == 0 && !force_splitk()) {
     const bool core_only = forced("smallm");
-    const int Rm = (M <= kMmaSlabMaxM && regime != DEC_REGIME_TC && !core_only)
-                       ? gemv_mma_rows(M, N, K, s->sms) : 0;
+    const int Rm = (regime != DEC_REGIME_TC && !core_only) ? gemv_mma_rows(M, N, K, s->sms) : 0;
     const int Rc = (!Rm && regime == DEC_REGIME_SMALLM) ? gemv_slab_rows(M, N, K, s->sms) : 0;
     if (Rm || Rc) {
       Ctx cx = make_ctx(s, st);
@@ -483,11 +483,17 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   // start on most SMs and leaves its down projection as a tail. There it gets
   // gd dedicated SMs for the whole block instead -- its share of the block's
   // bytes, from the expected number of distinct experts under uniform routing
-  // -- and the routed experts the others; used when gd >= 4 (M <= 4 at
-  // E = 384, k = 8).
+  // and a routed expert's bytes per shared-expert byte (Wd / H: the latent
+  // block's experts are narrower) -- and the routed experts the others. Used
+  // when few experts are expected (eu <= 32: M <= 4 at E = 384, k = 8) and
+  // 4 <= gd < SMs / 2. Same-GPU A/B of the latent block (L = 512), us at
+  // M = 1 / 2 / 4 / 8 / 16 / 64, the share without the Wd / H weight ->
+  // with it: 81.5 / 150.6 / 247.6 / 103.7 / 152.7 / 344.4 -> 56.4 / 66.7 /
+  // 78.5 / 106.9 / 157.3 / 382.8 (dedicated SMs from 8 tokens on lose: hence
+  // the bound on eu).
   const double eu = E * (1.0 - std::pow(1.0 - (double)topk / E, (double)M));
-  const int gd = (int)(s->sms / (1.0 + eu) + 0.5);
-  const bool dedicated = shared && gd >= 4 && gd < s->sms / 2;
+  const int gd = (int)(s->sms / (1.0 + eu * Wd / H) + 0.5);
+  const bool dedicated = shared && eu <= 32.0 && gd >= 4 && gd < s->sms / 2;
   const int egrid = dedicated ? s->sms - gd : s->sms;
   if (shared) {
     const int rc_ctas = router_ctas(E + L, H);

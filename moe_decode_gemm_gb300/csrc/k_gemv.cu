@@ -1,4 +1,4 @@
-// k_gemv.cu -- decode projection y = x·Wᵀ for 1-4 tokens without splitting K
+// k_gemv.cu -- decode projection y = x·Wᵀ for 1-16 tokens without splitting K
 // across CTAs: each CTA owns R consecutive weight rows (R = 8, 16 or 32) over
 // the whole K, so no partial sums leave the CTA -- no workspace, counters,
 // atomics or cluster barriers. What split-K spends after the last weight
@@ -18,7 +18,7 @@
 // (fma.rn.f32.bf16, fp32 sums). The 32/R lanes of a row and then the 8 warps
 // are summed in a fixed order, so results do not vary from run to run.
 //
-// gemv_mma_kernel (1-4 tokens, mma.sync): see its own comment below.
+// gemv_mma_kernel (1-16 tokens, mma.sync): see its own comment below.
 //
 // "vLLM 如何用智能体辅助优化 Kimi K3 解码性能", Part 1 §1 "针对工作负载调优形状"
 // (a small-matrix kernel for batch 1-2).
@@ -33,7 +33,7 @@ namespace dg {
 constexpr int kGvStage = 32768;         // weight bytes per stage
 constexpr int kGvThreads = 9 * 32;      // producer warp + 8 consumer warps
 constexpr int kGvMaxTokens = 2;        // CUDA-core slabs
-constexpr int kMmaMaxTokens = 4;       // tensor-core slabs
+constexpr int kMmaMaxTokens = 16;      // tensor-core slabs
 
 // Bytes of one stage: the weights, then each token's k range (16384/R k).
 constexpr int gemv_stage_bytes(int R) { return kGvStage + kGvMaxTokens * (kGvStage / R); }
@@ -183,29 +183,34 @@ __global__ void __launch_bounds__(kGvThreads, 2)
 }
 
 // ---------------------------------------------------------------- mma slabs
-// The same whole-row slabs for up to 4 tokens with the dot products on the
-// tensor cores (mma.sync.m16n8k16: the weights are the 16-row operand, the
-// tokens the 8-column one, columns past M zero). On the CUDA cores the
-// multiply-adds of a stage cost more than its copies once the dependency has
-// resolved (~0.5 us per 32 KB stage of one token; a copy of the kernel with
-// them left out was 1-2 us faster per call), while a stage here is 32 MMAs.
-// A stage is KBS k blocks of 64 of the CTA's R rows (16 KB of weights: one
-// 3-D TMA box, 128-byte swizzle) and the tokens' matching k range, one bulk
-// copy per token into rows padded by 16 bytes, so that the token rows of a B
-// fragment fall in distinct banks. Task j of a stage (row group j % (R/16),
-// k block j / (R/16)) goes to warp j % 8; a warp keeps one accumulator tile
-// over all its tasks, and the warps of a row group are summed in order at the
-// end, so results do not vary from run to run. Every CTA reads every token
-// row: at 16 tokens those reads match the weight bytes and the slabs lose to
-// the split-K kernels, which is why they stop at 4.
+// The same whole-row slabs with the dot products on the tensor cores
+// (mma.sync.m16n8k16: the weights are the 16-row operand, the tokens the
+// 8-column one, columns past M zero). On the CUDA cores the multiply-adds of
+// a stage cost more than its copies once the dependency has resolved (~0.5 us
+// per 32 KB stage of one token; a copy of the kernel with them left out was
+// 1-2 us faster per call), while a stage here is 32-64 MMAs. A stage is KBS k
+// blocks of 64 of the slab's R rows (16 KB of weights: one 3-D TMA box,
+// 128-byte swizzle) and the same k range of XR = 4, 8 or 16 token rows (one
+// 3-D TMA box, rows past M zero-filled, same swizzle). Task j of a stage (row
+// group j % (R/16), k block j / (R/16)) goes to warp j % 8; a warp keeps one
+// accumulator tile over all its tasks, and the warps of a row group are
+// summed in order at the end, so results do not vary from run to run.
+//
+// Every CTA reads the tokens' rows over all of K, XR/R of its weight bytes.
+// Measured alternatives (us per call, CUDA graph, N x K = 2048 x 7168): a bulk
+// copy per token row instead of the token box cost more with every token
+// (13.8 at 16 tokens, the box 8.9); slabs of 32 or 64 rows shared by a cluster
+// of 2 or 4 CTAs that split K (fewer token bytes per CTA, partials summed
+// through distributed shared memory) lost to one CTA per slab at every size
+// (8 tokens: 9.0 / 9.7 against 6.9).
 template <int R, int XR, int KBS>
 struct MmaSlab {
   static constexpr int RG = R / 16;                     // 16-row groups
   static constexpr int XN = (XR + 7) / 8;               // 8-token column tiles
   static constexpr int KS = KBS * 64;                   // k per stage
   static constexpr int WB = R * KS * 2;                 // weight bytes per stage
-  static constexpr int XS = KS + 8;                     // token row stride (elements)
-  static constexpr int SB = (WB + XR * XS * 2 + 1023) / 1024 * 1024;
+  static constexpr int XB = KBS * XR * 128;             // token bytes per stage (full box)
+  static constexpr int SB = (WB + XB + 1023) / 1024 * 1024;
   static constexpr int RED = kNCW * 16 * XN * 8 * 4;    // per-warp tiles for the final sum
   static constexpr int FIXED = 1024 + RED + 256;        // alignment, tiles, barriers, flags
   static constexpr int STAGES = (115712 - FIXED) / SB;  // two CTAs per SM
@@ -216,10 +221,10 @@ struct MmaSlab {
 
 template <int R, int XR, int KBS, int EPI>
 __global__ void __launch_bounds__(kGvThreads, 2)
-    gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const uint16_t* x, long long ldx,
+    gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                     const StreamArgs a) {
   using P = MmaSlab<R, XR, KBS>;
-  constexpr int STAGES = P::STAGES, KS = P::KS, SB = P::SB, XS = P::XS, RG = P::RG;
+  constexpr int STAGES = P::STAGES, KS = P::KS, SB = P::SB, RG = P::RG;
   constexpr int XN = P::XN, XM = XN * 8;               // token columns of the tiles
   constexpr int TPW = RG * KBS / kNCW;                 // tasks per warp per stage
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -241,7 +246,10 @@ __global__ void __launch_bounds__(kGvThreads, 2)
     s_flags[0] = 0;
     fence_mbar_init();
   }
-  if (threadIdx.x == 32) prefetch_tmap(&wmap);
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&wmap);
+    prefetch_tmap(&xmap);
+  }
   __syncthreads();
   griddep_launch_dependents();
 
@@ -251,20 +259,14 @@ __global__ void __launch_bounds__(kGvThreads, 2)
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
-      auto xbytes = [&](int i) -> uint32_t {
-        const int n = K - i * KS;
-        return (uint32_t)((n < KS ? n : KS) * 2);
-      };
+      const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
       auto issue_x = [&](int s, int i) {
-        uint16_t* xs = reinterpret_cast<uint16_t*>(smem + s * SB + P::WB);
-        for (int m = 0; m < M; ++m)
-          bulk_copy_g2s(xs + m * XS, x + m * ldx + (long long)i * KS, xbytes(i), &full[s]);
+        tma_load_3d(smem + s * SB + P::WB, &xmap, 0, 0, i * KBS, &full[s], pol_x);
       };
       const int npre = nst < STAGES ? nst : STAGES;
       int i = 0;
       for (; i < npre; ++i) {
-        mbar_arrive_expect_tx(&full[i], P::WB + M * xbytes(i));
+        mbar_arrive_expect_tx(&full[i], P::WB + P::XB);
         tma_load_3d(smem + i * SB, &wmap, 0, row0, i * KBS, &full[i], pol_w);
       }
       griddep_wait();
@@ -276,7 +278,7 @@ __global__ void __launch_bounds__(kGvThreads, 2)
           break;
         }
         if (s_flags[0]) break;
-        mbar_arrive_expect_tx(&full[s], P::WB + M * xbytes(i));
+        mbar_arrive_expect_tx(&full[s], P::WB + P::XB);
         tma_load_3d(smem + s * SB, &wmap, 0, row0, i * KBS, &full[s], pol_w);
         issue_x(s, i);
       }
@@ -309,7 +311,7 @@ __global__ void __launch_bounds__(kGvThreads, 2)
       }
       if (!s_flags[0]) {
         const uint32_t wst = smem_u32(smem + s * SB);
-        const uint16_t* xs = reinterpret_cast<const uint16_t*>(smem + s * SB + P::WB);
+        const uint8_t* xs = smem + s * SB + P::WB;   // [k block][XR tokens][128 B], swizzled
 #pragma unroll
         for (int q = 0; q < TPW; ++q) {
           const int kb = (w + q * kNCW) / RG;         // k block of this task within the stage
@@ -320,14 +322,17 @@ __global__ void __launch_bounds__(kGvThreads, 2)
               const int ach = kk * 2 + (mi >> 1);
               ldmatrix_x4(af[0], af[1], af[2], af[3],
                           wst + (kb * R + a_row) * 128 + ((ach ^ r8) << 4));
-              const int kx = kb * 64 + kk * 16 + bk;  // k of this lane's B pair in the stage
 #pragma unroll
               for (int nt = 0; nt < XN; ++nt) {
+                // token t's 16-byte chunks kk*2 and kk*2+1 of k block kb, the
+                // lane's k pair at byte bk*2 within each
                 const int t = nt * 8 + bn;
+                const int xrow = kb * XR + t;
                 uint32_t b0 = 0u, b1 = 0u;
                 if (t < M) {
-                  b0 = *reinterpret_cast<const uint32_t*>(xs + t * XS + kx);
-                  b1 = *reinterpret_cast<const uint32_t*>(xs + t * XS + kx + 8);
+                  const uint8_t* xr = xs + xrow * 128 + bk * 2;
+                  b0 = *reinterpret_cast<const uint32_t*>(xr + (((kk * 2) ^ (xrow & 7)) << 4));
+                  b1 = *reinterpret_cast<const uint32_t*>(xr + (((kk * 2 + 1) ^ (xrow & 7)) << 4));
                 }
                 if (nt * 8 < M) mma_bf16_16816(d[nt], af, b0, b1);
               }
@@ -349,16 +354,15 @@ __global__ void __launch_bounds__(kGvThreads, 2)
       }
     named_bar_sync(1, kNCW * 32);
     const int ct = threadIdx.x - 32;
-    if (!s_flags[0])
-      for (int e = ct; e < R * M; e += kNCW * 32) {
-        const int r = e % R, t = e / R;
-        const int grp = r / 16, rr = r % 16;
-        float v = 0.f;
+    for (int e = ct; e < R * M; e += kNCW * 32) {
+      const int r = e % R, t = e / R;
+      const int grp = r / 16, rr = r % 16;
+      float v = 0.f;
 #pragma unroll
-        for (int q = grp; q < kNCW; q += RG) v += red[(q * 16 + rr) * XM + t];
-        const int n = row0 + r;
-        if (n < a.nout) store_out<EPI, false>(a, GroupInfo{0, 0, M}, t, n, v);
-      }
+      for (int q = grp; q < kNCW; q += RG) v += red[(q * 16 + rr) * XM + t];
+      const int n = row0 + r;
+      if (!s_flags[0] && n < a.nout) store_out<EPI, false>(a, GroupInfo{0, 0, M}, t, n, v);
+    }
   }
   __syncthreads();
 }
@@ -372,8 +376,10 @@ static cudaError_t run_gemv_mma(const Ctx& cx, const void* x, long long ldx, con
   static_assert(2 * (SMEM + 1024) <= kSmemPerSm, "two CTAs per SM");
   static DevOnce once;
   if (cudaError_t e = setup_smem(once, kern, SMEM, true); e != cudaSuccess) return e;
-  CUtensorMap wmap;
-  if (!make_tmap_slab(&wmap, W, (uint64_t)N, (uint64_t)K, R, KBS)) return cudaErrorInvalidValue;
+  CUtensorMap wmap, xmap;
+  if (!make_tmap_slab(&wmap, W, (uint64_t)N, (uint64_t)K, R, KBS) ||
+      !make_tmap_slab(&xmap, x, (uint64_t)M, (uint64_t)K, XR, KBS, (uint64_t)ldx))
+    return cudaErrorInvalidValue;
   StreamArgs a = {};
   a.K = K;
   a.nout = N;
@@ -386,8 +392,7 @@ static cudaError_t run_gemv_mma(const Ctx& cx, const void* x, long long ldx, con
   a.out_len = (long long)M * N;
   a.res_len = res ? (long long)M * N : 0;
   const int grid = (N + R - 1) / R;
-  return launch_k(kern, dim3(grid), dim3(kGvThreads), SMEM, cx.stream, cx.pdl, wmap,
-                  reinterpret_cast<const uint16_t*>(x), ldx, a);
+  return launch_k(kern, dim3(grid), dim3(kGvThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
 }
 
 template <int R, int EPI>
@@ -429,8 +434,9 @@ int gemv_slab_rows(int M, int N, int K, int sms) {
   return 0;
 }
 
-// Rows per CTA for the mma slabs: 16 or 32 (one or two 16-row groups), by the
-// same rule; up to kMmaMaxTokens tokens.
+// Rows per CTA of the mma slabs: 16 or 32, the smaller whose grid keeps
+// between three quarters of the SMs and all of them busy; 0 when neither
+// does (or more than 16 tokens, or K % 64 != 0).
 int gemv_mma_rows(int M, int N, int K, int sms) {
   if (M < 1 || M > kMmaMaxTokens || (K % 64) != 0) return 0;
   for (int R = 16; R <= 32; R <<= 1) {
@@ -447,11 +453,22 @@ static cudaError_t mma_epi(const Ctx& cx, bool residual, const void* x, long lon
                   : run_gemv_mma<R, XR, KBS, EPI_BF16>(cx, x, ldx, W, res, y, M, N, K);
 }
 
+// Token rows per stage XR = 4, 8 or 16 (the least that holds M); k blocks
+// per stage so that a stage holds 16 KB of weights (8 at R = 16, 4 at 32).
+template <int R>
+static cudaError_t mma_rows(const Ctx& cx, bool residual, const void* x, long long ldx,
+                            const void* W, const void* res, void* y, int M, int N, int K) {
+  constexpr int KBS = 128 / R;
+  if (M <= 4) return mma_epi<R, 4, KBS>(cx, residual, x, ldx, W, res, y, M, N, K);
+  if (M <= 8) return mma_epi<R, 8, KBS>(cx, residual, x, ldx, W, res, y, M, N, K);
+  return mma_epi<R, 16, KBS>(cx, residual, x, ldx, W, res, y, M, N, K);
+}
+
 cudaError_t launch_gemv_mma(const Ctx& cx, bool residual, const void* x, const void* W,
                             const void* res, void* y, int M, int N, int K, int R) {
   const long long ldx = cx.ldx ? cx.ldx : K;
-  if (R == 16) return mma_epi<16, kMmaMaxTokens, 8>(cx, residual, x, ldx, W, res, y, M, N, K);
-  if (R == 32) return mma_epi<32, kMmaMaxTokens, 4>(cx, residual, x, ldx, W, res, y, M, N, K);
+  if (R == 16) return mma_rows<16>(cx, residual, x, ldx, W, res, y, M, N, K);
+  if (R == 32) return mma_rows<32>(cx, residual, x, ldx, W, res, y, M, N, K);
   return cudaErrorInvalidValue;
 }
 

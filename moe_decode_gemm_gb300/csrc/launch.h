@@ -12,10 +12,12 @@ namespace dg {
 bool make_tmap(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
                bool l2_promote_256, uint64_t ld = 0);
 
-// Weight rows [N, K] (K % 64 == 0) read in boxes of `rows` rows x `kboxes`
-// 64-wide k blocks (a 3-D view), 128-byte swizzle. Returns false on failure.
+// Rows [N, K] (K % 64 == 0; rows ld elements apart, ld = 0 meaning K, else
+// ld % 8 == 0) read in boxes of `rows` rows x `kboxes` 64-wide k blocks (a
+// 3-D view), 128-byte swizzle; rows past N read as zeros. Returns false on
+// failure.
 bool make_tmap_slab(CUtensorMap* map, const void* W, uint64_t N, uint64_t K, uint32_t rows,
-                    uint32_t kboxes);
+                    uint32_t kboxes, uint64_t ld = 0);
 
 struct Ctx {
   int sms;
@@ -53,8 +55,8 @@ int gemv_slab_rows(int M, int N, int K, int sms);
 cudaError_t launch_gemv_slab(const Ctx& cx, bool residual, const void* x, const void* W,
                              const void* res, void* y, int M, int N, int K, int R);
 
-// The same slabs for up to 4 tokens with mma.sync dot products: R = 16 or 32
-// rows per CTA (R from gemv_mma_rows; 0 means the shape does not suit it).
+// The same slabs for up to 16 tokens with mma.sync dot products: R = 16 or
+// 32 rows per CTA (R from gemv_mma_rows; 0 means the shape does not suit it).
 int gemv_mma_rows(int M, int N, int K, int sms);
 cudaError_t launch_gemv_mma(const Ctx& cx, bool residual, const void* x, const void* W,
                             const void* res, void* y, int M, int N, int K, int R);

@@ -33,8 +33,8 @@ def _expect_regime(M):
 
 
 def _expect_path(M):
-    """The regime of the last call: 1-4 tokens on whole-row slabs run on mma.sync."""
-    return "mma" if dg.last_slab() and M <= 4 else _expect_regime(M)
+    """The regime of the last call: whole-row slabs of 1-16 tokens run on mma.sync."""
+    return "mma" if dg.last_slab() and M <= 16 else _expect_regime(M)
 
 
 def _gpu_linear(x_bits, W_bits, S=None, res_bits=None):
@@ -131,7 +131,7 @@ def test_batch_sweep_k7168(M, N):
     cols = np.random.default_rng(N + M).choice(N, 384, replace=False)
     _, (regime, _) = _check_random(M, N, 7168, ("cfg2", M, N), cols=cols)
     assert regime == _expect_path(M)
-    assert dg.last_slab() == (N == 2048 and M <= 4)
+    assert dg.last_slab() == (N == 2048 and M <= 16)
 
 
 @pytest.mark.parametrize("M", [1, 4, 16, 64])
@@ -418,16 +418,19 @@ def test_slab_declines_shapes_it_does_not_fill(core_slabs):
 
 
 # ---------------------------------------------------------------- tensor-core slabs
-# 1-4 tokens: the same whole-row slabs (16 or 32 rows per CTA), with the dot
-# products on the tensor cores (mma.sync).
+# 1-16 tokens: the same whole-row slabs (16 or 32 rows per CTA) with the dot
+# products on the tensor cores (mma.sync), 4, 8 or 16 token rows per stage.
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 2048, 7168), (2, 2048, 7168), (3, 2048, 7168),
                                    (4, 4096, 4096), (1, 4096, 4096), (3, 3700, 2048),
-                                   (4, 2000, 1024), (2, 2048, 16384), (4, 4096, 1088)])
+                                   (4, 2000, 1024), (2, 2048, 16384), (4, 4096, 1088),
+                                   (5, 2048, 7168), (8, 2048, 7168), (16, 2048, 7168),
+                                   (12, 4096, 4096), (9, 2048, 16384), (16, 3700, 2048),
+                                   (7, 4096, 1088), (13, 2000, 1024)])
 def test_mma_slab_shapes(M, N, K):
-    # 16 / 32 rows per CTA, ragged last slab, K from 1024 to 16384 (1088: a
-    # last stage with one k block of 64)
+    # 16 / 32 rows per CTA, 4 / 8 / 16 token rows, ragged last slab, K from
+    # 1024 to 16384 (1088: a last stage with one k block of 64)
     y, (regime, split) = _check_random(M, N, K, ("mslab", M, N, K))
     assert regime == "mma" and dg.last_slab() and split == 1 and not dg.last_cluster()
     y2, _ = _gpu_linear(wl.normal_bf16((M, K), 1.0, "mslab", M, N, K, "x"),
@@ -435,7 +438,7 @@ def test_mma_slab_shapes(M, N, K):
     assert torch.equal(y, y2), "mma slab kernel not deterministic"
 
 
-@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 11, 16])
 def test_mma_slab_integer_inputs_match_oracle_and_split_k(M, monkeypatch):
     K, N = 4096, 2048
     x = wl.integer_bf16((M, K), -2, 2, "mslab-int", M, "x")
@@ -450,7 +453,7 @@ def test_mma_slab_integer_inputs_match_oracle_and_split_k(M, monkeypatch):
     assert torch.equal(y, ys)
 
 
-@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("M", [1, 4, 6, 16])
 def test_mma_slab_residual_and_row_strided_input(M):
     K, N, ldx = 4096, 2048, 4160
     wide = wl.normal_bf16((M, ldx), 1.0, "mslab-res", M, "x")
@@ -480,8 +483,8 @@ def test_mma_slab_for_one_or_two_tokens_matches_the_cuda_core_slab(M, monkeypatc
 
 def test_mma_slab_declines_shapes_it_does_not_fill():
     # too few rows for three quarters of the SMs, K not a multiple of 64,
-    # too many rows for 32 per CTA, more than 4 tokens
-    for M, N, K in [(4, 1024, 4096), (3, 4096, 1000), (4, 6000, 2048), (5, 2048, 7168),
-                    (16, 2048, 7168)]:
+    # too many rows for 32 per CTA, more than 16 tokens
+    for M, N, K in [(4, 1024, 4096), (3, 4096, 1000), (4, 6000, 2048), (8, 7168, 7168),
+                    (17, 2048, 4096)]:
         _check_random(M, N, K, ("mslab-no", M, N, K))
         assert not dg.last_slab(), (M, N, K)
