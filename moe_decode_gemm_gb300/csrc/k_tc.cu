@@ -31,7 +31,6 @@ namespace dg {
 constexpr int kTcStages = 4;
 constexpr int kTcXRows = 64;
 constexpr int kTcXSub = kTcXRows * 128;                   // 8 KB per box column
-constexpr int kTcStageBytes = kWBytes + kKSub * kTcXSub;  // 48 KB
 constexpr int kTcThreads = 320;
 constexpr int kTcEpi = 256;    // 8 epilogue warps: two per tensor-memory lane quarter
 constexpr int kTcCols = kTcXRows / 2;  // token columns each epilogue warp drains
@@ -334,17 +333,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // [r*128/S, (r+1)*128/S) of every token over the S partials in rank order
 // (ld.shared::cluster on mapa addresses); a second barrier keeps every CTA
 // alive while the others read it. No global partials, counters or atomics,
-// deterministic. Two 48 KB stages keep a CTA near 100 KB of shared memory, so
-// two fit on an SM: a call's CTAs load their first weight stages while the
-// previous call's CTAs on those SMs finish.
-constexpr int kTcClStages = 2;
+// deterministic. Two 48 KB stages (128 k) or four of 24 KB (64 k) keep a CTA
+// near 100 KB of shared memory, so two fit on an SM: a call's CTAs load their
+// first weight stages while the previous call's CTAs on those SMs finish.
 constexpr int kTcClCols = 64;  // one accumulator of up to 64 token columns
 
-constexpr int tc_cluster_smem() {
-  return 1024 + kTcClStages * kTcStageBytes + 8 * (2 * kTcClStages + 1) + 64;
-}
+// Stage shape of the cluster kernel: KSUB boxes of 64 k per stage (weights
+// 128 rows x 64 k = 16 KB and 64 token rows x 64 k = 8 KB each), as many
+// stages as fit in ~100 KB (two CTAs per SM).
+template <int KSUB>
+struct TcCl {
+  static constexpr int kStage = KSUB * (kWSub + kTcXSub);
+  static constexpr int kStages = (115712 - 1024 - 256) / kStage;
+  static constexpr int kSmem = 1024 + kStages * kStage + 8 * (2 * kStages + 1) + 64;
+  static_assert(kTileRows * kTcXRows * 4 <= kStages * kStage, "partial tile fits");
+};
 
-template <int EPI>
+template <int EPI, int KSUB>
 __global__ void __launch_bounds__(kTcThreads, 2)
     tc_cluster_kernel(const __grid_constant__ CUtensorMap wmap,
                       const __grid_constant__ CUtensorMap xmap, const StreamArgs a, const int NP,
@@ -352,7 +357,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTcClStages * kTcStageBytes);
+  constexpr int kTcClStages = TcCl<KSUB>::kStages, kStageB = TcCl<KSUB>::kStage;
+  constexpr int kWB = KSUB * kWSub;  // weight bytes per stage
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTcClStages * kStageB);
   uint64_t* empty = full + kTcClStages;
   uint64_t* tfull = empty + kTcClStages;  // [1] accumulator complete
   volatile int* s_flags = reinterpret_cast<volatile int*>(tfull + 1);  // [0] abort
@@ -393,18 +400,18 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      const uint32_t bytes = kWBytes + kKSub * NP * 128;
+      const uint32_t bytes = kWB + KSUB * NP * 128;
       auto issue_w = [&](int s, int kc) {
 #pragma unroll
-        for (int sb = 0; sb < kKSub; ++sb)
-          tma_load_2d(smem + s * kTcStageBytes + sb * kWSub, &wmap, (kc * kKSub + sb) * kKBlk,
+        for (int sb = 0; sb < KSUB; ++sb)
+          tma_load_2d(smem + s * kStageB + sb * kWSub, &wmap, (kc * KSUB + sb) * kKBlk,
                       tile * kTileRows, &full[s], pol_w);
       };
       auto issue_x = [&](int s, int kc) {
 #pragma unroll
-        for (int sb = 0; sb < kKSub; ++sb)
-          tma_load_2d(smem + s * kTcStageBytes + kWBytes + sb * kTcXSub, &xmap,
-                      (kc * kKSub + sb) * kKBlk, 0, &full[s], pol_x);
+        for (int sb = 0; sb < KSUB; ++sb)
+          tma_load_2d(smem + s * kStageB + kWB + sb * kTcXSub, &xmap,
+                      (kc * KSUB + sb) * kKBlk, 0, &full[s], pol_x);
       };
       // weights first (independent of the previous kernel), then tokens
       const int npre = nunits < kTcClStages ? nunits : kTcClStages;
@@ -445,10 +452,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         }
         tc_fence_after();
         if (!s_flags[0]) {
-          const uint32_t wb = smem_u32(smem + s * kTcStageBytes);
-          const uint32_t xb = wb + kWBytes;
+          const uint32_t wb = smem_u32(smem + s * kStageB);
+          const uint32_t xb = wb + kWB;
 #pragma unroll
-          for (int sb = 0; sb < kKSub; ++sb)
+          for (int sb = 0; sb < KSUB; ++sb)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t ad = umma_desc_sw128(wb + sb * kWSub + kk * 32);
@@ -517,13 +524,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   }
 }
 
-template <int EPI>
+template <int EPI, int KSUB>
 static cudaError_t run_tc_cluster(const Ctx& cx, const void* x, const void* W, const void* res,
                                   void* y, int M, int N, int K, int cl) {
-  constexpr int SMEM = tc_cluster_smem();
+  constexpr int SMEM = TcCl<KSUB>::kSmem;
   static_assert(2 * (SMEM + 1024) <= kSmemPerSm, "two CTAs per SM");
-  static_assert(kTileRows * kTcXRows * 4 <= kTcClStages * kTcStageBytes, "partial tile fits");
-  auto kern = tc_cluster_kernel<EPI>;
+  auto kern = tc_cluster_kernel<EPI, KSUB>;
   static DevOnce once;
   if (cudaError_t e = setup_smem(once, kern, SMEM, true); e != cudaSuccess) return e;
   const int NP = (M + 15) / 16 * 16;
@@ -533,7 +539,7 @@ static cudaError_t run_tc_cluster(const Ctx& cx, const void* x, const void* W, c
     return cudaErrorInvalidValue;
   StreamArgs a = {};
   a.K = K;
-  a.KB = (K + kKChunk - 1) / kKChunk;
+  a.KB = (K + KSUB * kKBlk - 1) / (KSUB * kKBlk);  // work units of KSUB boxes
   a.TILES = (N + kTileRows - 1) / kTileRows;
   a.nout = N;
   a.M = M;
@@ -552,8 +558,16 @@ cudaError_t launch_dense_tc_cluster(const Ctx& cx, bool residual, const void* x,
                                     const void* res, void* y, int M, int N, int K, int cl) {
   if (M < 16 || M > kTcXRows || cl < 2 || cl > 8 || cl > (K + kKChunk - 1) / kKChunk)
     return cudaErrorInvalidValue;
-  return residual ? run_tc_cluster<EPI_BF16_RES>(cx, x, W, res, y, M, N, K, cl)
-                  : run_tc_cluster<EPI_BF16>(cx, x, W, res, y, M, N, K, cl);
+  // Stages of 64 k (four of 24 KB) when each rank streams 768 k or more,
+  // else of 128 k (two of 48 KB). Same-GPU A/B, us, 128-k -> 64-k stages:
+  // 2048 x 7168 at M = 17 / 32 / 64: 9.55 / 9.88 / 11.46 -> 9.40 / 9.77 /
+  // 10.94; 2048 x 16384 at M = 32 / 64: 17.1 / 18.9 -> 16.2 / 17.5; but
+  // 2048 x 4096 at M = 24 (512 k per rank): 7.15 -> 7.37.
+  if (K / cl >= 768)
+    return residual ? run_tc_cluster<EPI_BF16_RES, 1>(cx, x, W, res, y, M, N, K, cl)
+                    : run_tc_cluster<EPI_BF16, 1>(cx, x, W, res, y, M, N, K, cl);
+  return residual ? run_tc_cluster<EPI_BF16_RES, 2>(cx, x, W, res, y, M, N, K, cl)
+                  : run_tc_cluster<EPI_BF16, 2>(cx, x, W, res, y, M, N, K, cl);
 }
 
 // PAIRED: W is [2I, K] (gate rows, then up rows) and N = I; y = bf16(silu(x·W1ᵀ)

@@ -252,10 +252,11 @@ def test_cluster_split_residual(split_k_only, M):
 # each rank accumulates its k share in tensor memory, drains it to shared
 # memory, and the ranks sum the partials through distributed shared memory.
 @pytest.mark.parametrize("M,N,K", [(33, 1900, 904), (17, 2000, 1288), (64, 1920, 1024),
-                                   (48, 2304, 4096), (64, 2048, 7168)])
+                                   (48, 2304, 4096), (64, 2048, 7168), (40, 2048, 16384),
+                                   (24, 1900, 6200)])
 def test_tc_cluster_split_shapes(M, N, K):
     # ragged last tile and last k chunk, uneven k shares, token counts not a
-    # multiple of 16
+    # multiple of 16; 128-k stages (up to 512 k per rank) and 64-k stages
     y, (regime, cl) = _check_random(M, N, K, ("tccluster", M, N, K))
     assert regime == "tc" and dg.last_cluster() and cl >= 2
     y2, _ = _gpu_linear(wl.normal_bf16((M, K), 1.0, "tccluster", M, N, K, "x"),
@@ -263,11 +264,11 @@ def test_tc_cluster_split_shapes(M, N, K):
     assert torch.equal(y, y2), "tcgen05 cluster split not deterministic"
 
 
-@pytest.mark.parametrize("M", [17, 32, 64])
-def test_tc_cluster_integer_inputs_match_stream_k(M):
+@pytest.mark.parametrize("M,K", [(17, 2048), (32, 2048), (64, 2048), (64, 8192)])
+def test_tc_cluster_integer_inputs_match_stream_k(M, K):
     # exact fp32 sums: the cluster split, the stream-K tcgen05 split and the
     # oracle give the same bits
-    K, N = 2048, 2048
+    N = 2048
     x = wl.integer_bf16((M, K), -2, 2, "tccl-int", M, "x")
     W = wl.integer_bf16((N, K), -2, 2, "tccl-int", M, "W")
     y, (regime, _) = _gpu_linear(x, W)
