@@ -211,7 +211,7 @@ struct MmaSlab {
   static constexpr int WB = R * KS * 2;                 // weight bytes per stage
   static constexpr int XB = KBS * XR * 128;             // token bytes per stage (full box)
   static constexpr int SB = (WB + XB + 1023) / 1024 * 1024;
-  static constexpr int RED = kNCW * 16 * XN * 8 * 4;    // per-warp tiles for the final sum
+  static constexpr int RED = kNCW * 16 * XR * 4;        // per-warp tiles (token rows only)
   static constexpr int FIXED = 1024 + RED + 256;        // alignment, tiles, barriers, flags
   static constexpr int STAGES = (115712 - FIXED) / SB;  // two CTAs per SM
   static constexpr int SMEM = FIXED + STAGES * SB;
@@ -225,14 +225,13 @@ __global__ void __launch_bounds__(kGvThreads, 2)
                     const StreamArgs a) {
   using P = MmaSlab<R, XR, KBS>;
   constexpr int STAGES = P::STAGES, KS = P::KS, SB = P::SB, RG = P::RG;
-  constexpr int XN = P::XN, XM = XN * 8;               // token columns of the tiles
+  constexpr int XN = P::XN;                            // 8-token column tiles
   constexpr int TPW = RG * KBS / kNCW;                 // tasks per warp per stage
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const int M = a.M, K = a.K;
-  float* red = reinterpret_cast<float*>(smem + STAGES * SB);     // [warp][16][XM]
-  // (M <= XR token rows are copied; columns from M on are zero)
+  float* red = reinterpret_cast<float*>(smem + STAGES * SB);     // [warp][16][XR]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * SB + P::RED);
   uint64_t* empty = full + STAGES;
   volatile int* s_flags = reinterpret_cast<volatile int*>(empty + STAGES);  // [0] abort
@@ -350,7 +349,7 @@ __global__ void __launch_bounds__(kGvThreads, 2)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int rr = g + (e >> 1) * 8, t = nt * 8 + tc + (e & 1);
-        red[(w * 16 + rr) * XM + t] = d[nt][e];
+        if (t < XR) red[(w * 16 + rr) * XR + t] = d[nt][e];
       }
     named_bar_sync(1, kNCW * 32);
     const int ct = threadIdx.x - 32;
@@ -359,7 +358,7 @@ __global__ void __launch_bounds__(kGvThreads, 2)
       const int grp = r / 16, rr = r % 16;
       float v = 0.f;
 #pragma unroll
-      for (int q = grp; q < kNCW; q += RG) v += red[(q * 16 + rr) * XM + t];
+      for (int q = grp; q < kNCW; q += RG) v += red[(q * 16 + rr) * XR + t];
       const int n = row0 + r;
       if (!s_flags[0] && n < a.nout) store_out<EPI, false>(a, GroupInfo{0, 0, M}, t, n, v);
     }
