@@ -213,6 +213,14 @@ __device__ __forceinline__ float ld_dsmem_f32(const void* local, uint32_t rank) 
   return v;
 }
 
+// fp32 store into the shared memory of CTA `rank` of this cluster, at the
+// address `local` has in this CTA's shared memory.
+__device__ __forceinline__ void st_dsmem_f32(void* local, uint32_t rank, float v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
 // int store into the shared memory of CTA `rank` of this cluster, at the
 // address `local` has in this CTA's shared memory.
 __device__ __forceinline__ void st_dsmem_s32(void* local, uint32_t rank, int v) {

@@ -328,14 +328,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // ------------------------------------------------------------------ cluster split
 // Small N: cluster i of S CTAs owns output tile i, rank r streams the r-th of
-// S equal shares of its k chunks into one tensor-memory accumulator, drains
-// it to its own shared memory, and after a cluster barrier sums rows
-// [r*128/S, (r+1)*128/S) of every token over the S partials in rank order
-// (ld.shared::cluster on mapa addresses); a second barrier keeps every CTA
-// alive while the others read it. No global partials, counters or atomics,
-// deterministic. Two 48 KB stages (128 k) or four of 24 KB (64 k) keep a CTA
-// near 100 KB of shared memory, so two fit on an SM: a call's CTAs load their
-// first weight stages while the previous call's CTAs on those SMs finish.
+// S equal shares of its k chunks into one tensor-memory accumulator; after a
+// cluster barrier every thread stores its row of the accumulator into the
+// shared memory of the rank that owns the row, and after a second barrier
+// each rank sums its rows over the S partials in rank order. No global
+// partials, counters or atomics, deterministic. Two 48 KB stages (128 k) or
+// four of 24 KB (64 k) keep a CTA near 100 KB of shared memory, so two fit on
+// an SM: a call's CTAs load their first weight stages while the previous
+// call's CTAs on those SMs finish.
 constexpr int kTcClCols = 64;  // one accumulator of up to 64 token columns
 
 // Stage shape of the cluster kernel: KSUB boxes of 64 k per stage (weights
@@ -391,6 +391,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
   const int KB = a.KB;
   const int cs = (int)cluster_size(), cr = (int)cluster_rank();
+  // epilogue warps (2-9): the accumulator's row r, token columns t0..t0+31
+  const int quarter = warp & 3;      // TMEM lanes this warp may access
+  const int half = (warp - 2) >> 2;  // which half of the token columns it drains
+  const int r = quarter * 32 + lane;
+  const int t0 = half * kTcCols;
+  float v[kTcCols];
   const int tile = (int)(blockIdx.x / cs);
   const int kc0 = cr * KB / cs;
   const int nunits = (cr + 1) * KB / cs - kc0;
@@ -474,48 +480,52 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   } else {
     // ---------------------------------------------------------------- epilogue
     griddep_wait();
-    const int quarter = warp & 3;      // TMEM lanes this warp may access
-    const int half = (warp - 2) >> 2;  // which half of the token columns it drains
-    const int r = quarter * 32 + lane;
-    const int t0 = half * kTcCols;
     if (!s_flags[0]) {
       if (!mbar_wait(tfull, 0, a.timeout_ns, a.status)) s_flags[0] = 1;
     }
     tc_fence_after();
-    float v[kTcCols];
 #pragma unroll
     for (int cc = 0; cc < kTcCols / 16; ++cc)
       if (t0 + cc * 16 < NP)
         tmem_ld16_sync(taddr + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(t0 + cc * 16),
                        v + cc * 16);
     tc_fence_before();
-    // This CTA's partial tile [token][128] at the start of its shared memory:
-    // the stages are free (every MMA, and so every copy, has completed).
-    float* part = reinterpret_cast<float*>(smem);
-#pragma unroll
-    for (int t = 0; t < kTcCols; ++t)
-      if (t0 + t < a.M) part[(t0 + t) * kTileRows + r] = v[t];
   }
-  // Every thread of the cluster: partials written -> visible cluster-wide.
+  // Rank q owns rows [q*R4, q*R4 + R4) of the tile (R4 = 128/cs rounded up to
+  // a multiple of 4, the last run cut at 128). After a first barrier (every
+  // rank's MMAs, and so its copies, are complete: its stage memory is free)
+  // each thread stores its row of the drained accumulator straight into the
+  // owner's shared memory, recv[source rank][token][row - owner's first row];
+  // after a second barrier each rank sums its rows over the sources in rank
+  // order from its own shared memory. Remote stores are posted: no remote
+  // round trip (a version that loaded the partials from the other ranks took
+  // ~2 us at 64 tokens).
+  const int R4 = ((kTileRows + cs - 1) / cs + 3) / 4 * 4;
+  float* recv = reinterpret_cast<float*>(smem);
   __syncwarp();
   cluster_sync_all();
-  if (warp >= 2) {
-    const int et = threadIdx.x - 64;
-    const int R = kTileRows / cs;
-    const GroupInfo gi{0, 0, a.M};
-    const float* part = reinterpret_cast<const float*>(smem);
-    if (!s_flags[0]) {
-      for (int e = et; e < R * a.M; e += kTcEpi) {
-        const int t = e / R, rr = cr * R + (e - t * R);
-        float acc = 0.f;
-        for (int q = 0; q < cs; ++q) acc += ld_dsmem_f32(part + t * kTileRows + rr, (uint32_t)q);
-        const int n = tile * kTileRows + rr;
-        if (n < a.nout) store_out<EPI, false>(a, gi, t, n, acc);
-      }
-    }
+  if (warp >= 2 && !s_flags[0]) {
+    const int q = r / R4, rl = r - q * R4;
+    float* dst = recv + (size_t)cr * kTcXRows * R4 + rl;  // this rank's slot in rank q
+#pragma unroll
+    for (int t = 0; t < kTcCols; ++t)
+      if (t0 + t < a.M) st_dsmem_f32(dst + (t0 + t) * R4, (uint32_t)q, v[t]);
   }
   __syncwarp();
-  cluster_sync_all();  // no CTA leaves while another still reads its partial
+  cluster_sync_all();
+  if (warp >= 2 && !s_flags[0]) {
+    const int r0 = cr * R4 < kTileRows ? cr * R4 : kTileRows;
+    const int r1 = r0 + R4 < kTileRows ? r0 + R4 : kTileRows;
+    const int RR = r1 - r0;
+    const GroupInfo gi{0, 0, a.M};
+    for (int e = threadIdx.x - 64; e < RR * a.M; e += kTcEpi) {
+      const int t = e / RR, rl = e - t * RR;
+      float acc = 0.f;
+      for (int src = 0; src < cs; ++src) acc += recv[((size_t)src * kTcXRows + t) * R4 + rl];
+      const int n = tile * kTileRows + r0 + rl;
+      if (n < a.nout) store_out<EPI, false>(a, gi, t, n, acc);
+    }
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

@@ -836,14 +836,20 @@ __global__ void __launch_bounds__(kThreads, MINB)
         for (int e = ct; e < a.M * kTileRows; e += kNCW * 32) part[e] = 0.f;
       }
       cluster_sync_all();
-      // Rank r sums rows [r*128/S, (r+1)*128/S) of every token over the S
-      // partials, in rank order, and writes them.
+      // Rank r sums its run of R4 rows of every token over the S partials,
+      // in rank order, and writes them: R4 = 128/S rounded up to a multiple
+      // of 4, the last rank's run cut at 128 (S need not divide 128: the
+      // router's clusters have up to 8 CTAs, one per 128 k of the hidden
+      // size; with 128/S rounded down, rows 125-127 of a tile were lost).
       const int cs = (int)cluster_size(), cr = (int)cluster_rank();
-      const int R = kTileRows / cs;
+      const int R4 = ((kTileRows + cs - 1) / cs + 3) / 4 * 4;
+      const int r0 = cr * R4 < kTileRows ? cr * R4 : kTileRows;
+      const int r1 = r0 + R4 < kTileRows ? r0 + R4 : kTileRows;
       const int tile = (int)(blockIdx.x / cs);
       if (!aborted && tile < TILES && nunits > 0) {
-        for (int e = ct; e < R * gi.c; e += kNCW * 32) {
-          const int t = e / R, r = cr * R + (e - t * R);
+        const int RR = r1 - r0;
+        for (int e = ct; e < RR * gi.c; e += kNCW * 32) {
+          const int t = e / RR, r = r0 + (e - t * RR);
           float v = 0.f;
           for (int qr = 0; qr < cs; ++qr) v += ld_dsmem_f32(part + t * kTileRows + r, (uint32_t)qr);
           emit(tile, r, t, v, 0.f);

@@ -117,6 +117,24 @@ def test_routing_limits_topk32_of_1024_experts_64_tokens():
     _check(*blk, k, "E=1024 k=32 M=64")
 
 
+@pytest.mark.parametrize("H", [320, 520, 696, 840])
+def test_router_clusters_of_any_size_cover_every_expert_row(H):
+    # The router runs one thread-block cluster of min(H/128 rounded up, 8)
+    # CTAs per 128 experts: 3, 5, 6 and 7 CTAs here, which do not divide the
+    # 128 rows of a tile. Experts 125-127 (the last rows of the first tile)
+    # are made the likeliest choices, so most tokens' top-k depends on them.
+    M, E, I, k = 16, 160, 128, 4
+    key = ("router-rows", H)
+    Wr = wl.normal_bf16((E, H), 1.0 / math.sqrt(H), *key, "Wr")
+    Wr[125:128] = wl.normal_bf16((3, H), 6.0 / math.sqrt(H), *key, "Wr-hot")
+    x, _ = gap_rows(Wr, M, H, k, *key, "x")
+    W13 = np.stack([wl.normal_bf16((2 * I, H), 0.02, *key, "W13", e) for e in range(E)])
+    W2 = np.stack([wl.normal_bf16((H, I), 0.02, *key, "W2", e) for e in range(E)])
+    idx = oracle.moe(x, Wr, lambda e: (W13[e], W2[e]), k, I, shared=None)["idx"]
+    assert np.isin(idx, [125, 126, 127]).any(axis=1).mean() >= 0.5, idx
+    _check(x, Wr, W13, W2, None, k, "router rows H=%d" % H)
+
+
 def test_skewed_routing_shares_experts_across_groups():
     # power-law expert popularity at 64 tokens (32-row expert groups): experts
     # serving 17-32 tokens (one wide group), one serving more than 32 (two
