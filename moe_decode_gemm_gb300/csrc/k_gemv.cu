@@ -8,12 +8,13 @@
 //
 // Two kernels share that plan. In both, one producer thread streams stages
 // of weights with one 3-D TMA box (R rows x k blocks of 64, 128-byte swizzle)
-// and the tokens' matching k range (a bulk copy per token, issued once the
-// previous kernel has finished; the weights of the first stages are in
-// flight before that), and eight consumer warps split each stage by k block.
+// and the tokens' matching k range (issued once the previous kernel has
+// finished; the weights of the first stages are in flight before that), and
+// eight consumer warps split each stage by k block.
 //
 // gemv_slab_kernel (1-2 tokens, CUDA cores): 32 KB stages of R rows x 16384/R
-// k; lane l of warp w takes row l % R of k block w*(32/R) + l/R and its 8
+// k, the token slices by one bulk copy per token; lane l of warp w takes row
+// l % R of k block w*(32/R) + l/R and its 8
 // chunks of 16 bytes, multiplying them with the tokens' matching chunks
 // (fma.rn.f32.bf16, fp32 sums). The 32/R lanes of a row and then the 8 warps
 // are summed in a fixed order, so results do not vary from run to run.
