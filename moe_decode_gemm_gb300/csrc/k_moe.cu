@@ -431,16 +431,33 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
        v += (long long)gridDim.x * blockDim.x) {
     const int m = (int)(v / per_row);
     const int n = (int)(v - (long long)m * per_row) * 4;
+    // Eight slots at a time: their gates and pair positions are loaded, then
+    // their expert outputs (independent loads, one round trip per batch of
+    // eight instead of two per slot), then added in slot order.
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      const float g = gate ? gate[m * k + j] : 1.0f;
-      const int p = gate ? pair_of[m * k + j] : m;
-      const float4 ov =
-          *reinterpret_cast<const float4*>(DG_AT(status, o, (long long)p * H + n, o_len - 3));
-      acc[0] = fmaf(g, ov.x, acc[0]);
-      acc[1] = fmaf(g, ov.y, acc[1]);
-      acc[2] = fmaf(g, ov.z, acc[2]);
-      acc[3] = fmaf(g, ov.w, acc[3]);
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      float g[8];
+      int p[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const int j = j0 + jj;
+        g[jj] = j < k ? (gate ? gate[m * k + j] : 1.0f) : 0.f;
+        p[jj] = j < k ? (gate ? pair_of[m * k + j] : m) : -1;
+      }
+      float4 ov[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj)
+        if (p[jj] >= 0)
+          ov[jj] = *reinterpret_cast<const float4*>(
+              DG_AT(status, o, (long long)p[jj] * H + n, o_len - 3));
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj)
+        if (p[jj] >= 0) {
+          acc[0] = fmaf(g[jj], ov[jj].x, acc[0]);
+          acc[1] = fmaf(g[jj], ov[jj].y, acc[1]);
+          acc[2] = fmaf(g[jj], ov[jj].z, acc[2]);
+          acc[3] = fmaf(g[jj], ov[jj].w, acc[3]);
+        }
     }
     if (s) {
       const float4 sv = *reinterpret_cast<const float4*>(s + (long long)m * H + n);
