@@ -29,7 +29,11 @@ constexpr int expert_pair_smem() {
 
 static StreamArgs base_args(const Ctx& cx, float* ws, int* ctr) {
   StreamArgs a = {};
-  a.mma_min_tokens = 3;  // 1-2 tokens: CUDA-core dot products
+  // mma.sync dot products for groups of any size: same-GPU A/B of the MoE
+  // block, us at M = 1 / 4 / 16 / 64, CUDA cores for groups of 1-2 tokens ->
+  // mma.sync: 142.0 / 428.4 / 1453.2 / 3745.9 -> 140.6 / 425.4 / 1446.0 /
+  // 3712.8 (most groups hold 1-2 tokens under uniform routing)
+  a.mma_min_tokens = 1;
   a.ws = ws;
   a.ctr = ctr;
   a.status = cx.status;
