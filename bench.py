@@ -133,11 +133,11 @@ def layer_bytes(M, U):
 # DRAM traffic (read + write) of the routed gate/up kernel per chosen expert,
 # from one ncu capture of a small case of each instance: 16 token rows per
 # stage (up to 16 tokens; 16 tokens over a 32-expert bank, 31 experts chosen:
-# 1826.3 MB in one launch) and 32 rows (beyond; 32 tokens, 32 experts:
-# 1887.5 MB). Its traffic grows in proportion to the experts it streams, so a
+# 1826.1 MB in one launch) and 32 rows (beyond; 32 tokens, 32 experts:
+# 1887.4 MB). Its traffic grows in proportion to the experts it streams, so a
 # full launch's traffic is this times its count.
 def w13_traffic_per_expert(M):
-    return 1826.3e6 / 31 if M <= 16 else 1887.5e6 / 32
+    return 1826.1e6 / 31 if M <= 16 else 1887.4e6 / 32
 
 
 def w13_launch_bytes(M, U):
