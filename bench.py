@@ -322,6 +322,30 @@ def per_config(dg, torch, dev, layer0, peak_gbs, cpu=True):
     return out
 
 
+def stack_config(args, world, pf_bytes):
+    """The workload description both arms print: the layer stack, its shapes
+    and how it is run. The bytes a step streams are given for uniform routing
+    (the expected number of distinct experts per layer)."""
+    nl = args.layers
+    eu = lambda M: E * (1.0 - (1.0 - K8 / E) ** M)
+    step_gb = nl * sum(layer_bytes(M, eu(M)) for M in BATCHES) / 1e9
+    return {
+        "workload": "decode layer stack: %d layers x (q/kv/o projections 7168->7168/1024/7168, "
+                    "q and kv as one fused 7168->8192 projection, + MoE H=7168 E=384 top-8 "
+                    "I=2048 + shared expert), batches %s" % (nl, list(BATCHES)),
+        "layers": nl, "batches": list(BATCHES), "hidden": H, "experts": E, "topk": K8,
+        "inter": I,
+        "routing": ("uniform (iid router scores)" if args.router_skew <= 0 else
+                    "skewed: router row e scaled by (e+1)^-%g, normalised" % args.router_skew),
+        "l2": "inputs larger than L2 (a step streams ~%.0f GB of distinct weights at uniform "
+              "routing)" % step_gb,
+        "prefetch": (False if args.no_prefetch else
+                     "next layer's Wq, first %d bytes (half of L2), side stream" % pf_bytes),
+        "streams": "decode stream priority -1 (high); shared expert and prefetch on "
+                   "lower-priority side streams", "parallelism": "replicas" if world > 1 else "1 GPU",
+    }
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -498,21 +522,7 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded random-init bf16 weights of the stated shapes, N(0,1) tokens)",
-        "config": {
-            "workload": "decode layer stack: %d layers x (q/kv/o projections 7168->7168/1024/7168, "
-                        "q and kv as one fused 7168->8192 projection, + MoE H=7168 E=384 top-8 "
-                        "I=2048 + shared expert), batches %s" % (nl, list(BATCHES)),
-            "layers": nl, "batches": list(BATCHES), "hidden": H, "experts": E, "topk": K8,
-            "inter": I,
-            "routing": ("uniform (iid router scores)" if args.router_skew <= 0 else
-                        "skewed: router row e scaled by (e+1)^-%g, normalised" % args.router_skew),
-            "l2": "inputs larger than L2 (each step streams ~%.0f GB of distinct "
-                              "weights)" % (step_bytes / 1e9),
-            "prefetch": (False if args.no_prefetch else
-                         "next layer's Wq, first %d bytes (half of L2), side stream" % pf_bytes),
-            "streams": "decode stream priority -1 (high); shared expert and prefetch on "
-                       "lower-priority side streams", "parallelism": "replicas" if world > 1 else "1 GPU",
-        },
+        "config": stack_config(args, world, pf_bytes),
         "pct_of_peak": round(100.0 * tbps * 1e3 / (peak_gbs * world), 2),
         "us_per_layer": {str(M): per_m[M]["us_per_layer"] for M in BATCHES},
         "breakdown": {str(M): per_m[M] for M in BATCHES},
@@ -675,6 +685,7 @@ def run_reference(args, rank, world, local_rank):
     if L is None:
         return {"impl": "reference", "unavailable": "the reference arm draws its weights on a GPU"}
     x_bits = wl.token_rows(1, H, "stack-x", 1)
+    pf_bytes = min(H * H * 2, torch.cuda.get_device_properties(dev).L2_cache_size // 2)
     for _ in range(args.warmup):
         oracle_layer_sample(L, x_bits)
     tb, tt = 0, 0.0
@@ -689,10 +700,10 @@ def run_reference(args, rank, world, local_rank):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(tt * 1e3 / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "decode layer stack (sample: one layer at batch 1 per step)",
-                   "layers": 1, "batches": [1]},
+        "config": stack_config(args, world, pf_bytes),
         "cpu_baseline": {"value": round(v, 6), "unit": "TB/s", "cores": cores, "kind": "oracle",
-                         "sample": "one decode layer at batch 1 per step, fp64"},
+                         "sample": "each step: layer 0 of that stack at batch 1 (q|kv, o, MoE "
+                                   "block with shared expert), fp64"},
         "e2e": {"value": round(v, 6), "unit": "TB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
