@@ -343,7 +343,7 @@ cudaError_t launch_experts_w2(const Ctx& cx, const void* W2, int M, int H, int E
 
 // Shared expert: a dense (ungrouped) pass over every token. Up to 16 tokens
 // the weight-streaming kernel, token rows per stage sized to M like the dense
-// projections (8 rows for 1-2 tokens on CUDA cores, 16 on mma.sync); from 17
+// projections (8 rows for 1-2 tokens, 16 up to 16; mma.sync, as every MoE kernel); from 17
 // tokens the gate/up and down projections are dense contractions for the
 // tcgen05 tensor cores (the SwiGLU gate/up kernel with both accumulators in
 // tensor memory, and the fp32-output projection).

@@ -14,10 +14,12 @@
 // one thread-block cluster, which sum their partials through distributed
 // shared memory.
 //
-// Consumers: a CUDA-core path for 1-2 tokens (a GEMV has no dense
-// contraction to give the tensor cores) and an mma.sync m16n8k16 path for
-// more tokens. Groups are the routed experts of an MoE block (the token list
-// of each comes from the router's scheduler) or one dense matrix.
+// Consumers: a CUDA-core path for groups of fewer than mma_min_tokens tokens
+// (the projections of 1-2 tokens: a GEMV has no dense contraction to give the
+// tensor cores) and an mma.sync m16n8k16 path for the rest (every group of
+// the MoE kernels, where it measured faster even at 1 token). Groups are the
+// routed experts of an MoE block (the token list of each comes from the
+// router's scheduler) or one dense matrix.
 //
 // Sources: "vLLM 如何用智能体辅助优化 Kimi K3 解码性能", Part 1 §1 (small-matrix
 // kernel at batch 1-2, split-K beyond) and Part 1 §3 (routed experts).
