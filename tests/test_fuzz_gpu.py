@@ -1,0 +1,78 @@
+"""Seeded random projection shapes through every dispatcher path.
+
+Each case draws M (1-64), N, K (a multiple of 8; often of 64, so that the
+whole-row slabs apply), an optional residual and an optional row stride for x,
+runs dec_linear through the C ABI, and compares a sample of output columns
+with the fp64 oracle at the stated tolerance. The shapes are chosen so that
+every kernel family appears: whole-row slabs (CUDA cores and mma.sync), the
+cluster splits, stream-K on CUDA cores / mma.sync / tcgen05, and the
+tile-aligned tcgen05 split.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from _util import assert_within_tol, to_f64
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from moe_decode_gemm_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a GPU"
+
+
+import moe_decode_gemm_gb300 as dg  # noqa: E402
+
+
+def _shape(seed):
+    rng = np.random.default_rng(seed)
+    M = int(rng.choice([1, 2, 3, 4, 5, 8, 12, 16, 17, 24, 32, 40, 64]))
+    N = int(rng.choice([int(rng.integers(1, 600)), int(rng.integers(900, 5000)), 2048, 4096]))
+    K = int(rng.choice([64 * int(rng.integers(1, 128)), 8 * int(rng.integers(1, 1024))]))
+    residual = bool(rng.integers(0, 2))
+    ldx = K + 8 * int(rng.integers(0, 4)) if rng.integers(0, 3) == 0 else 0
+    return M, N, K, residual, ldx
+
+
+SEEDS = list(range(48))
+
+
+@pytest.mark.parametrize("seed", SEEDS)
+def test_random_projection_matches_oracle(seed):
+    M, N, K, residual, ldx = _shape(seed)
+    key = ("fuzz", seed)
+    wide = wl.normal_bf16((M, ldx or K), 1.0, *key, "x")
+    W = wl.normal_bf16((N, K), 0.02, *key, "W")
+    r = wl.normal_bf16((M, N), 1.0, *key, "r") if residual else None
+    xt = wl.bits_to_torch(wide)[:, :K]
+    y = dg.dec_linear(xt, wl.bits_to_torch(W), residual=None if r is None else wl.bits_to_torch(r))
+    assert dg.sync_check() == dg.DEC_OK
+    cols = np.sort(np.random.default_rng(seed + 1000).choice(N, min(N, 256), replace=False))
+    ref, A = oracle.linear(wide[:, :K], W[cols])
+    if r is not None:
+        ref, A = oracle.residual(r[:, cols], ref, A)
+    assert_within_tol(to_f64(y)[:, cols], ref, A,
+                      "fuzz seed %d: M=%d N=%d K=%d residual=%s ldx=%d %s" %
+                      (seed, M, N, K, residual, ldx, dg.last_choice()))
+
+
+def test_random_shapes_reach_every_kernel_family():
+    # the draws above cover slabs, clusters and stream-K in every regime
+    seen = set()
+    for seed in SEEDS:
+        M, N, K, residual, ldx = _shape(seed)
+        x = torch.zeros((M, ldx or K), dtype=torch.bfloat16, device="cuda")[:, :K]
+        W = torch.zeros((N, K), dtype=torch.bfloat16, device="cuda")
+        dg.dec_linear(x, W)
+        regime, _ = dg.last_choice()
+        seen.add((regime, "slab" if dg.last_slab() else "cluster" if dg.last_cluster() else "split"))
+    assert dg.sync_check() == dg.DEC_OK
+    for want in [("mma", "slab"), ("smallm", "split"), ("mma", "split"), ("tc", "split"),
+                 ("tc", "cluster")]:
+        assert want in seen, (want, sorted(seen))
