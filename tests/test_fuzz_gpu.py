@@ -76,3 +76,45 @@ def test_random_shapes_reach_every_kernel_family():
     for want in [("mma", "slab"), ("smallm", "split"), ("mma", "split"), ("tc", "split"),
                  ("tc", "cluster")]:
         assert want in seen, (want, sorted(seen))
+
+
+# ---------------------------------------------------------------- MoE blocks
+def _moe_shape(seed):
+    rng = np.random.default_rng(10_000 + seed)
+    M = int(rng.choice([1, 2, 3, 5, 8, 13, 16, 24, 33, 48, 64]))
+    E = int(rng.choice([8, 16, 40, 64, 128, 200, 384]))
+    k = int(min(E, rng.choice([1, 2, 4, 6, 8, 12])))
+    H = 8 * int(rng.integers(16, 80))        # 128-632
+    I = 8 * int(rng.integers(16, 48))        # 128-376
+    shared = bool(rng.integers(0, 2))
+    residual = bool(rng.integers(0, 2))
+    return M, E, k, H, I, shared, residual
+
+
+@pytest.mark.parametrize("seed", list(range(16)))
+def test_random_moe_block_matches_oracle(seed):
+    import math
+    from _util import gap_rows
+    M, E, k, H, I, shared, residual = _moe_shape(seed)
+    key = ("fuzz-moe", seed)
+    Wr = wl.normal_bf16((E, H), 1.0 / math.sqrt(H), *key, "Wr")
+    x, _ = gap_rows(Wr, M, H, k, *key, "x")
+    W13 = np.stack([wl.normal_bf16((2 * I, H), 0.02, *key, "W13", e) for e in range(E)])
+    W2 = np.stack([wl.normal_bf16((H, I), 0.02, *key, "W2", e) for e in range(E)])
+    Ws = (wl.normal_bf16((2 * I, H), 0.02, *key, "Ws13"),
+          wl.normal_bf16((H, I), 0.02, *key, "Ws2")) if shared else None
+    res = wl.normal_bf16((M, H), 1.0, *key, "res") if residual else None
+    t = wl.bits_to_torch
+    idx = torch.full((M, k), -1, dtype=torch.int32, device="cuda")
+    out = dg.moe_decode(t(x), t(Wr), t(W13), t(W2), None if Ws is None else t(Ws[0]),
+                        None if Ws is None else t(Ws[1]), k, topk_idx=idx,
+                        residual=None if res is None else t(res))
+    assert dg.sync_check() == dg.DEC_OK
+    r = oracle.moe(x, Wr, lambda e: (W13[e], W2[e]), k, I, shared=Ws)
+    what = "fuzz moe seed %d: M=%d E=%d k=%d H=%d I=%d shared=%s residual=%s" % (
+        seed, M, E, k, H, I, shared, residual)
+    assert np.array_equal(idx.cpu().numpy(), r["idx"]), what + ": chosen experts differ"
+    ref, A = r["out"], r["absref"]
+    if res is not None:
+        ref, A = oracle.residual(res, ref, A)
+    assert_within_tol(to_f64(out), ref, A, what)
