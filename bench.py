@@ -13,7 +13,8 @@ layer's weights are its own and far exceed L2).
 
 Prints one JSON line (rank 0). Usage:
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--layers L] [--no-prefetch] [--no-cpu-baseline] [--cpu-seconds S]
+                  [--layers L] [--no-prefetch] [--prefetch-l2 F] [--no-cpu-baseline]
+                  [--cpu-seconds S]
                   [--no-configs] [--router-skew S]
 """
 from __future__ import annotations
@@ -322,6 +323,11 @@ def per_config(dg, torch, dev, layer0, peak_gbs, cpu=True):
     return out
 
 
+def prefetch_bytes(args, l2_bytes):
+    """Bytes of the next layer's fused q|kv weight pulled into L2 per layer."""
+    return int(min((H + KV) * H * 2, args.prefetch_l2 * l2_bytes)) // 16 * 16
+
+
 def stack_config(args, world, pf_bytes):
     """The workload description both arms print: the layer stack, its shapes
     and how it is run. The bytes a step streams are given for uniform routing
@@ -340,7 +346,8 @@ def stack_config(args, world, pf_bytes):
         "l2": "inputs larger than L2 (a step streams ~%.0f GB of distinct weights at uniform "
               "routing)" % step_gb,
         "prefetch": (False if args.no_prefetch else
-                     "next layer's Wq, first %d bytes (half of L2), side stream" % pf_bytes),
+                     "next layer's q|kv weight, first %d bytes (%g of L2), side stream"
+                     % (pf_bytes, args.prefetch_l2)),
         "streams": "decode stream priority -1 (high); shared expert and prefetch on "
                    "lower-priority side streams", "parallelism": "replicas" if world > 1 else "1 GPU",
     }
@@ -366,10 +373,11 @@ def run_ours(args, rank, world, local_rank):
     # the decode path leaves free.
     main = torch.cuda.Stream(device=dev, priority=-1)
     pref = torch.cuda.Stream(device=dev)
-    # Prefetch at most half of L2, so the lines it brings in are not evicted
-    # by the weights still streaming through L2 before the next layer reads them.
+    # Prefetch a fraction of L2 (half by default) of the next layer's fused
+    # q|kv weight, so the lines it brings in are not evicted by the weights
+    # still streaming through L2 before the next layer reads them.
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
-    pf_bytes = min(H * H * 2, l2_bytes // 2)
+    pf_bytes = prefetch_bytes(args, l2_bytes)
     acts = {}
     for M in BATCHES:
         x0 = wl.bits_to_torch(wl.token_rows(M, H, "stack-x", M), device=dev)
@@ -390,7 +398,7 @@ def run_ours(args, rank, world, local_rank):
         a = acts[M]
         for l, L in enumerate(layers):
             pf = None if args.no_prefetch else (pref, ev_fork[l],
-                                                layers[(l + 1) % nl].Wq.data_ptr(), pf_bytes)
+                                                layers[(l + 1) % nl].Wqkv.data_ptr(), pf_bytes)
             decode_layer(L, a["xs"][l], a["qkv"], a["r"], a["xs"][l + 1], K8, idx=a["idx"][l],
                          stream=main, prefetch=pf)
 
@@ -685,7 +693,7 @@ def run_reference(args, rank, world, local_rank):
     if L is None:
         return {"impl": "reference", "unavailable": "the reference arm draws its weights on a GPU"}
     x_bits = wl.token_rows(1, H, "stack-x", 1)
-    pf_bytes = min(H * H * 2, torch.cuda.get_device_properties(dev).L2_cache_size // 2)
+    pf_bytes = prefetch_bytes(args, torch.cuda.get_device_properties(dev).L2_cache_size)
     for _ in range(args.warmup):
         oracle_layer_sample(L, x_bits)
     tb, tt = 0, 0.0
@@ -718,6 +726,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=4)
     ap.add_argument("--no-prefetch", action="store_true")
+    ap.add_argument("--prefetch-l2", type=float, default=0.5,
+                    help="fraction of L2 to fill with the next layer's q|kv weight")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-configs", action="store_true",
