@@ -76,9 +76,10 @@ def kernel_label(name):
     if m:
         return "projection [slab %s rows/CTA %s, CUDA cores]" % (m.group(1),
                                                                 _EPI.get(m.group(2), m.group(2)))
-    m = re.search(r"tc_cluster_kernel<(\d+)>", name)
+    m = re.search(r"tc_cluster_kernel<(\d+)(?:,\s*(\d+))?>", name)
     if m:
-        return "projection [tcgen05 %s cluster]" % _EPI.get(m.group(1), m.group(1))
+        stage = "" if m.group(2) is None else ", %d k per stage" % (64 * int(m.group(2)))
+        return "projection [tcgen05 %s cluster%s]" % (_EPI.get(m.group(1), m.group(1)), stage)
     for k, lab in (("schedule_gather_kernel", "schedule + gather"),
                    ("combine_kernel", "combine"), ("add_kernel", "residual add"),
                    ("prefetch_kernel", "l2_prefetch")):

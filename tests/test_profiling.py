@@ -25,6 +25,8 @@ def test_labels_of_every_kernel_family():
             "projection [tcgen05 bf16+residual]",
         "void dg::tc_cluster_kernel<0>(CUtensorMap_st, CUtensorMap_st, dg::StreamArgs, int, unsigned int)":
             "projection [tcgen05 bf16 cluster]",
+        "void dg::tc_cluster_kernel<1, 1>(CUtensorMap_st, CUtensorMap_st, dg::StreamArgs, int, unsigned int)":
+            "projection [tcgen05 bf16+residual cluster, 64 k per stage]",
         "void dg::tc_linear_kernel<3, true>(CUtensorMap_st, CUtensorMap_st, dg::StreamArgs, int, unsigned int)":
             "shared expert gate/up [tcgen05 SwiGLU]",
         "void dg::tc_linear_kernel<2, false>(CUtensorMap_st, CUtensorMap_st, dg::StreamArgs, int, unsigned int)":
