@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(kGvThreads, 2)
 // of 2 or 4 CTAs that split K (fewer token bytes per CTA, partials summed
 // through distributed shared memory) lost to one CTA per slab at every size
 // (8 tokens: 9.0 / 9.7 against 6.9).
-template <int R, int XR, int KBS>
+template <int R, int XR, int KBS, int MINB>
 struct MmaSlab {
   static constexpr int RG = R / 16;                     // 16-row groups
   static constexpr int XN = (XR + 7) / 8;               // 8-token column tiles
@@ -214,17 +214,18 @@ struct MmaSlab {
   static constexpr int SB = (WB + XB + 1023) / 1024 * 1024;
   static constexpr int RED = kNCW * 16 * XR * 4;        // per-warp tiles (token rows only)
   static constexpr int FIXED = 1024 + RED + 256;        // alignment, tiles, barriers, flags
-  static constexpr int STAGES = (115712 - FIXED) / SB;  // two CTAs per SM
+  // two CTAs per SM (MINB = 2), or one with a ring twice as deep (MINB = 1)
+  static constexpr int STAGES = ((MINB == 2 ? 115712 : 225000) - FIXED) / SB;
   static constexpr int SMEM = FIXED + STAGES * SB;
   static_assert((RG * KBS) % kNCW == 0, "whole tasks per warp");
   static_assert(STAGES >= 2, "ring depth");
 };
 
-template <int R, int XR, int KBS, int EPI>
-__global__ void __launch_bounds__(kGvThreads, 2)
+template <int R, int XR, int KBS, int MINB, int EPI>
+__global__ void __launch_bounds__(kGvThreads, MINB)
     gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                     const StreamArgs a) {
-  using P = MmaSlab<R, XR, KBS>;
+  using P = MmaSlab<R, XR, KBS, MINB>;
   constexpr int STAGES = P::STAGES, KS = P::KS, SB = P::SB, RG = P::RG;
   constexpr int XN = P::XN;                            // 8-token column tiles
   constexpr int TPW = RG * KBS / kNCW;                 // tasks per warp per stage
@@ -367,13 +368,13 @@ __global__ void __launch_bounds__(kGvThreads, 2)
   __syncthreads();
 }
 
-template <int R, int XR, int KBS, int EPI>
+template <int R, int XR, int KBS, int MINB, int EPI>
 static cudaError_t run_gemv_mma(const Ctx& cx, const void* x, long long ldx, const void* W,
                                 const void* res, void* y, int M, int N, int K) {
   if (M > XR) return cudaErrorInvalidValue;
-  auto kern = gemv_mma_kernel<R, XR, KBS, EPI>;
-  constexpr int SMEM = MmaSlab<R, XR, KBS>::SMEM;
-  static_assert(2 * (SMEM + 1024) <= kSmemPerSm, "two CTAs per SM");
+  auto kern = gemv_mma_kernel<R, XR, KBS, MINB, EPI>;
+  constexpr int SMEM = MmaSlab<R, XR, KBS, MINB>::SMEM;
+  static_assert(MINB * (SMEM + 1024) <= kSmemPerSm, "CTAs per SM");
   static DevOnce once;
   if (cudaError_t e = setup_smem(once, kern, SMEM, true); e != cudaSuccess) return e;
   CUtensorMap wmap, xmap;
@@ -446,11 +447,24 @@ int gemv_mma_rows(int M, int N, int K, int sms) {
   return 0;
 }
 
+// One CTA per SM with a ring twice as deep when a CTA streams more than
+// 320 KB (its weight rows and token rows over all of K): same-GPU A/B, us,
+// two CTAs per SM -> one: 2048 x 7168 at M = 5 / 8 / 16: 6.89 / 6.90 / 8.87
+// -> 6.35 / 6.33 / 7.09 (344-459 KB); 2048 x 16384 at M = 1 / 8: 13.45 /
+// 13.93 -> 12.45 / 11.80; 4096 x 7168 at M = 4: 11.09 -> 10.70. Below, the
+// next call's CTAs loading their first stages while this one finishes
+// count for more: 4096 x 4096 at M = 1: 7.07 -> 7.37 (295 KB); 2048 x 7168
+// at M = 4: 6.40 -> 6.60 (287 KB).
+constexpr long long kDeepRingBytes = 320 * 1024;
+
 template <int R, int XR, int KBS>
 static cudaError_t mma_epi(const Ctx& cx, bool residual, const void* x, long long ldx,
                            const void* W, const void* res, void* y, int M, int N, int K) {
-  return residual ? run_gemv_mma<R, XR, KBS, EPI_BF16_RES>(cx, x, ldx, W, res, y, M, N, K)
-                  : run_gemv_mma<R, XR, KBS, EPI_BF16>(cx, x, ldx, W, res, y, M, N, K);
+  if ((long long)(R + XR) * K * 2 > kDeepRingBytes)
+    return residual ? run_gemv_mma<R, XR, KBS, 1, EPI_BF16_RES>(cx, x, ldx, W, res, y, M, N, K)
+                    : run_gemv_mma<R, XR, KBS, 1, EPI_BF16>(cx, x, ldx, W, res, y, M, N, K);
+  return residual ? run_gemv_mma<R, XR, KBS, 2, EPI_BF16_RES>(cx, x, ldx, W, res, y, M, N, K)
+                  : run_gemv_mma<R, XR, KBS, 2, EPI_BF16>(cx, x, ldx, W, res, y, M, N, K);
 }
 
 // Token rows per stage XR = 4, 8 or 16 (the least that holds M); k blocks
