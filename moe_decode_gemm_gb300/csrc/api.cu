@@ -252,7 +252,7 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
   const int regime = regime_for(M);
   // Whole-row slabs (R weight rows per CTA, no split over K) when such slabs
   // fill between three quarters of the SMs and all of them: up to 16 tokens
-  // on the tensor cores (16 or 32 rows per CTA), 1-2 tokens on the CUDA cores
+  // on the tensor cores (16, 32 or 48 rows per CTA), 1-2 tokens on the CUDA cores
   // where only 8 rows per CTA fill the SMs (or under DEC_FORCE=smallm).
   // Same-GPU A/B, us per call in a CUDA graph, split-K -> slab: N x K =
   // 2048 x 7168 at M = 1 / 2 / 4 / 5 / 8 / 12 / 16: 8.0 / 8.3 / 8.7 / 8.7 /

@@ -1,5 +1,5 @@
 // k_gemv.cu -- decode projection y = x·Wᵀ for 1-16 tokens without splitting K
-// across CTAs: each CTA owns R consecutive weight rows (R = 8, 16 or 32) over
+// across CTAs: each CTA owns R consecutive weight rows (R = 8 to 48) over
 // the whole K, so no partial sums leave the CTA -- no workspace, counters,
 // atomics or cluster barriers. What split-K spends after the last weight
 // byte (the wait for the slowest rank of a tile, the reduction of the
@@ -192,10 +192,11 @@ __global__ void __launch_bounds__(kGvThreads, 2)
 // 1-2 us faster per call), while a stage here is 32-64 MMAs. A stage is KBS k
 // blocks of 64 of the slab's R rows (16 KB of weights: one 3-D TMA box,
 // 128-byte swizzle) and the same k range of XR = 4, 8 or 16 token rows (one
-// 3-D TMA box, rows past M zero-filled, same swizzle). Task j of a stage (row
-// group j % (R/16), k block j / (R/16)) goes to warp j % 8; a warp keeps one
-// accumulator tile over all its tasks, and the warps of a row group are
-// summed in order at the end, so results do not vary from run to run.
+// 3-D TMA box, rows past M zero-filled, same swizzle). Warp w works on row
+// group w % (R/16) and takes every (warps of that group)-th k block of a
+// stage; it keeps one accumulator tile over all its tasks, and the warps of a
+// row group are summed in order at the end, so results do not vary from run
+// to run.
 //
 // Every CTA reads the tokens' rows over all of K, XR/R of its weight bytes.
 // Measured alternatives (us per call, CUDA graph, N x K = 2048 x 7168): a bulk
@@ -217,7 +218,7 @@ struct MmaSlab {
   // two CTAs per SM (MINB = 2), or one with a ring twice as deep (MINB = 1)
   static constexpr int STAGES = ((MINB == 2 ? 115712 : 225000) - FIXED) / SB;
   static constexpr int SMEM = FIXED + STAGES * SB;
-  static_assert((RG * KBS) % kNCW == 0, "whole tasks per warp");
+  static_assert(RG >= 1 && RG <= kNCW, "row groups");
   static_assert(STAGES >= 2, "ring depth");
 };
 
@@ -228,7 +229,6 @@ __global__ void __launch_bounds__(kGvThreads, MINB)
   using P = MmaSlab<R, XR, KBS, MINB>;
   constexpr int STAGES = P::STAGES, KS = P::KS, SB = P::SB, RG = P::RG;
   constexpr int XN = P::XN;                            // 8-token column tiles
-  constexpr int TPW = RG * KBS / kNCW;                 // tasks per warp per stage
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -297,6 +297,7 @@ __global__ void __launch_bounds__(kGvThreads, MINB)
     griddep_wait();
     const int w = warp - 1;
     const int rg = w % RG;                   // this warp's row group (every task of it)
+    const int nw = (kNCW - rg + RG - 1) / RG;  // warps of that row group
     const int mi = lane >> 3, r8 = lane & 7;
     const int a_row = rg * 16 + (mi & 1) * 8 + r8;
     const int bn = lane >> 2, bk = (lane & 3) * 2;  // B fragment: token, k pair
@@ -314,8 +315,8 @@ __global__ void __launch_bounds__(kGvThreads, MINB)
         const uint32_t wst = smem_u32(smem + s * SB);
         const uint8_t* xs = smem + s * SB + P::WB;   // [k block][XR tokens][128 B], swizzled
 #pragma unroll
-        for (int q = 0; q < TPW; ++q) {
-          const int kb = (w + q * kNCW) / RG;         // k block of this task within the stage
+        // the nw warps of row group rg take the stage's k blocks in turn
+        for (int kb = w / RG; kb < KBS; kb += nw) {
           if ((i * KBS + kb) * 64 < K) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
@@ -435,12 +436,13 @@ int gemv_slab_rows(int M, int N, int K, int sms) {
   return 0;
 }
 
-// Rows per CTA of the mma slabs: 16 or 32, the smaller whose grid keeps
-// between three quarters of the SMs and all of them busy; 0 when neither
-// does (or more than 16 tokens, or K % 64 != 0).
+// Rows per CTA of the mma slabs: 16, 32 or 48 (1-3 row groups), the
+// smallest whose grid fits on the SMs, if that grid keeps at least three
+// quarters of them busy; 0 when none does (or more than 16 tokens, or
+// K % 64 != 0).
 int gemv_mma_rows(int M, int N, int K, int sms) {
   if (M < 1 || M > kMmaMaxTokens || (K % 64) != 0) return 0;
-  for (int R = 16; R <= 32; R <<= 1) {
+  for (int R = 16; R <= 48; R += 16) {
     const long long grid = ((long long)N + R - 1) / R;
     if (grid <= sms) return grid * 4 < 3LL * sms ? 0 : R;
   }
@@ -472,7 +474,7 @@ static cudaError_t mma_epi(const Ctx& cx, bool residual, const void* x, long lon
 template <int R>
 static cudaError_t mma_rows(const Ctx& cx, bool residual, const void* x, long long ldx,
                             const void* W, const void* res, void* y, int M, int N, int K) {
-  constexpr int KBS = 128 / R;
+  constexpr int KBS = R == 48 ? 4 : 128 / R;  // 16, 16 or 24 KB of weights per stage
   if (M <= 4) return mma_epi<R, 4, KBS>(cx, residual, x, ldx, W, res, y, M, N, K);
   if (M <= 8) return mma_epi<R, 8, KBS>(cx, residual, x, ldx, W, res, y, M, N, K);
   return mma_epi<R, 16, KBS>(cx, residual, x, ldx, W, res, y, M, N, K);
@@ -483,6 +485,7 @@ cudaError_t launch_gemv_mma(const Ctx& cx, bool residual, const void* x, const v
   const long long ldx = cx.ldx ? cx.ldx : K;
   if (R == 16) return mma_rows<16>(cx, residual, x, ldx, W, res, y, M, N, K);
   if (R == 32) return mma_rows<32>(cx, residual, x, ldx, W, res, y, M, N, K);
+  if (R == 48) return mma_rows<48>(cx, residual, x, ldx, W, res, y, M, N, K);
   return cudaErrorInvalidValue;
 }
 

@@ -131,7 +131,7 @@ def test_batch_sweep_k7168(M, N):
     cols = np.random.default_rng(N + M).choice(N, 384, replace=False)
     _, (regime, _) = _check_random(M, N, 7168, ("cfg2", M, N), cols=cols)
     assert regime == _expect_path(M)
-    assert dg.last_slab() == (N == 2048 and M <= 16)
+    assert dg.last_slab() == (N in (2048, 7168) and M <= 16)
 
 
 @pytest.mark.parametrize("M", [1, 4, 16, 64])
@@ -332,9 +332,10 @@ def test_output_guard_bands_untouched():
 
 @pytest.mark.parametrize("M", [4, 16])
 @pytest.mark.parametrize("residual", [True, False])
-def test_wide_tiles_full_size_7168(M, residual):
-    # N = K = 7168 at 4 and 16 tokens takes the 256-row-tile instance (the
-    # layer stack's o projection, with the residual fused): every element
+def test_wide_tiles_full_size_7168(split_k_only, M, residual):
+    # N = K = 7168 at 4 and 16 tokens on split-K takes the 256-row-tile
+    # instance (the dispatcher gives this shape 48-row slabs; the 256-row
+    # instance serves the 8192-row fused q|kv projection): every element
     # against the oracle
     N = K = 7168
     x = wl.normal_bf16((M, K), 1.0, "wide", M, "x")
@@ -484,8 +485,32 @@ def test_mma_slab_for_one_or_two_tokens_matches_the_cuda_core_slab(M, monkeypatc
 
 def test_mma_slab_declines_shapes_it_does_not_fill():
     # too few rows for three quarters of the SMs, K not a multiple of 64,
-    # too many rows for 32 per CTA, more than 16 tokens
-    for M, N, K in [(4, 1024, 4096), (3, 4096, 1000), (4, 6000, 2048), (8, 7168, 7168),
-                    (17, 2048, 4096)]:
+    # too many rows for 48 per CTA, more than 16 tokens
+    for M, N, K in [(4, 1024, 4096), (3, 4096, 1000), (8, 7400, 7168), (17, 2048, 4096)]:
         _check_random(M, N, K, ("mslab-no", M, N, K))
         assert not dg.last_slab(), (M, N, K)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 7168, 7168), (5, 7168, 7168), (16, 7168, 4096),
+                                   (3, 6000, 7168), (12, 5800, 1088), (2, 7168, 16384)])
+def test_mma_slabs_of_48_rows(M, N, K):
+    # three 16-row groups per CTA (N from 4865 to 7296 rows): warps 0, 3, 6 /
+    # 1, 4, 7 / 2, 5 share a group's k blocks; ragged last slab; deep ring
+    cols = np.random.default_rng(N + K + M).choice(N, 512, replace=False)
+    y, (regime, split) = _check_random(M, N, K, ("mslab48", M, N, K), cols=cols)
+    assert regime == "mma" and dg.last_slab() and split == 1 and dg.last_grid() == (N + 47) // 48
+
+
+@pytest.mark.parametrize("M", [1, 8, 16])
+def test_mma_slabs_of_48_rows_integer_inputs_match_oracle_and_split_k(M, monkeypatch):
+    K, N = 2048, 7168
+    x = wl.integer_bf16((M, K), -2, 2, "mslab48-int", M, "x")
+    W = wl.integer_bf16((N, K), -2, 2, "mslab48-int", M, "W")
+    y, _ = _gpu_linear(x, W)
+    assert dg.last_slab()
+    ref, _ = oracle.linear(x, W)
+    assert np.array_equal(wl.torch_to_bits(y), oracle.f64_to_bf16_bits(ref))
+    monkeypatch.setenv("DEC_FORCE", "splitk")
+    ys, _ = _gpu_linear(x, W)
+    assert not dg.last_slab()
+    assert torch.equal(y, ys)
