@@ -76,7 +76,7 @@ extern "C" {
  * Accumulates in fp32 and rounds once to bf16 (nearest even). The kernel is
  * chosen from M: M <= 2 the small-matrix kernels; 3 <= M <= 16 split-K on
  * mma.sync; M >= 17 split-K on tcgen05 (at exactly 16 tokens mma.sync streams
- * faster). For 1-16 tokens, when K % 64 == 0 and slabs of 16, 32 or 48 whole
+ * faster). For 1-16 tokens, when K % 64 == 0 and slabs of 16, 32, 48 or 64 whole
  * weight rows per CTA fill between three quarters of the SMs and all of them,
  * no CTA splits K (the sum over K stays inside the CTA; dot products on
  * mma.sync, reported as DEC_REGIME_MMA); for 1-2 tokens where only slabs of 8

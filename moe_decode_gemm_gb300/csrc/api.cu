@@ -252,15 +252,17 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
   const int regime = regime_for(M);
   // Whole-row slabs (R weight rows per CTA, no split over K) when such slabs
   // fill between three quarters of the SMs and all of them: up to 16 tokens
-  // on the tensor cores (16, 32 or 48 rows per CTA), 1-2 tokens on the CUDA cores
+  // on the tensor cores (16, 32, 48 or 64 rows per CTA), 1-2 tokens on the CUDA cores
   // where only 8 rows per CTA fill the SMs (or under DEC_FORCE=smallm).
   // Same-GPU A/B, us per call in a CUDA graph, split-K -> slab: N x K =
   // 2048 x 7168 at M = 1 / 2 / 4 / 5 / 8 / 12 / 16: 8.0 / 8.3 / 8.7 / 8.7 /
   // 8.9 / 9.3 / 9.5 -> 6.4 / 6.4 / 6.4 / 7.0 / 6.9 / 8.8 / 8.9; 2048 x 16384
   // at M = 8: 16.6 -> 14.0; 4096 x 4096 at M = 1 / 8: 8.6 / 9.6 -> 7.2 / 7.4;
   // 4096 x 7168 at M = 8 / 16: 14.6 / 15.9 -> 11.6 / 14.4 (the CUDA-core
-  // slabs: 6.8 / 7.8 at M = 1 / 2 of 2048 x 7168). DEC_FORCE=splitk keeps
-  // the split-K kernels.
+  // slabs: 6.8 / 7.8 at M = 1 / 2 of 2048 x 7168); 48-row slabs: 7168 x 7168
+  // at M = 1 / 16: 18.6 / 20.8 -> 17.1 / 18.2; 64-row slabs: 8192 x 7168 at
+  // M = 1 / 8 / 16: 20.4 / 21.5 / 22.4 -> 18.9 / 19.4 / 21.3, 8192 x 4096 at
+  // M = 4: 16.7 -> 12.2. DEC_FORCE=splitk keeps the split-K kernels.
   if (S == 0 && !force_splitk()) {
     const bool core_only = forced("smallm");
     const int Rm = (regime != DEC_REGIME_TC && !core_only) ? gemv_mma_rows(M, N, K, s->sms) : 0;

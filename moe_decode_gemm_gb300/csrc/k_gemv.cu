@@ -1,5 +1,5 @@
 // k_gemv.cu -- decode projection y = x·Wᵀ for 1-16 tokens without splitting K
-// across CTAs: each CTA owns R consecutive weight rows (R = 8 to 48) over
+// across CTAs: each CTA owns R consecutive weight rows (R = 8 to 64) over
 // the whole K, so no partial sums leave the CTA -- no workspace, counters,
 // atomics or cluster barriers. What split-K spends after the last weight
 // byte (the wait for the slowest rank of a tile, the reduction of the
@@ -190,8 +190,8 @@ __global__ void __launch_bounds__(kGvThreads, 2)
 // a stage cost more than its copies once the dependency has resolved (~0.5 us
 // per 32 KB stage of one token; a copy of the kernel with them left out was
 // 1-2 us faster per call), while a stage here is 32-64 MMAs. A stage is KBS k
-// blocks of 64 of the slab's R rows (16 KB of weights: one 3-D TMA box,
-// 128-byte swizzle) and the same k range of XR = 4, 8 or 16 token rows (one
+// blocks of 64 of the slab's R rows (16 KB of weights, 24 KB at R = 48: one
+// 3-D TMA box, 128-byte swizzle) and the same k range of XR = 4, 8 or 16 token rows (one
 // 3-D TMA box, rows past M zero-filled, same swizzle). Warp w works on row
 // group w % (R/16) and takes every (warps of that group)-th k block of a
 // stage; it keeps one accumulator tile over all its tasks, and the warps of a
@@ -436,13 +436,13 @@ int gemv_slab_rows(int M, int N, int K, int sms) {
   return 0;
 }
 
-// Rows per CTA of the mma slabs: 16, 32 or 48 (1-3 row groups), the
+// Rows per CTA of the mma slabs: 16, 32, 48 or 64 (1-4 row groups), the
 // smallest whose grid fits on the SMs, if that grid keeps at least three
 // quarters of them busy; 0 when none does (or more than 16 tokens, or
 // K % 64 != 0).
 int gemv_mma_rows(int M, int N, int K, int sms) {
   if (M < 1 || M > kMmaMaxTokens || (K % 64) != 0) return 0;
-  for (int R = 16; R <= 48; R += 16) {
+  for (int R = 16; R <= 64; R += 16) {
     const long long grid = ((long long)N + R - 1) / R;
     if (grid <= sms) return grid * 4 < 3LL * sms ? 0 : R;
   }
@@ -470,11 +470,12 @@ static cudaError_t mma_epi(const Ctx& cx, bool residual, const void* x, long lon
 }
 
 // Token rows per stage XR = 4, 8 or 16 (the least that holds M); k blocks
-// per stage so that a stage holds 16 KB of weights (8 at R = 16, 4 at 32).
+// per stage so that a stage holds 16 KB of weights (8 at R = 16, 4 at 32, 2
+// at 64), 24 KB at R = 48 (4 k blocks, two per warp of a row group).
 template <int R>
 static cudaError_t mma_rows(const Ctx& cx, bool residual, const void* x, long long ldx,
                             const void* W, const void* res, void* y, int M, int N, int K) {
-  constexpr int KBS = R == 48 ? 4 : 128 / R;  // 16, 16 or 24 KB of weights per stage
+  constexpr int KBS = R == 48 ? 4 : 128 / R;
   if (M <= 4) return mma_epi<R, 4, KBS>(cx, residual, x, ldx, W, res, y, M, N, K);
   if (M <= 8) return mma_epi<R, 8, KBS>(cx, residual, x, ldx, W, res, y, M, N, K);
   return mma_epi<R, 16, KBS>(cx, residual, x, ldx, W, res, y, M, N, K);
@@ -486,6 +487,7 @@ cudaError_t launch_gemv_mma(const Ctx& cx, bool residual, const void* x, const v
   if (R == 16) return mma_rows<16>(cx, residual, x, ldx, W, res, y, M, N, K);
   if (R == 32) return mma_rows<32>(cx, residual, x, ldx, W, res, y, M, N, K);
   if (R == 48) return mma_rows<48>(cx, residual, x, ldx, W, res, y, M, N, K);
+  if (R == 64) return mma_rows<64>(cx, residual, x, ldx, W, res, y, M, N, K);
   return cudaErrorInvalidValue;
 }
 

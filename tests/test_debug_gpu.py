@@ -63,7 +63,7 @@ PROJ = [(1, 4000, 1000, None), (2, 1000, 4104, None), (1, 7168, 7168, None),
         (48, 7168, 2048, None), (17, 16384, 1024, None), (64, 300, 520, 3),
         (2, 2048, 4096, None), (1, 1100, 1024, None), (3, 2000, 7168, None),
         (4, 4096, 1088, None), (12, 4096, 1088, None), (16, 2000, 7168, None),
-        (24, 1900, 6200, None), (6, 6000, 2048, None)]
+        (24, 1900, 6200, None), (6, 6000, 2048, None), (8, 8192, 2048, None)]
 
 
 @pytest.mark.parametrize("M,N,K,S", PROJ)

@@ -334,8 +334,7 @@ def test_output_guard_bands_untouched():
 @pytest.mark.parametrize("residual", [True, False])
 def test_wide_tiles_full_size_7168(split_k_only, M, residual):
     # N = K = 7168 at 4 and 16 tokens on split-K takes the 256-row-tile
-    # instance (the dispatcher gives this shape 48-row slabs; the 256-row
-    # instance serves the 8192-row fused q|kv projection): every element
+    # instance (the dispatcher gives this shape 48-row slabs): every element
     # against the oracle
     N = K = 7168
     x = wl.normal_bf16((M, K), 1.0, "wide", M, "x")
@@ -485,8 +484,8 @@ def test_mma_slab_for_one_or_two_tokens_matches_the_cuda_core_slab(M, monkeypatc
 
 def test_mma_slab_declines_shapes_it_does_not_fill():
     # too few rows for three quarters of the SMs, K not a multiple of 64,
-    # too many rows for 48 per CTA, more than 16 tokens
-    for M, N, K in [(4, 1024, 4096), (3, 4096, 1000), (8, 7400, 7168), (17, 2048, 4096)]:
+    # too many rows for 64 per CTA, more than 16 tokens
+    for M, N, K in [(4, 1024, 4096), (3, 4096, 1000), (8, 9800, 7168), (17, 2048, 4096)]:
         _check_random(M, N, K, ("mslab-no", M, N, K))
         assert not dg.last_slab(), (M, N, K)
 
@@ -514,3 +513,44 @@ def test_mma_slabs_of_48_rows_integer_inputs_match_oracle_and_split_k(M, monkeyp
     ys, _ = _gpu_linear(x, W)
     assert not dg.last_slab()
     assert torch.equal(y, ys)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8192, 7168), (4, 8192, 7168), (16, 8192, 7168),
+                                   (3, 7400, 7168), (8, 9728, 2048), (12, 9000, 1088),
+                                   (2, 8192, 16384)])
+def test_mma_slabs_of_64_rows(M, N, K):
+    # four 16-row groups per CTA (N from 7297 to 9728 rows, the fused q|kv
+    # projection among them): warps w and w + 4 share group w's k blocks;
+    # ragged last slab; deep ring
+    cols = np.random.default_rng(N + K + M).choice(N, 512, replace=False)
+    y, (regime, split) = _check_random(M, N, K, ("mslab64", M, N, K), cols=cols)
+    assert regime == "mma" and dg.last_slab() and split == 1 and dg.last_grid() == (N + 63) // 64
+
+
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_mma_slabs_of_64_rows_integer_inputs_match_oracle_and_split_k(M, monkeypatch):
+    K, N = 2048, 8192
+    x = wl.integer_bf16((M, K), -2, 2, "mslab64-int", M, "x")
+    W = wl.integer_bf16((N, K), -2, 2, "mslab64-int", M, "W")
+    y, _ = _gpu_linear(x, W)
+    assert dg.last_slab() and dg.last_grid() == N // 64
+    ref, _ = oracle.linear(x, W)
+    assert np.array_equal(wl.torch_to_bits(y), oracle.f64_to_bf16_bits(ref))
+    monkeypatch.setenv("DEC_FORCE", "splitk")
+    ys, _ = _gpu_linear(x, W)
+    assert not dg.last_slab()
+    assert torch.equal(y, ys)
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_mma_slabs_of_64_rows_residual(M):
+    # every element of a 64-row slab call with the residual epilogue
+    N, K = 8192, 2048
+    x = wl.normal_bf16((M, K), 1.0, "mslab64-res", M, "x")
+    W = wl.normal_bf16((N, K), 0.02, "mslab64-res", M, "W")
+    r = wl.normal_bf16((M, N), 1.0, "mslab64-res", M, "r")
+    y, (regime, _) = _gpu_linear(x, W, res_bits=r)
+    assert regime == "mma" and dg.last_slab() and dg.last_grid() == N // 64
+    f, A = oracle.linear(x, W)
+    f, A = oracle.residual(r, f, A)
+    assert_within_tol(to_f64(y), f, A, "64-row slabs M=%d residual" % M)
