@@ -408,22 +408,66 @@ def run_ours(args, rank, world, local_rank):
         if not args.no_prefetch:
             main.wait_stream(pref)
 
-    def step_e2e():
-        for M in BATCHES:
-            a = acts[M]
-            with torch.cuda.stream(main):
-                a["xs"][0].copy_(a["x_host"], non_blocking=True)
-            stack(M)
-            with torch.cuda.stream(main):
-                a["out_host"].copy_(a["xs"][nl], non_blocking=True)
-        if not args.no_prefetch:
-            main.wait_stream(pref)
-
     # warm-up (allocates the library's workspace outside the timed region)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     assert dg.sync_check() == dg.DEC_OK
+
+    # The step as one CUDA graph, the way a serving engine replays a decode
+    # step of fixed shape: captured once, after the warm-up has allocated the
+    # library's workspace; every replay launches the same kernels on the same
+    # buffers (inputs in static buffers). --eager times the launches one by
+    # one instead; both numbers are printed.
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        n0 = dg.launch_count()
+        with torch.cuda.graph(g, stream=main):
+            fn()
+            if not args.no_prefetch:
+                main.wait_stream(pref)
+        n = dg.launch_count() - n0
+        torch.cuda.synchronize()
+        return g, n
+
+    graph, kernels_per_step = (None, None) if args.eager else capture(
+        lambda: [stack(M) for M in BATCHES])
+
+    def replay(g):
+        with torch.cuda.stream(main):
+            g.replay()
+
+    def timed_step():
+        if graph is None:
+            step()
+        else:
+            replay(graph)
+
+    def step_e2e():
+        # inputs in from pinned host memory, the step, results out
+        if graph is None:
+            for M in BATCHES:
+                a = acts[M]
+                with torch.cuda.stream(main):
+                    a["xs"][0].copy_(a["x_host"], non_blocking=True)
+                stack(M)
+                with torch.cuda.stream(main):
+                    a["out_host"].copy_(a["xs"][nl], non_blocking=True)
+            if not args.no_prefetch:
+                main.wait_stream(pref)
+            return
+        with torch.cuda.stream(main):
+            for M in BATCHES:
+                acts[M]["xs"][0].copy_(acts[M]["x_host"], non_blocking=True)
+            graph.replay()
+            for M in BATCHES:
+                acts[M]["out_host"].copy_(acts[M]["xs"][nl], non_blocking=True)
+
+    if graph is not None:
+        for _ in range(args.warmup):
+            timed_step()
+        torch.cuda.synchronize()
+        assert dg.sync_check() == dg.DEC_OK
 
     # active experts per (M, layer), from the returned indices
     U = {M: [len(set(acts[M]["idx"][l].cpu().numpy().ravel().tolist())) for l in range(nl)]
@@ -445,14 +489,30 @@ def run_ours(args, rank, world, local_rank):
     clocks.start()
     e0.record(main)
     for _ in range(args.steps):
-        step()
+        timed_step()
     e1.record(main)
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    launches = dg.launch_count() - launches0
+    launches = (dg.launch_count() - launches0 if graph is None
+                else kernels_per_step * args.steps)
     assert dg.sync_check() == dg.DEC_OK
     ms = e0.elapsed_time(e1)
+
+    # the same steps launched one by one (the eager number beside the graph's)
+    ms_eager = ms
+    if graph is not None:
+        q0 = torch.cuda.Event(enable_timing=True)
+        q1 = torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        q0.record(main)
+        for _ in range(args.steps):
+            step()
+        q1.record(main)
+        torch.cuda.synchronize()
+        assert dg.sync_check() == dg.DEC_OK
+        ms_eager = q0.elapsed_time(q1)
 
     # Roofline of the routed gate/up kernel, in a pass of its own: the
     # library's probe records CUDA events on the launching stream around every
@@ -472,20 +532,26 @@ def run_ours(args, rank, world, local_rank):
     # per-batch breakdown (untimed pass structure, same events)
     per_m = {}
     for M in BATCHES:
-        f0 = torch.cuda.Event(enable_timing=True)
-        f1 = torch.cuda.Event(enable_timing=True)
-        f0.record(main)
-        for _ in range(3):
-            stack(M)
-        f1.record(main)
-        torch.cuda.synchronize()
-        us_layer = f0.elapsed_time(f1) * 1000.0 / (3 * nl)
+        gm = None if graph is None else capture(lambda: stack(M))[0]
+        us = []
+        for fn in ([lambda: replay(gm)] if gm is not None else []) + [lambda: stack(M)]:
+            f0 = torch.cuda.Event(enable_timing=True)
+            f1 = torch.cuda.Event(enable_timing=True)
+            f0.record(main)
+            for _ in range(3):
+                fn()
+            f1.record(main)
+            if not args.no_prefetch:
+                main.wait_stream(pref)
+            torch.cuda.synchronize()
+            us.append(f0.elapsed_time(f1) * 1000.0 / (3 * nl))
+        del gm
         by = sum(layer_bytes(M, U[M][l]) for l in range(nl)) / nl
-        per_m[M] = {"us_per_layer": round(us_layer, 2), "TBps": round(by / us_layer / 1e6, 3),
+        per_m[M] = {"us_per_layer": round(us[0], 2), "TBps": round(by / us[0] / 1e6, 3),
+                    "us_per_layer_eager": round(us[-1], 2),
                     "active_experts": U[M], "kernels_per_layer": None}
-    if not args.no_prefetch:
-        main.wait_stream(pref)
     torch.cuda.synchronize()
+    assert dg.sync_check() == dg.DEC_OK
 
     # kernel count per layer: launches of one layer at M=1
     n0 = dg.launch_count()
@@ -509,7 +575,7 @@ def run_ours(args, rank, world, local_rank):
     ms_e2e = g0.elapsed_time(g1)
 
     # max over ranks
-    ms, ms_e2e = replica_max([ms, ms_e2e], world)
+    ms, ms_e2e, ms_eager = replica_max([ms, ms_e2e, ms_eager], world)
 
     peak_gbs, peak_kind = peaks()
     tbps = job_tbps(world, step_bytes, args.steps, ms)
@@ -537,6 +603,10 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(tbps_e2e, 4), "unit": "TB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": h2d},
         "gpu_launches": launches,
+        "launch": ("one CUDA graph per step (captured once; %d kernels per step)"
+                   % kernels_per_step if graph is not None else "eager (kernel by kernel)"),
+        "eager": {"value": round(job_tbps(world, step_bytes, args.steps, ms_eager), 4),
+                  "ms_per_step": round(ms_eager / args.steps, 4)},
         "roofline": {
             "kernel": "routed-expert gate/up (SwiGLU) weight-streaming kernel",
             "bound": "hbm",
@@ -726,6 +796,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=4)
     ap.add_argument("--no-prefetch", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="time the step's launches one by one instead of as a CUDA graph")
     ap.add_argument("--prefetch-l2", type=float, default=0.5,
                     help="fraction of L2 to fill with the next layer's q|kv weight")
     ap.add_argument("--no-cpu-baseline", action="store_true")

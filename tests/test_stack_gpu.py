@@ -209,3 +209,50 @@ def test_four_layer_stack_every_layer_and_drift(stack, M):
     print("4-layer drift at M=%d over tokens %s: max |gpu - oracle chain| = %.4g, "
           "max relative to |ref| + A = %.4g" % (M, tokens, float(drift.max()), rel))
     assert np.all(np.isfinite(gpu)) and math.isfinite(rel)
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_stack_replayed_as_one_cuda_graph_gives_the_eager_bits(stack, M):
+    """The benchmark times the step as one captured CUDA graph: the four
+    layers captured (prefetch and shared-expert side streams included) and
+    replayed twice give the same bits as the same calls launched one by one,
+    whose every stage the tests above check against the oracle."""
+    layers, _ = stack
+    x_bits = wl.token_rows(M, H, "stack-graph", M)
+    main = torch.cuda.Stream(priority=-1)
+    pref = torch.cuda.Stream()
+    evs = [torch.cuda.Event() for _ in range(NL)]
+    pf_bytes = min(H * H * 2, torch.cuda.get_device_properties(0).L2_cache_size // 2)
+    xs = [wl.bits_to_torch(x_bits)] + [torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+                                      for _ in range(NL)]
+    qkv = torch.empty((M, H + KV), dtype=torch.bfloat16, device="cuda")
+    r = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+    idxs = [torch.full((M, K8), -1, dtype=torch.int32, device="cuda") for _ in range(NL)]
+
+    def run():
+        for l in range(NL):
+            pf = (pref, evs[l], layers[(l + 1) % NL].Wq.data_ptr(), pf_bytes)
+            decode_layer(layers[l], xs[l], qkv, r, xs[l + 1], K8, idx=idxs[l], stream=main,
+                         prefetch=pf)
+        main.wait_stream(pref)
+
+    run()
+    torch.cuda.synchronize()
+    assert dg.sync_check(main) == dg.DEC_OK
+    eager = [x.clone() for x in xs[1:]] + [i.clone() for i in idxs]
+    for t in xs[1:] + idxs:
+        t.fill_(-1)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=main):
+        run()
+    for _ in range(2):
+        with torch.cuda.stream(main):
+            g.replay()
+        torch.cuda.synchronize()
+        assert dg.sync_check(main) == dg.DEC_OK
+        for a, b in zip(eager, xs[1:] + idxs):
+            assert torch.equal(a, b)
+        for t in xs[1:] + idxs:
+            t.fill_(-1)
+        torch.cuda.synchronize()
