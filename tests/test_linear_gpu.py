@@ -280,9 +280,9 @@ def test_tc_cluster_integer_inputs_match_stream_k(M, K):
     assert torch.equal(y, ys)
 
 
-@pytest.mark.parametrize("M", [17, 64])
-def test_tc_cluster_residual(M):
-    K, N = 1024, 2048
+@pytest.mark.parametrize("M,K", [(17, 1024), (64, 1024), (32, 4096)])
+def test_tc_cluster_residual(M, K):
+    N = 2048
     x = wl.normal_bf16((M, K), 1.0, "tccl-res", M, "x")
     W = wl.normal_bf16((N, K), 0.02, "tccl-res", M, "W")
     r = wl.normal_bf16((M, N), 1.0, "tccl-res", M, "r")
