@@ -68,10 +68,12 @@ def kernel_label(name):
         if m.group(1) == "2":  # the fp32-output instance runs the shared expert's down projection
             return "shared expert down [tcgen05 fp32]"
         return "projection [tcgen05 %s]" % _EPI.get(m.group(1), m.group(1))
-    m = re.search(r"gemv_mma_kernel<(\d+),\s*\d+,\s*\d+,\s*(\d+)>", name)
+    # <rows, token rows, k blocks per stage, CTAs per SM, epilogue>
+    m = re.search(r"gemv_mma_kernel<(\d+),\s*(\d+),\s*\d+,\s*(\d+),\s*(\d+)>", name)
     if m:
-        return "projection [slab %s rows/CTA %s, mma.sync]" % (m.group(1),
-                                                             _EPI.get(m.group(2), m.group(2)))
+        return "projection [slab %s rows/CTA XR=%s %s, mma.sync%s]" % (
+            m.group(1), m.group(2), _EPI.get(m.group(4), m.group(4)),
+            ", 2/SM" if m.group(3) == "2" else "")
     m = re.search(r"gemv_slab_kernel<(\d+),\s*(\d+)>", name)
     if m:
         return "projection [slab %s rows/CTA %s, CUDA cores]" % (m.group(1),

@@ -33,8 +33,10 @@ def test_labels_of_every_kernel_family():
             "shared expert down [tcgen05 fp32]",
         "void dg::gemv_slab_kernel<8, 0>(CUtensorMap_st, const unsigned short *, long long, dg::StreamArgs)":
             "projection [slab 8 rows/CTA bf16, CUDA cores]",
-        "void dg::gemv_mma_kernel<32, 4, 4, 1>(CUtensorMap_st, const unsigned short *, long long, dg::StreamArgs)":
-            "projection [slab 32 rows/CTA bf16+residual, mma.sync]",
+        "void dg::gemv_mma_kernel<32, 4, 4, 2, 1>(CUtensorMap_st, CUtensorMap_st, dg::StreamArgs)":
+            "projection [slab 32 rows/CTA XR=4 bf16+residual, mma.sync, 2/SM]",
+        "void dg::gemv_mma_kernel<64, 16, 2, 1, 0>(CUtensorMap_st, CU":
+            "projection [slab 64 rows/CTA XR=16 bf16, mma.sync]",
         "dg::schedule_gather_kernel(const uint4 *, const int *, int, int, int, int, uint4 *, int *)":
             "schedule + gather",
         "dg::combine_kernel(const float *, const float *, const float *)": "combine",
