@@ -444,24 +444,17 @@ def run_ours(args, rank, world, local_rank):
             replay(graph)
 
     def step_e2e():
-        # inputs in from pinned host memory, the step, results out
-        if graph is None:
-            for M in BATCHES:
-                a = acts[M]
-                with torch.cuda.stream(main):
-                    a["xs"][0].copy_(a["x_host"], non_blocking=True)
-                stack(M)
-                with torch.cuda.stream(main):
-                    a["out_host"].copy_(a["xs"][nl], non_blocking=True)
-            if not args.no_prefetch:
-                main.wait_stream(pref)
-            return
-        with torch.cuda.stream(main):
-            for M in BATCHES:
-                acts[M]["xs"][0].copy_(acts[M]["x_host"], non_blocking=True)
-            graph.replay()
-            for M in BATCHES:
-                acts[M]["out_host"].copy_(acts[M]["xs"][nl], non_blocking=True)
+        # the public API called layer by layer, as a user calls it (no graph):
+        # each batch's input in from pinned host memory, its result out
+        for M in BATCHES:
+            a = acts[M]
+            with torch.cuda.stream(main):
+                a["xs"][0].copy_(a["x_host"], non_blocking=True)
+            stack(M)
+            with torch.cuda.stream(main):
+                a["out_host"].copy_(a["xs"][nl], non_blocking=True)
+        if not args.no_prefetch:
+            main.wait_stream(pref)
 
     if graph is not None:
         for _ in range(args.warmup):
