@@ -78,6 +78,52 @@ def test_random_shapes_reach_every_kernel_family():
         assert want in seen, (want, sorted(seen))
 
 
+def _wide_shape(seed):
+    # 1-16 tokens over 4865-9728 rows: the 48- and 64-row slabs, and split-K
+    # where K is not a multiple of 64
+    rng = np.random.default_rng(20_000 + seed)
+    M = int(rng.integers(1, 17))
+    N = int(rng.integers(4865, 9729))
+    K = int(rng.choice([64 * int(rng.integers(8, 128)), 8 * int(rng.integers(64, 1024))]))
+    residual = bool(rng.integers(0, 2))
+    ldx = K + 8 * int(rng.integers(1, 4)) if rng.integers(0, 3) == 0 else 0
+    return M, N, K, residual, ldx
+
+
+WIDE_SEEDS = list(range(16))
+
+
+@pytest.mark.parametrize("seed", WIDE_SEEDS)
+def test_random_wide_projection_matches_oracle(seed):
+    M, N, K, residual, ldx = _wide_shape(seed)
+    key = ("fuzz-wide", seed)
+    wide = wl.normal_bf16((M, ldx or K), 1.0, *key, "x")
+    W = wl.normal_bf16((N, K), 0.02, *key, "W")
+    r = wl.normal_bf16((M, N), 1.0, *key, "r") if residual else None
+    xt = wl.bits_to_torch(wide)[:, :K]
+    y = dg.dec_linear(xt, wl.bits_to_torch(W), residual=None if r is None else wl.bits_to_torch(r))
+    assert dg.sync_check() == dg.DEC_OK
+    if K % 64 == 0:
+        rows = -(-N // dg.last_grid())
+        assert dg.last_slab() and rows in (48, 64), (M, N, K, rows)
+    cols = np.sort(np.random.default_rng(seed + 3000).choice(N, 256, replace=False))
+    ref, A = oracle.linear(wide[:, :K], W[cols])
+    if r is not None:
+        ref, A = oracle.residual(r[:, cols], ref, A)
+    assert_within_tol(to_f64(y)[:, cols], ref, A,
+                      "wide fuzz seed %d: M=%d N=%d K=%d residual=%s ldx=%d %s" %
+                      (seed, M, N, K, residual, ldx, dg.last_choice()))
+
+
+def test_random_wide_shapes_reach_both_slab_widths():
+    seen = set()
+    for seed in WIDE_SEEDS:
+        M, N, K, _, _ = _wide_shape(seed)
+        if K % 64 == 0:
+            seen.add(48 if N <= 48 * 152 else 64)
+    assert seen == {48, 64}, seen
+
+
 # ---------------------------------------------------------------- MoE blocks
 def _moe_shape(seed):
     rng = np.random.default_rng(10_000 + seed)
