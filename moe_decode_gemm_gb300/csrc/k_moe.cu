@@ -88,12 +88,19 @@ static cudaError_t run_router(const Ctx& cx, const void* x, const void* Wr, int 
                    xmap, xmap, a);
 }
 
+// From 17 tokens the router's product is a dense contraction (352 MFLOP at
+// 64 tokens over 384 x 7168): tcgen05 with the accumulator in tensor memory,
+// in the same cluster split and with the same top-k in the last cluster.
+// Same-GPU A/B, us per block, mma.sync -> tcgen05 router: MoE block at
+// M = 64: 3709 -> 3702 (the shared expert hides most of the router there);
+// latent block (L = 512) at M = 32 / 64: 238.9 / 343.3 -> 234.6 / 333.5.
 cudaError_t launch_router(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E, int k,
                           int32_t* idx_user, float* w_user, const MoeBufs& b, int L) {
   if (k < 1 || k > 32 || k > E || E > 1024 || L < 0) return cudaErrorInvalidValue;
   if (M <= 8) return run_router<8>(cx, x, Wr, M, H, E, k, idx_user, w_user, b, L);
   if (M <= 16) return run_router<16>(cx, x, Wr, M, H, E, k, idx_user, w_user, b, L);
-  return run_router<64>(cx, x, Wr, M, H, E, k, idx_user, w_user, b, L);
+  const RouteOut ro{b.logits, b.route_ctr, b.topk, b.gate, idx_user, w_user};
+  return launch_router_tc(cx, x, Wr, M, H, E, L, k, router_clusters(H), ro);
 }
 
 // ------------------------------------------------------------------ schedule + gather

@@ -349,7 +349,9 @@ struct TcCl {
   static_assert(kTileRows * kTcXRows * 4 <= kStages * kStage, "partial tile fits");
 };
 
-template <int EPI, int KSUB>
+// ROUTE: the router's product (EPI_F32 logits); the last of the TILES clusters
+// to write its logits then selects every token's top-k experts and gates.
+template <int EPI, int KSUB, bool ROUTE = false>
 __global__ void __launch_bounds__(kTcThreads, 2)
     tc_cluster_kernel(const __grid_constant__ CUtensorMap wmap,
                       const __grid_constant__ CUtensorMap xmap, const StreamArgs a, const int NP,
@@ -362,7 +364,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTcClStages * kStageB);
   uint64_t* empty = full + kTcClStages;
   uint64_t* tfull = empty + kTcClStages;  // [1] accumulator complete
-  volatile int* s_flags = reinterpret_cast<volatile int*>(tfull + 1);  // [0] abort
+  volatile int* s_flags = reinterpret_cast<volatile int*>(tfull + 1);  // [0] abort [2] route
   uint32_t* s_taddr = reinterpret_cast<uint32_t*>(const_cast<int*>(s_flags) + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -526,6 +528,32 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       if (n < a.nout) store_out<EPI, false>(a, gi, t, n, acc);
     }
   }
+  if (ROUTE && a.route_k > 0) {
+    // This cluster's logits are written (the barrier orders every thread's
+    // stores before the release of the arrival below). The last of the TILES
+    // clusters to arrive acquires them all and selects the experts: its
+    // epilogue warps take the tokens in turn.
+    __syncwarp();
+    cluster_sync_all();
+    if (cr == 0 && threadIdx.x == 0) {
+      const int old = atomic_add_acq_rel_gpu(a.route_ctr, 1);
+      const int last = old == a.TILES - 1 ? 1 : 0;
+      if (last) *a.route_ctr = 0;
+      for (int q = 0; q < cs; ++q) st_dsmem_s32(const_cast<int*>(&s_flags[2]), (uint32_t)q, last);
+    }
+    __syncwarp();
+    cluster_sync_all();
+    if (s_flags[2] && warp >= 2) {
+      const int K = a.route_k, nwc = kTcEpi / 32;
+      for (int m = cr * nwc + (warp - 2); m < a.M; m += cs * nwc)
+        if (DG_OK(a.status, (long long)(m + 1) * K <= a.pairs &&
+                                (long long)m * a.ldo + a.route_E <= a.out_len, m))
+          warp_topk_gates(reinterpret_cast<const float*>(a.out) + (long long)m * a.ldo, a.route_E,
+                          K, lane, a.route_idx + m * K, a.route_gate + m * K,
+                          a.route_idx_user ? a.route_idx_user + m * K : nullptr,
+                          a.route_w_user ? a.route_w_user + m * K : nullptr);
+    }
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -578,6 +606,53 @@ cudaError_t launch_dense_tc_cluster(const Ctx& cx, bool residual, const void* x,
                     : run_tc_cluster<EPI_BF16, 1>(cx, x, W, res, y, M, N, K, cl);
   return residual ? run_tc_cluster<EPI_BF16_RES, 2>(cx, x, W, res, y, M, N, K, cl)
                   : run_tc_cluster<EPI_BF16, 2>(cx, x, W, res, y, M, N, K, cl);
+}
+
+// Router scores and top-k on the tensor cores (17-64 tokens): logits =
+// x·Wrᵀ in fp32 over E + L rows (router rows, then the latent input rows),
+// cl CTAs per 128-row tile in one cluster, the top-k of the first E columns
+// in the last cluster.
+template <int KSUB>
+static cudaError_t run_router_tc(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E,
+                                 int L, int k, int cl, const RouteOut& ro) {
+  constexpr int SMEM = TcCl<KSUB>::kSmem;
+  auto kern = tc_cluster_kernel<EPI_F32, KSUB, true>;
+  static DevOnce once;
+  if (cudaError_t e = setup_smem(once, kern, SMEM, true); e != cudaSuccess) return e;
+  const int N = E + L, NP = (M + 15) / 16 * 16;
+  CUtensorMap wmap, xmap;
+  if (!make_tmap(&wmap, Wr, (uint64_t)N, (uint64_t)H, kTileRows, true)) return cudaErrorInvalidValue;
+  if (!make_tmap(&xmap, x, (uint64_t)M, (uint64_t)H, (uint32_t)NP, false))
+    return cudaErrorInvalidValue;
+  StreamArgs a = {};
+  a.K = H;
+  a.KB = (H + KSUB * kKBlk - 1) / (KSUB * kKBlk);
+  a.TILES = (N + kTileRows - 1) / kTileRows;
+  a.nout = N;
+  a.M = M;
+  a.out = ro.logits;
+  a.ldo = N;
+  a.status = cx.status;
+  a.out_len = (long long)M * N;
+  a.timeout_ns = cx.timeout_ns;
+  a.route_k = k;
+  a.route_E = E;
+  a.route_ctr = ro.ctr;
+  a.route_idx = ro.idx;
+  a.route_gate = ro.gate;
+  a.route_idx_user = ro.idx_user;
+  a.route_w_user = ro.w_user;
+  a.pairs = M * k;
+  return launch_kc(kern, dim3(a.TILES * cl), dim3(kTcThreads), SMEM, cx.stream, cx.pdl, cl, wmap,
+                   xmap, a, NP, umma_idesc_bf16(128, NP));
+}
+
+cudaError_t launch_router_tc(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E,
+                             int L, int k, int cl, const RouteOut& ro) {
+  if (M < 16 || M > kTcXRows || cl < 1 || cl > 8 || cl > (H + kKChunk - 1) / kKChunk)
+    return cudaErrorInvalidValue;
+  if (H / cl >= 768) return run_router_tc<1>(cx, x, Wr, M, H, E, L, k, cl, ro);
+  return run_router_tc<2>(cx, x, Wr, M, H, E, L, k, cl, ro);
 }
 
 // PAIRED: W is [2I, K] (gate rows, then up rows) and N = I; y = bf16(silu(x·W1ᵀ)

@@ -72,6 +72,20 @@ cudaError_t launch_dense_tc_f32(const Ctx& cx, const void* x, const void* W, flo
 // (x·W3ᵀ)) [M, I], 16 <= M <= 64; stream-K over `grid` CTAs.
 cudaError_t launch_swiglu_tc(const Ctx& cx, const void* x, const void* W13, void* h, int M, int I,
                              int K, int grid, float* ws, int* ctr);
+// Router outputs: fp32 logits [M, E + L], the arrival counter (zero at rest),
+// the chosen experts and gates [M, k], optional copies for the caller.
+struct RouteOut {
+  float* logits;
+  int* ctr;
+  int* idx;
+  float* gate;
+  int32_t* idx_user;
+  float* w_user;
+};
+// Router scores and top-k on tcgen05, 16 <= M <= 64: cl CTAs (a cluster) per
+// 128-row tile of the E + L rows.
+cudaError_t launch_router_tc(const Ctx& cx, const void* x, const void* Wr, int M, int H, int E,
+                             int L, int k, int cl, const RouteOut& ro);
 // tcgen05 cluster split: cl CTAs per 128-row tile (grid = tiles * cl).
 cudaError_t launch_dense_tc_cluster(const Ctx& cx, bool residual, const void* x, const void* W,
                                     const void* res, void* y, int M, int N, int K, int cl);

@@ -117,14 +117,17 @@ def test_routing_limits_topk32_of_1024_experts_64_tokens():
     _check(*blk, k, "E=1024 k=32 M=64")
 
 
+@pytest.mark.parametrize("M", [16, 40])
 @pytest.mark.parametrize("H", [320, 520, 696, 840])
-def test_router_clusters_of_any_size_cover_every_expert_row(H):
+def test_router_clusters_of_any_size_cover_every_expert_row(H, M):
     # The router runs one thread-block cluster of min(H/128 rounded up, 8)
     # CTAs per 128 experts: 3, 5, 6 and 7 CTAs here, which do not divide the
     # 128 rows of a tile. Experts 125-127 (the last rows of the first tile)
     # are made the likeliest choices, so most tokens' top-k depends on them.
-    M, E, I, k = 16, 160, 128, 4
-    key = ("router-rows", H)
+    # 16 tokens: mma.sync dot products; 40: tcgen05 (tensor-memory partials
+    # pushed to the rows' owners).
+    E, I, k = 160, 128, 4
+    key = ("router-rows", H) if M == 16 else ("router-rows", H, M)
     Wr = wl.normal_bf16((E, H), 1.0 / math.sqrt(H), *key, "Wr")
     Wr[125:128] = wl.normal_bf16((3, H), 6.0 / math.sqrt(H), *key, "Wr-hot")
     x, _ = gap_rows(Wr, M, H, k, *key, "x")
