@@ -78,9 +78,12 @@ def kernel_label(name):
     if m:
         return "projection [slab %s rows/CTA %s, CUDA cores]" % (m.group(1),
                                                                 _EPI.get(m.group(2), m.group(2)))
-    m = re.search(r"tc_cluster_kernel<(\d+)(?:,\s*(\d+))?>", name)
+    # <epilogue, k boxes per stage, router>
+    m = re.search(r"tc_cluster_kernel<(\d+)(?:,\s*(\d+))?(?:,\s*(\w+))?>", name)
     if m:
         stage = "" if m.group(2) is None else ", %d k per stage" % (64 * int(m.group(2)))
+        if m.group(3) in _TRUE:
+            return "router + top-k [tcgen05 cluster%s]" % stage
         return "projection [tcgen05 %s cluster%s]" % (_EPI.get(m.group(1), m.group(1)), stage)
     for k, lab in (("schedule_gather_kernel", "schedule + gather"),
                    ("combine_kernel", "combine"), ("add_kernel", "residual add"),

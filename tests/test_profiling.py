@@ -27,6 +27,10 @@ def test_labels_of_every_kernel_family():
             "projection [tcgen05 bf16 cluster]",
         "void dg::tc_cluster_kernel<1, 1>(CUtensorMap_st, CUtensorMap_st, dg::StreamArgs, int, unsigned int)":
             "projection [tcgen05 bf16+residual cluster, 64 k per stage]",
+        "void dg::tc_cluster_kernel<2, 1, true>(CUtensorMap_st, CUtensorMap_st, dg::StreamArgs, int, unsigned int)":
+            "router + top-k [tcgen05 cluster, 64 k per stage]",
+        "void dg::tc_cluster_kernel<0, 2, false>(CUtensorMap_st, CUtensorMap_st, dg::StreamArgs, int, unsigned int)":
+            "projection [tcgen05 bf16 cluster, 128 k per stage]",
         "void dg::tc_linear_kernel<3, true>(CUtensorMap_st, CUtensorMap_st, dg::StreamArgs, int, unsigned int)":
             "shared expert gate/up [tcgen05 SwiGLU]",
         "void dg::tc_linear_kernel<2, false>(CUtensorMap_st, CUtensorMap_st, dg::StreamArgs, int, unsigned int)":
