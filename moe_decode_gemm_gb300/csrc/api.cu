@@ -530,10 +530,20 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
     if ((rc = counted(launch_experts_w2(cx, W2, M, Wd, E, topk, I, s->mb, egrid, ws, ctr))))
       return rc;
   }
+  // Latent block, 1-16 tokens, where whole-row slabs of Wup fill the SMs: the
+  // up-projection after the join, on the slab kernel, with the shared
+  // expert's output and the residual added in its epilogue (one launch and
+  // one pass over u fewer than the split-K projection and the final sum).
+  // Same-GPU A/B (L = 512, hidden 7168), us per block at M = 1 / 2 / 4 / 8 /
+  // 16, split-K projection and final sum -> slab tail: 55.8 / 62.7 / 74.8 /
+  // 101.9 / 149.9 -> 52.8 / 58.4 / 69.6 / 101.8 / 149.0.
+  const int Ru = (L > 0 && !forced("splitk")) ? gemv_mma_rows(M, H, L, s->sms) : 0;
   if (L > 0) {
-    // z = bf16(sum_j g_j o_j) on width L, then u = z·Wupᵀ in fp32 (stream-K
-    // over every SM), then out = bf16(res + (u + s)) below.
+    // z = bf16(sum_j g_j o_j) on width L
     if ((rc = counted(launch_combine(cx, s->mb, false, nullptr, s->mb.z, M, L, topk)))) return rc;
+  }
+  if (L > 0 && !Ru) {
+    // u = z·Wupᵀ in fp32 (stream-K over every SM); out = bf16(res + (u + s)) below
     const int xr = M <= 2 ? 8 : (M <= 16 ? 16 : 64);
     const long long T = (long long)((H + 127) / 128) * ((L + 127) / 128);
     const int ugrid = (int)(T < s->sms ? T : s->sms);
@@ -548,6 +558,11 @@ static int moe_impl(const void* x, const void* Wr, const void* W13, const void* 
   // the programmatic (early-start) dependency so both are complete ones.
   cx.pdl = !shared;
   ProbeScope p(4, st);
+  if (Ru) {
+    cx.ldx = 0;
+    return counted(launch_gemv_mma(cx, res != nullptr, s->mb.z, Wup, res, out, M, H, L, Ru,
+                                   shared ? s->mb.s : nullptr));
+  }
   if (L > 0) return counted(launch_combine_up(cx, s->mb, shared, res, out, M, H));
   return counted(launch_combine(cx, s->mb, shared, res, out, M, H, topk));
 }

@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(kGvThreads, MINB)
 
 template <int R, int XR, int KBS, int MINB, int EPI>
 static cudaError_t run_gemv_mma(const Ctx& cx, const void* x, long long ldx, const void* W,
-                                const void* res, void* y, int M, int N, int K) {
+                                const void* res, const float* addf, void* y, int M, int N, int K) {
   if (M > XR) return cudaErrorInvalidValue;
   auto kern = gemv_mma_kernel<R, XR, KBS, MINB, EPI>;
   constexpr int SMEM = MmaSlab<R, XR, KBS, MINB>::SMEM;
@@ -393,6 +393,8 @@ static cudaError_t run_gemv_mma(const Ctx& cx, const void* x, long long ldx, con
   a.timeout_ns = cx.timeout_ns;
   a.out_len = (long long)M * N;
   a.res_len = res ? (long long)M * N : 0;
+  a.addf = addf;
+  a.addf_len = addf ? (long long)M * N : 0;
   const int grid = (N + R - 1) / R;
   return launch_k(kern, dim3(grid), dim3(kGvThreads), SMEM, cx.stream, cx.pdl, wmap, xmap, a);
 }
@@ -461,12 +463,15 @@ constexpr long long kDeepRingBytes = 320 * 1024;
 
 template <int R, int XR, int KBS>
 static cudaError_t mma_epi(const Ctx& cx, bool residual, const void* x, long long ldx,
-                           const void* W, const void* res, void* y, int M, int N, int K) {
+                           const void* W, const void* res, const float* addf, void* y, int M,
+                           int N, int K) {
   if ((long long)(R + XR) * K * 2 > kDeepRingBytes)
-    return residual ? run_gemv_mma<R, XR, KBS, 1, EPI_BF16_RES>(cx, x, ldx, W, res, y, M, N, K)
-                    : run_gemv_mma<R, XR, KBS, 1, EPI_BF16>(cx, x, ldx, W, res, y, M, N, K);
-  return residual ? run_gemv_mma<R, XR, KBS, 2, EPI_BF16_RES>(cx, x, ldx, W, res, y, M, N, K)
-                  : run_gemv_mma<R, XR, KBS, 2, EPI_BF16>(cx, x, ldx, W, res, y, M, N, K);
+    return residual
+               ? run_gemv_mma<R, XR, KBS, 1, EPI_BF16_RES>(cx, x, ldx, W, res, addf, y, M, N, K)
+               : run_gemv_mma<R, XR, KBS, 1, EPI_BF16>(cx, x, ldx, W, res, addf, y, M, N, K);
+  return residual
+             ? run_gemv_mma<R, XR, KBS, 2, EPI_BF16_RES>(cx, x, ldx, W, res, addf, y, M, N, K)
+             : run_gemv_mma<R, XR, KBS, 2, EPI_BF16>(cx, x, ldx, W, res, addf, y, M, N, K);
 }
 
 // Token rows per stage XR = 4, 8 or 16 (the least that holds M); k blocks
@@ -474,20 +479,22 @@ static cudaError_t mma_epi(const Ctx& cx, bool residual, const void* x, long lon
 // at 64), 24 KB at R = 48 (4 k blocks, two per warp of a row group).
 template <int R>
 static cudaError_t mma_rows(const Ctx& cx, bool residual, const void* x, long long ldx,
-                            const void* W, const void* res, void* y, int M, int N, int K) {
+                            const void* W, const void* res, const float* addf, void* y, int M,
+                            int N, int K) {
   constexpr int KBS = R == 48 ? 4 : 128 / R;
-  if (M <= 4) return mma_epi<R, 4, KBS>(cx, residual, x, ldx, W, res, y, M, N, K);
-  if (M <= 8) return mma_epi<R, 8, KBS>(cx, residual, x, ldx, W, res, y, M, N, K);
-  return mma_epi<R, 16, KBS>(cx, residual, x, ldx, W, res, y, M, N, K);
+  if (M <= 4) return mma_epi<R, 4, KBS>(cx, residual, x, ldx, W, res, addf, y, M, N, K);
+  if (M <= 8) return mma_epi<R, 8, KBS>(cx, residual, x, ldx, W, res, addf, y, M, N, K);
+  return mma_epi<R, 16, KBS>(cx, residual, x, ldx, W, res, addf, y, M, N, K);
 }
 
 cudaError_t launch_gemv_mma(const Ctx& cx, bool residual, const void* x, const void* W,
-                            const void* res, void* y, int M, int N, int K, int R) {
+                            const void* res, void* y, int M, int N, int K, int R,
+                            const float* addf) {
   const long long ldx = cx.ldx ? cx.ldx : K;
-  if (R == 16) return mma_rows<16>(cx, residual, x, ldx, W, res, y, M, N, K);
-  if (R == 32) return mma_rows<32>(cx, residual, x, ldx, W, res, y, M, N, K);
-  if (R == 48) return mma_rows<48>(cx, residual, x, ldx, W, res, y, M, N, K);
-  if (R == 64) return mma_rows<64>(cx, residual, x, ldx, W, res, y, M, N, K);
+  if (R == 16) return mma_rows<16>(cx, residual, x, ldx, W, res, addf, y, M, N, K);
+  if (R == 32) return mma_rows<32>(cx, residual, x, ldx, W, res, addf, y, M, N, K);
+  if (R == 48) return mma_rows<48>(cx, residual, x, ldx, W, res, addf, y, M, N, K);
+  if (R == 64) return mma_rows<64>(cx, residual, x, ldx, W, res, addf, y, M, N, K);
   return cudaErrorInvalidValue;
 }
 

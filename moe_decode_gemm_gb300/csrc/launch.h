@@ -55,11 +55,14 @@ int gemv_slab_rows(int M, int N, int K, int sms);
 cudaError_t launch_gemv_slab(const Ctx& cx, bool residual, const void* x, const void* W,
                              const void* res, void* y, int M, int N, int K, int R);
 
-// The same slabs for up to 16 tokens with mma.sync dot products: R = 16 or
-// 32 rows per CTA (R from gemv_mma_rows; 0 means the shape does not suit it).
+// The same slabs for up to 16 tokens with mma.sync dot products: R = 16, 32,
+// 48 or 64 rows per CTA (R from gemv_mma_rows; 0 means the shape does not
+// suit it). addf: optional fp32 [M, N] added to the product before the
+// residual, y = bf16(res + (x·Wᵀ + addf)).
 int gemv_mma_rows(int M, int N, int K, int sms);
 cudaError_t launch_gemv_mma(const Ctx& cx, bool residual, const void* x, const void* W,
-                            const void* res, void* y, int M, int N, int K, int R);
+                            const void* res, void* y, int M, int N, int K, int R,
+                            const float* addf = nullptr);
 
 // tcgen05 projection for 16 <= M <= 64.
 cudaError_t launch_dense_tc(const Ctx& cx, bool residual, const void* x, const void* W,

@@ -82,6 +82,8 @@ struct StreamArgs {
   void* out;
   long long ldo;             // elements between output rows
   const uint16_t* res;       // residual for EPI_BF16_RES ([M, ldo] bf16)
+  const float* addf;         // optional fp32 [M, ldo] added to the product before
+                             // the residual (EPI_BF16 / EPI_BF16_RES); null: none
   // split-K workspace
   float* ws;                 // [grid][2][128][XR] fp32 partial tiles
   int* ctr;                  // per output tile arrival counters (zero at rest)
@@ -100,7 +102,7 @@ struct StreamArgs {
   // a DEC_DEBUG build: out, res, ws (floats), ctr; pairs = rows of the pair
   // tables (grouped: M*k; router: M*k of route_idx); groups_len = entries of
   // grp_exp (grp_off has one more)
-  long long out_len, res_len, ws_len, ctr_len;
+  long long out_len, res_len, ws_len, ctr_len, addf_len;
   int pairs, groups_len;
 };
 
@@ -168,7 +170,10 @@ __device__ __forceinline__ void store_out(const StreamArgs& a, const GroupInfo& 
   const long long i = row * a.ldo + n;
   if (EPI == EPI_F32) {
     *DG_AT(a.status, reinterpret_cast<float*>(a.out), i, a.out_len) = v;
-  } else if (EPI == EPI_BF16_RES) {
+    return;
+  }
+  if (a.addf) v += *DG_AT(a.status, a.addf, i, a.addf_len);
+  if (EPI == EPI_BF16_RES) {
     const float r = bf_bits2f(*DG_AT(a.status, a.res, i, a.res_len));
     *DG_AT(a.status, reinterpret_cast<uint16_t*>(a.out), i, a.out_len) = f2bf_bits(r + v);
   } else {

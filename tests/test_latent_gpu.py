@@ -134,3 +134,31 @@ def test_full_hidden_latent_block(latent_bank, M):
     assert np.array_equal(idx.cpu().numpy(), r["idx"])
     ref, A = oracle.residual(res_bits, r["out"], r["absref"])
     assert_within_tol(to_f64(out)[tokens], ref[tokens], A[tokens], "latent full M=%d" % M)
+
+
+@pytest.mark.parametrize("shared,residual", [(False, False), (True, False), (False, True)])
+def test_full_hidden_latent_block_slab_tail_variants(latent_bank, shared, residual):
+    # 1-16 tokens at hidden 7168: the up-projection runs on whole-row slabs
+    # after the join, adding the shared expert's output (when there is one)
+    # and the residual (when given) in its epilogue
+    W13, W2, Ws13, Ws2, Wup, Wrl_bits = latent_bank
+    M = 8
+    x_bits, _ = gap_rows(Wrl_bits[:E], M, H, K8, "latent-tail", shared, residual)
+    t = wl.bits_to_torch
+    idx = torch.empty((M, K8), dtype=torch.int32, device="cuda")
+    res_bits = wl.normal_bf16((M, H), 1.0, "latent-tail", "res") if residual else None
+    out = dg.moe_decode_latent(t(x_bits), t(Wrl_bits), W13, W2, Wup, Ws13 if shared else None,
+                               Ws2 if shared else None, K8, topk_idx=idx,
+                               residual=t(res_bits) if residual else None)
+    assert dg.sync_check() == dg.DEC_OK
+    tokens = [0, 3, 7]
+    fetch = lambda e: (wl.torch_to_bits(W13[e]), wl.torch_to_bits(W2[e]))
+    sh = (wl.torch_to_bits(Ws13), wl.torch_to_bits(Ws2)) if shared else None
+    r = oracle.moe_latent(x_bits, Wrl_bits, E, fetch, K8, I, wl.torch_to_bits(Wup), shared=sh,
+                          tokens=tokens)
+    assert np.array_equal(idx.cpu().numpy(), r["idx"])
+    ref, A = r["out"], r["absref"]
+    if residual:
+        ref, A = oracle.residual(res_bits, ref, A)
+    assert_within_tol(to_f64(out)[tokens], ref[tokens], A[tokens],
+                      "latent tail shared=%s residual=%s" % (shared, residual))
