@@ -306,7 +306,10 @@ static int linear_impl(const void* x, const void* W, const void* res, void* y, i
   // with 8 ranks per tile: with 2-4 partials per tile the tile-aligned split
   // below sums them cheaply and its 4-stage ring streams a large share faster
   // than the cluster kernel's 2-stage one (M = 64, us, cluster -> aligned:
-  // 4096 x 7168 17.8 -> 16.2 at 4 ranks, 8192 x 7168 31.9 -> 24.9 at 2).
+  // 4096 x 7168 17.8 -> 16.2 at 4 ranks, 8192 x 7168 31.9 -> 24.9 at 2; with
+  // the cluster kernel's current stages and reduction, M = 32 / 64: 4096 x
+  // 7168 at 4 ranks 15.2 / 17.0 against 14.9 / 17.4, at 2 ranks 7168 x 7168
+  // 25.8 / 28.9 against 21.6 / 24.4, 8192 x 7168 29.9 against 26.1).
   if (S == 0 && regime == DEC_REGIME_TC && tiles * 8 <= s->sms && KB >= 8 &&
       tiles * 8 * 4 >= 3LL * s->sms && 256LL * K / 8 <= kTcClusterMaxBytes)
     cl = 8;
